@@ -1,0 +1,350 @@
+"""Checks that pin the fp64 oracle to facts other than itself.
+
+Each check takes the oracle's modules (``P`` = oracle.prologue, ``B`` =
+oracle.bf16) and calls their functions by attribute, so a test can plant a
+mistake in one oracle function (monkeypatch) and show that some check fails.
+A check raises AssertionError when the oracle disagrees with the fact it pins.
+
+What pins what:
+  bf16 rounding     exact rational nearest-even search (fractions.Fraction)
+  bf16 widening     struct unpacking of every 16-bit pattern
+  split / layouts   the pages' stated head-block orders (tests/golden/), a
+                    pure-permutation check, sectioned == interleaved
+  RMSNorm           rms == 1 (w=1, eps=0), the eps closed form, one-hot and
+                    constant vectors by hand, power-of-two scale invariance
+  RoPE              complex-multiplication form, pos 0 identity, pairwise norm,
+                    relative position, inv_freq closed values, cos(pos) at i=0
+  backward          central finite differences of the forward, eps=0
+                    orthogonality, R^T as the adjoint of R, dv passthrough
+  pool writes       exact placement and untouched bytes
+"""
+
+import math
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- bf16 ----
+
+def _exact_bf16_rne(x):
+    """Nearest bf16 to float x by exact rational comparison (ties -> even)."""
+    if math.isnan(x):
+        return 0x7FC0
+    sign = 0x8000 if math.copysign(1.0, x) < 0 else 0
+    ax = abs(x)
+    if math.isinf(ax):
+        return sign | 0x7F80
+    # Candidates: the bf16 patterns around the float32 truncation of |x|.
+    f32 = struct.unpack("<I", struct.pack("<f", min(ax, 3.4e38)))[0] >> 16
+    best, best_d = None, None
+    X = Fraction(ax)
+    for b in range(max(0, f32 - 2), min(0x7F80, f32 + 3) + 1):
+        if b == 0x7F80:
+            val = Fraction(2) ** 128  # overflow rounds like a value at 2**128
+        else:
+            val = Fraction(struct.unpack("<f", struct.pack("<I", b << 16))[0])
+        d = abs(X - val)
+        if best is None or d < best_d or (d == best_d and b % 2 == 0):
+            best, best_d = b, d
+    return sign | best
+
+
+def bf16_test_values(rng):
+    vals = list(rng.standard_normal(4000) * np.exp2(rng.integers(-30, 30, 4000)))
+    # exact ties and values one float64 ulp either side of a tie
+    for b in rng.integers(0x0001, 0x7F7F, 600):
+        lo = struct.unpack("<f", struct.pack("<I", int(b) << 16))[0]
+        hi = struct.unpack("<f", struct.pack("<I", (int(b) + 1) << 16))[0]
+        mid = (lo + hi) / 2.0
+        vals += [mid, np.nextafter(mid, 0.0), np.nextafter(mid, np.inf), -mid]
+    vals += [0.0, -0.0, 1e-45, 2.0 ** -133, 2.0 ** -134, 3 * 2.0 ** -135, 2.0 ** -126,
+             3.3895313892515355e38, 3.3961775292304e38, 3.4e38, 1e39, -1e39, 1.0, -1.0]
+    return np.array(vals, dtype=np.float64)
+
+
+def check_to_bf16_rne(B, rng):
+    x = bf16_test_values(rng)
+    got = B.to_bf16_rne(x)
+    want = np.array([_exact_bf16_rne(float(v)) for v in x], dtype=np.uint16)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, f"to_bf16_rne wrong at {x[bad[:5]]}: {got[bad[:5]]} vs {want[bad[:5]]}"
+
+
+def check_bf16_widen(B):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = B.bf16_bits_to_f64(bits)
+    want = np.array([struct.unpack("<f", struct.pack("<I", int(b) << 16))[0] for b in range(65536)])
+    ok = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert ok.all()
+
+
+# ------------------------------------------------------------- layouts ----
+
+def read_block_fixture(name):
+    """Parse a tests/golden head-block fixture into (n_q, n_kv, D, {kind: [blocks]})."""
+    meta, orders = {}, {"interleaved": [], "sectioned": []}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *rest = line.split()
+            if key in ("n_q", "n_kv", "head_dim"):
+                meta[key] = int(rest[0])
+            elif key in ("sectioned", "interleaved"):
+                orders[key] += rest
+            elif key == "interleaved_group":
+                orders["interleaved"] += rest[1:]
+    parse = lambda tok: (tok[0], int(tok[1:]))  # noqa: E731
+    return meta["n_q"], meta["n_kv"], meta["head_dim"], {
+        k: [parse(t) for t in v] for k, v in orders.items() if v}
+
+
+def check_head_block_fixture(P, name):
+    n_q, n_kv, D, orders = read_block_fixture(name)
+    for kind, want in orders.items():
+        got = P.head_blocks(P.PackedLayout(kind, n_q, n_kv, D))
+        assert got == want, f"{name} {kind}: {got[:12]} vs {want[:12]}"
+
+
+def check_split_is_permutation(P, layout, T=3):
+    """Each packed element lands in exactly one output slot, unchanged."""
+    ids = np.arange(T * layout.row_width, dtype=np.int64).reshape(T, layout.row_width)
+    q, k, v = P.split_heads(layout, ids)
+    assert q.shape == (T, layout.n_q, layout.head_dim)
+    assert k.shape == v.shape == (T, layout.n_kv, layout.head_dim)
+    allv = np.concatenate([q.ravel(), k.ravel(), v.ravel()])
+    assert np.array_equal(np.sort(allv), ids.ravel())
+    # token t's heads come from token t's row only
+    for t in range(T):
+        lo, hi = t * layout.row_width, (t + 1) * layout.row_width
+        for a in (q[t], k[t], v[t]):
+            assert a.min() >= lo and a.max() < hi
+    # and each head is one contiguous head_dim block of the row
+    for a in (q, k, v):
+        assert np.all(np.diff(a, axis=-1) == 1)
+        assert np.all(a[..., 0] % layout.head_dim == 0)
+
+
+def check_layout_equivalence(P, B, wl):
+    """Interleaved and sectioned packings of the same heads give identical results."""
+    from workloads import bits_u16
+
+    Li = P.PackedLayout("interleaved", wl.n_q, wl.n_kv, wl.head_dim)
+    Ls = P.PackedLayout("sectioned", wl.n_q, wl.n_kv, wl.head_dim)
+    wq, wk = wl.w_q.numpy(), wl.w_k.numpy()
+    oi = P.prologue_fwd(Li, bits_u16(wl.packed_rows()), wl.pos.numpy(), wq, wk, wl.eps, wl.rope_base, wl.nope)
+    os_ = P.prologue_fwd(Ls, bits_u16(wl.sectioned_rows()), wl.pos.numpy(), wq, wk, wl.eps, wl.rope_base, wl.nope)
+    for key in ("q", "k", "v_bits", "q_pre_bits", "k_pre_bits"):
+        assert np.array_equal(oi[key], os_[key]), key
+
+
+# ------------------------------------------------------------- RMSNorm ----
+
+def check_rms_norm(P, rng):
+    D = 64
+    ones = np.ones(D)
+    for scale in (1e-3, 1.0, 37.0):
+        x = rng.standard_normal((5, 7, D)) * scale
+        y = P.rms_norm(x, ones, 0.0)
+        assert np.allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, rtol=0, atol=1e-14)
+        # eps inside the root: rms(y) = sqrt(ms / (ms + eps))
+        eps = 0.25 * scale * scale
+        ms = np.mean(x * x, axis=-1)
+        y = P.rms_norm(x, ones, eps)
+        assert np.allclose(np.sqrt(np.mean(y * y, axis=-1)), np.sqrt(ms / (ms + eps)), rtol=1e-13, atol=0)
+    # one-hot: mean over D (not a sum, not D-1): y_0 = sqrt(D) * w_0 when eps = 0
+    w = rng.uniform(0.5, 1.5, D)
+    x = np.zeros(D)
+    x[0] = 3.0
+    y = P.rms_norm(x, w, 0.0)
+    assert abs(y[0] - math.sqrt(D) * w[0]) <= 1e-14 * math.sqrt(D) and np.all(y[1:] == 0)
+    # constant vector c: y = c / sqrt(c^2 + eps) * w
+    c, eps = -0.75, 1e-6
+    y = P.rms_norm(np.full(D, c), w, eps)
+    assert np.allclose(y, c / math.sqrt(c * c + eps) * w, rtol=1e-15, atol=0)
+    # two-element head, by hand: x = (3, 4): mean square 12.5
+    y = P.rms_norm(np.array([3.0, 4.0]), np.array([2.0, 0.5]), 0.5)
+    assert np.allclose(y, [3.0 / math.sqrt(13.0) * 2.0, 4.0 / math.sqrt(13.0) * 0.5], rtol=1e-15, atol=0)
+    # power-of-two scale invariance with eps = 0 (exact in binary floating point)
+    x = rng.standard_normal((4, D))
+    assert np.array_equal(P.rms_norm(x * 2.0 ** 9, w, 0.0), P.rms_norm(x, w, 0.0))
+    # each head is normalised on its own
+    x = rng.standard_normal((2, 3, D))
+    x2 = x.copy()
+    x2[:, 1, :] *= 10.0
+    assert np.array_equal(P.rms_norm(x, w, 1e-6)[:, 0], P.rms_norm(x2, w, 1e-6)[:, 0])
+
+
+# ---------------------------------------------------------------- RoPE ----
+
+def check_rope(P, rng):
+    D = 64
+    half = D // 2
+    # inverse frequencies: base**(-2i/D); i = 0 is exactly 1, i = D/4 is base**-0.5
+    f = P.rope_inv_freq(D, 10000.0)
+    assert f.shape == (half,) and f[0] == 1.0
+    assert abs(f[D // 4] - 0.01) <= 1e-17
+    assert abs(f[half - 1] - 10000.0 ** (-(D - 2) / D)) <= 1e-18
+    assert np.all(np.diff(f) < 0)
+    pos = rng.integers(0, 400000, 6)
+    y = rng.standard_normal((6, 3, D))
+    o = P.rope_rotate_half(y, pos, 500000.0)
+    # complex form: (y_i + i y_{i+D/2}) * exp(i pos inv_freq_i)
+    th = pos[:, None].astype(np.float64) * P.rope_inv_freq(D, 500000.0)[None, :]
+    z = (y[..., :half] + 1j * y[..., half:]) * np.exp(1j * th)[:, None, :]
+    assert np.allclose(o[..., :half], z.real, rtol=0, atol=1e-12)
+    assert np.allclose(o[..., half:], z.imag, rtol=0, atol=1e-12)
+    # i = 0 turns by exactly pos radians
+    assert np.allclose(o[:, :, 0], y[:, :, 0] * np.cos(pos.astype(float))[:, None]
+                       - y[:, :, half] * np.sin(pos.astype(float))[:, None], rtol=0, atol=1e-12)
+    # pairwise norm preserved
+    assert np.allclose(o[..., :half] ** 2 + o[..., half:] ** 2, y[..., :half] ** 2 + y[..., half:] ** 2,
+                       rtol=1e-12, atol=1e-13)
+    # position 0 is the identity
+    assert np.array_equal(P.rope_rotate_half(y, np.zeros(6, np.int64), 500000.0), y)
+    # relative position: <R_m q, R_n k> depends on n - m only
+    qv, kv = rng.standard_normal((1, 1, D)), rng.standard_normal((1, 1, D))
+    for m, n, s in ((3, 17, 1000), (100, 5, 250000), (0, 393215, -7)):
+        a = np.sum(P.rope_rotate_half(qv, [m], 1e4) * P.rope_rotate_half(kv, [n], 1e4))
+        b = np.sum(P.rope_rotate_half(qv, [m + s], 1e4) * P.rope_rotate_half(kv, [n + s], 1e4))
+        assert abs(a - b) <= 1e-9 * (1 + abs(a))
+    # R^T is the adjoint (and the inverse) of R
+    g = rng.standard_normal((6, 3, D))
+    lhs = np.sum(P.rope_rotate_half(g, pos, 5e5) * y)
+    rhs = np.sum(g * P.rope_rotate_half_transpose(y, pos, 5e5))
+    assert abs(lhs - rhs) <= 1e-11 * (1 + abs(lhs))
+    assert np.allclose(P.rope_rotate_half_transpose(o, pos, 500000.0), y, rtol=0, atol=1e-12)
+
+
+def check_nope_is_rope_at_zero(P, layout, rng, T=4):
+    from workloads import norm_weight, _gen
+
+    g = _gen(11)
+    x = rng.standard_normal((T, layout.row_width))
+    wq, wk = norm_weight(layout.head_dim, g).numpy(), norm_weight(layout.head_dim, g).numpy()
+    a = P.prologue_fwd_f64(layout, x, np.zeros(T, np.int64), wq, wk, 1e-6, 5e5, nope=False)
+    b = P.prologue_fwd_f64(layout, x, np.arange(T), wq, wk, 1e-6, 5e5, nope=True)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
+# ------------------------------------------------------------ backward ----
+
+def _loss(P, layout, x, wq, wk, pos, eps, base, nope, dq, dk, dv):
+    q, k, v = P.prologue_fwd_f64(layout, x, pos, wq, wk, eps, base, nope)
+    return np.sum(dq * q) + np.sum(dk * k) + np.sum(dv * v)
+
+
+def check_finite_differences(P, layout, rng, T=3, nope=False, n_probe=None, base=10000.0):
+    """Central differences of L = <dq,q> + <dk,k> + <dv,v> against prologue_bwd_f64."""
+    D = layout.head_dim
+    x = rng.standard_normal((T, layout.row_width))
+    wq, wk = rng.uniform(0.5, 1.5, D), rng.uniform(0.5, 1.5, D)
+    pos = rng.integers(0, 5000, T)
+    eps = 1e-3  # large enough to matter in the derivative
+    dq = rng.standard_normal((T, layout.n_q, D))
+    dk = rng.standard_normal((T, layout.n_kv, D))
+    dv = rng.standard_normal((T, layout.n_kv, D))
+    xq, xk, _ = P.split_heads(layout, x)
+    got = P.prologue_bwd_f64(layout, dq, dk, dv, xq, xk, pos, wq, wk, eps, base, nope)
+    args = (pos, eps, base, nope, dq, dk, dv)
+    h = 1e-6
+
+    idx = [(t, j) for t in range(T) for j in range(layout.row_width)]
+    if n_probe is not None:
+        pick = rng.choice(len(idx), size=min(n_probe, len(idx)), replace=False)
+        idx = [idx[i] for i in pick]
+    for t, j in idx:
+        xp, xm = x.copy(), x.copy()
+        xp[t, j] += h
+        xm[t, j] -= h
+        fd = (_loss(P, layout, xp, wq, wk, *args) - _loss(P, layout, xm, wq, wk, *args)) / (2 * h)
+        an = got["dpacked"][t, j]
+        assert abs(fd - an) <= 1e-6 * (1 + abs(an)), (t, j, fd, an)
+    for which, w in (("dw_q", wq), ("dw_k", wk)):
+        for d in range(D):
+            wp, wm = w.copy(), w.copy()
+            wp[d] += h
+            wm[d] -= h
+            if which == "dw_q":
+                lp = _loss(P, layout, x, wp, wk, *args)
+                lm = _loss(P, layout, x, wm, wk, *args)
+            else:
+                lp = _loss(P, layout, x, wq, wp, *args)
+                lm = _loss(P, layout, x, wq, wm, *args)
+            fd = (lp - lm) / (2 * h)
+            an = got[which][d]
+            assert abs(fd - an) <= 1e-6 * (1 + abs(an)), (which, d, fd, an)
+
+
+def check_backward_invariants(P, layout, rng, T=5):
+    D = layout.head_dim
+    x = rng.standard_normal((T, layout.row_width))
+    xq, xk, _ = P.split_heads(layout, x)
+    wq, wk = rng.uniform(0.5, 1.5, D), rng.uniform(0.5, 1.5, D)
+    dq = rng.standard_normal((T, layout.n_q, D))
+    dk = rng.standard_normal((T, layout.n_kv, D))
+    dv = rng.standard_normal((T, layout.n_kv, D))
+    pos = rng.integers(0, 131072, T)
+    out = P.prologue_bwd_f64(layout, dq, dk, dv, xq, xk, pos, wq, wk, 0.0, 5e5, False)
+    gq, gk, gv = P.split_heads(layout, out["dpacked"])
+    # v slots carry dv unchanged
+    assert np.array_equal(gv, dv)
+    # eps = 0: the norm is scale invariant, so its input gradient is orthogonal to x
+    for xs, gs in ((xq, gq), (xk, gk)):
+        dots = np.sum(xs * gs, axis=-1)
+        scale = np.sqrt(np.sum(xs * xs, axis=-1) * np.sum(gs * gs, axis=-1))
+        assert np.all(np.abs(dots) <= 1e-12 * scale)
+
+
+# --------------------------------------------------------------- pools ----
+
+def check_pool_placement(P, B, rng):
+    layout = P.PackedLayout("interleaved", 8, 2, 64)
+    T, num_pages, page_size = 7, 5, 4
+    bits = B.to_bf16_rne(rng.standard_normal((T, layout.row_width)))
+    slots = rng.choice(num_pages * page_size, size=T, replace=False)
+    page, off = slots // page_size, slots % page_size
+    shape = (num_pages, page_size, layout.n_kv, layout.head_dim)
+    kp0 = rng.integers(0, 65536, shape).astype(np.uint16)
+    vp0 = rng.integers(0, 65536, shape).astype(np.uint16)
+    wq, wk = rng.uniform(0.5, 1.5, 64), rng.uniform(0.5, 1.5, 64)
+    pos = rng.integers(0, 131072, T)
+    q, k, kp, vp = P.pool_write(layout, bits, pos, wq, wk, 1e-6, 5e5, False, page, off, kp0, vp0)
+    ref = P.prologue_fwd(layout, bits, pos, wq, wk, 1e-6, 5e5, False)
+    written = np.zeros((num_pages, page_size), bool)
+    for t in range(T):
+        written[page[t], off[t]] = True
+        assert np.array_equal(kp[page[t], off[t]], B.to_bf16_rne(ref["k"][t]))
+        # v goes in raw: the packed row's v-slot bits
+        assert np.array_equal(vp[page[t], off[t]], bits[t].reshape(-1, 64)[[5, 11]])
+    assert np.array_equal(kp[~written], kp0[~written])
+    assert np.array_equal(vp[~written], vp0[~written])
+    assert np.array_equal(q, ref["q"])
+
+
+def check_mla_rows(P, rng):
+    T = 5
+    x = rng.standard_normal((T, 576))
+    w = rng.uniform(0.5, 1.5, 512)
+    pos = rng.integers(0, 393216, T)
+    o = P.mla_rows_f64(x, pos, w, 0.0, 1e4, 512, 64)
+    # latent part: rms(y / w) == 1 with eps = 0; it ignores the rope part
+    assert np.allclose(np.sqrt(np.mean((o[:, :512] / w) ** 2, axis=-1)), 1.0, rtol=0, atol=1e-14)
+    x2 = x.copy()
+    x2[:, 512:] *= 100.0
+    assert np.array_equal(P.mla_rows_f64(x2, pos, w, 0.0, 1e4, 512, 64)[:, :512], o[:, :512])
+    # rope part: complex form with D = 64, base 1e4, not normalised, no weight
+    th = pos[:, None].astype(np.float64) * (1e4 ** (-np.arange(32) / 32.0))[None, :]
+    z = (x[:, 512:544] + 1j * x[:, 544:576]) * np.exp(1j * th)
+    assert np.allclose(o[:, 512:544], z.real, atol=1e-12, rtol=0)
+    assert np.allclose(o[:, 544:576], z.imag, atol=1e-12, rtol=0)
+    # position 0 leaves the rope part unchanged
+    o0 = P.mla_rows_f64(x, np.zeros(T, np.int64), w, 0.0, 1e4, 512, 64)
+    assert np.array_equal(o0[:, 512:], x[:, 512:])

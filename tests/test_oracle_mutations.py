@@ -1,0 +1,146 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and show that a pin catches each.
+
+If one of these stops failing, the pins have lost the power to tell a correct
+oracle from a wrong one.
+"""
+
+import numpy as np
+import pytest
+
+import oracle.bf16 as B
+import oracle.prologue as P
+import oracle_checks as C
+import workloads
+
+
+def _rope_sign_flipped(y, pos, base):
+    y = np.asarray(y, dtype=np.float64)
+    half = y.shape[-1] // 2
+    th = P.rope_angles(pos, y.shape[-1], base)[:, None, :]
+    a, b = y[..., :half], y[..., half:]
+    return np.concatenate([a * np.cos(th) + b * np.sin(th), b * np.cos(th) - a * np.sin(th)], axis=-1)
+
+
+def _rope_adjacent_pairs(y, pos, base):
+    y = np.asarray(y, dtype=np.float64)
+    th = P.rope_angles(pos, y.shape[-1], base)[:, None, :]
+    a, b = y[..., 0::2], y[..., 1::2]
+    out = np.empty_like(y)
+    out[..., 0::2] = a * np.cos(th) - b * np.sin(th)
+    out[..., 1::2] = b * np.cos(th) + a * np.sin(th)
+    return out
+
+
+def _inv_freq_wrong_exponent(head_dim, base):
+    return np.power(float(base), -np.arange(head_dim // 2, dtype=np.float64) / head_dim)
+
+
+def _norm_eps_outside(x, w, eps):
+    x = np.asarray(x, dtype=np.float64)
+    return x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps) * w
+
+
+def _norm_sum_not_mean(x, w, eps):
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps) * w
+
+
+def _norm_bwd_missing_term(x, w, g, eps):
+    x, g = np.asarray(x, dtype=np.float64), np.asarray(g, dtype=np.float64)
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return r * w * g, g * x * r
+
+
+def _norm_bwd_wrong_power(x, w, g, eps):
+    x, g = np.asarray(x, dtype=np.float64), np.asarray(g, dtype=np.float64)
+    D = x.shape[-1]
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    dot = np.sum(x * w * g, axis=-1, keepdims=True)
+    return r * w * g - x * (r ** 2 / D) * dot, g * x * r
+
+
+def _blocks_k_v_swapped(layout):
+    return [("v" if r == "k" else "k" if r == "v" else r, h) for r, h in _REAL_BLOCKS(layout)]
+
+
+def _blocks_q_transposed(layout):
+    # q head index taken as j * n_kv + g instead of g * G + j
+    out = []
+    for r, h in _REAL_BLOCKS(layout):
+        if r == "q" and layout.kind == "interleaved":
+            g, j = divmod(h, layout.group)
+            h = j * layout.n_kv + g
+        out.append((r, h))
+    return out
+
+
+_REAL_BLOCKS = P.head_blocks
+
+
+def _bf16_via_float32(x):
+    import torch
+
+    with np.errstate(over="ignore"):
+        t = torch.from_numpy(np.asarray(x, dtype=np.float64).astype(np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+_REAL_ROPE = P.rope_rotate_half
+
+
+def _rope_transpose_is_forward(d, pos, base):
+    return _REAL_ROPE(d, pos, base)
+
+
+def _checks_all(rng):
+    """Every pin, run in turn; raises AssertionError at the first that fails."""
+    C.check_to_bf16_rne(B, rng)
+    for name in ("head_blocks_8q_over_2kv.txt", "head_blocks_muse_spark_16kv.txt"):
+        C.check_head_block_fixture(P, name)
+    C.check_rms_norm(P, rng)
+    C.check_rope(P, rng)
+    C.check_finite_differences(P, P.PackedLayout("interleaved", 2, 1, 8), rng, T=2)
+    C.check_backward_invariants(P, P.PackedLayout("interleaved", 8, 2, 64), rng)
+    C.check_pool_placement(P, B, rng)
+    C.check_mla_rows(P, rng)
+
+
+def test_unmutated_oracle_passes_every_pin(rng):
+    _checks_all(rng)
+
+
+MUTATIONS = [
+    (P, "rope_rotate_half", _rope_sign_flipped),
+    (P, "rope_rotate_half", _rope_adjacent_pairs),
+    (P, "rope_inv_freq", _inv_freq_wrong_exponent),
+    (P, "rms_norm", _norm_eps_outside),
+    (P, "rms_norm", _norm_sum_not_mean),
+    (P, "rms_norm_backward", _norm_bwd_missing_term),
+    (P, "rms_norm_backward", _norm_bwd_wrong_power),
+    (P, "rope_rotate_half_transpose", _rope_transpose_is_forward),
+    (P, "head_blocks", _blocks_k_v_swapped),
+    (P, "head_blocks", _blocks_q_transposed),
+    (B, "to_bf16_rne", _bf16_via_float32),
+]
+
+
+@pytest.mark.parametrize("module,name,bad", MUTATIONS, ids=[m[2].__name__ for m in MUTATIONS])
+def test_planted_mistake_is_caught(module, name, bad, monkeypatch, rng):
+    monkeypatch.setattr(module, name, bad)
+    with pytest.raises(AssertionError):
+        _checks_all(rng)
+
+
+def test_planted_layout_mistake_breaks_layout_equivalence(monkeypatch):
+    # a sectioned table that swaps two q heads must break interleaved == sectioned
+    real = P.head_blocks
+
+    def swapped(layout):
+        b = real(layout)
+        if layout.kind == "sectioned":
+            b[0], b[1] = b[1], b[0]
+        return b
+
+    monkeypatch.setattr(P, "head_blocks", swapped)
+    with pytest.raises(AssertionError):
+        C.check_layout_equivalence(P, B, workloads.tiny())

@@ -1,0 +1,202 @@
+"""Seeded synthetic inputs for the packed-QKV prologue.
+
+This module only draws and lays out random inputs; it holds none of the
+prologue's arithmetic (no norm, no rotation, no rounding of results). Both the
+CUDA path's tests / benchmark and the fp64 oracle consume what it returns, so
+the two sides always see the same bits.
+
+Every draw uses ``torch.Generator('cpu').manual_seed(seed)`` and float32
+samples rounded to bf16. Norm weights are drawn U(0.5, 1.5), rounded to
+bf16-representable values and kept as float32 (so the float32 weights the
+kernels take and a bf16 reading of them are the same numbers).
+
+The five workloads mirror the shapes the pages measure: the Muse Spark packed
+projection [T, 16 kv heads, 10, 64] of "[muse_spark][perf] Split the packed
+qkv inside the q/k region" (Problem 1), and the 576-wide MLA kv latent rows
+(512 normed + 64 roped) written into a 64-token-page pool in "MLA DSpark: run
+each drafter layer's kv path beside its q path". No dataset is involved.
+"""
+
+from dataclasses import dataclass, field
+from typing import Optional
+
+import torch
+
+EPS = 1e-6
+
+
+def _gen(seed):
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+def normal_bf16(shape, g):
+    """N(0, 1) float32 draws rounded to bf16."""
+    return torch.randn(*shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def norm_weight(n, g):
+    """U(0.5, 1.5) draws rounded to bf16-representable values, kept as float32."""
+    u = torch.rand(n, generator=g, dtype=torch.float32) + 0.5
+    return u.to(torch.bfloat16).to(torch.float32)
+
+
+def random_slots(T, num_pages, page_size, g):
+    """Distinct (page, offset) pairs for T tokens: a seeded random permutation
+    of all pool slots, first T taken; no two tokens share a slot."""
+    if T > num_pages * page_size:
+        raise ValueError("more tokens than pool slots")
+    slot = torch.randperm(num_pages * page_size, generator=g)[:T]
+    return (slot // page_size).to(torch.int32), (slot % page_size).to(torch.int32)
+
+
+def sectioned_from_interleaved(packed, n_q, n_kv, head_dim):
+    """Re-lay interleaved rows [T, n_kv, G+2, D] as sectioned rows
+    [T, (n_q + 2 n_kv) * D] holding the same heads: q heads 0..n_q-1 (head
+    g*G + j is slot j of group g), then k heads (slot G), then v heads
+    (slot G+1)."""
+    G = n_q // n_kv
+    x = packed.reshape(packed.shape[0], n_kv, G + 2, head_dim)
+    q = x[:, :, :G, :].reshape(x.shape[0], n_q, head_dim)
+    k = x[:, :, G, :]
+    v = x[:, :, G + 1, :]
+    return torch.cat([q, k, v], dim=1).reshape(x.shape[0], -1).contiguous()
+
+
+@dataclass
+class GQAWorkload:
+    """Inputs of one GQA prologue call (all CPU tensors)."""
+
+    name: str
+    n_q: int
+    n_kv: int
+    head_dim: int
+    packed: torch.Tensor          # bf16 [T, n_kv, G+2, D] (interleaved)
+    pos: torch.Tensor             # int32 [T]
+    w_q: torch.Tensor             # float32 [D]
+    w_k: torch.Tensor             # float32 [D]
+    rope_base: float
+    nope: bool = False
+    eps: float = EPS
+    # training
+    dq: Optional[torch.Tensor] = None   # bf16 [T, n_q, D]
+    dk: Optional[torch.Tensor] = None   # bf16 [T, n_kv, D]
+    dv: Optional[torch.Tensor] = None   # bf16 [T, n_kv, D]
+    # paged pool destination
+    page: Optional[torch.Tensor] = None    # int32 [T]
+    offset: Optional[torch.Tensor] = None  # int32 [T]
+    num_pages: int = 0
+    page_size: int = 0
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def T(self):
+        return self.packed.shape[0]
+
+    @property
+    def row_width(self):
+        return (self.n_q + 2 * self.n_kv) * self.head_dim
+
+    def packed_rows(self):
+        """Interleaved packed input as [T, row_width]."""
+        return self.packed.reshape(self.T, self.row_width)
+
+    def sectioned_rows(self):
+        return sectioned_from_interleaved(self.packed, self.n_q, self.n_kv, self.head_dim)
+
+
+@dataclass
+class MLAWorkload:
+    name: str
+    rows: torch.Tensor            # bf16 [T, norm_dim + rope_dim]
+    pos: torch.Tensor             # int32 [T]
+    w: torch.Tensor               # float32 [norm_dim]
+    page: torch.Tensor
+    offset: torch.Tensor
+    num_pages: int
+    page_size: int
+    rope_base: float = 10000.0
+    norm_dim: int = 512
+    rope_dim: int = 64
+    eps: float = EPS
+
+    @property
+    def T(self):
+        return self.rows.shape[0]
+
+
+def gqa_inputs(T, n_q, n_kv, head_dim, seed, rope_base, nope=False, pos_high=None,
+               name="gqa", with_grads=False):
+    """Packed [T, n_kv, G+2, D] N(0,1) bf16, norm weights, positions.
+
+    Positions are 0..T-1 when pos_high is None, else uniform in [0, pos_high).
+    With with_grads, upstream gradients dq, dk, dv are N(0,1) bf16.
+    """
+    g = _gen(seed)
+    G = n_q // n_kv
+    packed = normal_bf16((T, n_kv, G + 2, head_dim), g)
+    w_q = norm_weight(head_dim, g)
+    w_k = norm_weight(head_dim, g)
+    if pos_high is None:
+        pos = torch.arange(T, dtype=torch.int32)
+    else:
+        pos = torch.randint(0, pos_high, (T,), generator=g, dtype=torch.int32)
+    wl = GQAWorkload(name, n_q, n_kv, head_dim, packed, pos, w_q, w_k, float(rope_base), nope)
+    if with_grads:
+        wl.dq = normal_bf16((T, n_q, head_dim), g)
+        wl.dk = normal_bf16((T, n_kv, head_dim), g)
+        wl.dv = normal_bf16((T, n_kv, head_dim), g)
+    return wl
+
+
+# --- the five workloads ------------------------------------------------------
+
+def tiny(seed=1):
+    """T=16, [16, 2 kv, 4 q + 1 k + 1 v, 64], base 10000, positions 0..15."""
+    return gqa_inputs(16, 8, 2, 64, seed, 10000.0, name="tiny_fwd_T16")
+
+
+def decode_pool(T, seed=2, num_pages=4096, page_size=64):
+    """Decode with a paged pool: [T,16,10,64], positions U[0,131072), base 5e5,
+    4096 pages x 64 tokens x 16 heads x 64, distinct random slots."""
+    wl = gqa_inputs(T, 128, 16, 64, seed, 500000.0, pos_high=131072, name=f"decode_pool_T{T}")
+    g = _gen(seed * 1000 + 7)
+    wl.page, wl.offset = random_slots(T, num_pages, page_size, g)
+    wl.num_pages, wl.page_size = num_pages, page_size
+    return wl
+
+
+def prefill(T, seed=3, nope=False):
+    """Prefill: [T,16,10,64], positions 0..T-1, base 5e5 (or NoPE)."""
+    return gqa_inputs(T, 128, 16, 64, seed, 500000.0, nope=nope,
+                      name=f"prefill_T{T}" + ("_nope" if nope else ""))
+
+
+def train(T, seed=4):
+    """Training fwd+bwd: [T,16,10,64], positions 0..T-1, base 5e5, N(0,1) grads."""
+    return gqa_inputs(T, 128, 16, 64, seed, 500000.0, name=f"train_T{T}", with_grads=True)
+
+
+def mla(T, seed=5, num_pages=8192, page_size=64):
+    """MLA latent rows [T, 576] N(0,1), positions U[0,393216), base 1e4,
+    pool of 8192 pages x 64 tokens x 576, distinct random slots."""
+    g = _gen(seed)
+    rows = normal_bf16((T, 576), g)
+    w = norm_weight(512, g)
+    pos = torch.randint(0, 393216, (T,), generator=g, dtype=torch.int32)
+    page, offset = random_slots(T, num_pages, page_size, _gen(seed * 1000 + 7))
+    return MLAWorkload(f"mla_T{T}", rows, pos, w, page, offset, num_pages, page_size)
+
+
+def random_pool_bits(shape, seed, device="cpu"):
+    """A pool pre-filled with random bits (int16 view of bf16 storage)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    bits = torch.randint(-32768, 32768, tuple(shape), generator=g, dtype=torch.int16, device=device)
+    return bits.view(torch.bfloat16)
+
+
+def bits_u16(t):
+    """The raw bits of a bf16 tensor as a NumPy uint16 array (CPU copy)."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")

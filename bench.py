@@ -1,0 +1,498 @@
+#!/usr/bin/env python
+"""Benchmark of the packed-QKV prologue on GB300.
+
+Default workload (the headline): training forward + backward at T = 16384
+tokens of the Muse Spark packing [T, 16 KV groups, 8 q + 1 k + 1 v, 64] (bf16,
+interleaved), RoPE base 5e5, eps 1e-6. One step = qkv_prologue_fwd with the
+pre-norm save + qkv_prologue_bwd (packed gradient and fp32 weight grads), the
+whole hot path on one batch. Inputs are resident in HBM and larger than L2
+(1.95 GB of algorithmic traffic per step), so no L2 flush is needed between
+steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). Under torchrun each rank runs the same
+per-GPU workload (weak scaling, no collective on the data path); the step
+time is the max over ranks.
+
+Metric: achieved HBM GB/s = algorithmic bytes (every input read once, every
+output written once) / step time; also us per call.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (% of GB300 peak) and µs/call, qkv prologue fwd+bwd at T=16k"
+FALLBACK_HBM_GBS = 6800.0
+
+# Muse Spark packing
+N_Q, N_KV, D = 128, 16, 64
+ROW = (N_Q + 2 * N_KV) * D          # 10240 values per token
+BF = 2
+
+
+def fwd_bytes_per_token(save_pre):
+    read = ROW * BF + 4                                   # packed row + position
+    write = ROW * BF                                      # q, k, v
+    if save_pre:
+        write += (N_Q + N_KV) * D * BF                    # split pre-norm q, k
+    return read + write
+
+
+def bwd_bytes_per_token():
+    read = ROW * BF + (N_Q + N_KV) * D * BF + 4           # dq, dk, dv + q_pre, k_pre + position
+    write = ROW * BF                                      # packed gradient
+    return read + write
+
+
+WEIGHT_BYTES = 2 * D * 4                                  # w_q, w_k (fp32)
+
+
+# ------------------------------------------------------------ helpers ----
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_digest():
+    csrc = os.path.join(ROOT, "rope_qkv_prologue_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def traffic_from_profile(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    sources have not changed since it was taken; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            prof = json.load(f)
+    except Exception:
+        return None
+    if prof.get("sources_sha256") != kernel_sources_digest():
+        return None
+    ent = prof.get("kernels", {}).get(kernel_key)
+    return None if ent is None else ent.get("dram_bytes_per_launch_full_size")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in a thread."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and parts[0] != self.uuid:
+                continue
+            self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = "samples inside the timed region"
+        if not win and self.samples:
+            # the timed region was shorter than the sampling period: nearest samples
+            mid = (t0 + t1) / 2
+            win = [min(self.samples, key=lambda s: abs(s[0] - mid))[1]]
+            note = "timed region shorter than one sample: nearest sample"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "nvidia-smi unavailable"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        smax = [num(p[2]) for p in win if num(p[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in win:
+            for name, val in zip(names, p[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(win), "note": note}
+
+
+# ------------------------------------------------------- our workload ----
+
+class TrainStep:
+    """Device-resident buffers of the T=16384 training workload."""
+
+    def __init__(self, dev, T):
+        import torch
+
+        import rope_qkv_prologue_gb300 as C
+        import workloads
+
+        self.C, self.T, self.dev = C, T, dev
+        wl = workloads.train(T)
+        self.wl = wl
+        self.L = C.layout("interleaved", N_Q, N_KV, D)
+        self.packed = wl.packed_rows().to(dev)
+        self.pos = wl.pos.to(dev)
+        self.w_q, self.w_k = wl.w_q.to(dev), wl.w_k.to(dev)
+        self.dq, self.dk, self.dv = wl.dq.to(dev), wl.dk.to(dev), wl.dv.to(dev)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.q = torch.empty(T, N_Q, D, **bf)
+        self.k = torch.empty(T, N_KV, D, **bf)
+        self.v = torch.empty(T, N_KV, D, **bf)
+        self.q_pre = torch.empty(T, N_Q, D, **bf)
+        self.k_pre = torch.empty(T, N_KV, D, **bf)
+        self.dpacked = torch.empty(T, ROW, **bf)
+        self.dw_q = torch.empty(D, dtype=torch.float32, device=dev)
+        self.dw_k = torch.empty(D, dtype=torch.float32, device=dev)
+        self.ws_bytes = C.qkv_prologue_bwd_workspace_size(self.L, T)
+        self.ws = torch.empty(max(16, self.ws_bytes), dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream(dev).cuda_stream
+        self.eps, self.base = wl.eps, wl.rope_base
+
+    def fwd(self):
+        self.C.qkv_prologue_fwd(self.L, self.T, self.packed, self.pos, self.w_q, self.w_k, self.eps, self.base,
+                                self.C.QKVP_SAVE_PRE, self.q, self.k, self.v, self.q_pre, self.k_pre, self.stream)
+
+    def bwd(self):
+        self.C.qkv_prologue_bwd(self.L, self.T, self.dq, self.dk, self.dv, self.q_pre, self.k_pre, self.pos,
+                                self.w_q, self.w_k, self.eps, self.base, 0, self.dpacked, self.dw_q, self.dw_k,
+                                self.ws, self.ws_bytes, self.stream)
+
+    def step(self):
+        self.fwd()
+        self.bwd()
+
+    def fwd_bytes(self):
+        return self.T * fwd_bytes_per_token(True) + WEIGHT_BYTES
+
+    def bwd_bytes(self):
+        return self.T * bwd_bytes_per_token() + 2 * WEIGHT_BYTES
+
+    def host_mirrors(self):
+        """Pinned host copies of the inputs and room for the outputs (e2e)."""
+        import torch
+
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)  # noqa: E731
+        self.h_in = {"packed": self.wl.packed_rows(), "pos": self.wl.pos, "w_q": self.wl.w_q, "w_k": self.wl.w_k,
+                     "dq": self.wl.dq, "dk": self.wl.dk, "dv": self.wl.dv}
+        self.h_in = {k: pin(v).copy_(v) for k, v in self.h_in.items()}
+        self.h_out = {k: pin(getattr(self, k)) for k in ("q", "k", "v", "dpacked", "dw_q", "dw_k")}
+        h2d = sum(t.numel() * t.element_size() for t in self.h_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in self.h_out.values())
+        return h2d, d2h
+
+    def e2e_step(self):
+        for k, h in self.h_in.items():
+            getattr(self, k).copy_(h, non_blocking=True)
+        self.step()
+        for k, h in self.h_out.items():
+            h.copy_(getattr(self, k), non_blocking=True)
+
+
+# ------------------------------------------------------------- arms ----
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    from rope_qkv_prologue_gb300 import _build
+
+    if rank == 0 or world == 1:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+
+    T = 16384
+    ws = TrainStep(dev, T)
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    uuid = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else (str(uuid) if uuid else None)
+    sampler = ClockSampler(uuid)
+    sampler.start()
+
+    for _ in range(args.warmup):
+        ws.step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record()
+    for i in range(K):
+        ev[i][0].record()
+        ws.fwd()
+        ev[i][1].record()
+        ws.bwd()
+        ev[i][2].record()
+    end.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    fwd_ms = statistics.fmean(a.elapsed_time(b) for a, b, _ in ev)
+    bwd_ms = statistics.fmean(b.elapsed_time(c) for _, b, c in ev)
+    time.sleep(0.25)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    # e2e: host buffers in, C-ABI calls, results back to host, every step
+    h2d, d2h = ws.host_mirrors()
+    e2e_steps = max(3, min(K, args.e2e_steps))
+    ws.e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        ws.e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
+
+    step_bytes = ws.fwd_bytes() + ws.bwd_bytes()
+    ms_per_step = elapsed_ms / K
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    fwd_gbs = ws.fwd_bytes() / (fwd_ms * 1e-3) / 1e9
+    bwd_gbs = ws.bwd_bytes() / (bwd_ms * 1e-3) / 1e9
+    if bwd_ms >= fwd_ms:
+        dom, dom_bytes, dom_ms, dom_key = "qkv_prologue_bwd (qkvp_bwd_kernel + dw finalize)", ws.bwd_bytes(), bwd_ms, "bwd"
+    else:
+        dom, dom_bytes, dom_ms, dom_key = "qkv_prologue_fwd (qkvp_fwd_kernel, save_pre)", ws.fwd_bytes(), fwd_ms, "fwd"
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "us_per_call": round(ms_per_step * 1e3, 2),
+        "pct_of_peak": round(100.0 * value / world / peak, 1),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 packed rows and upstream grads, U(0.5,1.5) norm weights)",
+        "config": {
+            "workload": "train fwd+bwd, T=16384, packed [T,16,10,64] interleaved, RoPE base 5e5, eps 1e-6, "
+                        "forward saves split pre-norm q/k",
+            "T": T, "n_q": N_Q, "n_kv": N_KV, "head_dim": D, "layout": "interleaved",
+            "bytes_per_step": step_bytes,
+            "l2": "no flush: inputs larger than L2 (1.95 GB of traffic per step vs 129 MB L2)",
+            "parallelism": f"replicas x{world} (tokens independent; no collective)",
+        },
+        "kernels": {
+            "fwd_us": round(fwd_ms * 1e3, 2), "fwd_GBps": round(fwd_gbs, 1),
+            "bwd_us": round(bwd_ms * 1e3, 2), "bwd_GBps": round(bwd_gbs, 1),
+        },
+        "roofline": {
+            "kernel": dom,
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic_from_profile(dom_key),
+        },
+        "clocks": clocks,
+        "e2e": {
+            "value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1),
+            "unit": "GB/s",
+            "ms_per_step": round(e2e_ms, 4),
+            "steps": e2e_steps,
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "path": "pinned host -> device copies, qkv_prologue_fwd + qkv_prologue_bwd, device -> pinned host",
+        },
+        "gpu_launches": 3 * K,
+        "gpu_launches_note": "per step: qkvp_fwd_kernel, qkvp_bwd_kernel, qkvp_dw_finalize_kernel",
+        "context": {
+            "pages_glue_us_train16k_two_layers_gb300": 824,
+            "pages_q_norm_kernel_us_train16k": 114,
+        },
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.cpu_tokens)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+class OracleSample:
+    """The fp64 oracle's forward + backward on the first n tokens of the
+    T=16384 training workload (inputs drawn once; only the oracle is timed)."""
+
+    def __init__(self, n_tokens, chunk=512):
+        import oracle.prologue as P
+        import workloads
+        from workloads import bits_u16 as u16
+
+        self.P, self.n, self.chunk = P, n_tokens, chunk
+        wl = workloads.train(16384)
+        self.wl = wl
+        self.L = P.PackedLayout("interleaved", N_Q, N_KV, D)
+        self.rows = u16(wl.packed_rows()[:n_tokens])
+        self.dq, self.dk, self.dv = u16(wl.dq[:n_tokens]), u16(wl.dk[:n_tokens]), u16(wl.dv[:n_tokens])
+        self.pos, self.wq, self.wk = wl.pos.numpy()[:n_tokens], wl.w_q.numpy(), wl.w_k.numpy()
+
+    def run(self):
+        """One pass; returns seconds spent in the oracle."""
+        P, wl = self.P, self.wl
+        t0 = time.perf_counter()
+        for s in range(0, self.n, self.chunk):
+            sl = slice(s, min(self.n, s + self.chunk))
+            o = P.prologue_fwd(self.L, self.rows[sl], self.pos[sl], self.wq, self.wk, wl.eps, wl.rope_base)
+            P.prologue_bwd(self.L, self.dq[sl], self.dk[sl], self.dv[sl], o["q_pre_bits"], o["k_pre_bits"],
+                           self.pos[sl], self.wq, self.wk, wl.eps, wl.rope_base)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(n_tokens):
+    secs = OracleSample(n_tokens).run()
+    bytes_ = n_tokens * (fwd_bytes_per_token(True) + bwd_bytes_per_token())
+    return {
+        "value": round(bytes_ / secs / 1e9, 5),
+        "unit": "GB/s",
+        "cores": 1,
+        "host_cores_available": len(os.sched_getaffinity(0)),
+        "kind": "oracle",
+        "sample": f"fp64 NumPy oracle forward+backward on the first {n_tokens} tokens of the T=16384 training "
+                  f"workload (chunks of 512 tokens), {secs:.1f} s; NumPy element-wise code runs on one thread",
+        "seconds": round(secs, 2),
+    }
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    K, W = args.steps, args.warmup
+    per_token_s = 0.0025
+    n = int(max(1, min(512, 120.0 / max(1, K + W) / per_token_s)))
+    sample = OracleSample(n)
+    for _ in range(W):
+        sample.run()
+    secs = [sample.run() for _ in range(K)]
+    step_s = statistics.fmean(secs)
+    bytes_ = n * (fwd_bytes_per_token(True) + bwd_bytes_per_token())
+    value = bytes_ / step_s / 1e9
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 5),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(step_s * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (same seeded workload as the CUDA arm)",
+        "config": {"workload": "train fwd+bwd, T=16384, packed [T,16,10,64] interleaved, RoPE base 5e5, eps 1e-6",
+                   "sample_tokens_per_step": n},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1,
+                         "host_cores_available": len(os.sched_getaffinity(0)), "kind": "oracle",
+                         "sample": f"fp64 NumPy oracle forward+backward on the first {n} tokens per step"},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-tokens", type=int, default=6144)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

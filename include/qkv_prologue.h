@@ -1,0 +1,224 @@
+/*
+ * qkv_prologue.h -- C ABI of the packed-QKV attention prologue for GB300 (sm_103a).
+ *
+ * The operation (sources: three pull-request pages; each entry point below
+ * names the page and section that define it):
+ *
+ *   forward   packed projection row of one token
+ *               -> split into heads (interleaved per KV group, or sectioned)
+ *               -> per-head RMSNorm of q and k:  y = x / sqrt(mean(x^2) + eps) * w
+ *               -> rotate-half RoPE of q and k (skipped on NoPE layers)
+ *               -> contiguous q, k, v   (v is a bit copy)
+ *                  or q contiguous + k, v written into a paged KV pool
+ *   backward  gradients of q, k, v -> gradient of the packed row, written
+ *             once in the packed layout, plus the two RMSNorm weight grads.
+ *
+ * RoPE convention: for i < D/2, inv_freq_i = rope_base^(-2 i / D),
+ * theta = pos * inv_freq_i, and
+ *     o_i       = y_i cos(theta) - y_{i+D/2} sin(theta)
+ *     o_{i+D/2} = y_{i+D/2} cos(theta) + y_i sin(theta).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer except `layout` and `workspace_bytes`-style scalars is a
+ *    DEVICE pointer. The caller owns every buffer; the library allocates no
+ *    memory and never synchronises. Work is enqueued asynchronously on
+ *    `stream` (a cudaStream_t; NULL = the legacy default stream) on the
+ *    current CUDA device.
+ *  - bf16 tensors are passed as `void*` (IEEE bfloat16 bit patterns),
+ *    row-major, and must start on a 16-byte boundary. `row_stride` (in
+ *    elements) must be a multiple of 8. Index tensors are int32, weights and
+ *    weight gradients float32, 16-byte aligned.
+ *  - Arguments are checked on the host before anything touches the device.
+ *    On error nothing is enqueued and a negative qkvp_status is returned.
+ *  - T == 0 is valid and enqueues nothing.
+ *  - Outputs must not overlap inputs (results are undefined if they do).
+ *  - Results are deterministic: the same inputs on the same device give the
+ *    same bits, including the weight gradients (no float atomics).
+ */
+#ifndef QKV_PROLOGUE_H_
+#define QKV_PROLOGUE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QKVP_API __attribute__((visibility("default")))
+#else
+#define QKVP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QKVP_VERSION 1
+
+/* Status codes (return values). */
+typedef enum {
+  QKVP_OK = 0,
+  QKVP_ERR_NULL = -1,      /* a required pointer is NULL                       */
+  QKVP_ERR_SHAPE = -2,     /* bad T / head counts / head_dim / row_stride       */
+  QKVP_ERR_ALIGN = -3,     /* a tensor is not 16-byte aligned                   */
+  QKVP_ERR_ARCH = -4,      /* no CUDA device, or the device is not sm_103       */
+  QKVP_ERR_WORKSPACE = -5, /* backward workspace smaller than required          */
+  QKVP_ERR_LAUNCH = -6,    /* the CUDA runtime reported an error at launch      */
+  QKVP_ERR_FLAGS = -7,     /* unknown or contradictory flag bits                */
+  QKVP_ERR_VALUE = -8      /* eps < 0, rope_base <= 0, non-finite, pool sizes   */
+} qkvp_status;
+
+/* Packed layouts.
+ *
+ * QKVP_INTERLEAVED: a row is [n_kv groups][G + 2 slots][head_dim] with
+ *   G = n_q / n_kv: slots 0..G-1 of group g are q heads g*G .. g*G+G-1, slot G
+ *   is k head g, slot G+1 is v head g ("[muse_spark][perf] Split the packed
+ *   qkv inside the q/k region", Problem 1: [T, 16 kv heads, 10, 64]).
+ * QKVP_SECTIONED: a row is [n_q q heads | n_kv k heads | n_kv v heads], each
+ *   head_dim wide ("[muon] Per-head Newton-Schulz for fused QKV projections",
+ *   What this PR does).
+ * Both hold exactly (n_q + 2 n_kv) * head_dim values per row, at row_stride.
+ *
+ * QKVP_LATENT: an MLA kv latent row of norm_dim + rope_dim values: the first
+ *   norm_dim are RMSNorm-ed with one weight, the last rope_dim are rotated by
+ *   rotate-half RoPE with no norm and no weight ("MLA DSpark: run each drafter
+ *   layer's kv path beside its q path", Description). n_q, n_kv, head_dim are
+ *   ignored; norm_dim must be a multiple of 8 and at most 1024, rope_dim 64.
+ */
+typedef enum { QKVP_INTERLEAVED = 0, QKVP_SECTIONED = 1, QKVP_LATENT = 2 } qkvp_layout_kind;
+
+typedef struct {
+  int32_t kind;       /* qkvp_layout_kind                                     */
+  int32_t n_q;        /* query heads; a positive multiple of n_kv              */
+  int32_t n_kv;       /* key/value heads (KV groups)                           */
+  int32_t head_dim;   /* 64 or 128                                             */
+  int64_t row_stride; /* elements between consecutive tokens' rows; 0 = dense  */
+  int32_t norm_dim;   /* LATENT only (512 for the DSpark drafter)              */
+  int32_t rope_dim;   /* LATENT only (64)                                      */
+} qkvp_layout;
+
+/* Flags. */
+enum {
+  QKVP_NOPE = 1,           /* NoPE layer: RMSNorm only, no rotation            */
+  QKVP_SAVE_PRE = 2,       /* forward also writes the split pre-norm q and k   */
+  QKVP_ACCUMULATE_DW = 4   /* backward adds into dw_q / dw_k instead of writing */
+};
+
+/* Device-side status bits (pool writes): set with an atomic OR in
+ * *dev_status when a token's page or offset is out of range; that token's
+ * pool store is skipped, nothing traps. */
+enum { QKVP_DEV_BAD_PAGE = 1, QKVP_DEV_BAD_OFFSET = 2 };
+
+/* ---------------------------------------------------------------------------
+ * qkv_prologue_fwd -- split + per-head RMSNorm + RoPE, contiguous outputs.
+ *
+ * Defines: "[muse_spark][perf] Split the packed qkv inside the q/k region",
+ * Solution 1-3 and the after-diagram (split -> norm -> RoPE, copy v), and the
+ * training note on the q norm kernel (it also writes the split q).
+ *
+ * layout      host pointer. INTERLEAVED or SECTIONED (GQA), or LATENT.
+ * T           tokens (>= 0).
+ * packed      bf16 [T, row_stride] (GQA) or [T, row_stride] latent rows.
+ * pos         int32 [T] positions (any int32; ignored with QKVP_NOPE).
+ * w_q, w_k    float32 [head_dim] RMSNorm weights of q and k heads. LATENT:
+ *             w_k is the float32 [norm_dim] latent weight, w_q is ignored.
+ * eps         RMSNorm epsilon (>= 0, added inside the square root).
+ * rope_base   RoPE base (> 0).
+ * flags       QKVP_NOPE | QKVP_SAVE_PRE (SAVE_PRE: GQA only).
+ * q           bf16 [T, n_q, head_dim] out.           LATENT: ignored.
+ * k           bf16 [T, n_kv, head_dim] out.          LATENT: [T, norm_dim+rope_dim] out.
+ * v           bf16 [T, n_kv, head_dim] out (copy).   LATENT: ignored.
+ * q_pre,k_pre bf16 [T, n_q | n_kv, head_dim] out, only with QKVP_SAVE_PRE
+ *             (bit copies of the input heads, for the backward).
+ * ------------------------------------------------------------------------- */
+QKVP_API int qkv_prologue_fwd(const qkvp_layout* layout, int64_t T, const void* packed,
+                     const int32_t* pos, const float* w_q, const float* w_k, float eps,
+                     double rope_base, uint32_t flags, void* q, void* k, void* v,
+                     void* q_pre, void* k_pre, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * qkv_prologue_pool_write -- the forward with a paged-pool destination.
+ *
+ * Defines: "MLA DSpark: run each drafter layer's kv path beside its q path",
+ * Description (the norm/RoPE kernel stores rows straight into the pool at
+ * the given pages / offsets, with no staging buffer and no scatter) and Test
+ * Coverage (the direct write equals the staged path + scatter, bit for bit:
+ * qkv_prologue_fwd followed by qkv_prologue_pool_scatter).
+ *
+ * GQA layouts: q is written contiguous [T, n_q, head_dim]; the normed (+roped)
+ *   k heads of token t go to k_pool[page[t], offset[t]] and its raw v heads to
+ *   v_pool[page[t], offset[t]]; pools are bf16 [num_pages, page_size, n_kv,
+ *   head_dim].
+ * LATENT: the normed/roped row of token t goes to k_pool[page[t], offset[t]]
+ *   of a bf16 [num_pages, page_size, norm_dim + rope_dim] pool; q, v_pool and
+ *   w_q are ignored (may be NULL).
+ * page, offset  int32 [T]. A token whose page is outside [0, num_pages) or
+ *   offset outside [0, page_size) is not stored; the matching QKVP_DEV_* bit
+ *   is OR-ed into *dev_status when dev_status (int32, device) is not NULL.
+ * Two tokens naming the same slot race; the caller must not do that.
+ * flags: QKVP_NOPE only.
+ * ------------------------------------------------------------------------- */
+QKVP_API int qkv_prologue_pool_write(const qkvp_layout* layout, int64_t T, const void* packed,
+                            const int32_t* pos, const float* w_q, const float* w_k, float eps,
+                            double rope_base, uint32_t flags, void* q, const int32_t* page,
+                            const int32_t* offset, void* k_pool, void* v_pool,
+                            int32_t num_pages, int32_t page_size, int32_t* dev_status,
+                            void* stream);
+
+/* ---------------------------------------------------------------------------
+ * qkv_prologue_pool_scatter -- the staged write's scatter step.
+ *
+ * Defines the "staged scatter write" that "MLA DSpark: run each drafter
+ * layer's kv path beside its q path" (Test Coverage) compares the direct pool
+ * write against. Copies contiguous rows into pool slots, bit for bit:
+ * GQA: k_rows, v_rows bf16 [T, n_kv, head_dim] -> k_pool, v_pool slots.
+ * LATENT: k_rows bf16 [T, norm_dim + rope_dim] -> k_pool slots (v ignored).
+ * Index checks and dev_status as for qkv_prologue_pool_write.
+ * ------------------------------------------------------------------------- */
+QKVP_API int qkv_prologue_pool_scatter(const qkvp_layout* layout, int64_t T, const void* k_rows,
+                              const void* v_rows, const int32_t* page, const int32_t* offset,
+                              void* k_pool, void* v_pool, int32_t num_pages, int32_t page_size,
+                              int32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * qkv_prologue_bwd_workspace_size -- bytes of device workspace that
+ * qkv_prologue_bwd needs for this layout and T on the CURRENT device
+ * (0 when T == 0; returns 0 for an invalid layout).
+ * ------------------------------------------------------------------------- */
+QKVP_API size_t qkv_prologue_bwd_workspace_size(const qkvp_layout* layout, int64_t T);
+
+/* ---------------------------------------------------------------------------
+ * qkv_prologue_bwd -- one-pass backward writing the packed gradient.
+ *
+ * Defines: "[muse_spark][perf] Split the packed qkv inside the q/k region",
+ * TLDR and Solution 3 (the norm-backward kernels write the packed grad; no
+ * cat) and Results / Numerics (weight grads unchanged by the fusion).
+ *
+ * dq      bf16 [T, n_q, head_dim]   gradient of the forward's q output.
+ * dk, dv  bf16 [T, n_kv, head_dim]  gradients of k and v.
+ * q_pre, k_pre  bf16 split pre-norm heads saved by the forward (QKVP_SAVE_PRE).
+ * pos, w_q, w_k, eps, rope_base, flags(QKVP_NOPE) as in the forward.
+ * dpacked bf16 [T, row_stride] out, in the layout's packing: q/k slots get
+ *         the RMSNorm+RoPE input gradient, v slots get dv unchanged.
+ * dw_q, dw_k  float32 [head_dim] out: sum over tokens and heads of the weight
+ *         gradient. Overwritten, or added to with QKVP_ACCUMULATE_DW.
+ * workspace   device scratch of at least qkv_prologue_bwd_workspace_size
+ *         bytes (any contents; 16-byte aligned); QKVP_ERR_WORKSPACE if smaller.
+ * GQA layouts only.
+ * ------------------------------------------------------------------------- */
+QKVP_API int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const void* dk,
+                     const void* dv, const void* q_pre, const void* k_pre, const int32_t* pos,
+                     const float* w_q, const float* w_k, float eps, double rope_base,
+                     uint32_t flags, void* dpacked, float* dw_q, float* dw_k, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/* Static, human-readable text for a qkvp_status value. */
+QKVP_API const char* qkv_prologue_status_string(int status);
+
+/* QKVP_VERSION of the compiled library. */
+QKVP_API int qkv_prologue_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QKV_PROLOGUE_H_ */

@@ -1,0 +1,493 @@
+// Host side of the C ABI: argument checks, RoPE frequency tables, launch
+// geometry and dispatch to the kernels. Nothing here allocates device memory
+// or synchronises; every launch goes to the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "launch.h"
+#include "qkv_prologue.h"
+
+namespace qkvp {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxHeadsTimesChunks = 32768;  // keeps in-item chunk indices below 2^16
+
+// ------------------------------------------------------------ device ----
+
+struct DeviceInfo {
+  bool probed = false;
+  int status = QKVP_OK;
+  int sms = 0;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+// The current device, checked once per device: it must be sm_103 (the only
+// architecture the library is compiled for).
+int current_device(int* sms) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return QKVP_ERR_ARCH;
+  }
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0, sms_ = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms_, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return QKVP_ERR_ARCH;
+    }
+    d.status = (major == 10 && minor == 3) ? QKVP_OK : QKVP_ERR_ARCH;
+    d.sms = sms_;
+    d.probed = true;
+  }
+  *sms = d.sms;
+  return d.status;
+}
+
+int blocks_per_sm(const void* kernel, int threads, size_t smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  return n > 0 ? n : 1;
+}
+
+int launch(const void* kernel, int64_t grid, int threads, size_t smem, cudaStream_t s, void* arg) {
+  void* args[] = {arg};
+  cudaError_t err = cudaLaunchKernel(kernel, dim3((unsigned)grid), dim3(threads), args, smem, s);
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return err == cudaErrorNoKernelImageForDevice || err == cudaErrorInvalidDeviceFunction
+               ? QKVP_ERR_ARCH
+               : QKVP_ERR_LAUNCH;
+  }
+  return QKVP_OK;
+}
+
+// -------------------------------------------------------------- RoPE ----
+
+// turns_i = frac(inv_freq_i / 2pi) * 2^64 with inv_freq_i = base^(-2i/D):
+// the angle per unit position as a 0.64 fixed-point fraction of one turn.
+// The kernels multiply it by the position modulo 2^64, which reduces the
+// angle exactly. Double precision leaves < 2^-56 turn of error per unit
+// position (about 2^-37 turn at position 2^19).
+void rope_table(double base, int head_dim, RopeTable* out) {
+  static thread_local double last_base = -1.0;
+  static thread_local int last_dim = 0;
+  static thread_local RopeTable last;
+  if (base != last_base || head_dim != last_dim) {
+    const double two_pi = 6.283185307179586476925286766559;
+    std::memset(&last, 0, sizeof(last));
+    for (int i = 0; i < head_dim / 2; ++i) {
+      const double inv_freq = std::pow(base, -2.0 * i / head_dim);
+      const double frac = std::fmod(inv_freq / two_pi, 1.0);
+      const double scaled = std::ldexp(frac, 64);
+      last.turns[i] = scaled >= 18446744073709551616.0 ? 0 : (uint64_t)scaled;
+    }
+    last_base = base;
+    last_dim = head_dim;
+  }
+  *out = last;
+}
+
+// ------------------------------------------------------------ checks ----
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+struct Gqa {
+  int heads = 0;          // n_q + 2 n_kv
+  int64_t row = 0;        // elements per row (heads * head_dim)
+  int64_t stride = 0;     // row stride in elements
+};
+
+int check_gqa(const qkvp_layout* L, int64_t T, Gqa* g) {
+  if (!L) return QKVP_ERR_NULL;
+  if (L->kind != QKVP_INTERLEAVED && L->kind != QKVP_SECTIONED) return QKVP_ERR_SHAPE;
+  if (T < 0 || L->n_q <= 0 || L->n_kv <= 0 || L->n_q % L->n_kv != 0) return QKVP_ERR_SHAPE;
+  if (L->head_dim != 64 && L->head_dim != 128) return QKVP_ERR_SHAPE;
+  const int64_t heads = (int64_t)L->n_q + 2 * (int64_t)L->n_kv;
+  if (heads * (L->head_dim / 8) > kMaxHeadsTimesChunks) return QKVP_ERR_SHAPE;
+  g->heads = (int)heads;
+  g->row = heads * L->head_dim;
+  g->stride = L->row_stride == 0 ? g->row : L->row_stride;
+  if (g->stride < g->row || g->stride % 8 != 0) return QKVP_ERR_SHAPE;
+  return QKVP_OK;
+}
+
+struct Latent {
+  int64_t row = 0;
+  int64_t stride = 0;
+};
+
+int check_latent(const qkvp_layout* L, int64_t T, Latent* g) {
+  if (!L) return QKVP_ERR_NULL;
+  if (L->kind != QKVP_LATENT || T < 0) return QKVP_ERR_SHAPE;
+  if (L->norm_dim < 8 || L->norm_dim > 1024 || L->norm_dim % 8 != 0 || L->rope_dim != 64)
+    return QKVP_ERR_SHAPE;
+  g->row = (int64_t)L->norm_dim + L->rope_dim;
+  g->stride = L->row_stride == 0 ? g->row : L->row_stride;
+  if (g->stride < g->row || g->stride % 8 != 0) return QKVP_ERR_SHAPE;
+  return QKVP_OK;
+}
+
+int check_scalars(float eps, double rope_base, bool rope) {
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return QKVP_ERR_VALUE;
+  if (rope && (!(rope_base > 0.0) || !std::isfinite(rope_base))) return QKVP_ERR_VALUE;
+  return QKVP_OK;
+}
+
+int check_pool(int32_t num_pages, int32_t page_size) {
+  if (num_pages <= 0 || page_size <= 0) return QKVP_ERR_VALUE;
+  if ((int64_t)num_pages * page_size > INT32_MAX) return QKVP_ERR_VALUE;
+  return QKVP_OK;
+}
+
+uint32_t magic(uint32_t d) { return (uint32_t)((1ull << 32) / d + 1); }
+
+// Work items of the GQA kernels: `chunks_per_thread * kThreads` consecutive
+// (token, chunk) pairs.
+void gqa_items(int64_t T, int cpt, int chunks_per_thread, int64_t* item_chunks, int64_t* n_items,
+               int* max_tok) {
+  const int64_t L = (int64_t)chunks_per_thread * kThreads;
+  *item_chunks = L;
+  *n_items = (T * cpt + L - 1) / L;
+  *max_tok = (int)((cpt + L - 2) / cpt + 1);
+}
+
+int64_t bwd_parts(int64_t n_items) { return n_items < kMaxBwdParts ? n_items : kMaxBwdParts; }
+
+#define QKVP_TRY(expr)          \
+  do {                          \
+    const int _st = (expr);     \
+    if (_st != QKVP_OK) return _st; \
+  } while (0)
+
+}  // namespace
+}  // namespace qkvp
+
+using namespace qkvp;
+
+extern "C" {
+
+int qkv_prologue_version(void) { return QKVP_VERSION; }
+
+const char* qkv_prologue_status_string(int status) {
+  switch (status) {
+    case QKVP_OK: return "ok";
+    case QKVP_ERR_NULL: return "a required pointer is NULL";
+    case QKVP_ERR_SHAPE: return "invalid shape (T, head counts, head_dim, row_stride or layout kind)";
+    case QKVP_ERR_ALIGN: return "a tensor is not 16-byte aligned (index tensors: 4-byte)";
+    case QKVP_ERR_ARCH: return "no usable CUDA device, or the device is not sm_103";
+    case QKVP_ERR_WORKSPACE: return "backward workspace smaller than qkv_prologue_bwd_workspace_size";
+    case QKVP_ERR_LAUNCH: return "CUDA launch failed";
+    case QKVP_ERR_FLAGS: return "unknown or unsupported flag bits for this call";
+    case QKVP_ERR_VALUE: return "invalid scalar (eps, rope_base, num_pages or page_size)";
+    default: return "unknown status";
+  }
+}
+
+// ------------------------------------------------------------- forward ----
+
+static int gqa_forward(const qkvp_layout* L, int64_t T, const void* packed, const int32_t* pos,
+                       const float* w_q, const float* w_k, float eps, double rope_base,
+                       uint32_t flags, void* q, void* k, void* v, void* q_pre, void* k_pre,
+                       const int32_t* page, const int32_t* offset, void* k_pool, void* v_pool,
+                       int32_t num_pages, int32_t page_size, int32_t* dev_status, bool pool,
+                       cudaStream_t stream) {
+  Gqa g;
+  QKVP_TRY(check_gqa(L, T, &g));
+  const uint32_t allowed = pool ? (uint32_t)QKVP_NOPE : (uint32_t)(QKVP_NOPE | QKVP_SAVE_PRE);
+  if (flags & ~allowed) return QKVP_ERR_FLAGS;
+  const bool rope = !(flags & QKVP_NOPE);
+  const bool save = (flags & QKVP_SAVE_PRE) != 0;
+  QKVP_TRY(check_scalars(eps, rope_base, rope));
+  if (!packed || !w_q || !w_k || !q || (rope && !pos)) return QKVP_ERR_NULL;
+  if (pool) {
+    if (!page || !offset || !k_pool || !v_pool) return QKVP_ERR_NULL;
+    QKVP_TRY(check_pool(num_pages, page_size));
+  } else {
+    if (!k || !v) return QKVP_ERR_NULL;
+    if (save && (!q_pre || !k_pre)) return QKVP_ERR_NULL;
+  }
+  const void* vec[] = {packed, w_q, w_k, q, pool ? k_pool : k, pool ? v_pool : v,
+                       save ? q_pre : nullptr, save ? k_pre : nullptr};
+  for (const void* p : vec)
+    if (p && !aligned16(p)) return QKVP_ERR_ALIGN;
+  if ((pos && !aligned4(pos)) || (page && !aligned4(page)) || (offset && !aligned4(offset)) ||
+      (dev_status && !aligned4(dev_status)))
+    return QKVP_ERR_ALIGN;
+  if (T == 0) return QKVP_OK;
+
+  int sms = 0;
+  QKVP_TRY(current_device(&sms));
+  FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.packed = static_cast<const uint4*>(packed);
+  a.row_stride16 = g.stride / 8;
+  a.pos = pos;
+  a.w_q = w_q;
+  a.w_k = w_k;
+  a.eps = eps;
+  a.inv_head_dim = 1.0f / (float)L->head_dim;
+  a.T = T;
+  a.n_q = L->n_q;
+  a.n_kv = L->n_kv;
+  a.group = L->n_q / L->n_kv;
+  a.cpt = g.heads * (L->head_dim / 8);
+  a.cpt_magic = magic((uint32_t)a.cpt);
+  a.gs_magic = magic((uint32_t)(a.group + 2));
+  gqa_items(T, a.cpt, kFwdChunksPerThread, &a.item_chunks, &a.n_items, &a.max_tok);
+  a.q = static_cast<uint4*>(q);
+  a.k = static_cast<uint4*>(k);
+  a.v = static_cast<uint4*>(v);
+  a.q_pre = static_cast<uint4*>(q_pre);
+  a.k_pre = static_cast<uint4*>(k_pre);
+  a.page = page;
+  a.offset = offset;
+  a.k_pool = static_cast<uint4*>(k_pool);
+  a.v_pool = static_cast<uint4*>(v_pool);
+  a.num_pages = num_pages;
+  a.page_size = page_size;
+  a.dev_status = dev_status;
+  if (rope) rope_table(rope_base, L->head_dim, &a.rope);
+
+  const FwdVariant var{L->head_dim, L->kind == QKVP_SECTIONED, rope, save, pool};
+  const void* kern = L->head_dim == 64 ? fwd_kernel_d64(var) : fwd_kernel_d128(var);
+  const size_t smem = (size_t)a.max_tok * (L->head_dim / 2) * 2 * sizeof(float) +
+                      (size_t)a.max_tok * sizeof(int32_t);
+  const int64_t cap = (int64_t)sms * blocks_per_sm(kern, kThreads, smem);
+  const int64_t grid = a.n_items < cap ? a.n_items : cap;
+  return launch(kern, grid, kThreads, smem, stream, &a);
+}
+
+static int latent_forward(const qkvp_layout* L, int64_t T, const void* rows, const int32_t* pos,
+                          const float* w, float eps, double rope_base, uint32_t flags, void* out,
+                          const int32_t* page, const int32_t* offset, void* pool,
+                          int32_t num_pages, int32_t page_size, int32_t* dev_status,
+                          bool to_pool, cudaStream_t stream) {
+  Latent g;
+  QKVP_TRY(check_latent(L, T, &g));
+  if (flags & ~(uint32_t)QKVP_NOPE) return QKVP_ERR_FLAGS;
+  const bool rope = !(flags & QKVP_NOPE);
+  QKVP_TRY(check_scalars(eps, rope_base, rope));
+  if (!rows || !w || (rope && !pos)) return QKVP_ERR_NULL;
+  if (to_pool) {
+    if (!page || !offset || !pool) return QKVP_ERR_NULL;
+    QKVP_TRY(check_pool(num_pages, page_size));
+  } else if (!out) {
+    return QKVP_ERR_NULL;
+  }
+  if (!aligned16(rows) || !aligned16(w) || (out && !aligned16(out)) || (pool && !aligned16(pool)))
+    return QKVP_ERR_ALIGN;
+  if ((pos && !aligned4(pos)) || (page && !aligned4(page)) || (offset && !aligned4(offset)) ||
+      (dev_status && !aligned4(dev_status)))
+    return QKVP_ERR_ALIGN;
+  if (T == 0) return QKVP_OK;
+
+  int sms = 0;
+  QKVP_TRY(current_device(&sms));
+  LatentArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.rows = static_cast<const uint4*>(rows);
+  a.row_stride16 = g.stride / 8;
+  a.pos = pos;
+  a.w = w;
+  a.eps = eps;
+  a.inv_norm_dim = 1.0f / (float)L->norm_dim;
+  a.T = T;
+  a.norm_chunks = L->norm_dim / 8;
+  a.row_chunks = (int32_t)(g.row / 8);
+  a.out = static_cast<uint4*>(out);
+  a.page = page;
+  a.offset = offset;
+  a.pool = static_cast<uint4*>(pool);
+  a.num_pages = num_pages;
+  a.page_size = page_size;
+  a.dev_status = dev_status;
+  if (rope) rope_table(rope_base, L->rope_dim, &a.rope);
+  const int ncl = a.norm_chunks <= 32 ? 1 : (a.norm_chunks <= 64 ? 2 : 4);
+  const void* kern = latent_kernel(to_pool, rope, ncl);
+  const int threads = kLatentWarps * 32;
+  const int64_t per_cta = (int64_t)kLatentWarps * kLatentTokensPerWarp;
+  const int64_t need = (T + per_cta - 1) / per_cta;
+  const int64_t cap = (int64_t)sms * blocks_per_sm(kern, threads, 0);
+  return launch(kern, need < cap ? need : cap, threads, 0, stream, &a);
+}
+
+int qkv_prologue_fwd(const qkvp_layout* layout, int64_t T, const void* packed, const int32_t* pos,
+                     const float* w_q, const float* w_k, float eps, double rope_base,
+                     uint32_t flags, void* q, void* k, void* v, void* q_pre, void* k_pre,
+                     void* stream) {
+  if (!layout) return QKVP_ERR_NULL;
+  if (layout->kind == QKVP_LATENT)
+    return latent_forward(layout, T, packed, pos, w_k, eps, rope_base, flags, k, nullptr, nullptr,
+                          nullptr, 0, 0, nullptr, false, static_cast<cudaStream_t>(stream));
+  return gqa_forward(layout, T, packed, pos, w_q, w_k, eps, rope_base, flags, q, k, v, q_pre,
+                     k_pre, nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, false,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int qkv_prologue_pool_write(const qkvp_layout* layout, int64_t T, const void* packed,
+                            const int32_t* pos, const float* w_q, const float* w_k, float eps,
+                            double rope_base, uint32_t flags, void* q, const int32_t* page,
+                            const int32_t* offset, void* k_pool, void* v_pool, int32_t num_pages,
+                            int32_t page_size, int32_t* dev_status, void* stream) {
+  if (!layout) return QKVP_ERR_NULL;
+  if (layout->kind == QKVP_LATENT)
+    return latent_forward(layout, T, packed, pos, w_k, eps, rope_base, flags, nullptr, page,
+                          offset, k_pool, num_pages, page_size, dev_status, true,
+                          static_cast<cudaStream_t>(stream));
+  return gqa_forward(layout, T, packed, pos, w_q, w_k, eps, rope_base, flags, q, nullptr, nullptr,
+                     nullptr, nullptr, page, offset, k_pool, v_pool, num_pages, page_size,
+                     dev_status, true, static_cast<cudaStream_t>(stream));
+}
+
+int qkv_prologue_pool_scatter(const qkvp_layout* layout, int64_t T, const void* k_rows,
+                              const void* v_rows, const int32_t* page, const int32_t* offset,
+                              void* k_pool, void* v_pool, int32_t num_pages, int32_t page_size,
+                              int32_t* dev_status, void* stream) {
+  if (!layout) return QKVP_ERR_NULL;
+  int64_t row = 0;
+  const bool latent = layout->kind == QKVP_LATENT;
+  if (latent) {
+    Latent g;
+    QKVP_TRY(check_latent(layout, T, &g));
+    row = g.row;
+  } else {
+    Gqa g;
+    QKVP_TRY(check_gqa(layout, T, &g));
+    row = (int64_t)layout->n_kv * layout->head_dim;
+  }
+  if (!k_rows || !k_pool || !page || !offset) return QKVP_ERR_NULL;
+  if (!latent && (!v_rows || !v_pool)) return QKVP_ERR_NULL;
+  QKVP_TRY(check_pool(num_pages, page_size));
+  if (!aligned16(k_rows) || !aligned16(k_pool) || (!latent && (!aligned16(v_rows) || !aligned16(v_pool))))
+    return QKVP_ERR_ALIGN;
+  if (!aligned4(page) || !aligned4(offset) || (dev_status && !aligned4(dev_status)))
+    return QKVP_ERR_ALIGN;
+  if (T == 0) return QKVP_OK;
+  int sms = 0;
+  QKVP_TRY(current_device(&sms));
+  ScatterArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.src_a = static_cast<const uint4*>(k_rows);
+  a.src_b = latent ? nullptr : static_cast<const uint4*>(v_rows);
+  a.pool_a = static_cast<uint4*>(k_pool);
+  a.pool_b = latent ? nullptr : static_cast<uint4*>(v_pool);
+  a.T = T;
+  a.row_chunks = (int32_t)(row / 8);
+  a.page = page;
+  a.offset = offset;
+  a.num_pages = num_pages;
+  a.page_size = page_size;
+  a.dev_status = dev_status;
+  const void* kern = scatter_kernel();
+  const int64_t need = (T * a.row_chunks + 255) / 256;
+  const int64_t cap = (int64_t)sms * blocks_per_sm(kern, 256, 0);
+  return launch(kern, need < cap ? need : cap, 256, 0, static_cast<cudaStream_t>(stream), &a);
+}
+
+// ------------------------------------------------------------ backward ----
+
+size_t qkv_prologue_bwd_workspace_size(const qkvp_layout* layout, int64_t T) {
+  Gqa g;
+  if (check_gqa(layout, T, &g) != QKVP_OK || T == 0) return 0;
+  int64_t item_chunks = 0, n_items = 0;
+  int max_tok = 0;
+  gqa_items(T, g.heads * (layout->head_dim / 8), kBwdChunksPerThread, &item_chunks, &n_items,
+            &max_tok);
+  return (size_t)bwd_parts(n_items) * 2 * layout->head_dim * sizeof(float);
+}
+
+int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const void* dk,
+                     const void* dv, const void* q_pre, const void* k_pre, const int32_t* pos,
+                     const float* w_q, const float* w_k, float eps, double rope_base,
+                     uint32_t flags, void* dpacked, float* dw_q, float* dw_k, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  Gqa g;
+  QKVP_TRY(check_gqa(layout, T, &g));
+  if (flags & ~(uint32_t)(QKVP_NOPE | QKVP_ACCUMULATE_DW)) return QKVP_ERR_FLAGS;
+  const bool rope = !(flags & QKVP_NOPE);
+  const bool accumulate = (flags & QKVP_ACCUMULATE_DW) != 0;
+  QKVP_TRY(check_scalars(eps, rope_base, rope));
+  if (!dq || !dk || !dv || !q_pre || !k_pre || !w_q || !w_k || !dpacked || !dw_q || !dw_k ||
+      (rope && !pos))
+    return QKVP_ERR_NULL;
+  const void* vec[] = {dq, dk, dv, q_pre, k_pre, w_q, w_k, dpacked, dw_q, dw_k};
+  for (const void* p : vec)
+    if (!aligned16(p)) return QKVP_ERR_ALIGN;
+  if (pos && !aligned4(pos)) return QKVP_ERR_ALIGN;
+  const size_t need = qkv_prologue_bwd_workspace_size(layout, T);
+  if (T > 0 && (!workspace || workspace_bytes < need)) return workspace ? QKVP_ERR_WORKSPACE : QKVP_ERR_NULL;
+  if (workspace && !aligned16(workspace)) return QKVP_ERR_ALIGN;
+
+  int sms = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    if (accumulate) return QKVP_OK;
+    QKVP_TRY(current_device(&sms));
+    const size_t bytes = (size_t)layout->head_dim * sizeof(float);
+    if (cudaMemsetAsync(dw_q, 0, bytes, s) != cudaSuccess || cudaMemsetAsync(dw_k, 0, bytes, s) != cudaSuccess) {
+      cudaGetLastError();
+      return QKVP_ERR_LAUNCH;
+    }
+    return QKVP_OK;
+  }
+  QKVP_TRY(current_device(&sms));
+
+  BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.dq = static_cast<const uint4*>(dq);
+  a.dk = static_cast<const uint4*>(dk);
+  a.dv = static_cast<const uint4*>(dv);
+  a.q_pre = static_cast<const uint4*>(q_pre);
+  a.k_pre = static_cast<const uint4*>(k_pre);
+  a.pos = pos;
+  a.w_q = w_q;
+  a.w_k = w_k;
+  a.eps = eps;
+  a.inv_head_dim = 1.0f / (float)layout->head_dim;
+  a.T = T;
+  a.n_q = layout->n_q;
+  a.n_kv = layout->n_kv;
+  a.group = layout->n_q / layout->n_kv;
+  a.cpt = g.heads * (layout->head_dim / 8);
+  a.cpt_magic = magic((uint32_t)a.cpt);
+  a.gs_magic = magic((uint32_t)(a.group + 2));
+  gqa_items(T, a.cpt, kBwdChunksPerThread, &a.item_chunks, &a.n_items, &a.max_tok);
+  a.dpacked = static_cast<uint4*>(dpacked);
+  a.row_stride16 = g.stride / 8;
+  a.partials = static_cast<float*>(workspace);
+  if (rope) rope_table(rope_base, layout->head_dim, &a.rope);
+
+  const void* kern = bwd_kernel(layout->head_dim, layout->kind == QKVP_SECTIONED, rope);
+  const size_t smem = (size_t)a.max_tok * (layout->head_dim / 2) * 2 * sizeof(float);
+  int64_t grid = (int64_t)sms * blocks_per_sm(kern, kThreads, smem);
+  if (grid > a.n_items) grid = a.n_items;
+  if (grid > kMaxBwdParts) grid = kMaxBwdParts;
+  QKVP_TRY(launch(kern, grid, kThreads, smem, s, &a));
+
+  FinalizeArgs f;
+  f.partials = a.partials;
+  f.nparts = (int32_t)grid;
+  f.head_dim = layout->head_dim;
+  f.dw_q = dw_q;
+  f.dw_k = dw_k;
+  f.accumulate = accumulate ? 1 : 0;
+  const int fgrid = 2 * layout->head_dim / kFinalizeOutputsPerCta;
+  return launch(dw_finalize_kernel(), fgrid, kFinalizeThreads, 0, s, &f);
+}
+
+}  // extern "C"

@@ -1,0 +1,142 @@
+// Internal interface between the host API (api.cpp) and the kernel launchers.
+// Plain structs of device pointers and sizes, passed to the kernels by value.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qkvp {
+
+constexpr int kThreads = 256;         // threads per CTA for the GQA kernels
+constexpr int kMaxHalf = 64;          // RoPE frequencies for head_dim 128
+constexpr int kFwdChunksPerThread = 10;
+constexpr int kBwdChunksPerThread = 6;
+constexpr int kMaxBwdParts = 1024;    // cap on per-CTA weight-grad partial rows
+
+enum Role : int { kRoleQ = 0, kRoleK = 1, kRoleV = 2 };
+
+struct RopeTable {
+  uint64_t turns[kMaxHalf];  // frac(inv_freq_i / 2pi) * 2^64
+};
+
+// Forward (contiguous or paged-pool destination), GQA layouts.
+struct FwdArgs {
+  const uint4* packed;
+  int64_t row_stride16;   // packed row stride, 16-byte chunks
+  const int32_t* pos;
+  const float* w_q;
+  const float* w_k;
+  float eps;
+  float inv_head_dim;
+  int64_t T;
+  int32_t n_q, n_kv, group;
+  int32_t cpt;            // 16-byte chunks per token = heads * head_dim / 8
+  uint32_t cpt_magic;     // floor(2^32 / cpt) + 1
+  uint32_t gs_magic;      // floor(2^32 / (group + 2)) + 1
+  int64_t item_chunks;    // chunks per work item
+  int64_t n_items;
+  int32_t max_tok;        // tokens an item can touch (shared-memory table rows)
+  uint4* q;
+  uint4* k;
+  uint4* v;
+  uint4* q_pre;
+  uint4* k_pre;
+  const int32_t* page;
+  const int32_t* offset;
+  uint4* k_pool;
+  uint4* v_pool;
+  int32_t num_pages, page_size;
+  int32_t* dev_status;
+  RopeTable rope;
+};
+
+struct BwdArgs {
+  const uint4* dq;
+  const uint4* dk;
+  const uint4* dv;
+  const uint4* q_pre;
+  const uint4* k_pre;
+  const int32_t* pos;
+  const float* w_q;
+  const float* w_k;
+  float eps;
+  float inv_head_dim;
+  int64_t T;
+  int32_t n_q, n_kv, group;
+  int32_t cpt;
+  uint32_t cpt_magic;
+  uint32_t gs_magic;
+  int64_t item_chunks;
+  int64_t n_items;
+  int32_t max_tok;
+  uint4* dpacked;
+  int64_t row_stride16;
+  float* partials;        // [grid][2][head_dim]
+  RopeTable rope;
+};
+
+struct LatentArgs {
+  const uint4* rows;
+  int64_t row_stride16;
+  const int32_t* pos;
+  const float* w;
+  float eps;
+  float inv_norm_dim;
+  int64_t T;
+  int32_t norm_chunks;    // norm_dim / 8
+  int32_t row_chunks;     // (norm_dim + rope_dim) / 8
+  uint4* out;             // contiguous destination [T, row_chunks] (or null)
+  const int32_t* page;
+  const int32_t* offset;
+  uint4* pool;            // pool destination (or null)
+  int32_t num_pages, page_size;
+  int32_t* dev_status;
+  RopeTable rope;
+};
+
+struct ScatterArgs {
+  const uint4* src_a;     // [T, row_chunks]
+  const uint4* src_b;     // optional second source (v), same shape
+  uint4* pool_a;
+  uint4* pool_b;
+  int64_t T;
+  int32_t row_chunks;
+  const int32_t* page;
+  const int32_t* offset;
+  int32_t num_pages, page_size;
+  int32_t* dev_status;
+};
+
+struct FwdVariant {
+  int head_dim;       // 64 or 128
+  bool sectioned;
+  bool rope;
+  bool save_pre;
+  bool pool;
+};
+
+// Kernel entry points (host stubs for cudaLaunchKernel / occupancy queries).
+// Each takes its argument struct by value as the only parameter.
+const void* fwd_kernel_d64(const FwdVariant& v);
+const void* fwd_kernel_d128(const FwdVariant& v);
+const void* bwd_kernel(int head_dim, bool sectioned, bool rope);
+const void* dw_finalize_kernel();
+const void* latent_kernel(bool pool, bool rope, int norm_chunks_per_lane);
+const void* scatter_kernel();
+
+// qkvp_dw_finalize_kernel arguments.
+struct FinalizeArgs {
+  const float* partials;  // [nparts][2][head_dim]
+  int32_t nparts;
+  int32_t head_dim;
+  float* dw_q;
+  float* dw_k;
+  int32_t accumulate;
+};
+constexpr int kFinalizeOutputsPerCta = 4;
+constexpr int kFinalizeThreads = 256;
+
+constexpr int kLatentWarps = 8;        // warps per CTA of the latent kernel
+constexpr int kLatentTokensPerWarp = 2;
+
+}  // namespace qkvp

@@ -1,0 +1,235 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any device call.
+
+The argument-check tests pass fake (never dereferenced) addresses, so they only
+run where no CUDA device is visible: a check that wrongly passed must not lead
+to a kernel launch on fake pointers.
+"""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+def _declared_functions():
+    names = set()
+    for f in os.listdir(HEADER_DIR):
+        if f.endswith(".h"):
+            src = open(os.path.join(HEADER_DIR, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"QKVP_API\s+[\w\s\*]+?\b(qkv_prologue_\w+)\s*\(", src))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    assert {"qkv_prologue_fwd", "qkv_prologue_bwd", "qkv_prologue_pool_write",
+            "qkv_prologue_pool_scatter", "qkv_prologue_bwd_workspace_size",
+            "qkv_prologue_status_string", "qkv_prologue_version"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    missing = _declared_functions() - exported
+    assert not missing, missing
+    # and nothing else of ours leaks out of the library
+    ours = {s for s in exported if "qkvp" in s.lower() or "qkv_prologue" in s}
+    assert ours == _declared_functions()
+    dl = ctypes.CDLL(lib.LIB_PATH)
+    for name in _declared_functions():
+        assert getattr(dl, name) is not None
+
+
+def test_binding_exposes_the_same_names(lib):
+    for name in _declared_functions():
+        assert callable(getattr(lib, name))
+
+
+def test_version_and_status_strings(lib):
+    assert lib.qkv_prologue_version() == lib.QKVP_VERSION == 1
+    for code in range(-8, 1):
+        s = lib.qkv_prologue_status_string(code)
+        assert s and s != "unknown status"
+    assert lib.qkv_prologue_status_string(-99) == "unknown status"
+
+
+def test_constants_match_header(lib):
+    src = open(os.path.join(HEADER_DIR, "qkv_prologue.h")).read()
+    for name in ("QKVP_OK", "QKVP_ERR_NULL", "QKVP_ERR_SHAPE", "QKVP_ERR_ALIGN", "QKVP_ERR_ARCH",
+                 "QKVP_ERR_WORKSPACE", "QKVP_ERR_LAUNCH", "QKVP_ERR_FLAGS", "QKVP_ERR_VALUE",
+                 "QKVP_INTERLEAVED", "QKVP_SECTIONED", "QKVP_LATENT", "QKVP_NOPE", "QKVP_SAVE_PRE",
+                 "QKVP_ACCUMULATE_DW", "QKVP_DEV_BAD_PAGE", "QKVP_DEV_BAD_OFFSET"):
+        m = re.search(rf"\b{name}\s*=\s*(-?\d+)", src)
+        assert m, name
+        assert int(m.group(1)) == getattr(lib, name), name
+
+
+def test_layout_struct_matches_c_layout(lib):
+    # int32 kind, n_q, n_kv, head_dim; int64 row_stride; int32 norm_dim, rope_dim
+    L = lib.qkvp_layout
+    assert ctypes.sizeof(L) == 32
+    assert L.row_stride.offset == 16 and L.norm_dim.offset == 24 and L.rope_dim.offset == 28
+
+
+def test_workspace_size(lib):
+    L = lib.layout("interleaved", 128, 16, 64)
+    assert lib.qkv_prologue_bwd_workspace_size(L, 0) == 0
+    # one partial row [2, 64] fp32 per CTA, at most 1024 rows
+    assert lib.qkv_prologue_bwd_workspace_size(L, 1) == 512
+    assert lib.qkv_prologue_bwd_workspace_size(L, 16384) == 1024 * 512
+    assert lib.qkv_prologue_bwd_workspace_size(lib.layout("interleaved", 8, 3, 64), 16) == 0
+    assert lib.qkv_prologue_bwd_workspace_size(lib.layout("interleaved", 32, 8, 128), 100) > 0
+
+
+# ----------------------------------------------------- host-side checks ----
+
+def _no_gpu():
+    try:
+        import torch
+
+        return not torch.cuda.is_available()
+    except Exception:
+        return True
+
+
+cpu_only = pytest.mark.skipif(not _no_gpu(), reason="fake-pointer argument checks run only without a GPU")
+
+A = 0x10000  # a 16-byte aligned fake device address (never dereferenced)
+
+
+def _fwd(lib, L=None, T=4, packed=A, pos=A, wq=A, wk=A, eps=1e-6, base=1e4, flags=0, q=A, k=A, v=A,
+         q_pre=None, k_pre=None):
+    L = L or lib.layout("interleaved", 8, 2, 64)
+    return lib.qkv_prologue_fwd(L, T, packed, pos, wq, wk, eps, base, flags, q, k, v, q_pre, k_pre, stream=0,
+                                check=False)
+
+
+@cpu_only
+def test_fwd_argument_checks(lib):
+    C = lib
+    assert _fwd(C) == C.QKVP_ERR_ARCH  # valid arguments: it gets as far as the device check
+    assert _fwd(C, T=0) == C.QKVP_OK  # empty batch: no device needed
+    assert _fwd(C, T=-1) == C.QKVP_ERR_SHAPE
+    assert _fwd(C, L=C.layout("interleaved", 8, 3, 64)) == C.QKVP_ERR_SHAPE
+    assert _fwd(C, L=C.layout("interleaved", 8, 2, 96)) == C.QKVP_ERR_SHAPE
+    assert _fwd(C, L=C.layout("interleaved", 0, 2, 64)) == C.QKVP_ERR_SHAPE
+    assert _fwd(C, L=C.layout(7, 8, 2, 64)) == C.QKVP_ERR_SHAPE
+    # the row must hold the exact fused total (n_q + 2 n_kv) * head_dim values
+    assert _fwd(C, L=C.layout("interleaved", 8, 2, 64, row_stride=700)) == C.QKVP_ERR_SHAPE
+    assert _fwd(C, L=C.layout("interleaved", 8, 2, 64, row_stride=772)) == C.QKVP_ERR_SHAPE
+    assert _fwd(C, L=C.layout("interleaved", 8, 2, 64, row_stride=776)) == C.QKVP_ERR_ARCH
+    assert _fwd(C, packed=None) == C.QKVP_ERR_NULL
+    assert _fwd(C, q=None) == C.QKVP_ERR_NULL
+    assert _fwd(C, pos=None) == C.QKVP_ERR_NULL
+    assert _fwd(C, pos=None, flags=C.QKVP_NOPE) == C.QKVP_ERR_ARCH  # NoPE needs no positions
+    assert _fwd(C, flags=C.QKVP_SAVE_PRE) == C.QKVP_ERR_NULL
+    assert _fwd(C, flags=C.QKVP_SAVE_PRE, q_pre=A, k_pre=A) == C.QKVP_ERR_ARCH
+    assert _fwd(C, flags=8) == C.QKVP_ERR_FLAGS
+    assert _fwd(C, flags=C.QKVP_ACCUMULATE_DW) == C.QKVP_ERR_FLAGS
+    assert _fwd(C, packed=A + 8) == C.QKVP_ERR_ALIGN
+    assert _fwd(C, k=A + 2) == C.QKVP_ERR_ALIGN
+    assert _fwd(C, pos=A + 2) == C.QKVP_ERR_ALIGN
+    assert _fwd(C, eps=-1.0) == C.QKVP_ERR_VALUE
+    assert _fwd(C, eps=float("nan")) == C.QKVP_ERR_VALUE
+    assert _fwd(C, base=0.0) == C.QKVP_ERR_VALUE
+    assert _fwd(C, base=float("inf")) == C.QKVP_ERR_VALUE
+    assert _fwd(C, base=0.0, flags=C.QKVP_NOPE) == C.QKVP_ERR_ARCH
+    with pytest.raises(C.QkvpError):
+        C.qkv_prologue_fwd(C.layout("interleaved", 8, 3, 64), 4, A, A, A, A, 1e-6, 1e4, 0, A, A, A, stream=0)
+
+
+@cpu_only
+def test_latent_argument_checks(lib):
+    C = lib
+    L = C.layout("latent", norm_dim=512, rope_dim=64)
+    ok = dict(L=L, T=4, packed=A, pos=A, wq=None, wk=A, q=None, k=A, v=None)
+    assert _fwd(C, **ok) == C.QKVP_ERR_ARCH
+    assert _fwd(C, **{**ok, "L": C.layout("latent", norm_dim=500, rope_dim=64)}) == C.QKVP_ERR_SHAPE
+    assert _fwd(C, **{**ok, "L": C.layout("latent", norm_dim=512, rope_dim=32)}) == C.QKVP_ERR_SHAPE
+    assert _fwd(C, **{**ok, "L": C.layout("latent", norm_dim=2048, rope_dim=64)}) == C.QKVP_ERR_SHAPE
+    assert _fwd(C, **{**ok, "wk": None}) == C.QKVP_ERR_NULL
+    assert _fwd(C, **{**ok, "flags": C.QKVP_SAVE_PRE}) == C.QKVP_ERR_FLAGS
+    pw = C.qkv_prologue_pool_write
+    assert pw(L, 4, A, A, None, A, 1e-6, 1e4, 0, None, A, A, A, None, 8192, 64, None, stream=0,
+              check=False) == C.QKVP_ERR_ARCH
+    assert pw(L, 4, A, A, None, A, 1e-6, 1e4, 0, None, A, A, A, None, 0, 64, None, stream=0,
+              check=False) == C.QKVP_ERR_VALUE
+    assert pw(L, 4, A, A, None, A, 1e-6, 1e4, 0, None, None, A, A, None, 8192, 64, None, stream=0,
+              check=False) == C.QKVP_ERR_NULL
+
+
+@cpu_only
+def test_pool_argument_checks(lib):
+    C = lib
+    L = C.layout("interleaved", 128, 16, 64)
+
+    def pw(**kw):
+        a = dict(T=4, packed=A, pos=A, wq=A, wk=A, flags=0, q=A, page=A, off=A, kp=A, vp=A, pages=4096,
+                 psize=64, status=None)
+        a.update(kw)
+        return C.qkv_prologue_pool_write(L, a["T"], a["packed"], a["pos"], a["wq"], a["wk"], 1e-6, 5e5,
+                                         a["flags"], a["q"], a["page"], a["off"], a["kp"], a["vp"], a["pages"],
+                                         a["psize"], a["status"], stream=0, check=False)
+
+    assert pw() == C.QKVP_ERR_ARCH
+    assert pw(vp=None) == C.QKVP_ERR_NULL
+    assert pw(page=None) == C.QKVP_ERR_NULL
+    assert pw(pages=0) == C.QKVP_ERR_VALUE
+    assert pw(psize=-1) == C.QKVP_ERR_VALUE
+    assert pw(pages=2 ** 30, psize=64) == C.QKVP_ERR_VALUE
+    assert pw(flags=C.QKVP_SAVE_PRE) == C.QKVP_ERR_FLAGS
+    assert pw(kp=A + 4) == C.QKVP_ERR_ALIGN
+    assert pw(status=A + 1) == C.QKVP_ERR_ALIGN
+    sc = C.qkv_prologue_pool_scatter
+    assert sc(L, 4, A, A, A, A, A, A, 4096, 64, None, stream=0, check=False) == C.QKVP_ERR_ARCH
+    assert sc(L, 4, A, None, A, A, A, A, 4096, 64, None, stream=0, check=False) == C.QKVP_ERR_NULL
+    assert sc(L, 0, A, A, A, A, A, A, 4096, 64, None, stream=0, check=False) == C.QKVP_OK
+
+
+@cpu_only
+def test_bwd_argument_checks(lib):
+    C = lib
+    L = C.layout("interleaved", 128, 16, 64)
+    need = C.qkv_prologue_bwd_workspace_size(L, 100)
+
+    def bwd(**kw):
+        a = dict(L=L, T=100, dq=A, dk=A, dv=A, qp=A, kp=A, pos=A, wq=A, wk=A, flags=0, dp=A, dwq=A, dwk=A,
+                 ws=A, wsb=need)
+        a.update(kw)
+        return C.qkv_prologue_bwd(a["L"], a["T"], a["dq"], a["dk"], a["dv"], a["qp"], a["kp"], a["pos"], a["wq"],
+                                  a["wk"], 1e-6, 5e5, a["flags"], a["dp"], a["dwq"], a["dwk"], a["ws"], a["wsb"],
+                                  stream=0, check=False)
+
+    assert bwd() == C.QKVP_ERR_ARCH
+    assert bwd(wsb=need - 1) == C.QKVP_ERR_WORKSPACE
+    assert bwd(ws=None) == C.QKVP_ERR_NULL
+    assert bwd(ws=A + 8) == C.QKVP_ERR_ALIGN
+    assert bwd(qp=None) == C.QKVP_ERR_NULL
+    assert bwd(dwk=None) == C.QKVP_ERR_NULL
+    assert bwd(flags=C.QKVP_SAVE_PRE) == C.QKVP_ERR_FLAGS
+    assert bwd(flags=C.QKVP_NOPE | C.QKVP_ACCUMULATE_DW, pos=None) == C.QKVP_ERR_ARCH
+    assert bwd(L=C.layout("latent", norm_dim=512, rope_dim=64)) == C.QKVP_ERR_SHAPE
+    assert bwd(T=0, flags=C.QKVP_ACCUMULATE_DW, ws=None, wsb=0) == C.QKVP_OK
+    # T == 0 without ACCUMULATE_DW zeroes dw, which needs the device
+    assert bwd(T=0, ws=None, wsb=0) == C.QKVP_ERR_ARCH
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    # a copy of the package without the .so must refuse to import
+    import shutil
+    import sys
+
+    pkg = os.path.join(ROOT, "rope_qkv_prologue_gb300")
+    dst = tmp_path / "rope_qkv_prologue_gb300"
+    shutil.copytree(pkg, dst, ignore=shutil.ignore_patterns("*.so", "_build", "__pycache__"))
+    code = "import rope_qkv_prologue_gb300"
+    res = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True)
+    assert res.returncode != 0 and "libqkv_prologue.so is missing" in res.stderr

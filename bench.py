@@ -256,10 +256,10 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    from rope_qkv_prologue_gb300 import _build
+    import __graft_entry__
 
     if rank == 0 or world == 1:
-        _build.build()
+        __graft_entry__.build()
     if world > 1:
         dist.barrier()
 

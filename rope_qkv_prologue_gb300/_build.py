@@ -1,6 +1,6 @@
 """Build the C-ABI shared library in-tree with nvcc (sm_103a only).
 
-    python -m rope_qkv_prologue_gb300._build        # or: build()
+    python rope_qkv_prologue_gb300/_build.py        # or: __graft_entry__.build()
 
 Each translation unit compiles in parallel to rope_qkv_prologue_gb300/_build/,
 then nvcc links rope_qkv_prologue_gb300/libqkv_prologue.so (CUDA runtime

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libqkv_prologue.so")
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f"{LIB_PATH} is missing: build the CUDA library first "
-        "(python -m rope_qkv_prologue_gb300._build, or __graft_entry__.build())")
+        "(python rope_qkv_prologue_gb300/_build.py, or __graft_entry__.build())")
 
 _lib = ctypes.CDLL(LIB_PATH)
 

@@ -33,9 +33,9 @@ def _cuda_available():
 @pytest.fixture(scope="session")
 def lib():
     """The compiled C-ABI library (built in-tree on first use)."""
-    from rope_qkv_prologue_gb300 import _build
+    import __graft_entry__
 
-    _build.build()
+    __graft_entry__.build()
     import rope_qkv_prologue_gb300 as qp
 
     return qp

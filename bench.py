@@ -263,7 +263,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
 
-    T = 16384
+    T = args.tokens
     ws = TrainStep(dev, T)
     props = torch.cuda.get_device_properties(dev)
     uuid = getattr(props, "uuid", None)
@@ -348,11 +348,11 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 packed rows and upstream grads, U(0.5,1.5) norm weights)",
         "config": {
-            "workload": "train fwd+bwd, T=16384, packed [T,16,10,64] interleaved, RoPE base 5e5, eps 1e-6, "
+            "workload": f"train fwd+bwd, T={T}, packed [T,16,10,64] interleaved, RoPE base 5e5, eps 1e-6, "
                         "forward saves split pre-norm q/k",
             "T": T, "n_q": N_Q, "n_kv": N_KV, "head_dim": D, "layout": "interleaved",
             "bytes_per_step": step_bytes,
-            "l2": "no flush: inputs larger than L2 (1.95 GB of traffic per step vs 129 MB L2)",
+            "l2": f"no flush: inputs larger than L2 ({step_bytes / 1e9:.2f} GB of traffic per step vs 129 MB L2)",
             "parallelism": f"replicas x{world} (tokens independent; no collective)",
         },
         "kernels": {
@@ -483,6 +483,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--tokens", type=int, default=16384,
+                    help="T of the training workload (16384 is the headline; smaller T for profiling runs)")
     ap.add_argument("--cpu-tokens", type=int, default=6144)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

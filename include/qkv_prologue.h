@@ -100,7 +100,11 @@ typedef struct {
 enum {
   QKVP_NOPE = 1,           /* NoPE layer: RMSNorm only, no rotation            */
   QKVP_SAVE_PRE = 2,       /* forward also writes the split pre-norm q and k   */
-  QKVP_ACCUMULATE_DW = 4   /* backward adds into dw_q / dw_k instead of writing */
+  QKVP_ACCUMULATE_DW = 4,  /* backward adds into dw_q / dw_k instead of writing */
+  QKVP_FORCE_GENERIC = 8   /* GQA forward / backward: use the general kernels
+                              even where the shared-memory pipelined ones
+                              apply (same output bits; for A/B checks). The
+                              weight-grad sums may differ in rounding. */
 };
 
 /* Device-side status bits (pool writes): set with an atomic OR in
@@ -210,6 +214,15 @@ QKVP_API int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* 
                      const float* w_q, const float* w_k, float eps, double rope_base,
                      uint32_t flags, void* dpacked, float* dw_q, float* dw_k, void* workspace,
                      size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * qkv_prologue_device_error -- read (and with clear != 0, reset) the
+ * library's device error word on the current device. Bit 1 means a
+ * pipelined kernel's bounded wait on its shared-memory pipeline gave up
+ * (after 2 s) and the kernel returned early: the results of that launch are
+ * invalid. Synchronises with the device (it copies the word to the host).
+ * ------------------------------------------------------------------------- */
+QKVP_API int qkv_prologue_device_error(int clear, int* value);
 
 /* Static, human-readable text for a qkvp_status value. */
 QKVP_API const char* qkv_prologue_status_string(int status);

@@ -41,6 +41,7 @@ QKVP_LATENT = 2
 QKVP_NOPE = 1
 QKVP_SAVE_PRE = 2
 QKVP_ACCUMULATE_DW = 4
+QKVP_FORCE_GENERIC = 8
 
 QKVP_DEV_BAD_PAGE = 1
 QKVP_DEV_BAD_OFFSET = 2
@@ -82,6 +83,7 @@ _SIGS = {
                           _vp, ctypes.c_size_t, _vp], ctypes.c_int),
     "qkv_prologue_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "qkv_prologue_version": ([], ctypes.c_int),
+    "qkv_prologue_device_error": ([ctypes.c_int, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -130,6 +132,13 @@ def qkv_prologue_status_string(status):
 
 def qkv_prologue_version():
     return _lib.qkv_prologue_version()
+
+
+def qkv_prologue_device_error(clear=True, check=True):
+    """The library's device error word on the current device (0 = no error)."""
+    v = ctypes.c_int(0)
+    _ret(_lib.qkv_prologue_device_error(int(bool(clear)), ctypes.byref(v)), "qkv_prologue_device_error", check)
+    return v.value
 
 
 def qkv_prologue_fwd(L, T, packed, pos, w_q, w_k, eps, rope_base, flags, q, k, v,

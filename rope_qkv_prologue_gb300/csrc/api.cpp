@@ -23,6 +23,7 @@ struct DeviceInfo {
   bool probed = false;
   int status = QKVP_OK;
   int sms = 0;
+  int smem_per_sm = 0;
 };
 
 std::mutex g_dev_mutex;
@@ -30,7 +31,7 @@ DeviceInfo g_dev[kMaxDevices];
 
 // The current device, checked once per device: it must be sm_103 (the only
 // architecture the library is compiled for).
-int current_device(int* sms) {
+int current_device(int* sms, int* smem_per_sm = nullptr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
@@ -39,18 +40,21 @@ int current_device(int* sms) {
   std::lock_guard<std::mutex> lock(g_dev_mutex);
   DeviceInfo& d = g_dev[dev];
   if (!d.probed) {
-    int major = 0, minor = 0, sms_ = 0;
+    int major = 0, minor = 0, sms_ = 0, smem_ = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms_, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaDeviceGetAttribute(&sms_, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) {
       cudaGetLastError();
       return QKVP_ERR_ARCH;
     }
     d.status = (major == 10 && minor == 3) ? QKVP_OK : QKVP_ERR_ARCH;
     d.sms = sms_;
+    d.smem_per_sm = smem_;
     d.probed = true;
   }
   *sms = d.sms;
+  if (smem_per_sm) *smem_per_sm = d.smem_per_sm;
   return d.status;
 }
 
@@ -61,6 +65,62 @@ int blocks_per_sm(const void* kernel, int threads, size_t smem) {
     return 1;
   }
   return n > 0 ? n : 1;
+}
+
+// Opt a kernel in to `smem` bytes of dynamic shared memory (once per device
+// and kernel; the attribute only ever grows).
+bool allow_smem(const void* kernel, size_t smem) {
+  if (smem <= 48 * 1024) return true;
+  struct Entry {
+    int dev;
+    const void* kernel;
+    size_t bytes;
+  };
+  static std::mutex mu;
+  static Entry cache[256];
+  static int n = 0;
+  int dev = -1;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (cache[i].dev == dev && cache[i].kernel == kernel && cache[i].bytes >= smem) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (n < 256) cache[n++] = Entry{dev, kernel, smem};
+  return true;
+}
+
+// Tile geometry of the streaming kernels, or false when the layout does not
+// fit them: the 256 consumer threads must split a token row into groups of
+// tpg threads that each take exactly `steps` chunks (steps <= kStreamMaxSteps),
+// and two CTAs with at least two stages each must fit in one SM's shared
+// memory. token_bytes = bytes staged per token.
+bool stream_geometry(int cpt, int cph, int hd, int64_t T, int64_t token_bytes, int smem_per_sm,
+                     int static_smem, StreamGeom* g, size_t* smem) {
+  const int nct = kStreamConsumerWarps * 32;
+  const int budget = smem_per_sm / 2 - 1024 - static_smem;
+  for (int tpg = nct; tpg >= cph; tpg /= 2) {
+    if (cpt % tpg != 0) continue;
+    const int steps = cpt / tpg;
+    if (steps > kStreamMaxSteps) return false;
+    const int tpt = nct / tpg;
+    const int64_t stage = (int64_t)tpt * token_bytes;
+    const int fixed = StreamSmem::tables(hd) + 128;
+    const int64_t per_stage = stage + StreamSmem::table_stride(hd, tpt);
+    int64_t stages = (budget - fixed) / per_stage;
+    if (stages < 2) return false;
+    if (stages > kMaxStages) stages = kMaxStages;
+    g->tpt = tpt;
+    g->stages = (int32_t)stages;
+    g->steps = steps;
+    g->stage_bytes = (int32_t)stage;
+    g->n_tiles = (T + tpt - 1) / tpt;
+    *smem = (size_t)StreamSmem::data(hd, tpt, (int)stages) + (size_t)stages * stage;
+    return true;
+  }
+  return false;
 }
 
 int launch(const void* kernel, int64_t grid, int threads, size_t smem, cudaStream_t s, void* arg) {
@@ -208,7 +268,8 @@ static int gqa_forward(const qkvp_layout* L, int64_t T, const void* packed, cons
                        cudaStream_t stream) {
   Gqa g;
   QKVP_TRY(check_gqa(L, T, &g));
-  const uint32_t allowed = pool ? (uint32_t)QKVP_NOPE : (uint32_t)(QKVP_NOPE | QKVP_SAVE_PRE);
+  const uint32_t allowed = (pool ? (uint32_t)QKVP_NOPE : (uint32_t)(QKVP_NOPE | QKVP_SAVE_PRE)) |
+                           (uint32_t)QKVP_FORCE_GENERIC;
   if (flags & ~allowed) return QKVP_ERR_FLAGS;
   const bool rope = !(flags & QKVP_NOPE);
   const bool save = (flags & QKVP_SAVE_PRE) != 0;
@@ -230,8 +291,8 @@ static int gqa_forward(const qkvp_layout* L, int64_t T, const void* packed, cons
     return QKVP_ERR_ALIGN;
   if (T == 0) return QKVP_OK;
 
-  int sms = 0;
-  QKVP_TRY(current_device(&sms));
+  int sms = 0, smem_per_sm = 0;
+  QKVP_TRY(current_device(&sms, &smem_per_sm));
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));
   a.packed = static_cast<const uint4*>(packed);
@@ -264,9 +325,20 @@ static int gqa_forward(const qkvp_layout* L, int64_t T, const void* packed, cons
   if (rope) rope_table(rope_base, L->head_dim, &a.rope);
 
   const FwdVariant var{L->head_dim, L->kind == QKVP_SECTIONED, rope, save, pool};
+  size_t smem = 0;
+  if (!(flags & QKVP_FORCE_GENERIC) &&
+      stream_geometry(a.cpt, L->head_dim / 8, L->head_dim, T, (int64_t)a.cpt * 16, smem_per_sm, 0, &a.sg, &smem) &&
+      (a.err = device_error_word()) != nullptr) {
+    a.sg.dense = g.stride == g.row;
+    const void* kern = L->head_dim == 64 ? fwd_stream_kernel_d64(var) : fwd_stream_kernel_d128(var);
+    if (allow_smem(kern, smem)) {
+      const int threads = (kStreamConsumerWarps + 1) * 32;
+      const int64_t cap = (int64_t)sms * blocks_per_sm(kern, threads, smem);
+      return launch(kern, a.sg.n_tiles < cap ? a.sg.n_tiles : cap, threads, smem, stream, &a);
+    }
+  }
   const void* kern = L->head_dim == 64 ? fwd_kernel_d64(var) : fwd_kernel_d128(var);
-  const size_t smem = (size_t)a.max_tok * (L->head_dim / 2) * 2 * sizeof(float) +
-                      (size_t)a.max_tok * sizeof(int32_t);
+  smem = (size_t)a.max_tok * (L->head_dim / 2) * 2 * sizeof(float) + (size_t)a.max_tok * sizeof(int32_t);
   const int64_t cap = (int64_t)sms * blocks_per_sm(kern, kThreads, smem);
   const int64_t grid = a.n_items < cap ? a.n_items : cap;
   return launch(kern, grid, kThreads, smem, stream, &a);
@@ -408,7 +480,8 @@ size_t qkv_prologue_bwd_workspace_size(const qkvp_layout* layout, int64_t T) {
   int max_tok = 0;
   gqa_items(T, g.heads * (layout->head_dim / 8), kBwdChunksPerThread, &item_chunks, &n_items,
             &max_tok);
-  return (size_t)bwd_parts(n_items) * 2 * layout->head_dim * sizeof(float);
+  // one partial row per CTA: at most max(work items, tokens), capped
+  return (size_t)bwd_parts(n_items > T ? n_items : T) * 2 * layout->head_dim * sizeof(float);
 }
 
 int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const void* dk,
@@ -418,7 +491,7 @@ int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const
                      size_t workspace_bytes, void* stream) {
   Gqa g;
   QKVP_TRY(check_gqa(layout, T, &g));
-  if (flags & ~(uint32_t)(QKVP_NOPE | QKVP_ACCUMULATE_DW)) return QKVP_ERR_FLAGS;
+  if (flags & ~(uint32_t)(QKVP_NOPE | QKVP_ACCUMULATE_DW | QKVP_FORCE_GENERIC)) return QKVP_ERR_FLAGS;
   const bool rope = !(flags & QKVP_NOPE);
   const bool accumulate = (flags & QKVP_ACCUMULATE_DW) != 0;
   QKVP_TRY(check_scalars(eps, rope_base, rope));
@@ -433,7 +506,7 @@ int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const
   if (T > 0 && (!workspace || workspace_bytes < need)) return workspace ? QKVP_ERR_WORKSPACE : QKVP_ERR_NULL;
   if (workspace && !aligned16(workspace)) return QKVP_ERR_ALIGN;
 
-  int sms = 0;
+  int sms = 0, smem_per_sm = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (T == 0) {
     if (accumulate) return QKVP_OK;
@@ -445,7 +518,7 @@ int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const
     }
     return QKVP_OK;
   }
-  QKVP_TRY(current_device(&sms));
+  QKVP_TRY(current_device(&sms, &smem_per_sm));
 
   BwdArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -472,12 +545,35 @@ int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const
   a.partials = static_cast<float*>(workspace);
   if (rope) rope_table(rope_base, layout->head_dim, &a.rope);
 
-  const void* kern = bwd_kernel(layout->head_dim, layout->kind == QKVP_SECTIONED, rope);
-  const size_t smem = (size_t)a.max_tok * (layout->head_dim / 2) * 2 * sizeof(float);
-  int64_t grid = (int64_t)sms * blocks_per_sm(kern, kThreads, smem);
-  if (grid > a.n_items) grid = a.n_items;
-  if (grid > kMaxBwdParts) grid = kMaxBwdParts;
-  QKVP_TRY(launch(kern, grid, kThreads, smem, s, &a));
+  const bool sectioned = layout->kind == QKVP_SECTIONED;
+  const int hd = layout->head_dim;
+  const int64_t token_bytes = (int64_t)(2 * layout->n_q + 3 * layout->n_kv) * hd * 2;
+  const int static_smem = kStreamConsumerWarps * 2 * hd * (int)sizeof(float);
+  size_t smem = 0;
+  int64_t grid = 0;
+  bool streamed = false;
+  if (!(flags & QKVP_FORCE_GENERIC) &&
+      stream_geometry(a.cpt, hd / 8, hd, T, token_bytes, smem_per_sm, static_smem, &a.sg, &smem) &&
+      (a.err = device_error_word()) != nullptr) {
+    a.sg.dense = 1;
+    const void* kern = bwd_stream_kernel(hd, sectioned, rope);
+    if (allow_smem(kern, smem)) {
+      const int threads = (kStreamConsumerWarps + 1) * 32;
+      grid = (int64_t)sms * blocks_per_sm(kern, threads, smem);
+      if (grid > a.sg.n_tiles) grid = a.sg.n_tiles;
+      if (grid > kMaxBwdParts) grid = kMaxBwdParts;
+      QKVP_TRY(launch(kern, grid, threads, smem, s, &a));
+      streamed = true;
+    }
+  }
+  if (!streamed) {
+    const void* kern = bwd_kernel(hd, sectioned, rope);
+    smem = (size_t)a.max_tok * (hd / 2) * 2 * sizeof(float);
+    grid = (int64_t)sms * blocks_per_sm(kern, kThreads, smem);
+    if (grid > a.n_items) grid = a.n_items;
+    if (grid > kMaxBwdParts) grid = kMaxBwdParts;
+    QKVP_TRY(launch(kern, grid, kThreads, smem, s, &a));
+  }
 
   FinalizeArgs f;
   f.partials = a.partials;
@@ -488,6 +584,13 @@ int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const
   f.accumulate = accumulate ? 1 : 0;
   const int fgrid = 2 * layout->head_dim / kFinalizeOutputsPerCta;
   return launch(dw_finalize_kernel(), fgrid, kFinalizeThreads, 0, s, &f);
+}
+
+int qkv_prologue_device_error(int clear, int* value) {
+  if (!value) return QKVP_ERR_NULL;
+  int sms = 0;
+  QKVP_TRY(current_device(&sms));
+  return read_device_error(clear != 0, value) == 0 ? QKVP_OK : QKVP_ERR_LAUNCH;
 }
 
 }  // extern "C"

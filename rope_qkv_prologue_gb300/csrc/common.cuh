@@ -43,6 +43,117 @@ __device__ __forceinline__ void st_keep(uint4* p, const uint4& v) { *p = v; }
 // Output read much later (saved activations): cache-streaming store.
 __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }
 
+// --------------------------------------------------- paired float math ----
+//
+// Element-wise math runs on pairs of floats with Blackwell's paired fp32
+// instructions (__fmul2_rn / __ffma2_rn: two IEEE float operations, each
+// rounded exactly as the scalar operation would be). Every kernel computes a
+// chunk through the helpers below, so all code paths (streaming or register,
+// contiguous or pool destination) produce the same bits for the same inputs.
+
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+__device__ __forceinline__ void unpack_pairs(const uint4& v, float2 (&p)[4]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = f2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+}
+
+__device__ __forceinline__ uint4 pack_pairs(const float2 (&p)[4]) {
+  return make_uint4(pack2(p[0].x, p[0].y), pack2(p[1].x, p[1].y), pack2(p[2].x, p[2].y), pack2(p[3].x, p[3].y));
+}
+
+__device__ __forceinline__ void load_pairs(const float* p, float2 (&w)[4]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  w[0] = f2(a.x, a.y); w[1] = f2(a.z, a.w); w[2] = f2(b.x, b.y); w[3] = f2(b.z, b.w);
+}
+
+// Sum of squares of this lane's 8 values, then over the CPH lanes of the head.
+template <int CPH>
+__device__ __forceinline__ float head_sum_sq(const float2 (&x)[4]) {
+  float2 a = __fmul2_rn(x[0], x[0]);
+  a = __ffma2_rn(x[1], x[1], a);
+  a = __ffma2_rn(x[2], x[2], a);
+  a = __ffma2_rn(x[3], x[3], a);
+  float ss = a.x + a.y;
+#pragma unroll
+  for (int o = 1; o < CPH; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  return ss;
+}
+
+// Forward of one chunk (8 values of one head; the head's CPH lanes call this
+// together): y = x * r * w with r = (mean(x^2) + eps)^-1/2, then rotate-half:
+// o = y * cos + y_partner * ssin, where the partner (element +- D/2) is in
+// lane ^ CPH/2 and ssin = -sin for the first half of the head, +sin for the
+// second.
+template <int CPH, bool ROPE>
+__device__ __forceinline__ void chunk_forward(const uint4& xr, const float2 (&w)[4], float eps, float inv_hd,
+                                              const float2 (&c)[4], const float2 (&ssin)[4], float2 (&y)[4]) {
+  float2 x[4];
+  unpack_pairs(xr, x);
+  const float r = rsqrtf(fmaf(head_sum_sq<CPH>(x), inv_hd, eps));
+  const float2 rr = f2(r, r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) y[i] = __fmul2_rn(__fmul2_rn(x[i], rr), w[i]);
+  if (ROPE) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 yp = f2(__shfl_xor_sync(0xffffffffu, y[i].x, CPH / 2),
+                           __shfl_xor_sync(0xffffffffu, y[i].y, CPH / 2));
+      y[i] = __ffma2_rn(y[i], c[i], __fmul2_rn(yp, ssin[i]));
+    }
+  }
+}
+
+// Backward of one chunk. d: gradient of the roped output; x: pre-norm input.
+//   g  = R(theta)^T d = d * cos + d_partner * ssin   (ssin = +sin / -sin for
+//        the first / second half of the head: the transpose flips the sign)
+//   r  = (mean(x^2) + eps)^-1/2
+//   dx = r (w g) - x (r^3 / D) sum(x w g)
+// Also returns gx = g * x (the weight gradient is gx * r) and r.
+template <int CPH, bool ROPE>
+__device__ __forceinline__ void chunk_backward(const uint4& dr, const uint4& xr, const float2 (&w)[4], float eps,
+                                               float inv_hd, const float2 (&c)[4], const float2 (&ssin)[4],
+                                               float2 (&dx)[4], float2 (&gx)[4], float& r_out) {
+  float2 d[4], x[4], g[4], wg[4];
+  unpack_pairs(dr, d);
+  unpack_pairs(xr, x);
+  if (ROPE) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 dp = f2(__shfl_xor_sync(0xffffffffu, d[i].x, CPH / 2),
+                           __shfl_xor_sync(0xffffffffu, d[i].y, CPH / 2));
+      g[i] = __ffma2_rn(d[i], c[i], __fmul2_rn(dp, ssin[i]));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) g[i] = d[i];
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) wg[i] = __fmul2_rn(w[i], g[i]);
+  float2 sq = __fmul2_rn(x[0], x[0]), dt = __fmul2_rn(x[0], wg[0]);
+#pragma unroll
+  for (int i = 1; i < 4; ++i) {
+    sq = __ffma2_rn(x[i], x[i], sq);
+    dt = __ffma2_rn(x[i], wg[i], dt);
+  }
+  float ss = sq.x + sq.y, dot = dt.x + dt.y;
+#pragma unroll
+  for (int o = 1; o < CPH; o <<= 1) {
+    ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    dot += __shfl_xor_sync(0xffffffffu, dot, o);
+  }
+  const float r = rsqrtf(fmaf(ss, inv_hd, eps));
+  const float kx = r * r * r * dot * inv_hd;
+  const float2 rr = f2(r, r), nk = f2(-kx, -kx);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    dx[i] = __ffma2_rn(x[i], nk, __fmul2_rn(rr, wg[i]));
+    gx[i] = __fmul2_rn(g[i], x[i]);
+  }
+  r_out = r;
+}
+
 // ---------------------------------------------------------- division ----
 
 // n / d for n < 2^16 and 2 <= d <= 2^16 with m = floor(2^32 / d) + 1:

@@ -60,22 +60,17 @@ __device__ __forceinline__ void classify(uint32_t hp, int n_q, int n_kv, int gro
   }
 }
 
-template <int HD>
-__device__ __forceinline__ void load_weights(const float* w, int e, float (&out)[8]) {
-  const float4* p = reinterpret_cast<const float4*>(w) + 2 * e;
-  const float4 a = __ldg(p), b = __ldg(p + 1);
-  out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
-  out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
-}
-
+// cos and signed sin of frequencies f0 .. f0+7 of table row tl, as pairs;
+// ssin = sign * sin.
 template <int HALF>
-__device__ __forceinline__ void read_cos_sin(const float* s_cos, const float* s_sin, uint32_t tl,
-                                             int f0, float (&c)[8], float (&s)[8]) {
-  const float4* cp = reinterpret_cast<const float4*>(s_cos + tl * HALF + f0);
-  const float4* sp = reinterpret_cast<const float4*>(s_sin + tl * HALF + f0);
-  const float4 c0 = cp[0], c1 = cp[1], s0 = sp[0], s1 = sp[1];
-  c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w; c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
-  s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w; s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
+__device__ __forceinline__ void read_cos_sin(const float* s_cos, const float* s_sin, uint32_t tl, int f0,
+                                             float sign, float2 (&c)[4], float2 (&ssin)[4]) {
+  float2 sn[4];
+  load_pairs(s_cos + tl * HALF + f0, c);
+  load_pairs(s_sin + tl * HALF + f0, sn);
+  const float2 sg = f2(sign, sign);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) ssin[i] = __fmul2_rn(sn[i], sg);
 }
 
 // Fill the shared cos/sin table for tokens t_first .. t_first + ntok - 1.
@@ -106,11 +101,11 @@ __global__ void __launch_bounds__(kThreads, 2) qkvp_fwd_kernel(const FwdArgs a) 
 
   const int tid = threadIdx.x;
   const int e = tid & (CPH - 1);
-  const bool lo = e < CPH / 2;
+  const float sign = e < CPH / 2 ? -1.f : 1.f;
   const int f0 = (e & (CPH / 2 - 1)) * 8;
-  float wq[8], wk[8];
-  load_weights<HD>(a.w_q, e, wq);
-  load_weights<HD>(a.w_k, e, wk);
+  float2 wq[4], wk[4];
+  load_pairs(a.w_q + 8 * e, wq);
+  load_pairs(a.w_k + 8 * e, wk);
 
   const int64_t total = a.T * a.cpt;
   for (int64_t item = blockIdx.x; item < a.n_items; item += gridDim.x) {
@@ -158,29 +153,15 @@ __global__ void __launch_bounds__(kThreads, 2) qkvp_fwd_kernel(const FwdArgs a) 
       uint32_t oh;
       classify<SECTIONED>(j >> G::LOG_CPH, a.n_q, a.n_kv, a.group, a.gs_magic, role, oh);
 
-      float x[8], y[8];
-      unpack8(xv[u], x);
-      float ss = 0.f;
+      float2 w[4], c[4], ssin[4], y[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
-#pragma unroll
-      for (int o = 1; o < CPH; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float r = rsqrtf(fmaf(ss, a.inv_head_dim, a.eps));
-#pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = x[i] * r * (role == kRoleQ ? wq[i] : wk[i]);
-      if (ROPE) {
-        float c[8], s[8];
-        read_cos_sin<HALF>(s_cos, s_sin, tl, f0, c, s);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float yp = __shfl_xor_sync(0xffffffffu, y[i], CPH / 2);
-          y[i] = fmaf(y[i], c[i], yp * (lo ? -s[i] : s[i]));
-        }
-      }
+      for (int i = 0; i < 4; ++i) w[i] = role == kRoleQ ? wq[i] : wk[i];
+      if (ROPE) read_cos_sin<HALF>(s_cos, s_sin, tl, f0, sign, c, ssin);
+      chunk_forward<CPH, ROPE>(xv[u], w, a.eps, a.inv_head_dim, c, ssin, y);
       if (!valid) continue;
 
       const int64_t t = t_first + tl;
-      const uint4 out = pack8(y);
+      const uint4 out = pack_pairs(y);
       if (role == kRoleQ) {
         const int64_t idx = (t * a.n_q + oh) * CPH + e;
         st_keep(a.q + idx, out);
@@ -228,13 +209,13 @@ __global__ void __launch_bounds__(kThreads, 2) qkvp_bwd_kernel(const BwdArgs a) 
 
   const int tid = threadIdx.x;
   const int e = tid & (CPH - 1);
-  const bool lo = e < CPH / 2;
+  const float sign = e < CPH / 2 ? 1.f : -1.f;  // R(theta)^T: the partner term flips sign
   const int f0 = (e & (CPH / 2 - 1)) * 8;
-  float wq[8], wk[8], accq[8], acck[8];
-  load_weights<HD>(a.w_q, e, wq);
-  load_weights<HD>(a.w_k, e, wk);
+  float2 wq[4], wk[4], accq[4], acck[4];
+  load_pairs(a.w_q + 8 * e, wq);
+  load_pairs(a.w_k + 8 * e, wk);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) accq[i] = acck[i] = 0.f;
+  for (int i = 0; i < 4; ++i) accq[i] = acck[i] = f2(0.f, 0.f);
 
   const int64_t total = a.T * a.cpt;
   for (int64_t item = blockIdx.x; item < a.n_items; item += gridDim.x) {
@@ -288,68 +269,47 @@ __global__ void __launch_bounds__(kThreads, 2) qkvp_bwd_kernel(const BwdArgs a) 
       uint32_t oh;
       classify<SECTIONED>(j >> G::LOG_CPH, a.n_q, a.n_kv, a.group, a.gs_magic, role, oh);
 
-      float d[8], x[8], g[8];
-      unpack8(dv[u], d);
-      unpack8(xv[u], x);
-      if (ROPE) {
-        float c[8], s[8];
-        read_cos_sin<HALF>(s_cos, s_sin, tl, f0, c, s);
+      float2 w[4], c[4], ssin[4], dx[4], gx[4];
+      float r;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float dp = __shfl_xor_sync(0xffffffffu, d[i], CPH / 2);
-          g[i] = fmaf(d[i], c[i], dp * (lo ? s[i] : -s[i]));
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) g[i] = d[i];
-      }
-      float ss = 0.f, dot = 0.f, wg[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        wg[i] = (role == kRoleQ ? wq[i] : wk[i]) * g[i];
-        ss = fmaf(x[i], x[i], ss);
-        dot = fmaf(x[i], wg[i], dot);
-      }
-#pragma unroll
-      for (int o = 1; o < CPH; o <<= 1) {
-        ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        dot += __shfl_xor_sync(0xffffffffu, dot, o);
-      }
-      const float r = rsqrtf(fmaf(ss, a.inv_head_dim, a.eps));
-      const float kx = r * r * r * dot * a.inv_head_dim;
-      float dx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) dx[i] = fmaf(r, wg[i], -x[i] * kx);
+      for (int i = 0; i < 4; ++i) w[i] = role == kRoleQ ? wq[i] : wk[i];
+      if (ROPE) read_cos_sin<HALF>(s_cos, s_sin, tl, f0, sign, c, ssin);
+      chunk_backward<CPH, ROPE>(dv[u], xv[u], w, a.eps, a.inv_head_dim, c, ssin, dx, gx, r);
       if (!valid) continue;
 
-      const float mq = role == kRoleQ ? r : 0.f;
-      const float mk = role == kRoleK ? r : 0.f;
+      const float rq = role == kRoleQ ? r : 0.f, rk = role == kRoleK ? r : 0.f;
+      const float2 rq2 = f2(rq, rq), rk2 = f2(rk, rk);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float gx = g[i] * x[i];
-        accq[i] = fmaf(gx, mq, accq[i]);
-        acck[i] = fmaf(gx, mk, acck[i]);
+      for (int i = 0; i < 4; ++i) {
+        accq[i] = __ffma2_rn(gx[i], rq2, accq[i]);
+        acck[i] = __ffma2_rn(gx[i], rk2, acck[i]);
       }
       const int64_t t = t_first + tl;
-      st_keep(a.dpacked + t * a.row_stride16 + j, role == kRoleV ? dv[u] : pack8(dx));
+      st_keep(a.dpacked + t * a.row_stride16 + j, role == kRoleV ? dv[u] : pack_pairs(dx));
     }
   }
 
   // Weight-grad partials: lanes of a warp with the same e, then the warps.
+  float aq[8], ak[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    aq[2 * i] = accq[i].x; aq[2 * i + 1] = accq[i].y;
+    ak[2 * i] = acck[i].x; ak[2 * i + 1] = acck[i].y;
+  }
 #pragma unroll
   for (int o = CPH; o < 32; o <<= 1) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      accq[i] += __shfl_xor_sync(0xffffffffu, accq[i], o);
-      acck[i] += __shfl_xor_sync(0xffffffffu, acck[i], o);
+      aq[i] += __shfl_xor_sync(0xffffffffu, aq[i], o);
+      ak[i] += __shfl_xor_sync(0xffffffffu, ak[i], o);
     }
   }
   const int lane = tid & 31, warp = tid >> 5;
   if (lane < CPH) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      s_red[warp][0][lane * 8 + i] = accq[i];
-      s_red[warp][1][lane * 8 + i] = acck[i];
+      s_red[warp][0][lane * 8 + i] = aq[i];
+      s_red[warp][1][lane * 8 + i] = ak[i];
     }
   }
   __syncthreads();

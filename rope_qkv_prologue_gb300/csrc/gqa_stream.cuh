@@ -1,0 +1,375 @@
+// Streaming (shared-memory staged) forward and backward kernels of the
+// packed-QKV prologue: the fast path for the common head layouts.
+//
+// Pipeline. A persistent CTA = kStreamConsumerWarps consumer warps + 1
+// producer warp. The batch is cut into tiles of `tpt` consecutive tokens; CTA b
+// takes tiles b, b + grid, ... The producer warp waits for a free stage of the
+// shared-memory ring, issues bulk copies of the tile's source rows into it
+// (one copy per source tensor when rows are dense), writes the tile's cos/sin
+// table (and, for pool writes, the checked page slots) next to it, and arrives
+// on the stage's "full" mbarrier, which also waits for the copied bytes.
+// Consumers wait on "full", compute from shared memory, store results straight
+// to HBM with 16-byte stores, and arrive on the stage's "empty" mbarrier.
+//
+// Work mapping. The 256 consumer threads are split into tpt groups of
+// tpg = 256 / tpt threads; group g owns token g of every tile, and thread i of
+// a group owns the 16-byte chunks j = i + tpg * m (m < steps) of that token's
+// row, where steps = cpt / tpg exactly (the host only picks this path when
+// that division is exact). So across all tiles a thread always sees the same
+// head positions: their role (q / k / v), output head and weight row are
+// worked out once, before the tile loop, and it needs the cos/sin of one
+// token per tile (loaded once per tile, reused for every step). A head of
+// head_dim values is CPH consecutive chunks held by CPH consecutive lanes, so
+// RMSNorm sums and the rotate-half partner exchange stay xor-shuffles.
+// Element-wise float math uses Blackwell's paired fp32 instructions
+// (__ffma2_rn / __fmul2_rn: two IEEE float operations per instruction, each
+// rounded exactly like the scalar one).
+#pragma once
+
+#include "common.cuh"
+#include "gqa_kernels.cuh"
+#include "pipeline.cuh"
+#include "qkv_prologue.h"
+
+namespace qkvp {
+
+// The producer warp of a streaming CTA: fills stages, writes tables, and (on a
+// wait that timed out) drains the copies it issued before returning.
+// `load(stage_ptr, t0, ntok, bar, policy)` (run by lane 0 only) announces the
+// tile's byte count on `bar` and issues its bulk copies.
+template <int HALF, bool ROPE, bool POOL, class LoadTile>
+__device__ __forceinline__ void stream_producer(unsigned char* smem, int hd, int tpt, int stages,
+                                                int stage_bytes, int64_t n_tiles, int64_t T,
+                                                const int32_t* pos, const RopeTable& rope,
+                                                const int32_t* page, const int32_t* offset,
+                                                int32_t num_pages, int32_t page_size,
+                                                int32_t* dev_status, int* err, LoadTile load) {
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + StreamSmem::kBarriers);
+  uint64_t* empty = full + kMaxStages;
+  unsigned char* data = smem + StreamSmem::data(hd, tpt, stages);
+  const int lane = threadIdx.x & 31;
+  const uint64_t policy = policy_evict_first();
+  int s = 0;
+  uint32_t phase = 0;
+  int64_t issued = 0;
+  bool ok = true;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    if (issued >= stages) {
+      const bool freed = mbar_wait(&empty[s], phase ^ 1, err);
+      if (!__all_sync(0xffffffffu, freed)) {
+        ok = false;
+        break;
+      }
+    }
+    const int64_t t0 = tile * tpt;
+    const int ntok = (int)min((int64_t)tpt, T - t0);
+    if (lane == 0) load(data + (size_t)s * stage_bytes, t0, ntok, &full[s], policy);
+    float* tab = reinterpret_cast<float*>(smem + StreamSmem::tables(hd) + s * StreamSmem::table_stride(hd, tpt));
+    if (ROPE) {
+      for (int i = lane; i < ntok * HALF; i += 32) {
+        const int tl = i / HALF, f = i - (i / HALF) * HALF;
+        float c, sn;
+        rope_cos_sin(pos[t0 + tl], rope.turns[f], &c, &sn);
+        tab[i] = c;
+        tab[tpt * HALF + i] = sn;
+      }
+    }
+    if (POOL) {
+      int32_t* slot = reinterpret_cast<int32_t*>(tab + 2 * tpt * HALF);
+      for (int i = lane; i < ntok; i += 32) {
+        const int32_t pg = page[t0 + i], of = offset[t0 + i];
+        int bad = 0;
+        if (pg < 0 || pg >= num_pages) bad |= QKVP_DEV_BAD_PAGE;
+        if (of < 0 || of >= page_size) bad |= QKVP_DEV_BAD_OFFSET;
+        if (bad && dev_status) atomicOr(dev_status, bad);
+        slot[i] = bad ? -1 : pg * page_size + of;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&full[s]);
+    ++issued;
+    if (++s == stages) {
+      s = 0;
+      phase ^= 1;
+    }
+  }
+  if (!ok && lane == 0) {
+    // Let the copies already issued land before this CTA can exit.
+    const int64_t first = issued > stages ? issued - stages : 0;
+    for (int64_t k = first; k < issued; ++k) mbar_wait(&full[k % stages], (uint32_t)((k / stages) & 1), err);
+  }
+}
+
+// ------------------------------------------------------------- forward ----
+
+template <int HD, bool SECTIONED, bool ROPE, bool SAVE, bool POOL>
+__global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 2)
+    qkvp_fwd_stream_kernel(const FwdArgs a) {
+  using G = Geom<HD>;
+  constexpr int CPH = G::CPH, HALF = G::HALF, NCT = kStreamConsumerWarps * 32, MAXM = kStreamMaxSteps;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + StreamSmem::kBarriers);
+  uint64_t* empty = full + kMaxStages;
+  float* s_w = reinterpret_cast<float*>(smem + StreamSmem::kWeights);
+  const int tpt = a.sg.tpt, stages = a.sg.stages, steps = a.sg.steps, stage_bytes = a.sg.stage_bytes;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kStreamConsumerWarps);
+    }
+    mbar_init_fence();
+  }
+  for (int i = threadIdx.x; i < 2 * HD; i += blockDim.x) s_w[i] = i < HD ? a.w_q[i] : a.w_k[i - HD];
+  __syncthreads();
+
+  if (threadIdx.x >= NCT) {
+    const uint32_t row_bytes = (uint32_t)a.cpt * 16u;
+    const bool dense = a.sg.dense != 0;
+    stream_producer<HALF, ROPE, POOL>(
+        smem, HD, tpt, stages, stage_bytes, a.sg.n_tiles, a.T, a.pos, a.rope, a.page, a.offset, a.num_pages,
+        a.page_size, a.dev_status, a.err,
+        [&](unsigned char* dst, int64_t t0, int ntok, uint64_t* bar, uint64_t pol) {
+          mbar_expect_tx(bar, (uint32_t)ntok * row_bytes);
+          if (dense) {
+            bulk_load(dst, a.packed + t0 * a.row_stride16, (uint32_t)ntok * row_bytes, bar, pol);
+          } else {
+            for (int i = 0; i < ntok; ++i)
+              bulk_load(dst + (size_t)i * row_bytes, a.packed + (t0 + i) * a.row_stride16, row_bytes, bar, pol);
+          }
+        });
+    return;
+  }
+
+  // ---- consumers ----
+  const int ct = threadIdx.x, lane = ct & 31;
+  const int tpg = NCT / tpt;            // threads per token
+  const int tl = ct / tpg;              // token of the tile this thread works on
+  const int ig = ct - tl * tpg;         // index inside the group
+  const int e = ct & (CPH - 1);
+  const float sign = e < CPH / 2 ? -1.f : 1.f;
+  const int f0 = (e & (CPH / 2 - 1)) * 8;
+  // Per step: output head and role, fixed for the whole kernel.
+  uint32_t info[MAXM];
+#pragma unroll
+  for (int m = 0; m < MAXM; ++m) {
+    int role = kRoleV;
+    uint32_t oh = 0;
+    if (m < steps) classify<SECTIONED>((uint32_t)(ig + tpg * m) >> G::LOG_CPH, a.n_q, a.n_kv, a.group,
+                                       a.gs_magic, role, oh);
+    info[m] = oh | ((uint32_t)role << 16);
+  }
+  const int src0 = tl * a.cpt + ig;  // stage chunk of step 0
+  const unsigned char* data = smem + StreamSmem::data(HD, tpt, stages);
+
+  int s = 0;
+  uint32_t phase = 0;
+  for (int64_t tile = blockIdx.x; tile < a.sg.n_tiles; tile += gridDim.x) {
+    const bool got = mbar_wait(&full[s], phase, a.err);
+    if (!__all_sync(0xffffffffu, got)) break;
+    const int64_t t0 = tile * tpt;
+    const int64_t t = t0 + tl;
+    const bool valid = t < a.T;
+    const uint4* sx = reinterpret_cast<const uint4*>(data + (size_t)s * stage_bytes);
+    const float* tab = reinterpret_cast<const float*>(smem + StreamSmem::tables(HD) + s * StreamSmem::table_stride(HD, tpt));
+    float2 c2[4], s2[4];
+    if (ROPE) {
+      float2 sn[4];
+      load_pairs(tab + tl * HALF + f0, c2);
+      load_pairs(tab + tpt * HALF + tl * HALF + f0, sn);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s2[i] = __fmul2_rn(sn[i], f2(sign, sign));
+    }
+    int32_t slot = -1;
+    if (POOL) slot = reinterpret_cast<const int32_t*>(tab + 2 * tpt * HALF)[tl];
+    uint4* qrow = a.q + t * a.n_q * CPH;
+    uint4* krow = POOL ? a.k_pool + (int64_t)slot * a.n_kv * CPH : a.k + t * a.n_kv * CPH;
+    uint4* vrow = POOL ? a.v_pool + (int64_t)slot * a.n_kv * CPH : a.v + t * a.n_kv * CPH;
+    uint4* qprow = SAVE ? a.q_pre + t * a.n_q * CPH : nullptr;
+    uint4* kprow = SAVE ? a.k_pre + t * a.n_kv * CPH : nullptr;
+
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+      if (m >= steps) break;
+      const uint4 xr = sx[src0 + tpg * m];
+      const int role = (int)(info[m] >> 16);
+      const int oidx = (int)(info[m] & 0xffffu) * CPH + e;
+      float2 w[4], y[4];
+      load_pairs(s_w + (role == kRoleQ ? 0 : HD) + 8 * e, w);
+      chunk_forward<CPH, ROPE>(xr, w, a.eps, a.inv_head_dim, c2, s2, y);
+      if (!valid) continue;
+      if (role == kRoleQ) {
+        qrow[oidx] = pack_pairs(y);
+        if (SAVE) st_stream(qprow + oidx, xr);
+      } else if (role == kRoleK) {
+        if (!POOL || slot >= 0) krow[oidx] = pack_pairs(y);
+        if (SAVE) st_stream(kprow + oidx, xr);
+      } else {
+        if (!POOL || slot >= 0) vrow[oidx] = xr;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (++s == stages) {
+      s = 0;
+      phase ^= 1;
+    }
+  }
+}
+
+// ------------------------------------------------------------ backward ----
+
+template <int HD, bool SECTIONED, bool ROPE>
+__global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 2)
+    qkvp_bwd_stream_kernel(const BwdArgs a) {
+  using G = Geom<HD>;
+  constexpr int CPH = G::CPH, HALF = G::HALF, NCT = kStreamConsumerWarps * 32, MAXM = kStreamMaxSteps;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ float s_red[kStreamConsumerWarps][2][HD];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + StreamSmem::kBarriers);
+  uint64_t* empty = full + kMaxStages;
+  float* s_w = reinterpret_cast<float*>(smem + StreamSmem::kWeights);
+  const int tpt = a.sg.tpt, stages = a.sg.stages, steps = a.sg.steps, stage_bytes = a.sg.stage_bytes;
+  // Stage sections (16-byte chunks): dq, dk, dv, q_pre, k_pre, each [tpt][heads][CPH].
+  const int qc = a.n_q * CPH, kc = a.n_kv * CPH;
+  const int sec_dk = tpt * qc, sec_dv = sec_dk + tpt * kc, sec_qp = sec_dv + tpt * kc, sec_kp = sec_qp + tpt * qc;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kStreamConsumerWarps);
+    }
+    mbar_init_fence();
+  }
+  for (int i = threadIdx.x; i < 2 * HD; i += blockDim.x) s_w[i] = i < HD ? a.w_q[i] : a.w_k[i - HD];
+  __syncthreads();
+
+  if (threadIdx.x >= NCT) {
+    stream_producer<HALF, ROPE, false>(
+        smem, HD, tpt, stages, stage_bytes, a.sg.n_tiles, a.T, a.pos, a.rope, nullptr, nullptr, 0, 0, nullptr, a.err,
+        [&](unsigned char* dst, int64_t t0, int ntok, uint64_t* bar, uint64_t pol) {
+          const uint32_t qb = (uint32_t)qc * 16u, kb = (uint32_t)kc * 16u;
+          mbar_expect_tx(bar, (uint32_t)ntok * (2 * qb + 3 * kb));
+          uint4* d = reinterpret_cast<uint4*>(dst);
+          bulk_load(d, a.dq + t0 * qc, ntok * qb, bar, pol);
+          bulk_load(d + sec_dk, a.dk + t0 * kc, ntok * kb, bar, pol);
+          bulk_load(d + sec_dv, a.dv + t0 * kc, ntok * kb, bar, pol);
+          bulk_load(d + sec_qp, a.q_pre + t0 * qc, ntok * qb, bar, pol);
+          bulk_load(d + sec_kp, a.k_pre + t0 * kc, ntok * kb, bar, pol);
+        });
+    return;
+  }
+
+  const int ct = threadIdx.x, lane = ct & 31;
+  const int tpg = NCT / tpt;
+  const int tl = ct / tpg;
+  const int ig = ct - tl * tpg;
+  const int e = ct & (CPH - 1);
+  const float sign = e < CPH / 2 ? 1.f : -1.f;  // R(theta)^T: the partner term flips sign
+  const int f0 = (e & (CPH / 2 - 1)) * 8;
+  // Per step: stage chunk of d (low 16 bits) and of x (high 16 bits), role.
+  uint32_t offs[MAXM];
+  uint32_t roles = 0;
+#pragma unroll
+  for (int m = 0; m < MAXM; ++m) {
+    int role = kRoleV;
+    uint32_t oh = 0;
+    if (m < steps) classify<SECTIONED>((uint32_t)(ig + tpg * m) >> G::LOG_CPH, a.n_q, a.n_kv, a.group,
+                                       a.gs_magic, role, oh);
+    uint32_t d_off, x_off;
+    if (role == kRoleQ) {
+      d_off = (tl * a.n_q + oh) * CPH + e;
+      x_off = sec_qp + d_off;
+    } else if (role == kRoleK) {
+      d_off = sec_dk + (tl * a.n_kv + oh) * CPH + e;
+      x_off = sec_kp + (tl * a.n_kv + oh) * CPH + e;
+    } else {
+      d_off = sec_dv + (tl * a.n_kv + oh) * CPH + e;
+      x_off = d_off;  // unused
+    }
+    offs[m] = d_off | (x_off << 16);
+    roles |= (uint32_t)role << (2 * m);
+  }
+  const int out0 = ig;  // chunk of step 0 within the token's packed-gradient row
+  const unsigned char* data = smem + StreamSmem::data(HD, tpt, stages);
+  float2 accq[4], acck[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) accq[i] = acck[i] = f2(0.f, 0.f);
+
+  int s = 0;
+  uint32_t phase = 0;
+  for (int64_t tile = blockIdx.x; tile < a.sg.n_tiles; tile += gridDim.x) {
+    const bool got = mbar_wait(&full[s], phase, a.err);
+    if (!__all_sync(0xffffffffu, got)) break;
+    const int64_t t = tile * tpt + tl;
+    const bool valid = t < a.T;
+    const uint4* sx = reinterpret_cast<const uint4*>(data + (size_t)s * stage_bytes);
+    const float* tab = reinterpret_cast<const float*>(smem + StreamSmem::tables(HD) + s * StreamSmem::table_stride(HD, tpt));
+    float2 c2[4], s2[4];
+    if (ROPE) {
+      float2 sn[4];
+      load_pairs(tab + tl * HALF + f0, c2);
+      load_pairs(tab + tpt * HALF + tl * HALF + f0, sn);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s2[i] = __fmul2_rn(sn[i], f2(sign, sign));
+    }
+    uint4* drow = a.dpacked + t * a.row_stride16;
+
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+      if (m >= steps) break;
+      const int role = (int)((roles >> (2 * m)) & 3u);
+      const uint4 dr = sx[offs[m] & 0xffffu];
+      const uint4 xr = sx[offs[m] >> 16];
+      float2 w[4], dx[4], gx[4];
+      float r;
+      load_pairs(s_w + (role == kRoleQ ? 0 : HD) + 8 * e, w);
+      chunk_backward<CPH, ROPE>(dr, xr, w, a.eps, a.inv_head_dim, c2, s2, dx, gx, r);
+      if (!valid) continue;
+      const float rq = role == kRoleQ ? r : 0.f, rk = role == kRoleK ? r : 0.f;
+      const float2 rq2 = f2(rq, rq), rk2 = f2(rk, rk);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        accq[i] = __ffma2_rn(gx[i], rq2, accq[i]);
+        acck[i] = __ffma2_rn(gx[i], rk2, acck[i]);
+      }
+      drow[out0 + tpg * m] = role == kRoleV ? dr : pack_pairs(dx);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (++s == stages) {
+      s = 0;
+      phase ^= 1;
+    }
+  }
+
+  // Weight-grad partials: lanes of a warp with the same e, then the warps, in
+  // a fixed order (deterministic).
+  float aq[8] = {accq[0].x, accq[0].y, accq[1].x, accq[1].y, accq[2].x, accq[2].y, accq[3].x, accq[3].y};
+  float ak[8] = {acck[0].x, acck[0].y, acck[1].x, acck[1].y, acck[2].x, acck[2].y, acck[3].x, acck[3].y};
+#pragma unroll
+  for (int o = CPH; o < 32; o <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      aq[i] += __shfl_xor_sync(0xffffffffu, aq[i], o);
+      ak[i] += __shfl_xor_sync(0xffffffffu, ak[i], o);
+    }
+  }
+  const int warp = ct >> 5;
+  if (lane < CPH) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      s_red[warp][0][lane * 8 + i] = aq[i];
+      s_red[warp][1][lane * 8 + i] = ak[i];
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(NCT) : "memory");  // consumer warps only
+  for (int i = ct; i < 2 * HD; i += NCT) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kStreamConsumerWarps; ++w) sum += s_red[w][i / HD][i % HD];
+    a.partials[(int64_t)blockIdx.x * 2 * HD + i] = sum;
+  }
+}
+
+}  // namespace qkvp

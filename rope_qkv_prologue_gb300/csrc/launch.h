@@ -15,6 +15,41 @@ constexpr int kMaxBwdParts = 1024;    // cap on per-CTA weight-grad partial rows
 
 enum Role : int { kRoleQ = 0, kRoleK = 1, kRoleV = 2 };
 
+// Streaming (shared-memory staged) kernels.
+constexpr int kMaxStages = 8;            // depth of the shared-memory ring (max)
+constexpr int kStreamConsumerWarps = 8;  // + 1 producer warp per CTA
+constexpr int kStreamMaxSteps = 6;       // 16-byte chunks per consumer thread per tile (max)
+constexpr int kStreamSmemPerCta = 110 * 1024;  // dynamic shared memory budget: 2 CTAs per SM
+
+#if defined(__CUDACC__)
+#define QKVP_HD __host__ __device__
+#else
+#define QKVP_HD
+#endif
+
+// Shared-memory layout of a streaming CTA (byte offsets).
+struct StreamSmem {
+  static constexpr int kBarriers = 0;                  // uint64 full[kMaxStages], empty[kMaxStages]
+  static constexpr int kWeights = 2 * kMaxStages * 8;  // float w_q[hd], w_k[hd]
+  QKVP_HD static int tables(int hd) { return kWeights + 2 * hd * 4; }
+  // per stage: float cos[tpt][hd/2], sin[tpt][hd/2], then int32 slot[tpt]
+  QKVP_HD static int table_stride(int hd, int tpt) { return (tpt * hd * 4 + tpt * 4 + 15) & ~15; }
+  // stage data, 128-byte aligned
+  QKVP_HD static int data(int hd, int tpt, int stages) {
+    return (tables(hd) + stages * table_stride(hd, tpt) + 127) & ~127;
+  }
+};
+
+struct StreamGeom {
+  int32_t tpt;          // tokens per tile
+  int32_t stages;       // stages in the ring
+  int32_t steps;        // chunks per consumer thread per tile
+  int32_t stage_bytes;  // bytes of one stage's data
+  int64_t n_tiles;
+  int32_t dense;        // packed rows are contiguous: one bulk copy per tile
+  int32_t pad_;
+};
+
 struct RopeTable {
   uint64_t turns[kMaxHalf];  // frac(inv_freq_i / 2pi) * 2^64
 };
@@ -47,6 +82,8 @@ struct FwdArgs {
   uint4* v_pool;
   int32_t num_pages, page_size;
   int32_t* dev_status;
+  int* err;               // library device error word
+  StreamGeom sg;
   RopeTable rope;
 };
 
@@ -72,6 +109,8 @@ struct BwdArgs {
   uint4* dpacked;
   int64_t row_stride16;
   float* partials;        // [grid][2][head_dim]
+  int* err;
+  StreamGeom sg;
   RopeTable rope;
 };
 
@@ -123,6 +162,15 @@ const void* bwd_kernel(int head_dim, bool sectioned, bool rope);
 const void* dw_finalize_kernel();
 const void* latent_kernel(bool pool, bool rope, int norm_chunks_per_lane);
 const void* scatter_kernel();
+const void* fwd_stream_kernel_d64(const FwdVariant& v);
+const void* fwd_stream_kernel_d128(const FwdVariant& v);
+const void* bwd_stream_kernel(int head_dim, bool sectioned, bool rope);
+
+// Address of the library's device error word on the current device (nullptr
+// if it cannot be obtained), and its value (read and optionally cleared,
+// synchronously).
+int* device_error_word();
+int read_device_error(bool clear, int* value);
 
 // qkvp_dw_finalize_kernel arguments.
 struct FinalizeArgs {

@@ -31,7 +31,7 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     assert {"qkv_prologue_fwd", "qkv_prologue_bwd", "qkv_prologue_pool_write",
             "qkv_prologue_pool_scatter", "qkv_prologue_bwd_workspace_size",
-            "qkv_prologue_status_string", "qkv_prologue_version"} <= names
+            "qkv_prologue_status_string", "qkv_prologue_version", "qkv_prologue_device_error"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -66,7 +66,7 @@ def test_constants_match_header(lib):
     for name in ("QKVP_OK", "QKVP_ERR_NULL", "QKVP_ERR_SHAPE", "QKVP_ERR_ALIGN", "QKVP_ERR_ARCH",
                  "QKVP_ERR_WORKSPACE", "QKVP_ERR_LAUNCH", "QKVP_ERR_FLAGS", "QKVP_ERR_VALUE",
                  "QKVP_INTERLEAVED", "QKVP_SECTIONED", "QKVP_LATENT", "QKVP_NOPE", "QKVP_SAVE_PRE",
-                 "QKVP_ACCUMULATE_DW", "QKVP_DEV_BAD_PAGE", "QKVP_DEV_BAD_OFFSET"):
+                 "QKVP_ACCUMULATE_DW", "QKVP_FORCE_GENERIC", "QKVP_DEV_BAD_PAGE", "QKVP_DEV_BAD_OFFSET"):
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", src)
         assert m, name
         assert int(m.group(1)) == getattr(lib, name), name
@@ -84,6 +84,8 @@ def test_workspace_size(lib):
     assert lib.qkv_prologue_bwd_workspace_size(L, 0) == 0
     # one partial row [2, 64] fp32 per CTA, at most 1024 rows
     assert lib.qkv_prologue_bwd_workspace_size(L, 1) == 512
+    for T in range(1, 40):  # at least one row per token up to the cap
+        assert lib.qkv_prologue_bwd_workspace_size(L, T) >= 512 * T
     assert lib.qkv_prologue_bwd_workspace_size(L, 16384) == 1024 * 512
     assert lib.qkv_prologue_bwd_workspace_size(lib.layout("interleaved", 8, 3, 64), 16) == 0
     assert lib.qkv_prologue_bwd_workspace_size(lib.layout("interleaved", 32, 8, 128), 100) > 0
@@ -132,7 +134,8 @@ def test_fwd_argument_checks(lib):
     assert _fwd(C, pos=None, flags=C.QKVP_NOPE) == C.QKVP_ERR_ARCH  # NoPE needs no positions
     assert _fwd(C, flags=C.QKVP_SAVE_PRE) == C.QKVP_ERR_NULL
     assert _fwd(C, flags=C.QKVP_SAVE_PRE, q_pre=A, k_pre=A) == C.QKVP_ERR_ARCH
-    assert _fwd(C, flags=8) == C.QKVP_ERR_FLAGS
+    assert _fwd(C, flags=16) == C.QKVP_ERR_FLAGS
+    assert _fwd(C, flags=C.QKVP_FORCE_GENERIC) == C.QKVP_ERR_ARCH
     assert _fwd(C, flags=C.QKVP_ACCUMULATE_DW) == C.QKVP_ERR_FLAGS
     assert _fwd(C, packed=A + 8) == C.QKVP_ERR_ALIGN
     assert _fwd(C, k=A + 2) == C.QKVP_ERR_ALIGN

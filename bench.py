@@ -65,6 +65,21 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(values, device):
+    """Element-wise max of per-rank timings over the process group (any backend)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_gbs(bytes_per_rank_step, world, ms_per_step):
+    """Whole-job throughput: the bytes all ranks moved / the slowest rank's time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -316,13 +331,11 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     if world > 1:
-        t = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
+        elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], dev)
 
     step_bytes = ws.fwd_bytes() + ws.bwd_bytes()
     ms_per_step = elapsed_ms / K
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(step_bytes, world, ms_per_step)
     peak, peak_src = measured_peak()
     fwd_gbs = ws.fwd_bytes() / (fwd_ms * 1e-3) / 1e9
     bwd_gbs = ws.bwd_bytes() / (bwd_ms * 1e-3) / 1e9
@@ -371,7 +384,7 @@ def run_ours(args):
         },
         "clocks": clocks,
         "e2e": {
-            "value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1),
+            "value": round(whole_job_gbs(step_bytes, world, e2e_ms), 1),
             "unit": "GB/s",
             "ms_per_step": round(e2e_ms, 4),
             "steps": e2e_steps,

@@ -216,6 +216,34 @@ QKVP_API int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* 
                      size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * qkv_prologue_bwd_noalloc -- qkv_prologue_bwd without a caller workspace.
+ *
+ * The pages have no counterpart to this call: it exists for callers of this
+ * library that may not allocate device memory and have no buffer to lend,
+ * e.g. a plugin in an engine that owns all device memory through its own
+ * pool, or a latency-critical loop where cudaMalloc (which can synchronise
+ * the device) is not allowed. Same arguments, results and errors as
+ * qkv_prologue_bwd, minus the workspace: the weight-gradient partial sums go
+ * to a fixed 512 KiB array inside the library's device memory, which every
+ * GPU that loads the library holds until the process exits.
+ *  - Limit: qkv_prologue_bwd_workspace_size(layout, T) must be <= 512 KiB
+ *    (always true for head_dim 64; head_dim 128 up to 512 tokens), otherwise
+ *    QKVP_ERR_WORKSPACE is returned and nothing is enqueued.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - All calls share the array and it keeps the last call's contents (nothing
+ *    in it needs to start at zero). Calls whose work can overlap on the GPU
+ *    (different streams without ordering) race on it: order them.
+ *  - Allocates nothing (no cudaMalloc / cudaFree, no allocating library call).
+ * ------------------------------------------------------------------------- */
+QKVP_API int qkv_prologue_bwd_noalloc(const qkvp_layout* layout, int64_t T, const void* dq,
+                                      const void* dk, const void* dv, const void* q_pre,
+                                      const void* k_pre, const int32_t* pos, const float* w_q,
+                                      const float* w_k, float eps, double rope_base, uint32_t flags,
+                                      void* dpacked, float* dw_q, float* dw_k, void* stream);
+
+/* ---------------------------------------------------------------------------
  * qkv_prologue_device_error -- read (and with clear != 0, reset) the
  * library's device error word on the current device. Bit 1 means a
  * pipelined kernel's bounded wait on its shared-memory pipeline gave up

@@ -81,6 +81,8 @@ _SIGS = {
     "qkv_prologue_bwd_workspace_size": ([_LP, _i64], ctypes.c_size_t),
     "qkv_prologue_bwd": ([_LP, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _f64, _u32, _vp, _vp, _vp,
                           _vp, ctypes.c_size_t, _vp], ctypes.c_int),
+    "qkv_prologue_bwd_noalloc": ([_LP, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _f64, _u32, _vp, _vp,
+                                  _vp, _vp], ctypes.c_int),
     "qkv_prologue_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "qkv_prologue_version": ([], ctypes.c_int),
     "qkv_prologue_device_error": ([ctypes.c_int, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
@@ -178,3 +180,14 @@ def qkv_prologue_bwd(L, T, dq, dk, dv, q_pre, k_pre, pos, w_q, w_k, eps, rope_ba
                                int(flags), _ptr(dpacked), _ptr(dw_q), _ptr(dw_k), _ptr(workspace),
                                int(workspace_bytes), _stream(stream))
     return _ret(st, "qkv_prologue_bwd", check)
+
+
+def qkv_prologue_bwd_noalloc(L, T, dq, dk, dv, q_pre, k_pre, pos, w_q, w_k, eps, rope_base, flags, dpacked,
+                             dw_q, dw_k, stream=None, check=True):
+    """qkv_prologue_bwd for callers that cannot allocate: the library's own fixed
+    512 KiB device array replaces the workspace (see the C header for limits)."""
+    st = _lib.qkv_prologue_bwd_noalloc(ctypes.byref(L), int(T), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(q_pre),
+                                       _ptr(k_pre), _ptr(pos), _ptr(w_q), _ptr(w_k), float(eps),
+                                       float(rope_base), int(flags), _ptr(dpacked), _ptr(dw_q), _ptr(dw_k),
+                                       _stream(stream))
+    return _ret(st, "qkv_prologue_bwd_noalloc", check)

@@ -225,6 +225,21 @@ def test_bwd_argument_checks(lib):
     assert bwd(T=0, ws=None, wsb=0) == C.QKVP_ERR_ARCH
 
 
+@cpu_only
+def test_noalloc_backward_argument_checks(lib):
+    C = lib
+
+    def bwd(L, T, flags=0):
+        return C.qkv_prologue_bwd_noalloc(L, T, A, A, A, A, A, A, A, A, 1e-6, 5e5, flags, A, A, A, stream=0,
+                                          check=False)
+
+    # larger than the fixed 512 KiB array: refused before any device call
+    assert bwd(C.layout("interleaved", 32, 8, 128), 2048) == C.QKVP_ERR_WORKSPACE
+    assert bwd(C.layout("interleaved", 8, 3, 64), 16) == C.QKVP_ERR_SHAPE
+    assert bwd(C.layout("interleaved", 128, 16, 64), 0, C.QKVP_ACCUMULATE_DW) == C.QKVP_OK
+    assert bwd(C.layout("interleaved", 128, 16, 64), 16384) == C.QKVP_ERR_ARCH   # fits; needs the device
+
+
 def test_binding_fails_loudly_without_the_library(tmp_path):
     # a copy of the package without the .so must refuse to import
     import shutil

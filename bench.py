@@ -186,16 +186,63 @@ class ClockSampler:
 
 # ------------------------------------------------------- our workload ----
 
-class TrainStep:
-    """Device-resident buffers of the T=16384 training workload."""
+class _Step:
+    """Device buffers of one workload plus its C-ABI calls.
+
+    `calls` lists (name, fn, algorithmic bytes) in step order; `h_in` maps the
+    attribute name of each input to its host tensor (for the e2e timing) and
+    `out_names` names the outputs copied back to the host."""
+
+    kernels_per_step = 1
+
+    def _common(self, dev):
+        import torch
+
+        import rope_qkv_prologue_gb300 as C
+
+        self.C, self.dev = C, dev
+        self.stream = torch.cuda.current_stream(dev).cuda_stream
+        self.bf = dict(dtype=torch.bfloat16, device=dev)
+
+    def step(self):
+        for _, fn, _ in self.calls:
+            fn()
+
+    def step_bytes(self):
+        return sum(b for _, _, b in self.calls)
+
+    def host_mirrors(self):
+        """Pinned host copies of the inputs and room for the outputs (e2e)."""
+        import torch
+
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)  # noqa: E731
+        self.h_in_pinned = {k: pin(v).copy_(v) for k, v in self.h_in.items()}
+        self.h_out = {k: pin(getattr(self, k)) for k in self.out_names}
+        h2d = sum(t.numel() * t.element_size() for t in self.h_in_pinned.values())
+        d2h = sum(t.numel() * t.element_size() for t in self.h_out.values())
+        return h2d, d2h
+
+    def e2e_step(self):
+        for k, h in self.h_in_pinned.items():
+            getattr(self, k).copy_(h, non_blocking=True)
+        self.step()
+        for k, h in self.h_out.items():
+            h.copy_(getattr(self, k), non_blocking=True)
+
+
+class TrainStep(_Step):
+    """Training forward (with the pre-norm save) + backward, Muse Spark packing."""
+
+    kernels_per_step = 3  # forward, backward, dw finalize
 
     def __init__(self, dev, T):
         import torch
 
-        import rope_qkv_prologue_gb300 as C
         import workloads
 
-        self.C, self.T, self.dev = C, T, dev
+        self._common(dev)
+        C = self.C
+        self.T = T
         wl = workloads.train(T)
         self.wl = wl
         self.L = C.layout("interleaved", N_Q, N_KV, D)
@@ -203,7 +250,7 @@ class TrainStep:
         self.pos = wl.pos.to(dev)
         self.w_q, self.w_k = wl.w_q.to(dev), wl.w_k.to(dev)
         self.dq, self.dk, self.dv = wl.dq.to(dev), wl.dk.to(dev), wl.dv.to(dev)
-        bf = dict(dtype=torch.bfloat16, device=dev)
+        bf = self.bf
         self.q = torch.empty(T, N_Q, D, **bf)
         self.k = torch.empty(T, N_KV, D, **bf)
         self.v = torch.empty(T, N_KV, D, **bf)
@@ -214,8 +261,16 @@ class TrainStep:
         self.dw_k = torch.empty(D, dtype=torch.float32, device=dev)
         self.ws_bytes = C.qkv_prologue_bwd_workspace_size(self.L, T)
         self.ws = torch.empty(max(16, self.ws_bytes), dtype=torch.uint8, device=dev)
-        self.stream = torch.cuda.current_stream(dev).cuda_stream
         self.eps, self.base = wl.eps, wl.rope_base
+        self.calls = [("qkv_prologue_fwd (qkvp_fwd_stream_kernel, save_pre)", self.fwd,
+                       T * fwd_bytes_per_token(True) + WEIGHT_BYTES),
+                      ("qkv_prologue_bwd (qkvp_bwd_stream_kernel + dw finalize)", self.bwd,
+                       T * bwd_bytes_per_token() + 2 * WEIGHT_BYTES)]
+        self.h_in = {"packed": wl.packed_rows(), "pos": wl.pos, "w_q": wl.w_q, "w_k": wl.w_k,
+                     "dq": wl.dq, "dk": wl.dk, "dv": wl.dv}
+        self.out_names = ("q", "k", "v", "dpacked", "dw_q", "dw_k")
+        self.describe = (f"train fwd+bwd, T={T}, packed [T,16,10,64] interleaved, RoPE base 5e5, eps 1e-6, "
+                         "forward saves split pre-norm q/k")
 
     def fwd(self):
         self.C.qkv_prologue_fwd(self.L, self.T, self.packed, self.pos, self.w_q, self.w_k, self.eps, self.base,
@@ -226,35 +281,108 @@ class TrainStep:
                                 self.w_q, self.w_k, self.eps, self.base, 0, self.dpacked, self.dw_q, self.dw_k,
                                 self.ws, self.ws_bytes, self.stream)
 
-    def step(self):
-        self.fwd()
-        self.bwd()
 
-    def fwd_bytes(self):
-        return self.T * fwd_bytes_per_token(True) + WEIGHT_BYTES
+class PrefillStep(_Step):
+    """Prefill forward, contiguous q/k/v (RoPE, or NoPE)."""
 
-    def bwd_bytes(self):
-        return self.T * bwd_bytes_per_token() + 2 * WEIGHT_BYTES
-
-    def host_mirrors(self):
-        """Pinned host copies of the inputs and room for the outputs (e2e)."""
+    def __init__(self, dev, T, nope):
         import torch
 
-        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)  # noqa: E731
-        self.h_in = {"packed": self.wl.packed_rows(), "pos": self.wl.pos, "w_q": self.wl.w_q, "w_k": self.wl.w_k,
-                     "dq": self.wl.dq, "dk": self.wl.dk, "dv": self.wl.dv}
-        self.h_in = {k: pin(v).copy_(v) for k, v in self.h_in.items()}
-        self.h_out = {k: pin(getattr(self, k)) for k in ("q", "k", "v", "dpacked", "dw_q", "dw_k")}
-        h2d = sum(t.numel() * t.element_size() for t in self.h_in.values())
-        d2h = sum(t.numel() * t.element_size() for t in self.h_out.values())
-        return h2d, d2h
+        import workloads
 
-    def e2e_step(self):
-        for k, h in self.h_in.items():
-            getattr(self, k).copy_(h, non_blocking=True)
-        self.step()
-        for k, h in self.h_out.items():
-            h.copy_(getattr(self, k), non_blocking=True)
+        self._common(dev)
+        self.T, self.nope = T, nope
+        wl = workloads.prefill(T, nope=nope)
+        self.wl, self.L = wl, self.C.layout("interleaved", N_Q, N_KV, D)
+        self.packed, self.pos = wl.packed_rows().to(dev), wl.pos.to(dev)
+        self.w_q, self.w_k = wl.w_q.to(dev), wl.w_k.to(dev)
+        self.q = torch.empty(T, N_Q, D, **self.bf)
+        self.k = torch.empty(T, N_KV, D, **self.bf)
+        self.v = torch.empty(T, N_KV, D, **self.bf)
+        self.calls = [("qkv_prologue_fwd (qkvp_fwd_stream_kernel)", self.fwd,
+                       T * fwd_bytes_per_token(False) - (4 * T if nope else 0) + WEIGHT_BYTES)]
+        self.h_in = {"packed": wl.packed_rows(), "pos": wl.pos, "w_q": wl.w_q, "w_k": wl.w_k}
+        self.out_names = ("q", "k", "v")
+        self.describe = f"prefill fwd, T={T}, packed [T,16,10,64] interleaved, " + ("NoPE" if nope else "RoPE base 5e5")
+
+    def fwd(self):
+        C = self.C
+        C.qkv_prologue_fwd(self.L, self.T, self.packed, self.pos, self.w_q, self.w_k, self.wl.eps, self.wl.rope_base,
+                           C.QKVP_NOPE if self.nope else 0, self.q, self.k, self.v, None, None, self.stream)
+
+
+class DecodeStep(_Step):
+    """Decode forward with the direct paged-pool write (pools 4096 x 64 x 16 x 64)."""
+
+    def __init__(self, dev, T):
+        import torch
+
+        import workloads
+
+        self._common(dev)
+        self.T = T
+        wl = workloads.decode_pool(T)
+        self.wl, self.L = wl, self.C.layout("interleaved", N_Q, N_KV, D)
+        self.packed, self.pos = wl.packed_rows().to(dev), wl.pos.to(dev)
+        self.w_q, self.w_k = wl.w_q.to(dev), wl.w_k.to(dev)
+        self.page, self.offset = wl.page.to(dev), wl.offset.to(dev)
+        shape = (wl.num_pages, wl.page_size, N_KV, D)
+        self.k_pool = workloads.random_pool_bits(shape, 21, dev)
+        self.v_pool = workloads.random_pool_bits(shape, 22, dev)
+        self.q = torch.empty(T, N_Q, D, **self.bf)
+        self.calls = [("qkv_prologue_pool_write (qkvp_fwd_stream_kernel, pool)", self.fwd,
+                       T * (fwd_bytes_per_token(False) + 8) + WEIGHT_BYTES)]
+        self.h_in = {"packed": wl.packed_rows(), "pos": wl.pos, "w_q": wl.w_q, "w_k": wl.w_k,
+                     "page": wl.page, "offset": wl.offset}
+        self.out_names = ("q",)
+        self.describe = (f"decode fwd + direct pool write, T={T}, packed [T,16,10,64], pools 4096 pages x "
+                         "[64,16,64] bf16, positions U[0,131072), base 5e5")
+
+    def fwd(self):
+        C, wl = self.C, self.wl
+        C.qkv_prologue_pool_write(self.L, self.T, self.packed, self.pos, self.w_q, self.w_k, wl.eps, wl.rope_base, 0,
+                                  self.q, self.page, self.offset, self.k_pool, self.v_pool, wl.num_pages,
+                                  wl.page_size, None, self.stream)
+
+
+class MlaStep(_Step):
+    """MLA kv latent rows normed/roped straight into the paged pool (8192 x 64 x 576)."""
+
+    def __init__(self, dev, T):
+        import workloads
+
+        self._common(dev)
+        self.T = T
+        wl = workloads.mla(T)
+        self.wl = wl
+        self.L = self.C.layout("latent", norm_dim=512, rope_dim=64)
+        self.rows, self.pos, self.w = wl.rows.to(dev), wl.pos.to(dev), wl.w.to(dev)
+        self.page, self.offset = wl.page.to(dev), wl.offset.to(dev)
+        self.pool = workloads.random_pool_bits((wl.num_pages, wl.page_size, 576), 51, dev)
+        self.calls = [("qkv_prologue_pool_write (qkvp_latent_kernel, pool)", self.fwd,
+                       T * (1152 + 4 + 1152 + 8) + 512 * 4)]
+        self.h_in = {"rows": wl.rows, "pos": wl.pos, "w": wl.w, "page": wl.page, "offset": wl.offset}
+        self.out_names = ()
+        self.describe = (f"MLA latent rows [T,576] -> pool 8192 x [64,576], T={T}, 512 normed + 64 roped "
+                         "(base 1e4), positions U[0,393216)")
+
+    def fwd(self):
+        C, wl = self.C, self.wl
+        C.qkv_prologue_pool_write(self.L, self.T, self.rows, self.pos, None, self.w, wl.eps, wl.rope_base, 0, None,
+                                  self.page, self.offset, self.pool, None, wl.num_pages, wl.page_size, None,
+                                  self.stream)
+
+
+def make_workload(name, dev, tokens):
+    if name == "train":
+        return TrainStep(dev, tokens or 16384)
+    if name in ("prefill", "prefill_nope"):
+        return PrefillStep(dev, tokens or 16384, name == "prefill_nope")
+    if name == "decode":
+        return DecodeStep(dev, tokens or 256)
+    if name == "mla":
+        return MlaStep(dev, tokens or 32768)
+    raise ValueError(name)
 
 
 # ------------------------------------------------------------- arms ----
@@ -278,8 +406,14 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
 
-    T = args.tokens
-    ws = TrainStep(dev, T)
+    ws = make_workload(args.workload, dev, args.tokens)
+    T = ws.T
+    step_bytes = ws.step_bytes()
+    l2_bytes = props_l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    # A step that moves less than twice the L2 gets the L2 flushed before it,
+    # and only the step itself (between per-step events) is timed.
+    flush = step_bytes < 2 * l2_bytes
+    flush_buf = torch.empty(max(2 * props_l2, 1 << 28), dtype=torch.uint8, device=dev) if flush else None
     props = torch.cuda.get_device_properties(dev)
     uuid = getattr(props, "uuid", None)
     uuid = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else (str(uuid) if uuid else None)
@@ -293,29 +427,56 @@ def run_ours(args):
         dist.barrier()
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    n_calls = len(ws.calls)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_calls + 1)] for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t_wall0 = time.time()
     start.record()
     for i in range(K):
+        if flush:
+            flush_buf.zero_()
         ev[i][0].record()
-        ws.fwd()
-        ev[i][1].record()
-        ws.bwd()
-        ev[i][2].record()
+        for c, (_, fn, _) in enumerate(ws.calls):
+            fn()
+            ev[i][c + 1].record()
     end.record()
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if world > 1:
         dist.barrier()
-    elapsed_ms = start.elapsed_time(end)
-    fwd_ms = statistics.fmean(a.elapsed_time(b) for a, b, _ in ev)
-    bwd_ms = statistics.fmean(b.elapsed_time(c) for _, b, c in ev)
+    call_ms = [statistics.fmean(e[c].elapsed_time(e[c + 1]) for e in ev) for c in range(n_calls)]
+    elapsed_ms = sum(call_ms) * K if flush else start.elapsed_time(end)
     time.sleep(0.25)
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
+
+    # the same step replayed from a CUDA graph (launch overhead removed)
+    graph_ms = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cap):
+            ws.stream = cap.cuda_stream
+            ws.step()  # warm on the capture stream
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=cap):
+                ws.step()
+        ws.stream = torch.cuda.current_stream(dev).cuda_stream
+        torch.cuda.synchronize()
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(min(K, 200))]
+        for a, b in gev:
+            if flush:
+                flush_buf.zero_()
+            a.record()
+            g.replay()
+            b.record()
+        torch.cuda.synchronize()
+        graph_ms = statistics.fmean(a.elapsed_time(b) for a, b in gev)
+    except Exception as exc:  # graph capture is a measurement extra, not the product path
+        graph_ms = f"unavailable: {type(exc).__name__}: {exc}"
+        ws.stream = torch.cuda.current_stream(dev).cuda_stream
 
     # e2e: host buffers in, C-ABI calls, results back to host, every step
     h2d, d2h = ws.host_mirrors()
@@ -333,17 +494,12 @@ def run_ours(args):
     if world > 1:
         elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], dev)
 
-    step_bytes = ws.fwd_bytes() + ws.bwd_bytes()
     ms_per_step = elapsed_ms / K
     value = whole_job_gbs(step_bytes, world, ms_per_step)
     peak, peak_src = measured_peak()
-    fwd_gbs = ws.fwd_bytes() / (fwd_ms * 1e-3) / 1e9
-    bwd_gbs = ws.bwd_bytes() / (bwd_ms * 1e-3) / 1e9
-    if bwd_ms >= fwd_ms:
-        dom, dom_bytes, dom_ms, dom_key = "qkv_prologue_bwd (qkvp_bwd_kernel + dw finalize)", ws.bwd_bytes(), bwd_ms, "bwd"
-    else:
-        dom, dom_bytes, dom_ms, dom_key = "qkv_prologue_fwd (qkvp_fwd_kernel, save_pre)", ws.fwd_bytes(), fwd_ms, "fwd"
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    dom = max(range(n_calls), key=lambda c: call_ms[c])
+    dom_name, _, dom_bytes = ws.calls[dom]
+    achieved = dom_bytes / (call_ms[dom] * 1e-3) / 1e9
 
     out = {
         "metric": METRIC,
@@ -359,28 +515,30 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16 packed rows and upstream grads, U(0.5,1.5) norm weights)",
+        "data": "synthetic (seeded N(0,1) bf16 rows and upstream grads, U(0.5,1.5) norm weights)",
         "config": {
-            "workload": f"train fwd+bwd, T={T}, packed [T,16,10,64] interleaved, RoPE base 5e5, eps 1e-6, "
-                        "forward saves split pre-norm q/k",
-            "T": T, "n_q": N_Q, "n_kv": N_KV, "head_dim": D, "layout": "interleaved",
+            "workload": ws.describe,
+            "T": T, "n_q": N_Q, "n_kv": N_KV, "head_dim": D,
             "bytes_per_step": step_bytes,
-            "l2": f"no flush: inputs larger than L2 ({step_bytes / 1e9:.2f} GB of traffic per step vs 129 MB L2)",
+            "l2": (f"flushed before every step ({flush_buf.numel() >> 20} MiB write, outside the timed calls)"
+                   if flush else
+                   f"no flush: inputs larger than L2 ({step_bytes / 1e9:.2f} GB of traffic per step vs "
+                   f"{l2_bytes >> 20} MiB L2)"),
             "parallelism": f"replicas x{world} (tokens independent; no collective)",
         },
-        "kernels": {
-            "fwd_us": round(fwd_ms * 1e3, 2), "fwd_GBps": round(fwd_gbs, 1),
-            "bwd_us": round(bwd_ms * 1e3, 2), "bwd_GBps": round(bwd_gbs, 1),
-        },
+        "kernels": {name: {"us": round(call_ms[c] * 1e3, 2),
+                           "GBps": round(b / (call_ms[c] * 1e-3) / 1e9, 1)}
+                    for c, (name, _, b) in enumerate(ws.calls)},
+        "graph_replay_us_per_step": round(graph_ms * 1e3, 2) if isinstance(graph_ms, float) else graph_ms,
         "roofline": {
-            "kernel": dom,
+            "kernel": dom_name,
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback 6.8 TB/s",
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": traffic_from_profile(dom_key),
+            "traffic": traffic_from_profile(f"{args.workload}:{dom}"),
         },
         "clocks": clocks,
         "e2e": {
@@ -390,16 +548,17 @@ def run_ours(args):
             "steps": e2e_steps,
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "path": "pinned host -> device copies, qkv_prologue_fwd + qkv_prologue_bwd, device -> pinned host",
+            "path": "pinned host -> device copies of the inputs, the C-ABI calls, device -> pinned host copies "
+                    "of the outputs, every step",
         },
-        "gpu_launches": 3 * K,
-        "gpu_launches_note": "per step: qkvp_fwd_kernel, qkvp_bwd_kernel, qkvp_dw_finalize_kernel",
+        "gpu_launches": ws.kernels_per_step * K,
+        "gpu_launches_note": f"{ws.kernels_per_step} library kernel(s) per step",
         "context": {
             "pages_glue_us_train16k_two_layers_gb300": 824,
             "pages_q_norm_kernel_us_train16k": 114,
         },
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "train":
         out["cpu_baseline"] = cpu_baseline(args.cpu_tokens)
     if rank == 0:
         print(json.dumps(out), flush=True)
@@ -496,8 +655,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--tokens", type=int, default=16384,
-                    help="T of the training workload (16384 is the headline; smaller T for profiling runs)")
+    ap.add_argument("--workload", choices=["train", "prefill", "prefill_nope", "decode", "mla"], default="train",
+                    help="train (the headline) | prefill | prefill_nope | decode (pool write) | mla (latent pool write)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="T (0 = the workload's default: 16384 train/prefill, 256 decode, 32768 mla)")
     ap.add_argument("--cpu-tokens", type=int, default=6144)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -58,13 +58,36 @@ int current_device(int* sms, int* smem_per_sm = nullptr) {
   return d.status;
 }
 
+// Resident CTAs per SM for (kernel, threads, smem) on the current device,
+// queried once and cached (a launch then makes no query call).
 int blocks_per_sm(const void* kernel, int threads, size_t smem) {
+  struct Entry {
+    int dev;
+    const void* kernel;
+    int threads;
+    size_t smem;
+    int blocks;
+  };
+  static std::mutex mu;
+  static Entry cache[512];
+  static int n_cached = 0;
+  int dev = -1;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_cached; ++i)
+      if (cache[i].dev == dev && cache[i].kernel == kernel && cache[i].threads == threads && cache[i].smem == smem)
+        return cache[i].blocks;
+  }
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) {
     cudaGetLastError();
     return 1;
   }
-  return n > 0 ? n : 1;
+  n = n > 0 ? n : 1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (n_cached < 512) cache[n_cached++] = Entry{dev, kernel, threads, smem, n};
+  return n;
 }
 
 // Opt a kernel in to `smem` bytes of dynamic shared memory (once per device
@@ -93,14 +116,14 @@ bool allow_smem(const void* kernel, size_t smem) {
 }
 
 // Tile geometry of the streaming kernels, or false when the layout does not
-// fit them: the 256 consumer threads must split a token row into groups of
+// fit them: the consumer threads must split a token row into groups of
 // tpg threads that each take exactly `steps` chunks (steps <= kStreamMaxSteps),
-// and two CTAs with at least two stages each must fit in one SM's shared
-// memory. token_bytes = bytes staged per token.
-bool stream_geometry(int cpt, int cph, int hd, int64_t T, int64_t token_bytes, int smem_per_sm,
-                     int static_smem, StreamGeom* g, size_t* smem) {
-  const int nct = kStreamConsumerWarps * 32;
-  const int budget = smem_per_sm / 2 - 1024 - static_smem;
+// and shape.ctas_per_sm CTAs with at least two stages each must fit in one
+// SM's shared memory. token_bytes = bytes staged per token.
+bool stream_geometry(const StreamShape& shape, int cpt, int cph, int hd, int64_t T, int64_t token_bytes,
+                     int smem_per_sm, int static_smem, StreamGeom* g, size_t* smem) {
+  const int nct = shape.warps * 32;
+  const int budget = smem_per_sm / shape.ctas_per_sm - 1024 - static_smem;
   for (int tpg = nct; tpg >= cph; tpg /= 2) {
     if (cpt % tpg != 0) continue;
     const int steps = cpt / tpg;
@@ -327,12 +350,13 @@ static int gqa_forward(const qkvp_layout* L, int64_t T, const void* packed, cons
   const FwdVariant var{L->head_dim, L->kind == QKVP_SECTIONED, rope, save, pool};
   size_t smem = 0;
   if (!(flags & QKVP_FORCE_GENERIC) &&
-      stream_geometry(a.cpt, L->head_dim / 8, L->head_dim, T, (int64_t)a.cpt * 16, smem_per_sm, 0, &a.sg, &smem) &&
+      stream_geometry(fwd_stream_shape(save), a.cpt, L->head_dim / 8, L->head_dim, T, (int64_t)a.cpt * 16,
+                      smem_per_sm, 0, &a.sg, &smem) &&
       (a.err = device_error_word()) != nullptr) {
     a.sg.dense = g.stride == g.row;
     const void* kern = L->head_dim == 64 ? fwd_stream_kernel_d64(var) : fwd_stream_kernel_d128(var);
     if (allow_smem(kern, smem)) {
-      const int threads = (kStreamConsumerWarps + 1) * 32;
+      const int threads = (fwd_stream_shape(save).warps + 1) * 32;
       const int64_t cap = (int64_t)sms * blocks_per_sm(kern, threads, smem);
       return launch(kern, a.sg.n_tiles < cap ? a.sg.n_tiles : cap, threads, smem, stream, &a);
     }
@@ -548,17 +572,18 @@ int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const
   const bool sectioned = layout->kind == QKVP_SECTIONED;
   const int hd = layout->head_dim;
   const int64_t token_bytes = (int64_t)(2 * layout->n_q + 3 * layout->n_kv) * hd * 2;
-  const int static_smem = kStreamConsumerWarps * 2 * hd * (int)sizeof(float);
+  const StreamShape shape = bwd_stream_shape();
+  const int static_smem = shape.warps * 2 * hd * (int)sizeof(float);
   size_t smem = 0;
   int64_t grid = 0;
   bool streamed = false;
   if (!(flags & QKVP_FORCE_GENERIC) &&
-      stream_geometry(a.cpt, hd / 8, hd, T, token_bytes, smem_per_sm, static_smem, &a.sg, &smem) &&
+      stream_geometry(shape, a.cpt, hd / 8, hd, T, token_bytes, smem_per_sm, static_smem, &a.sg, &smem) &&
       (a.err = device_error_word()) != nullptr) {
     a.sg.dense = 1;
     const void* kern = bwd_stream_kernel(hd, sectioned, rope);
     if (allow_smem(kern, smem)) {
-      const int threads = (kStreamConsumerWarps + 1) * 32;
+      const int threads = (shape.warps + 1) * 32;
       grid = (int64_t)sms * blocks_per_sm(kern, threads, smem);
       if (grid > a.sg.n_tiles) grid = a.sg.n_tiles;
       if (grid > kMaxBwdParts) grid = kMaxBwdParts;

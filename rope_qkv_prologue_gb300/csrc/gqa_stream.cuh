@@ -1,7 +1,7 @@
 // Streaming (shared-memory staged) forward and backward kernels of the
 // packed-QKV prologue: the fast path for the common head layouts.
 //
-// Pipeline. A persistent CTA = kStreamConsumerWarps consumer warps + 1
+// Pipeline. A persistent CTA = NCW consumer warps + 1
 // producer warp. The batch is cut into tiles of `tpt` consecutive tokens; CTA b
 // takes tiles b, b + grid, ... The producer warp waits for a free stage of the
 // shared-memory ring, issues bulk copies of the tile's source rows into it
@@ -11,8 +11,8 @@
 // Consumers wait on "full", compute from shared memory, store results straight
 // to HBM with 16-byte stores, and arrive on the stage's "empty" mbarrier.
 //
-// Work mapping. The 256 consumer threads are split into tpt groups of
-// tpg = 256 / tpt threads; group g owns token g of every tile, and thread i of
+// Work mapping. The consumer threads (256 by default) are split into tpt groups of
+// tpg = consumers / tpt threads; group g owns token g of every tile, and thread i of
 // a group owns the 16-byte chunks j = i + tpg * m (m < steps) of that token's
 // row, where steps = cpt / tpg exactly (the host only picks this path when
 // that division is exact). So across all tiles a thread always sees the same
@@ -32,6 +32,30 @@
 #include "qkv_prologue.h"
 
 namespace qkvp {
+
+// Norm weights in shared memory, laid out so that the CPH lanes of a head read
+// them without bank conflicts: for role r (q, k), half h of a lane's 8 values
+// and lane position e, the 4 floats w_r[8e + 4h .. 8e + 4h + 3] sit at
+// r * HD + h * 4 * CPH + 4 * e. One 16-byte read per lane and half then covers
+// 8 consecutive 16-byte words across the head's lanes.
+template <int HD>
+__device__ __forceinline__ void fill_split_weights(const float* w_q, const float* w_k, float* s_w) {
+  constexpr int CPH = HD / 8;
+  for (int i = threadIdx.x; i < 2 * HD; i += blockDim.x) {
+    const int r = i / HD, rem = i % HD;
+    const int h = rem / (4 * CPH), e = (rem % (4 * CPH)) / 4, k = rem % 4;
+    s_w[i] = (r == 0 ? w_q : w_k)[8 * e + 4 * h + k];
+  }
+}
+
+template <int HD>
+__device__ __forceinline__ void load_split_weights(const float* s_w, int role, int e, float2 (&w)[4]) {
+  constexpr int CPH = HD / 8;
+  const float* p = s_w + (role == kRoleQ ? 0 : HD) + 4 * e;
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4 * CPH);
+  w[0] = f2(a.x, a.y); w[1] = f2(a.z, a.w); w[2] = f2(b.x, b.y); w[3] = f2(b.z, b.w);
+}
 
 // The producer warp of a streaming CTA: fills stages, writes tables, and (on a
 // wait that timed out) drains the copies it issued before returning.
@@ -102,11 +126,10 @@ __device__ __forceinline__ void stream_producer(unsigned char* smem, int hd, int
 
 // ------------------------------------------------------------- forward ----
 
-template <int HD, bool SECTIONED, bool ROPE, bool SAVE, bool POOL>
-__global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 2)
-    qkvp_fwd_stream_kernel(const FwdArgs a) {
+template <int HD, bool SECTIONED, bool ROPE, bool SAVE, bool POOL, int NCW, int CPS>
+__global__ void __launch_bounds__((NCW + 1) * 32, CPS) qkvp_fwd_stream_kernel(const FwdArgs a) {
   using G = Geom<HD>;
-  constexpr int CPH = G::CPH, HALF = G::HALF, NCT = kStreamConsumerWarps * 32, MAXM = kStreamMaxSteps;
+  constexpr int CPH = G::CPH, HALF = G::HALF, NCT = NCW * 32, MAXM = kStreamMaxSteps;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + StreamSmem::kBarriers);
   uint64_t* empty = full + kMaxStages;
@@ -116,11 +139,11 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kStreamConsumerWarps);
+      mbar_init(&empty[s], NCW);
     }
     mbar_init_fence();
   }
-  for (int i = threadIdx.x; i < 2 * HD; i += blockDim.x) s_w[i] = i < HD ? a.w_q[i] : a.w_k[i - HD];
+  fill_split_weights<HD>(a.w_q, a.w_k, s_w);
   __syncthreads();
 
   if (threadIdx.x >= NCT) {
@@ -195,7 +218,7 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 2)
       const int role = (int)(info[m] >> 16);
       const int oidx = (int)(info[m] & 0xffffu) * CPH + e;
       float2 w[4], y[4];
-      load_pairs(s_w + (role == kRoleQ ? 0 : HD) + 8 * e, w);
+      load_split_weights<HD>(s_w, role, e, w);
       chunk_forward<CPH, ROPE>(xr, w, a.eps, a.inv_head_dim, c2, s2, y);
       if (!valid) continue;
       if (role == kRoleQ) {
@@ -219,13 +242,12 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 2)
 
 // ------------------------------------------------------------ backward ----
 
-template <int HD, bool SECTIONED, bool ROPE>
-__global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 2)
-    qkvp_bwd_stream_kernel(const BwdArgs a) {
+template <int HD, bool SECTIONED, bool ROPE, int NCW, int CPS>
+__global__ void __launch_bounds__((NCW + 1) * 32, CPS) qkvp_bwd_stream_kernel(const BwdArgs a) {
   using G = Geom<HD>;
-  constexpr int CPH = G::CPH, HALF = G::HALF, NCT = kStreamConsumerWarps * 32, MAXM = kStreamMaxSteps;
+  constexpr int CPH = G::CPH, HALF = G::HALF, NCT = NCW * 32, MAXM = kStreamMaxSteps;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ float s_red[kStreamConsumerWarps][2][HD];
+  __shared__ float s_red[NCW][2][HD];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + StreamSmem::kBarriers);
   uint64_t* empty = full + kMaxStages;
   float* s_w = reinterpret_cast<float*>(smem + StreamSmem::kWeights);
@@ -237,11 +259,11 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kStreamConsumerWarps);
+      mbar_init(&empty[s], NCW);
     }
     mbar_init_fence();
   }
-  for (int i = threadIdx.x; i < 2 * HD; i += blockDim.x) s_w[i] = i < HD ? a.w_q[i] : a.w_k[i - HD];
+  fill_split_weights<HD>(a.w_q, a.w_k, s_w);
   __syncthreads();
 
   if (threadIdx.x >= NCT) {
@@ -323,7 +345,7 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 2)
       const uint4 xr = sx[offs[m] >> 16];
       float2 w[4], dx[4], gx[4];
       float r;
-      load_pairs(s_w + (role == kRoleQ ? 0 : HD) + 8 * e, w);
+      load_split_weights<HD>(s_w, role, e, w);
       chunk_backward<CPH, ROPE>(dr, xr, w, a.eps, a.inv_head_dim, c2, s2, dx, gx, r);
       if (!valid) continue;
       const float rq = role == kRoleQ ? r : 0.f, rk = role == kRoleK ? r : 0.f;
@@ -367,7 +389,7 @@ __global__ void __launch_bounds__((kStreamConsumerWarps + 1) * 32, 2)
   for (int i = ct; i < 2 * HD; i += NCT) {
     float sum = 0.f;
 #pragma unroll
-    for (int w = 0; w < kStreamConsumerWarps; ++w) sum += s_red[w][i / HD][i % HD];
+    for (int w = 0; w < NCW; ++w) sum += s_red[w][i / HD][i % HD];
     a.partials[(int64_t)blockIdx.x * 2 * HD + i] = sum;
   }
 }

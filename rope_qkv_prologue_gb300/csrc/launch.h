@@ -16,10 +16,20 @@ constexpr int kMaxBwdParts = 1024;    // cap on per-CTA weight-grad partial rows
 enum Role : int { kRoleQ = 0, kRoleK = 1, kRoleV = 2 };
 
 // Streaming (shared-memory staged) kernels.
-constexpr int kMaxStages = 8;            // depth of the shared-memory ring (max)
-constexpr int kStreamConsumerWarps = 8;  // + 1 producer warp per CTA
+// Shape of the pipelined kernels: consumer warps per CTA (+1 producer warp)
+// and the CTAs per SM the shared-memory budget is cut for. Measured on GB300
+// (T = 16384, Muse Spark packing): the forward with the pre-norm save runs best
+// as one CTA of 8 consumer warps per SM with a deep ring; the plain forward
+// (and pool write) with 16 consumer warps per SM in one CTA; the backward as
+// two CTAs of 8 consumer warps per SM.
+struct StreamShape {
+  int warps;
+  int ctas_per_sm;
+};
+constexpr StreamShape fwd_stream_shape(bool save_pre) { return save_pre ? StreamShape{8, 1} : StreamShape{16, 1}; }
+constexpr StreamShape bwd_stream_shape() { return StreamShape{8, 2}; }
+constexpr int kMaxStages = 8;  // depth of the shared-memory ring (max)
 constexpr int kStreamMaxSteps = 6;       // 16-byte chunks per consumer thread per tile (max)
-constexpr int kStreamSmemPerCta = 110 * 1024;  // dynamic shared memory budget: 2 CTAs per SM
 
 #if defined(__CUDACC__)
 #define QKVP_HD __host__ __device__

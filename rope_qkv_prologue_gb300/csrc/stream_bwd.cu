@@ -11,7 +11,8 @@ __device__ int g_qkvp_device_error = 0;
 namespace {
 template <int HD, bool S, bool R>
 const void* ptr() {
-  return reinterpret_cast<const void*>(&qkvp_bwd_stream_kernel<HD, S, R>);
+  constexpr StreamShape sh = bwd_stream_shape();
+  return reinterpret_cast<const void*>(&qkvp_bwd_stream_kernel<HD, S, R, sh.warps, sh.ctas_per_sm>);
 }
 template <int HD>
 const void* pick(bool sectioned, bool rope) {

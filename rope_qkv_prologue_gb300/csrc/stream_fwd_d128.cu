@@ -6,7 +6,8 @@ namespace qkvp {
 namespace {
 template <bool S, bool R, bool SV, bool P>
 const void* ptr() {
-  return reinterpret_cast<const void*>(&qkvp_fwd_stream_kernel<128, S, R, SV, P>);
+  constexpr StreamShape sh = fwd_stream_shape(SV);
+  return reinterpret_cast<const void*>(&qkvp_fwd_stream_kernel<128, S, R, SV, P, sh.warps, sh.ctas_per_sm>);
 }
 template <bool S, bool R>
 const void* pick(const FwdVariant& v) {

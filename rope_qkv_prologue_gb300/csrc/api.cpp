@@ -3,6 +3,7 @@
 // or synchronises; every launch goes to the caller's stream.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -59,7 +60,9 @@ int current_device(int* sms, int* smem_per_sm = nullptr) {
 }
 
 // Resident CTAs per SM for (kernel, threads, smem) on the current device,
-// queried once and cached (a launch then makes no query call).
+// queried once and cached (a launch then makes no query call). 0 means the
+// kernel cannot be launched with these resources; callers then take another
+// kernel.
 int blocks_per_sm(const void* kernel, int threads, size_t smem) {
   struct Entry {
     int dev;
@@ -82,9 +85,8 @@ int blocks_per_sm(const void* kernel, int threads, size_t smem) {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) {
     cudaGetLastError();
-    return 1;
+    n = 0;
   }
-  n = n > 0 ? n : 1;
   std::lock_guard<std::mutex> lock(mu);
   if (n_cached < 512) cache[n_cached++] = Entry{dev, kernel, threads, smem, n};
   return n;
@@ -116,19 +118,22 @@ bool allow_smem(const void* kernel, size_t smem) {
 }
 
 // Tile geometry of the streaming kernels, or false when the layout does not
-// fit them: the consumer threads must split a token row into groups of
-// tpg threads that each take exactly `steps` chunks (steps <= kStreamMaxSteps),
-// and shape.ctas_per_sm CTAs with at least two stages each must fit in one
-// SM's shared memory. token_bytes = bytes staged per token.
-bool stream_geometry(const StreamShape& shape, int cpt, int cph, int hd, int64_t T, int64_t token_bytes,
+// fit them. A tile holds tpt tokens; each token's upt units (chunk pairs) are
+// split over tpg = consumers / tpt threads taking steps = ceil(upt / tpg)
+// units each (steps <= kStreamMaxSteps); lph = lanes per head. The smallest tpt whose last step is at least
+// kMinStepFill full is taken, so a tile stays small and the ring deep; at
+// least two stages per CTA must fit in the shared memory left to each of the
+// shape.ctas_per_sm CTAs of an SM. token_bytes = bytes staged per token.
+bool stream_geometry(const StreamShape& shape, int upt, int lph, int hd, int64_t T, int64_t token_bytes,
                      int smem_per_sm, int static_smem, StreamGeom* g, size_t* smem) {
+  constexpr double kMinStepFill = 0.8;  // useful chunks / (steps * tpg)
   const int nct = shape.warps * 32;
   const int budget = smem_per_sm / shape.ctas_per_sm - 1024 - static_smem;
-  for (int tpg = nct; tpg >= cph; tpg /= 2) {
-    if (cpt % tpg != 0) continue;
-    const int steps = cpt / tpg;
-    if (steps > kStreamMaxSteps) return false;
-    const int tpt = nct / tpg;
+  for (int tpt = 1; nct / tpt >= lph && (nct / tpt) % lph == 0; tpt *= 2) {
+    const int tpg = nct / tpt;
+    const int steps = (upt + tpg - 1) / tpg;
+    if (steps > kStreamMaxSteps) return false;  // larger tiles only add steps
+    if ((double)upt / ((double)steps * tpg) < kMinStepFill) continue;
     const int64_t stage = (int64_t)tpt * token_bytes;
     const int fixed = StreamSmem::tables(hd) + 128;
     const int64_t per_stage = stage + StreamSmem::table_stride(hd, tpt);
@@ -350,20 +355,21 @@ static int gqa_forward(const qkvp_layout* L, int64_t T, const void* packed, cons
   const FwdVariant var{L->head_dim, L->kind == QKVP_SECTIONED, rope, save, pool};
   size_t smem = 0;
   if (!(flags & QKVP_FORCE_GENERIC) &&
-      stream_geometry(fwd_stream_shape(save), a.cpt, L->head_dim / 8, L->head_dim, T, (int64_t)a.cpt * 16,
+      stream_geometry(fwd_stream_shape(save), a.cpt / 2, L->head_dim / 16, L->head_dim, T, (int64_t)a.cpt * 16,
                       smem_per_sm, 0, &a.sg, &smem) &&
       (a.err = device_error_word()) != nullptr) {
     a.sg.dense = g.stride == g.row;
     const void* kern = L->head_dim == 64 ? fwd_stream_kernel_d64(var) : fwd_stream_kernel_d128(var);
-    if (allow_smem(kern, smem)) {
-      const int threads = (fwd_stream_shape(save).warps + 1) * 32;
-      const int64_t cap = (int64_t)sms * blocks_per_sm(kern, threads, smem);
+    const int threads = (fwd_stream_shape(save).warps + 1) * 32;
+    const int bps = allow_smem(kern, smem) ? blocks_per_sm(kern, threads, smem) : 0;
+    if (bps > 0) {
+      const int64_t cap = (int64_t)sms * bps;
       return launch(kern, a.sg.n_tiles < cap ? a.sg.n_tiles : cap, threads, smem, stream, &a);
     }
   }
   const void* kern = L->head_dim == 64 ? fwd_kernel_d64(var) : fwd_kernel_d128(var);
   smem = (size_t)a.max_tok * (L->head_dim / 2) * 2 * sizeof(float) + (size_t)a.max_tok * sizeof(int32_t);
-  const int64_t cap = (int64_t)sms * blocks_per_sm(kern, kThreads, smem);
+  const int64_t cap = (int64_t)sms * std::max(1, blocks_per_sm(kern, kThreads, smem));
   const int64_t grid = a.n_items < cap ? a.n_items : cap;
   return launch(kern, grid, kThreads, smem, stream, &a);
 }
@@ -418,7 +424,7 @@ static int latent_forward(const qkvp_layout* L, int64_t T, const void* rows, con
   const int threads = kLatentWarps * 32;
   const int64_t per_cta = (int64_t)kLatentWarps * kLatentTokensPerWarp;
   const int64_t need = (T + per_cta - 1) / per_cta;
-  const int64_t cap = (int64_t)sms * blocks_per_sm(kern, threads, 0);
+  const int64_t cap = (int64_t)sms * std::max(1, blocks_per_sm(kern, threads, 0));
   return launch(kern, need < cap ? need : cap, threads, 0, stream, &a);
 }
 
@@ -491,7 +497,7 @@ int qkv_prologue_pool_scatter(const qkvp_layout* layout, int64_t T, const void* 
   a.dev_status = dev_status;
   const void* kern = scatter_kernel();
   const int64_t need = (T * a.row_chunks + 255) / 256;
-  const int64_t cap = (int64_t)sms * blocks_per_sm(kern, 256, 0);
+  const int64_t cap = (int64_t)sms * std::max(1, blocks_per_sm(kern, 256, 0));
   return launch(kern, need < cap ? need : cap, 256, 0, static_cast<cudaStream_t>(stream), &a);
 }
 
@@ -578,13 +584,14 @@ int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const
   int64_t grid = 0;
   bool streamed = false;
   if (!(flags & QKVP_FORCE_GENERIC) &&
-      stream_geometry(shape, a.cpt, hd / 8, hd, T, token_bytes, smem_per_sm, static_smem, &a.sg, &smem) &&
+      stream_geometry(shape, a.cpt / 2, hd / 16, hd, T, token_bytes, smem_per_sm, static_smem, &a.sg, &smem) &&
       (a.err = device_error_word()) != nullptr) {
     a.sg.dense = 1;
     const void* kern = bwd_stream_kernel(hd, sectioned, rope);
-    if (allow_smem(kern, smem)) {
-      const int threads = (shape.warps + 1) * 32;
-      grid = (int64_t)sms * blocks_per_sm(kern, threads, smem);
+    const int threads = (shape.warps + 1) * 32;
+    const int bps = allow_smem(kern, smem) ? blocks_per_sm(kern, threads, smem) : 0;
+    if (bps > 0) {
+      grid = (int64_t)sms * bps;
       if (grid > a.sg.n_tiles) grid = a.sg.n_tiles;
       if (grid > kMaxBwdParts) grid = kMaxBwdParts;
       QKVP_TRY(launch(kern, grid, threads, smem, s, &a));
@@ -594,7 +601,7 @@ int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const
   if (!streamed) {
     const void* kern = bwd_kernel(hd, sectioned, rope);
     smem = (size_t)a.max_tok * (hd / 2) * 2 * sizeof(float);
-    grid = (int64_t)sms * blocks_per_sm(kern, kThreads, smem);
+    grid = (int64_t)sms * std::max(1, blocks_per_sm(kern, kThreads, smem));
     if (grid > a.n_items) grid = a.n_items;
     if (grid > kMaxBwdParts) grid = kMaxBwdParts;
     QKVP_TRY(launch(kern, grid, kThreads, smem, s, &a));

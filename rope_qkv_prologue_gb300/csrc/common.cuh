@@ -154,6 +154,129 @@ __device__ __forceinline__ void chunk_backward(const uint4& dr, const uint4& xr,
   r_out = r;
 }
 
+// ---------------------------------------------- pair-per-lane variants ----
+//
+// The same arithmetic with a different lane layout: one lane holds chunk e of
+// a head ("lo", values 8e .. 8e+7) and its rotate-half partner chunk e + CPH/2
+// ("hi"), so CPH/2 lanes share a head. The sum of squares is added in exactly
+// the tree order of head_sum_sq (xor rounds 1, 2, .. inside each half, then
+// lo + hi), and the rotation uses the same operations on the same operands,
+// so results are bit-identical to chunk_forward / chunk_backward.
+
+__device__ __forceinline__ float chunk_partial_sq(const float2 (&x)[4]) {
+  float2 a = __fmul2_rn(x[0], x[0]);
+  a = __ffma2_rn(x[1], x[1], a);
+  a = __ffma2_rn(x[2], x[2], a);
+  a = __ffma2_rn(x[3], x[3], a);
+  return a.x + a.y;
+}
+
+// Sum over the head of per-chunk partials p_lo, p_hi held by the CPH/2 lanes.
+template <int CPH>
+__device__ __forceinline__ float pair_head_sum(float lo, float hi) {
+#pragma unroll
+  for (int o = 1; o < CPH / 2; o <<= 1) {
+    lo += __shfl_xor_sync(0xffffffffu, lo, o);
+    hi += __shfl_xor_sync(0xffffffffu, hi, o);
+  }
+  return lo + hi;
+}
+
+// Forward of a chunk pair: y = x * r * w, then o_lo = y_lo cos - y_hi sin,
+// o_hi = y_hi cos + y_lo sin (c, sn: cos and sin of the lane's 8 frequencies).
+template <int CPH, bool ROPE>
+__device__ __forceinline__ void pair_forward(const uint4& xlo, const uint4& xhi, const float2 (&wlo)[4],
+                                             const float2 (&whi)[4], float eps, float inv_hd, const float2 (&c)[4],
+                                             const float2 (&sn)[4], float2 (&ylo)[4], float2 (&yhi)[4]) {
+  float2 lo[4], hi[4];
+  unpack_pairs(xlo, lo);
+  unpack_pairs(xhi, hi);
+  const float ss = pair_head_sum<CPH>(chunk_partial_sq(lo), chunk_partial_sq(hi));
+  const float r = rsqrtf(fmaf(ss, inv_hd, eps));
+  const float2 rr = f2(r, r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    ylo[i] = __fmul2_rn(__fmul2_rn(lo[i], rr), wlo[i]);
+    yhi[i] = __fmul2_rn(__fmul2_rn(hi[i], rr), whi[i]);
+  }
+  if (ROPE) {
+    const float2 neg = f2(-1.f, -1.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 ns = __fmul2_rn(sn[i], neg);
+      const float2 a = __ffma2_rn(ylo[i], c[i], __fmul2_rn(yhi[i], ns));
+      const float2 b = __ffma2_rn(yhi[i], c[i], __fmul2_rn(ylo[i], sn[i]));
+      ylo[i] = a;
+      yhi[i] = b;
+    }
+  }
+}
+
+// Backward of a chunk pair (see chunk_backward): g_lo = d_lo cos + d_hi sin,
+// g_hi = d_hi cos - d_lo sin, then the RMSNorm backward with the head's r.
+template <int CPH, bool ROPE>
+__device__ __forceinline__ void pair_backward(const uint4& dlo_r, const uint4& dhi_r, const uint4& xlo_r,
+                                              const uint4& xhi_r, const float2 (&wlo)[4], const float2 (&whi)[4],
+                                              float eps, float inv_hd, const float2 (&c)[4], const float2 (&sn)[4],
+                                              float2 (&dxlo)[4], float2 (&dxhi)[4], float2 (&gxlo)[4],
+                                              float2 (&gxhi)[4], float& r_out) {
+  float2 dlo[4], dhi[4], xlo[4], xhi[4], glo[4], ghi[4];
+  unpack_pairs(dlo_r, dlo);
+  unpack_pairs(dhi_r, dhi);
+  unpack_pairs(xlo_r, xlo);
+  unpack_pairs(xhi_r, xhi);
+  if (ROPE) {
+    const float2 neg = f2(-1.f, -1.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 ns = __fmul2_rn(sn[i], neg);
+      glo[i] = __ffma2_rn(dlo[i], c[i], __fmul2_rn(dhi[i], sn[i]));
+      ghi[i] = __ffma2_rn(dhi[i], c[i], __fmul2_rn(dlo[i], ns));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      glo[i] = dlo[i];
+      ghi[i] = dhi[i];
+    }
+  }
+  float2 wglo[4], wghi[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    wglo[i] = __fmul2_rn(wlo[i], glo[i]);
+    wghi[i] = __fmul2_rn(whi[i], ghi[i]);
+  }
+  float2 sql = __fmul2_rn(xlo[0], xlo[0]), sqh = __fmul2_rn(xhi[0], xhi[0]);
+  float2 dtl = __fmul2_rn(xlo[0], wglo[0]), dth = __fmul2_rn(xhi[0], wghi[0]);
+#pragma unroll
+  for (int i = 1; i < 4; ++i) {
+    sql = __ffma2_rn(xlo[i], xlo[i], sql);
+    sqh = __ffma2_rn(xhi[i], xhi[i], sqh);
+    dtl = __ffma2_rn(xlo[i], wglo[i], dtl);
+    dth = __ffma2_rn(xhi[i], wghi[i], dth);
+  }
+  float sl = sql.x + sql.y, sh = sqh.x + sqh.y, ql = dtl.x + dtl.y, qh = dth.x + dth.y;
+#pragma unroll
+  for (int o = 1; o < CPH / 2; o <<= 1) {
+    sl += __shfl_xor_sync(0xffffffffu, sl, o);
+    sh += __shfl_xor_sync(0xffffffffu, sh, o);
+    ql += __shfl_xor_sync(0xffffffffu, ql, o);
+    qh += __shfl_xor_sync(0xffffffffu, qh, o);
+  }
+  const float ss = sl + sh, dot = ql + qh;
+  const float r = rsqrtf(fmaf(ss, inv_hd, eps));
+  const float kx = r * r * r * dot * inv_hd;
+  const float2 rr = f2(r, r), nk = f2(-kx, -kx);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    dxlo[i] = __ffma2_rn(xlo[i], nk, __fmul2_rn(rr, wglo[i]));
+    dxhi[i] = __ffma2_rn(xhi[i], nk, __fmul2_rn(rr, wghi[i]));
+    gxlo[i] = __fmul2_rn(glo[i], xlo[i]);
+    gxhi[i] = __fmul2_rn(ghi[i], xhi[i]);
+  }
+  r_out = r;
+}
+
 // ---------------------------------------------------------- division ----
 
 // n / d for n < 2^16 and 2 <= d <= 2^16 with m = floor(2^32 / d) + 1:

@@ -11,16 +11,18 @@
 // Consumers wait on "full", compute from shared memory, store results straight
 // to HBM with 16-byte stores, and arrive on the stage's "empty" mbarrier.
 //
-// Work mapping. The consumer threads (256 by default) are split into tpt groups of
-// tpg = consumers / tpt threads; group g owns token g of every tile, and thread i of
-// a group owns the 16-byte chunks j = i + tpg * m (m < steps) of that token's
-// row, where steps = cpt / tpg exactly (the host only picks this path when
-// that division is exact). So across all tiles a thread always sees the same
-// head positions: their role (q / k / v), output head and weight row are
-// worked out once, before the tile loop, and it needs the cos/sin of one
-// token per tile (loaded once per tile, reused for every step). A head of
-// head_dim values is CPH consecutive chunks held by CPH consecutive lanes, so
-// RMSNorm sums and the rotate-half partner exchange stay xor-shuffles.
+// Work mapping. A token row of cpt 16-byte chunks is cut into cpt / 2 units:
+// unit (h, e) = chunk e of head h together with its rotate-half partner chunk
+// e + CPH/2, so the rotation needs no data from other lanes and a head is
+// spread over CPH/2 lanes (its RMSNorm sum: two xor-shuffle rounds for
+// head_dim 64). The consumer threads are split into tpt groups of tpg =
+// consumers / tpt threads; group g owns token g of every tile, and thread i of
+// a group owns units j = i + tpg * m (m < steps, j < cpt / 2), steps =
+// ceil(cpt / 2 / tpg) (the last step may cover only part of the group; the
+// host keeps that waste small). So across all tiles a thread always sees the
+// same head positions: their role (q / k / v), output head and weight rows
+// are worked out once, before the tile loop, and it needs the cos/sin of one
+// token per tile (loaded once per tile, reused for every step).
 // Element-wise float math uses Blackwell's paired fp32 instructions
 // (__ffma2_rn / __fmul2_rn: two IEEE float operations per instruction, each
 // rounded exactly like the scalar one).
@@ -55,6 +57,17 @@ __device__ __forceinline__ void load_split_weights(const float* s_w, int role, i
   const float4 a = *reinterpret_cast<const float4*>(p);
   const float4 b = *reinterpret_cast<const float4*>(p + 4 * CPH);
   w[0] = f2(a.x, a.y); w[1] = f2(a.z, a.w); w[2] = f2(b.x, b.y); w[3] = f2(b.z, b.w);
+}
+
+// Register cap of a streaming kernel: as many registers per thread as let
+// CPS CTAs of NCW + 1 warps stay resident on an SM. The register file is
+// split over the SM's 4 schedulers (16384 registers each) and a warp lives on
+// one of them, so the cap is 16384 / (ceil(warps / 4) * 32), in steps of 8,
+// at most 255. Without it the compiler can stop short of the budget and spill
+// inside the tile loop.
+constexpr int stream_max_regs_raw(int ncw, int cps) { return 16384 / (((cps * (ncw + 1) + 3) / 4) * 32) / 8 * 8; }
+constexpr int stream_max_regs(int ncw, int cps) {
+  return stream_max_regs_raw(ncw, cps) > 255 ? 255 : stream_max_regs_raw(ncw, cps);
 }
 
 // The producer warp of a streaming CTA: fills stages, writes tables, and (on a
@@ -127,7 +140,7 @@ __device__ __forceinline__ void stream_producer(unsigned char* smem, int hd, int
 // ------------------------------------------------------------- forward ----
 
 template <int HD, bool SECTIONED, bool ROPE, bool SAVE, bool POOL, int NCW, int CPS>
-__global__ void __launch_bounds__((NCW + 1) * 32, CPS) qkvp_fwd_stream_kernel(const FwdArgs a) {
+__global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_fwd_stream_kernel(const FwdArgs a) {
   using G = Geom<HD>;
   constexpr int CPH = G::CPH, HALF = G::HALF, NCT = NCW * 32, MAXM = kStreamMaxSteps;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -165,24 +178,27 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) qkvp_fwd_stream_kernel(co
   }
 
   // ---- consumers ----
+  // Unit j of a token = chunk pair (lo = chunk e of head h, hi = chunk e + PPH)
+  // with h = j / PPH, e = j % PPH; PPH = CPH / 2 lanes share a head.
+  constexpr int PPH = CPH / 2, LOG_PPH = G::LOG_CPH - 1;
   const int ct = threadIdx.x, lane = ct & 31;
+  const int upt = a.cpt / 2;            // units per token
   const int tpg = NCT / tpt;            // threads per token
   const int tl = ct / tpg;              // token of the tile this thread works on
   const int ig = ct - tl * tpg;         // index inside the group
-  const int e = ct & (CPH - 1);
-  const float sign = e < CPH / 2 ? -1.f : 1.f;
-  const int f0 = (e & (CPH / 2 - 1)) * 8;
-  // Per step: output head and role, fixed for the whole kernel.
+  const int e = ig & (PPH - 1);         // the same for every step (tpg is a multiple of PPH)
+  // Per step: output head, role and packed-head parity, fixed for the whole kernel.
   uint32_t info[MAXM];
 #pragma unroll
   for (int m = 0; m < MAXM; ++m) {
     int role = kRoleV;
-    uint32_t oh = 0;
-    if (m < steps) classify<SECTIONED>((uint32_t)(ig + tpg * m) >> G::LOG_CPH, a.n_q, a.n_kv, a.group,
-                                       a.gs_magic, role, oh);
-    info[m] = oh | ((uint32_t)role << 16);
+    uint32_t oh = 0, h = 0;
+    if (m < steps && ig + tpg * m < upt) {
+      h = (uint32_t)(ig + tpg * m) >> LOG_PPH;
+      classify<SECTIONED>(h, a.n_q, a.n_kv, a.group, a.gs_magic, role, oh);
+    }
+    info[m] = oh | ((uint32_t)role << 16) | ((h & 1u) << 18);
   }
-  const int src0 = tl * a.cpt + ig;  // stage chunk of step 0
   const unsigned char* data = smem + StreamSmem::data(HD, tpt, stages);
 
   int s = 0;
@@ -193,15 +209,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) qkvp_fwd_stream_kernel(co
     const int64_t t0 = tile * tpt;
     const int64_t t = t0 + tl;
     const bool valid = t < a.T;
-    const uint4* sx = reinterpret_cast<const uint4*>(data + (size_t)s * stage_bytes);
+    const uint4* sx = reinterpret_cast<const uint4*>(data + (size_t)s * stage_bytes) + tl * a.cpt;
     const float* tab = reinterpret_cast<const float*>(smem + StreamSmem::tables(HD) + s * StreamSmem::table_stride(HD, tpt));
     float2 c2[4], s2[4];
     if (ROPE) {
-      float2 sn[4];
-      load_pairs(tab + tl * HALF + f0, c2);
-      load_pairs(tab + tpt * HALF + tl * HALF + f0, sn);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) s2[i] = __fmul2_rn(sn[i], f2(sign, sign));
+      load_pairs(tab + tl * HALF + 8 * e, c2);
+      load_pairs(tab + tpt * HALF + tl * HALF + 8 * e, s2);
     }
     int32_t slot = -1;
     if (POOL) slot = reinterpret_cast<const int32_t*>(tab + 2 * tpt * HALF)[tl];
@@ -214,21 +227,41 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) qkvp_fwd_stream_kernel(co
 #pragma unroll
     for (int m = 0; m < MAXM; ++m) {
       if (m >= steps) break;
-      const uint4 xr = sx[src0 + tpg * m];
-      const int role = (int)(info[m] >> 16);
-      const int oidx = (int)(info[m] & 0xffffu) * CPH + e;
-      float2 w[4], y[4];
-      load_split_weights<HD>(s_w, role, e, w);
-      chunk_forward<CPH, ROPE>(xr, w, a.eps, a.inv_head_dim, c2, s2, y);
-      if (!valid) continue;
+      const int j = ig + tpg * m;
+      const bool in_row = j < upt;
+      // stage chunks of the pair; odd heads read hi first so that the two heads a
+      // quarter-warp covers fall in different shared-memory banks
+      const int clo = in_row ? ((j >> LOG_PPH) * CPH + e) : 0;
+      const bool odd = (info[m] >> 18) & 1u;
+      const uint4 first = sx[odd ? clo + PPH : clo];
+      const uint4 second = sx[odd ? clo : clo + PPH];
+      const uint4 xlo = odd ? second : first, xhi = odd ? first : second;
+      const int role = (int)((info[m] >> 16) & 3u);
+      const int olo = (int)(info[m] & 0xffffu) * CPH + e;
+      float2 wlo[4], whi[4], ylo[4], yhi[4];
+      load_split_weights<HD>(s_w, role, e, wlo);
+      load_split_weights<HD>(s_w, role, e + PPH, whi);
+      pair_forward<CPH, ROPE>(xlo, xhi, wlo, whi, a.eps, a.inv_head_dim, c2, s2, ylo, yhi);
+      if (!valid || !in_row) continue;
       if (role == kRoleQ) {
-        qrow[oidx] = pack_pairs(y);
-        if (SAVE) st_stream(qprow + oidx, xr);
+        qrow[olo] = pack_pairs(ylo);
+        qrow[olo + PPH] = pack_pairs(yhi);
+        if (SAVE) {
+          st_stream(qprow + olo, xlo);
+          st_stream(qprow + olo + PPH, xhi);
+        }
       } else if (role == kRoleK) {
-        if (!POOL || slot >= 0) krow[oidx] = pack_pairs(y);
-        if (SAVE) st_stream(kprow + oidx, xr);
-      } else {
-        if (!POOL || slot >= 0) vrow[oidx] = xr;
+        if (!POOL || slot >= 0) {
+          krow[olo] = pack_pairs(ylo);
+          krow[olo + PPH] = pack_pairs(yhi);
+        }
+        if (SAVE) {
+          st_stream(kprow + olo, xlo);
+          st_stream(kprow + olo + PPH, xhi);
+        }
+      } else if (!POOL || slot >= 0) {
+        vrow[olo] = xlo;
+        vrow[olo + PPH] = xhi;
       }
     }
     __syncwarp();
@@ -243,7 +276,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) qkvp_fwd_stream_kernel(co
 // ------------------------------------------------------------ backward ----
 
 template <int HD, bool SECTIONED, bool ROPE, int NCW, int CPS>
-__global__ void __launch_bounds__((NCW + 1) * 32, CPS) qkvp_bwd_stream_kernel(const BwdArgs a) {
+__global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(const BwdArgs a) {
   using G = Geom<HD>;
   constexpr int CPH = G::CPH, HALF = G::HALF, NCT = NCW * 32, MAXM = kStreamMaxSteps;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -282,24 +315,30 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) qkvp_bwd_stream_kernel(co
     return;
   }
 
+  // Unit j of a token = chunk pair (lo = chunk e of packed head h, hi = chunk
+  // e + PPH), as in the forward.
+  constexpr int PPH = CPH / 2, LOG_PPH = G::LOG_CPH - 1;
   const int ct = threadIdx.x, lane = ct & 31;
+  const int upt = a.cpt / 2;
   const int tpg = NCT / tpt;
   const int tl = ct / tpg;
   const int ig = ct - tl * tpg;
-  const int e = ct & (CPH - 1);
-  const float sign = e < CPH / 2 ? 1.f : -1.f;  // R(theta)^T: the partner term flips sign
-  const int f0 = (e & (CPH / 2 - 1)) * 8;
-  // Per step: stage chunk of d (low 16 bits) and of x (high 16 bits), role.
+  const int e = ig & (PPH - 1);
+  // Per step: stage chunk of d_lo (low 16 bits) and of x_lo (high 16 bits);
+  // 2 role bits and 1 parity bit (of the output head) per step.
   uint32_t offs[MAXM];
-  uint32_t roles = 0;
+  uint32_t roles = 0, odds = 0;
 #pragma unroll
   for (int m = 0; m < MAXM; ++m) {
     int role = kRoleV;
     uint32_t oh = 0;
-    if (m < steps) classify<SECTIONED>((uint32_t)(ig + tpg * m) >> G::LOG_CPH, a.n_q, a.n_kv, a.group,
-                                       a.gs_magic, role, oh);
+    const bool in_row = m < steps && ig + tpg * m < upt;
+    if (in_row)
+      classify<SECTIONED>((uint32_t)(ig + tpg * m) >> LOG_PPH, a.n_q, a.n_kv, a.group, a.gs_magic, role, oh);
     uint32_t d_off, x_off;
-    if (role == kRoleQ) {
+    if (!in_row) {
+      d_off = x_off = 0;  // any chunk of the stage; the step is skipped
+    } else if (role == kRoleQ) {
       d_off = (tl * a.n_q + oh) * CPH + e;
       x_off = sec_qp + d_off;
     } else if (role == kRoleK) {
@@ -311,12 +350,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) qkvp_bwd_stream_kernel(co
     }
     offs[m] = d_off | (x_off << 16);
     roles |= (uint32_t)role << (2 * m);
+    odds |= (oh & 1u) << m;
   }
-  const int out0 = ig;  // chunk of step 0 within the token's packed-gradient row
   const unsigned char* data = smem + StreamSmem::data(HD, tpt, stages);
-  float2 accq[4], acck[4];
+  float2 aql[4], aqh[4], akl[4], akh[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) accq[i] = acck[i] = f2(0.f, 0.f);
+  for (int i = 0; i < 4; ++i) aql[i] = aqh[i] = akl[i] = akh[i] = f2(0.f, 0.f);
 
   int s = 0;
   uint32_t phase = 0;
@@ -329,33 +368,42 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) qkvp_bwd_stream_kernel(co
     const float* tab = reinterpret_cast<const float*>(smem + StreamSmem::tables(HD) + s * StreamSmem::table_stride(HD, tpt));
     float2 c2[4], s2[4];
     if (ROPE) {
-      float2 sn[4];
-      load_pairs(tab + tl * HALF + f0, c2);
-      load_pairs(tab + tpt * HALF + tl * HALF + f0, sn);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) s2[i] = __fmul2_rn(sn[i], f2(sign, sign));
+      load_pairs(tab + tl * HALF + 8 * e, c2);
+      load_pairs(tab + tpt * HALF + tl * HALF + 8 * e, s2);
     }
     uint4* drow = a.dpacked + t * a.row_stride16;
 
 #pragma unroll
     for (int m = 0; m < MAXM; ++m) {
       if (m >= steps) break;
+      const int j = ig + tpg * m;
       const int role = (int)((roles >> (2 * m)) & 3u);
-      const uint4 dr = sx[offs[m] & 0xffffu];
-      const uint4 xr = sx[offs[m] >> 16];
-      float2 w[4], dx[4], gx[4];
+      const bool odd = (odds >> m) & 1u;
+      const int dl = (int)(offs[m] & 0xffffu), xl = (int)(offs[m] >> 16);
+      // odd output heads read hi first (different shared-memory banks)
+      const uint4 d1 = sx[odd ? dl + PPH : dl], d2 = sx[odd ? dl : dl + PPH];
+      const uint4 x1 = sx[odd ? xl + PPH : xl], x2 = sx[odd ? xl : xl + PPH];
+      const uint4 dlo = odd ? d2 : d1, dhi = odd ? d1 : d2;
+      const uint4 xlo = odd ? x2 : x1, xhi = odd ? x1 : x2;
+      float2 wlo[4], whi[4], dxlo[4], dxhi[4], gxlo[4], gxhi[4];
       float r;
-      load_split_weights<HD>(s_w, role, e, w);
-      chunk_backward<CPH, ROPE>(dr, xr, w, a.eps, a.inv_head_dim, c2, s2, dx, gx, r);
-      if (!valid) continue;
+      load_split_weights<HD>(s_w, role, e, wlo);
+      load_split_weights<HD>(s_w, role, e + PPH, whi);
+      pair_backward<CPH, ROPE>(dlo, dhi, xlo, xhi, wlo, whi, a.eps, a.inv_head_dim, c2, s2, dxlo, dxhi, gxlo,
+                               gxhi, r);
+      if (!valid || j >= upt) continue;
       const float rq = role == kRoleQ ? r : 0.f, rk = role == kRoleK ? r : 0.f;
       const float2 rq2 = f2(rq, rq), rk2 = f2(rk, rk);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        accq[i] = __ffma2_rn(gx[i], rq2, accq[i]);
-        acck[i] = __ffma2_rn(gx[i], rk2, acck[i]);
+        aql[i] = __ffma2_rn(gxlo[i], rq2, aql[i]);
+        aqh[i] = __ffma2_rn(gxhi[i], rq2, aqh[i]);
+        akl[i] = __ffma2_rn(gxlo[i], rk2, akl[i]);
+        akh[i] = __ffma2_rn(gxhi[i], rk2, akh[i]);
       }
-      drow[out0 + tpg * m] = role == kRoleV ? dr : pack_pairs(dx);
+      const int plo = (j >> LOG_PPH) * CPH + e;  // packed-row chunk of lo
+      drow[plo] = role == kRoleV ? dlo : pack_pairs(dxlo);
+      drow[plo + PPH] = role == kRoleV ? dhi : pack_pairs(dxhi);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
@@ -365,24 +413,34 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) qkvp_bwd_stream_kernel(co
     }
   }
 
-  // Weight-grad partials: lanes of a warp with the same e, then the warps, in
-  // a fixed order (deterministic).
-  float aq[8] = {accq[0].x, accq[0].y, accq[1].x, accq[1].y, accq[2].x, accq[2].y, accq[3].x, accq[3].y};
-  float ak[8] = {acck[0].x, acck[0].y, acck[1].x, acck[1].y, acck[2].x, acck[2].y, acck[3].x, acck[3].y};
+  // Weight-grad partials: lanes of a warp with the same e (lane % PPH), then
+  // the warps, in a fixed order (deterministic).
+  float ql[8], qh[8], kl[8], kh[8];
 #pragma unroll
-  for (int o = CPH; o < 32; o <<= 1) {
+  for (int i = 0; i < 4; ++i) {
+    ql[2 * i] = aql[i].x; ql[2 * i + 1] = aql[i].y;
+    qh[2 * i] = aqh[i].x; qh[2 * i + 1] = aqh[i].y;
+    kl[2 * i] = akl[i].x; kl[2 * i + 1] = akl[i].y;
+    kh[2 * i] = akh[i].x; kh[2 * i + 1] = akh[i].y;
+  }
+#pragma unroll
+  for (int o = PPH; o < 32; o <<= 1) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      aq[i] += __shfl_xor_sync(0xffffffffu, aq[i], o);
-      ak[i] += __shfl_xor_sync(0xffffffffu, ak[i], o);
+      ql[i] += __shfl_xor_sync(0xffffffffu, ql[i], o);
+      qh[i] += __shfl_xor_sync(0xffffffffu, qh[i], o);
+      kl[i] += __shfl_xor_sync(0xffffffffu, kl[i], o);
+      kh[i] += __shfl_xor_sync(0xffffffffu, kh[i], o);
     }
   }
   const int warp = ct >> 5;
-  if (lane < CPH) {
+  if (lane < PPH) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      s_red[warp][0][lane * 8 + i] = aq[i];
-      s_red[warp][1][lane * 8 + i] = ak[i];
+      s_red[warp][0][lane * 8 + i] = ql[i];
+      s_red[warp][0][(lane + PPH) * 8 + i] = qh[i];
+      s_red[warp][1][lane * 8 + i] = kl[i];
+      s_red[warp][1][(lane + PPH) * 8 + i] = kh[i];
     }
   }
   asm volatile("bar.sync 1, %0;" ::"r"(NCT) : "memory");  // consumer warps only

@@ -18,16 +18,16 @@ enum Role : int { kRoleQ = 0, kRoleK = 1, kRoleV = 2 };
 // Streaming (shared-memory staged) kernels.
 // Shape of the pipelined kernels: consumer warps per CTA (+1 producer warp)
 // and the CTAs per SM the shared-memory budget is cut for. Measured on GB300
-// (T = 16384, Muse Spark packing): the forward with the pre-norm save runs best
-// as one CTA of 8 consumer warps per SM with a deep ring; the plain forward
-// (and pool write) with 16 consumer warps per SM in one CTA; the backward as
-// two CTAs of 8 consumer warps per SM.
+// (T = 16384, Muse Spark packing): one CTA of 10 consumer warps per SM with
+// a deep ring is best for the forward (with and without the pre-norm save)
+// and the backward; with 11 warps per SM the register cap is 168 per thread,
+// enough for the pair-per-lane backward without spills.
 struct StreamShape {
   int warps;
   int ctas_per_sm;
 };
-constexpr StreamShape fwd_stream_shape(bool save_pre) { return save_pre ? StreamShape{8, 1} : StreamShape{16, 1}; }
-constexpr StreamShape bwd_stream_shape() { return StreamShape{8, 2}; }
+constexpr StreamShape fwd_stream_shape(bool) { return StreamShape{10, 1}; }
+constexpr StreamShape bwd_stream_shape() { return StreamShape{10, 1}; }
 constexpr int kMaxStages = 8;  // depth of the shared-memory ring (max)
 constexpr int kStreamMaxSteps = 6;       // 16-byte chunks per consumer thread per tile (max)
 

@@ -194,6 +194,7 @@ class _Step:
     `out_names` names the outputs copied back to the host."""
 
     kernels_per_step = 1
+    xflags = 0  # extra flags for every call (QKVP_FORCE_GENERIC for A/B runs)
 
     def _common(self, dev):
         import torch
@@ -274,11 +275,12 @@ class TrainStep(_Step):
 
     def fwd(self):
         self.C.qkv_prologue_fwd(self.L, self.T, self.packed, self.pos, self.w_q, self.w_k, self.eps, self.base,
-                                self.C.QKVP_SAVE_PRE, self.q, self.k, self.v, self.q_pre, self.k_pre, self.stream)
+                                self.C.QKVP_SAVE_PRE | self.xflags, self.q, self.k, self.v, self.q_pre, self.k_pre,
+                                self.stream)
 
     def bwd(self):
         self.C.qkv_prologue_bwd(self.L, self.T, self.dq, self.dk, self.dv, self.q_pre, self.k_pre, self.pos,
-                                self.w_q, self.w_k, self.eps, self.base, 0, self.dpacked, self.dw_q, self.dw_k,
+                                self.w_q, self.w_k, self.eps, self.base, self.xflags, self.dpacked, self.dw_q, self.dw_k,
                                 self.ws, self.ws_bytes, self.stream)
 
 
@@ -308,7 +310,8 @@ class PrefillStep(_Step):
     def fwd(self):
         C = self.C
         C.qkv_prologue_fwd(self.L, self.T, self.packed, self.pos, self.w_q, self.w_k, self.wl.eps, self.wl.rope_base,
-                           C.QKVP_NOPE if self.nope else 0, self.q, self.k, self.v, None, None, self.stream)
+                           (C.QKVP_NOPE if self.nope else 0) | self.xflags, self.q, self.k, self.v, None, None,
+                           self.stream)
 
 
 class DecodeStep(_Step):
@@ -340,7 +343,8 @@ class DecodeStep(_Step):
 
     def fwd(self):
         C, wl = self.C, self.wl
-        C.qkv_prologue_pool_write(self.L, self.T, self.packed, self.pos, self.w_q, self.w_k, wl.eps, wl.rope_base, 0,
+        C.qkv_prologue_pool_write(self.L, self.T, self.packed, self.pos, self.w_q, self.w_k, wl.eps, wl.rope_base,
+                                  self.xflags,
                                   self.q, self.page, self.offset, self.k_pool, self.v_pool, wl.num_pages,
                                   wl.page_size, None, self.stream)
 
@@ -368,7 +372,8 @@ class MlaStep(_Step):
 
     def fwd(self):
         C, wl = self.C, self.wl
-        C.qkv_prologue_pool_write(self.L, self.T, self.rows, self.pos, None, self.w, wl.eps, wl.rope_base, 0, None,
+        C.qkv_prologue_pool_write(self.L, self.T, self.rows, self.pos, None, self.w, wl.eps, wl.rope_base, self.xflags,
+                                  None,
                                   self.page, self.offset, self.pool, None, wl.num_pages, wl.page_size, None,
                                   self.stream)
 
@@ -407,6 +412,8 @@ def run_ours(args):
         dist.barrier()
 
     ws = make_workload(args.workload, dev, args.tokens)
+    if args.force_generic:
+        ws.xflags = ws.C.QKVP_FORCE_GENERIC
     T = ws.T
     step_bytes = ws.step_bytes()
     l2_bytes = props_l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -414,6 +421,13 @@ def run_ours(args):
     # and only the step itself (between per-step events) is timed.
     flush = step_bytes < 2 * l2_bytes
     flush_buf = torch.empty(max(2 * props_l2, 1 << 28), dtype=torch.uint8, device=dev) if flush else None
+    flush_rd = torch.ones(max(2 * props_l2, 1 << 28) // 4, dtype=torch.int32, device=dev) if flush else None
+
+    def flush_l2():
+        # write a buffer larger than L2, then read another one: the write-back of
+        # the first buffer's dirty lines happens here, not inside the timed call
+        flush_buf.zero_()
+        flush_rd.sum()
     props = torch.cuda.get_device_properties(dev)
     uuid = getattr(props, "uuid", None)
     uuid = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else (str(uuid) if uuid else None)
@@ -435,7 +449,7 @@ def run_ours(args):
     start.record()
     for i in range(K):
         if flush:
-            flush_buf.zero_()
+            flush_l2()
         ev[i][0].record()
         for c, (_, fn, _) in enumerate(ws.calls):
             fn()
@@ -452,7 +466,7 @@ def run_ours(args):
     clocks = sampler.summary(t_wall0, t_wall1)
 
     # the same step replayed from a CUDA graph (launch overhead removed)
-    graph_ms = None
+    graph_ms = graph_warm_ms = None
     try:
         g = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream(dev)
@@ -468,12 +482,30 @@ def run_ours(args):
         gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(min(K, 200))]
         for a, b in gev:
             if flush:
-                flush_buf.zero_()
+                flush_l2()
             a.record()
             g.replay()
             b.record()
         torch.cuda.synchronize()
         graph_ms = statistics.fmean(a.elapsed_time(b) for a, b in gev)
+        # and back to back with warm L2 (the decode case: the projection that made
+        # the inputs ran just before): 50 steps captured in one graph, replayed
+        # once, so the host's launch rate does not enter the figure
+        gb = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            ws.stream = cap.cuda_stream
+            with torch.cuda.graph(gb, stream=cap):
+                for _ in range(50):
+                    ws.step()
+        ws.stream = torch.cuda.current_stream(dev).cuda_stream
+        gb.replay()
+        torch.cuda.synchronize()
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0.record()
+        gb.replay()
+        w1.record()
+        torch.cuda.synchronize()
+        graph_warm_ms = w0.elapsed_time(w1) / 50
     except Exception as exc:  # graph capture is a measurement extra, not the product path
         graph_ms = f"unavailable: {type(exc).__name__}: {exc}"
         ws.stream = torch.cuda.current_stream(dev).cuda_stream
@@ -520,7 +552,8 @@ def run_ours(args):
             "workload": ws.describe,
             "T": T, "n_q": N_Q, "n_kv": N_KV, "head_dim": D,
             "bytes_per_step": step_bytes,
-            "l2": (f"flushed before every step ({flush_buf.numel() >> 20} MiB write, outside the timed calls)"
+            "l2": (f"flushed before every step ({flush_buf.numel() >> 20} MiB write, then a {flush_buf.numel() >> 20} MiB "
+                   "read so the write-back is done; both outside the timed calls)"
                    if flush else
                    f"no flush: inputs larger than L2 ({step_bytes / 1e9:.2f} GB of traffic per step vs "
                    f"{l2_bytes >> 20} MiB L2)"),
@@ -530,6 +563,7 @@ def run_ours(args):
                            "GBps": round(b / (call_ms[c] * 1e-3) / 1e9, 1)}
                     for c, (name, _, b) in enumerate(ws.calls)},
         "graph_replay_us_per_step": round(graph_ms * 1e3, 2) if isinstance(graph_ms, float) else graph_ms,
+        "graph_replay_warm_us_per_step": round(graph_warm_ms * 1e3, 2) if isinstance(graph_warm_ms, float) else None,
         "roofline": {
             "kernel": dom_name,
             "bound": "hbm",
@@ -660,6 +694,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=0,
                     help="T (0 = the workload's default: 16384 train/prefill, 256 decode, 32768 mla)")
     ap.add_argument("--cpu-tokens", type=int, default=6144)
+    ap.add_argument("--force-generic", action="store_true",
+                    help="run the general kernels instead of the pipelined ones (A/B comparison)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

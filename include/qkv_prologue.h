@@ -101,10 +101,10 @@ enum {
   QKVP_NOPE = 1,           /* NoPE layer: RMSNorm only, no rotation            */
   QKVP_SAVE_PRE = 2,       /* forward also writes the split pre-norm q and k   */
   QKVP_ACCUMULATE_DW = 4,  /* backward adds into dw_q / dw_k instead of writing */
-  QKVP_FORCE_GENERIC = 8   /* GQA forward / backward: use the general kernels
-                              even where the shared-memory pipelined ones
-                              apply (same output bits; for A/B checks). The
-                              weight-grad sums may differ in rounding. */
+  QKVP_FORCE_GENERIC = 8   /* use the general kernels even where the
+                              shared-memory pipelined ones apply (same output
+                              bits; for A/B checks). The backward's weight-grad
+                              sums may differ in rounding. */
 };
 
 /* Device-side status bits (pool writes): set with an atomic OR in
@@ -127,7 +127,7 @@ enum { QKVP_DEV_BAD_PAGE = 1, QKVP_DEV_BAD_OFFSET = 2 };
  *             w_k is the float32 [norm_dim] latent weight, w_q is ignored.
  * eps         RMSNorm epsilon (>= 0, added inside the square root).
  * rope_base   RoPE base (> 0).
- * flags       QKVP_NOPE | QKVP_SAVE_PRE (SAVE_PRE: GQA only).
+ * flags       QKVP_NOPE | QKVP_SAVE_PRE (SAVE_PRE: GQA only) | QKVP_FORCE_GENERIC.
  * q           bf16 [T, n_q, head_dim] out.           LATENT: ignored.
  * k           bf16 [T, n_kv, head_dim] out.          LATENT: [T, norm_dim+rope_dim] out.
  * v           bf16 [T, n_kv, head_dim] out (copy).   LATENT: ignored.
@@ -159,7 +159,7 @@ QKVP_API int qkv_prologue_fwd(const qkvp_layout* layout, int64_t T, const void* 
  *   offset outside [0, page_size) is not stored; the matching QKVP_DEV_* bit
  *   is OR-ed into *dev_status when dev_status (int32, device) is not NULL.
  * Two tokens naming the same slot race; the caller must not do that.
- * flags: QKVP_NOPE only.
+ * flags: QKVP_NOPE, QKVP_FORCE_GENERIC.
  * ------------------------------------------------------------------------- */
 QKVP_API int qkv_prologue_pool_write(const qkvp_layout* layout, int64_t T, const void* packed,
                             const int32_t* pos, const float* w_q, const float* w_k, float eps,

@@ -381,7 +381,7 @@ static int latent_forward(const qkvp_layout* L, int64_t T, const void* rows, con
                           bool to_pool, cudaStream_t stream) {
   Latent g;
   QKVP_TRY(check_latent(L, T, &g));
-  if (flags & ~(uint32_t)QKVP_NOPE) return QKVP_ERR_FLAGS;
+  if (flags & ~(uint32_t)(QKVP_NOPE | QKVP_FORCE_GENERIC)) return QKVP_ERR_FLAGS;
   const bool rope = !(flags & QKVP_NOPE);
   QKVP_TRY(check_scalars(eps, rope_base, rope));
   if (!rows || !w || (rope && !pos)) return QKVP_ERR_NULL;
@@ -398,8 +398,8 @@ static int latent_forward(const qkvp_layout* L, int64_t T, const void* rows, con
     return QKVP_ERR_ALIGN;
   if (T == 0) return QKVP_OK;
 
-  int sms = 0;
-  QKVP_TRY(current_device(&sms));
+  int sms = 0, smem_per_sm = 0;
+  QKVP_TRY(current_device(&sms, &smem_per_sm));
   LatentArgs a;
   std::memset(&a, 0, sizeof(a));
   a.rows = static_cast<const uint4*>(rows);
@@ -420,6 +420,35 @@ static int latent_forward(const qkvp_layout* L, int64_t T, const void* rows, con
   a.dev_status = dev_status;
   if (rope) rope_table(rope_base, L->rope_dim, &a.rope);
   const int ncl = a.norm_chunks <= 32 ? 1 : (a.norm_chunks <= 64 ? 2 : 4);
+
+  // Pipelined kernel: tiles of kLatentTileTokens rows, kLatentStreamCtasPerSm
+  // CTAs per SM, each ring as deep as the shared memory allows (>= 2 stages).
+  // Its table per stage holds the positions and the pool slots (layout of a
+  // 2-wide "head": one int per row each).
+  if (!(flags & QKVP_FORCE_GENERIC) && (a.err = device_error_word()) != nullptr) {
+    const int tpt = kLatentTileTokens, thd = 2;
+    const int64_t stage = (int64_t)tpt * a.row_chunks * 16;
+    const int budget = smem_per_sm / kLatentStreamCtasPerSm - 1024;
+    const int64_t per_stage = stage + StreamSmem::table_stride(thd, tpt);
+    int64_t stages = (budget - StreamSmem::tables(thd) - 128) / per_stage;
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages >= 2) {
+      a.sg.tpt = tpt;
+      a.sg.stages = (int32_t)stages;
+      a.sg.steps = 1;
+      a.sg.stage_bytes = (int32_t)stage;
+      a.sg.n_tiles = (T + tpt - 1) / tpt;
+      a.sg.dense = g.stride == g.row;
+      const size_t smem = (size_t)StreamSmem::data(thd, tpt, (int)stages) + (size_t)stages * stage;
+      const void* kern = latent_stream_kernel(to_pool, rope, ncl);
+      const int threads = (kLatentStreamWarps + 1) * 32;
+      const int bps = allow_smem(kern, smem) ? blocks_per_sm(kern, threads, smem) : 0;
+      if (bps > 0) {
+        const int64_t cap = (int64_t)sms * bps;
+        return launch(kern, a.sg.n_tiles < cap ? a.sg.n_tiles : cap, threads, smem, stream, &a);
+      }
+    }
+  }
   const void* kern = latent_kernel(to_pool, rope, ncl);
   const int threads = kLatentWarps * 32;
   const int64_t per_cta = (int64_t)kLatentWarps * kLatentTokensPerWarp;

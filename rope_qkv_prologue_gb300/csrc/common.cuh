@@ -277,6 +277,50 @@ __device__ __forceinline__ void pair_backward(const uint4& dlo_r, const uint4& d
   r_out = r;
 }
 
+// ------------------------------------------------------ MLA latent rows ----
+//
+// Norm part of an MLA latent row: lane l of a warp holds norm chunks l, l + 32,
+// ... (NCL of them, zero beyond norm_chunks). Both latent kernels use these,
+// so they agree bit for bit.
+
+template <int NCL>
+__device__ __forceinline__ float latent_sum_sq(const uint4 (&xr)[NCL], float2 (&x)[NCL][4]) {
+  float ss = 0.f;
+#pragma unroll
+  for (int m = 0; m < NCL; ++m) {
+    unpack_pairs(xr[m], x[m]);
+    ss += chunk_partial_sq(x[m]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  return ss;
+}
+
+__device__ __forceinline__ uint4 latent_norm_chunk(const float2 (&x)[4], float r, const float2 (&w)[4]) {
+  const float2 rr = f2(r, r);
+  float2 y[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) y[i] = __fmul2_rn(__fmul2_rn(x[i], rr), w[i]);
+  return pack_pairs(y);
+}
+
+// Rotate-half of one rope chunk pair: lo = values 8e .. 8e+7 of the rope
+// part, hi = their partners 8e + 32 .. (c, sn: cos / sin of frequencies
+// 8e .. 8e+7).
+__device__ __forceinline__ void latent_rope_pair(const uint4& rlo, const uint4& rhi, const float (&c)[8],
+                                                 const float (&sn)[8], uint4& olo, uint4& ohi) {
+  float xl[8], xh[8], yl[8], yh[8];
+  unpack8(rlo, xl);
+  unpack8(rhi, xh);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    yl[i] = fmaf(xl[i], c[i], xh[i] * -sn[i]);
+    yh[i] = fmaf(xh[i], c[i], xl[i] * sn[i]);
+  }
+  olo = pack8(yl);
+  ohi = pack8(yh);
+}
+
 // ---------------------------------------------------------- division ----
 
 // n / d for n < 2^16 and 2 <= d <= 2^16 with m = floor(2^32 / d) + 1:

@@ -74,7 +74,7 @@ constexpr int stream_max_regs(int ncw, int cps) {
 // wait that timed out) drains the copies it issued before returning.
 // `load(stage_ptr, t0, ntok, bar, policy)` (run by lane 0 only) announces the
 // tile's byte count on `bar` and issues its bulk copies.
-template <int HALF, bool ROPE, bool POOL, class LoadTile>
+template <int HALF, bool ROPE, bool POOL, class LoadTile, bool STAGE_POS = false>
 __device__ __forceinline__ void stream_producer(unsigned char* smem, int hd, int tpt, int stages,
                                                 int stage_bytes, int64_t n_tiles, int64_t T,
                                                 const int32_t* pos, const RopeTable& rope,
@@ -110,6 +110,10 @@ __device__ __forceinline__ void stream_producer(unsigned char* smem, int hd, int
         tab[i] = c;
         tab[tpt * HALF + i] = sn;
       }
+    }
+    if (STAGE_POS) {  // positions only (the consumers compute the angles)
+      int32_t* sp = reinterpret_cast<int32_t*>(tab);
+      for (int i = lane; i < ntok; i += 32) sp[i] = pos[t0 + i];
     }
     if (POOL) {
       int32_t* slot = reinterpret_cast<int32_t*>(tab + 2 * tpt * HALF);

@@ -22,12 +22,14 @@ __global__ void __launch_bounds__(kLatentWarps * 32) qkvp_latent_kernel(const La
   const bool lo = (lane & 7) < 4;
   const int f0 = (lane & 3) * 8;
 
-  float w[NCL][8];
+  float2 w[NCL][4];
 #pragma unroll
   for (int m = 0; m < NCL; ++m) {
     const int chunk = lane + 32 * m;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w[m][i] = chunk < a.norm_chunks ? __ldg(a.w + chunk * 8 + i) : 0.f;
+    for (int i = 0; i < 4; ++i)
+      w[m][i] = chunk < a.norm_chunks ? f2(__ldg(a.w + chunk * 8 + 2 * i), __ldg(a.w + chunk * 8 + 2 * i + 1))
+                                      : f2(0.f, 0.f);
   }
 
   for (int64_t t0 = warp_id * TPW; t0 < a.T; t0 += n_warps * TPW) {
@@ -51,16 +53,8 @@ __global__ void __launch_bounds__(kLatentWarps * 32) qkvp_latent_kernel(const La
     for (int k = 0; k < TPW; ++k) {
       const int64_t t = t0 + k;
       if (t >= a.T) break;  // warp-uniform
-      float ss = 0.f;
-      float x[NCL][8];
-#pragma unroll
-      for (int m = 0; m < NCL; ++m) {
-        unpack8(xn[k][m], x[m]);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) ss = fmaf(x[m][i], x[m][i], ss);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      float2 x[NCL][4];
+      const float ss = latent_sum_sq<NCL>(xn[k], x);
       const float r = rsqrtf(fmaf(ss, a.inv_norm_dim, a.eps));
 
       float xq[8], o8[8];
@@ -97,12 +91,7 @@ __global__ void __launch_bounds__(kLatentWarps * 32) qkvp_latent_kernel(const La
 #pragma unroll
       for (int m = 0; m < NCL; ++m) {
         const int chunk = lane + 32 * m;
-        if (chunk < a.norm_chunks) {
-          float y[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) y[i] = x[m][i] * r * w[m][i];
-          st_keep(dst + chunk, pack8(y));
-        }
+        if (chunk < a.norm_chunks) st_keep(dst + chunk, latent_norm_chunk(x[m], r, w[m]));
       }
       if (rope_lane) st_keep(dst + a.norm_chunks + lane, ROPE ? pack8(o8) : xr[k]);
     }

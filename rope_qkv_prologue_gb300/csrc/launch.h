@@ -140,6 +140,8 @@ struct LatentArgs {
   uint4* pool;            // pool destination (or null)
   int32_t num_pages, page_size;
   int32_t* dev_status;
+  int* err;               // library device error word (pipelined kernel)
+  StreamGeom sg;          // pipelined kernel geometry
   RopeTable rope;
 };
 
@@ -175,6 +177,7 @@ const void* scatter_kernel();
 const void* fwd_stream_kernel_d64(const FwdVariant& v);
 const void* fwd_stream_kernel_d128(const FwdVariant& v);
 const void* bwd_stream_kernel(int head_dim, bool sectioned, bool rope);
+const void* latent_stream_kernel(bool pool, bool rope, int norm_chunks_per_lane);
 
 // Address of the library's device error word on the current device (nullptr
 // if it cannot be obtained), and its value (read and optionally cleared,
@@ -196,5 +199,8 @@ constexpr int kFinalizeThreads = 256;
 
 constexpr int kLatentWarps = 8;        // warps per CTA of the latent kernel
 constexpr int kLatentTokensPerWarp = 2;
+constexpr int kLatentTileTokens = 32;     // rows per tile of the pipelined latent kernel
+constexpr int kLatentStreamWarps = 4;     // its consumer warps (+1 producer); tile = 8 rows per warp
+constexpr int kLatentStreamCtasPerSm = 2;
 
 }  // namespace qkvp

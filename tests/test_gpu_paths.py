@@ -83,3 +83,25 @@ def test_no_pipeline_wait_ever_gave_up(lib, cuda):
     _run(lib, wl, "interleaved", cuda, 0)
     torch.cuda.synchronize()
     assert lib.qkv_prologue_device_error(clear=False) == 0
+
+
+@pytest.mark.parametrize("T", [1, 16, 100, 32768])
+@pytest.mark.parametrize("pool", [False, True])
+def test_latent_pipelined_and_general_kernels_agree(lib, cuda, T, pool):
+    C = lib
+    wl = workloads.mla(T)
+    L = C.layout("latent", norm_dim=512, rope_dim=64)
+    rows, pos, w = wl.rows.to(cuda), wl.pos.to(cuda), wl.w.to(cuda)
+    page, off = wl.page.to(cuda), wl.offset.to(cuda)
+    outs = []
+    for flags in (0, C.QKVP_FORCE_GENERIC):
+        if pool:
+            dst = workloads.random_pool_bits((wl.num_pages, wl.page_size, 576), 61, cuda)
+            C.qkv_prologue_pool_write(L, T, rows, pos, None, w, wl.eps, wl.rope_base, flags, None, page, off, dst,
+                                      None, wl.num_pages, wl.page_size)
+        else:
+            dst = torch.empty(T, 576, dtype=torch.bfloat16, device=cuda)
+            C.qkv_prologue_fwd(L, T, rows, pos, None, w, wl.eps, wl.rope_base, flags, None, dst, None)
+        outs.append(dst)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))

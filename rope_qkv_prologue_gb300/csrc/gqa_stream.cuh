@@ -247,25 +247,33 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_fwd_stream_kernel(co
       load_split_weights<HD>(s_w, role, e + PPH, whi);
       pair_forward<CPH, ROPE>(xlo, xhi, wlo, whi, a.eps, a.inv_head_dim, c2, s2, ylo, yhi);
       if (!valid || !in_row) continue;
+      // Plain contiguous forward: cache-streaming stores (measured faster on GB300
+      // at every size tried); with the pre-norm save, or into a pool that
+      // attention reads next, write-back stores.
+      constexpr bool STREAM_OUT = !SAVE && !POOL;
+      auto put = [](uint4* p, const uint4& v) {
+        if (STREAM_OUT) st_stream(p, v);
+        else st_keep(p, v);
+      };
       if (role == kRoleQ) {
-        qrow[olo] = pack_pairs(ylo);
-        qrow[olo + PPH] = pack_pairs(yhi);
+        put(qrow + olo, pack_pairs(ylo));
+        put(qrow + olo + PPH, pack_pairs(yhi));
         if (SAVE) {
           st_stream(qprow + olo, xlo);
           st_stream(qprow + olo + PPH, xhi);
         }
       } else if (role == kRoleK) {
         if (!POOL || slot >= 0) {
-          krow[olo] = pack_pairs(ylo);
-          krow[olo + PPH] = pack_pairs(yhi);
+          put(krow + olo, pack_pairs(ylo));
+          put(krow + olo + PPH, pack_pairs(yhi));
         }
         if (SAVE) {
           st_stream(kprow + olo, xlo);
           st_stream(kprow + olo + PPH, xhi);
         }
       } else if (!POOL || slot >= 0) {
-        vrow[olo] = xlo;
-        vrow[olo + PPH] = xhi;
+        put(vrow + olo, xlo);
+        put(vrow + olo + PPH, xhi);
       }
     }
     __syncwarp();
@@ -406,8 +414,8 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(co
         akh[i] = __ffma2_rn(gxhi[i], rk2, akh[i]);
       }
       const int plo = (j >> LOG_PPH) * CPH + e;  // packed-row chunk of lo
-      drow[plo] = role == kRoleV ? dlo : pack_pairs(dxlo);
-      drow[plo + PPH] = role == kRoleV ? dhi : pack_pairs(dxhi);
+      st_keep(drow + plo, role == kRoleV ? dlo : pack_pairs(dxlo));
+      st_keep(drow + plo + PPH, role == kRoleV ? dhi : pack_pairs(dxhi));
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);

@@ -139,6 +139,7 @@ bool stream_geometry(const StreamShape& shape, int upt, int lph, int hd, int64_t
     const int64_t per_stage = stage + StreamSmem::table_stride(hd, tpt);
     int64_t stages = (budget - fixed) / per_stage;
     if (stages < 2) return false;
+    if (stages > shape.max_stages) stages = shape.max_stages;
     if (stages > kMaxStages) stages = kMaxStages;
     g->tpt = tpt;
     g->stages = (int32_t)stages;
@@ -355,8 +356,8 @@ static int gqa_forward(const qkvp_layout* L, int64_t T, const void* packed, cons
   const FwdVariant var{L->head_dim, L->kind == QKVP_SECTIONED, rope, save, pool};
   size_t smem = 0;
   if (!(flags & QKVP_FORCE_GENERIC) &&
-      stream_geometry(fwd_stream_shape(save), a.cpt / 2, L->head_dim / 16, L->head_dim, T, (int64_t)a.cpt * 16,
-                      smem_per_sm, 0, &a.sg, &smem) &&
+      stream_geometry(fwd_stream_shape(save, rope), a.cpt / 2, L->head_dim / 16, L->head_dim, T,
+                      (int64_t)a.cpt * 16, smem_per_sm, 0, &a.sg, &smem) &&
       (a.err = device_error_word()) != nullptr) {
     a.sg.dense = g.stride == g.row;
     const void* kern = L->head_dim == 64 ? fwd_stream_kernel_d64(var) : fwd_stream_kernel_d128(var);

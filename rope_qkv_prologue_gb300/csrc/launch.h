@@ -16,18 +16,25 @@ constexpr int kMaxBwdParts = 1024;    // cap on per-CTA weight-grad partial rows
 enum Role : int { kRoleQ = 0, kRoleK = 1, kRoleV = 2 };
 
 // Streaming (shared-memory staged) kernels.
-// Shape of the pipelined kernels: consumer warps per CTA (+1 producer warp)
-// and the CTAs per SM the shared-memory budget is cut for. Measured on GB300
-// (T = 16384, Muse Spark packing): one CTA of 10 consumer warps per SM with
-// a deep ring is best for the forward (with and without the pre-norm save)
-// and the backward; with 11 warps per SM the register cap is 168 per thread,
-// enough for the pair-per-lane backward without spills.
+// Shape of the pipelined kernels: consumer warps per CTA (+1 producer warp),
+// the CTAs per SM the shared-memory budget is cut for, and the deepest ring
+// to use. Measured on GB300 (T = 16384, Muse Spark packing): one CTA of 10
+// consumer warps per SM is best for the forward (with and without the
+// pre-norm save) and the backward (with 11 warps per SM the register cap is
+// 168 per thread, enough for the pair-per-lane backward without spills). The
+// ring depth paces the reads: the backward and the NoPE forward, whose
+// consumers finish a tile quickly, run faster with at most 4 stages in flight
+// than with 8 (deeper rings issue the reads in bursts that interleave worse
+// with the writes); the RoPE forwards run best with 8.
 struct StreamShape {
   int warps;
   int ctas_per_sm;
+  int max_stages;
 };
-constexpr StreamShape fwd_stream_shape(bool) { return StreamShape{10, 1}; }
-constexpr StreamShape bwd_stream_shape() { return StreamShape{10, 1}; }
+constexpr StreamShape fwd_stream_shape(bool save_pre, bool rope = true) {
+  return StreamShape{10, 1, (save_pre || rope) ? 8 : 4};
+}
+constexpr StreamShape bwd_stream_shape() { return StreamShape{10, 1, 4}; }
 constexpr int kMaxStages = 8;  // depth of the shared-memory ring (max)
 constexpr int kStreamMaxSteps = 6;       // 16-byte chunks per consumer thread per tile (max)
 

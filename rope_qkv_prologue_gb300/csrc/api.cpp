@@ -152,9 +152,22 @@ bool stream_geometry(const StreamShape& shape, int upt, int lph, int hd, int64_t
   return false;
 }
 
+// Launch with programmatic stream serialization: the kernel may be launched
+// while the previous kernel in the stream is still running; every kernel of the
+// library waits (griddepcontrol.wait) for it before touching memory.
 int launch(const void* kernel, int64_t grid, int threads, size_t smem, cudaStream_t s, void* arg) {
   void* args[] = {arg};
-  cudaError_t err = cudaLaunchKernel(kernel, dim3((unsigned)grid), dim3(threads), args, smem, s);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t err = cudaLaunchKernelExC(&cfg, kernel, args);
   if (err != cudaSuccess) {
     cudaGetLastError();
     return err == cudaErrorNoKernelImageForDevice || err == cudaErrorInvalidDeviceFunction

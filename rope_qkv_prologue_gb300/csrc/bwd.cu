@@ -9,6 +9,7 @@ namespace qkvp {
 // the rows into kFinalizeThreads / kFinalizeOutputsPerCta interleaved slices
 // and a fixed-shape tree adds the slices.
 __global__ void __launch_bounds__(kFinalizeThreads) qkvp_dw_finalize_kernel(const FinalizeArgs a) {
+  griddep_wait();
   constexpr int K = kFinalizeOutputsPerCta, SLICES = kFinalizeThreads / K;
   __shared__ double s_sum[SLICES][K];
   const int jj = threadIdx.x % K, slice = threadIdx.x / K;

@@ -14,6 +14,17 @@
 
 namespace qkvp {
 
+// -------------------------------------------- programmatic dependent launch ----
+//
+// Every kernel of the library is launched with programmatic stream
+// serialization, so its launch and set-up may overlap the tail of the kernel
+// before it in the stream. griddep_wait() blocks until every earlier grid has
+// finished and its memory is visible: each kernel calls it before its first
+// global-memory access. griddep_launch_dependents() lets the next kernel's
+// launch begin (it still waits for this one to finish before touching memory).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::); }
+
 // ---------------------------------------------------------------- bf16 ----
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {

@@ -92,6 +92,7 @@ __device__ __forceinline__ void fill_rope_table(const int32_t* pos, const RopeTa
 
 template <int HD, bool SECTIONED, bool ROPE, bool SAVE, bool POOL>
 __global__ void __launch_bounds__(kThreads, 2) qkvp_fwd_kernel(const FwdArgs a) {
+  griddep_wait();
   using G = Geom<HD>;
   constexpr int CPH = G::CPH, HALF = G::HALF, U = kFwdChunksPerThread;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -200,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 2) qkvp_fwd_kernel(const FwdArgs a) 
 
 template <int HD, bool SECTIONED, bool ROPE>
 __global__ void __launch_bounds__(kThreads, 2) qkvp_bwd_kernel(const BwdArgs a) {
+  griddep_wait();
   using G = Geom<HD>;
   constexpr int CPH = G::CPH, HALF = G::HALF, U = kBwdChunksPerThread;
   extern __shared__ __align__(16) unsigned char smem[];

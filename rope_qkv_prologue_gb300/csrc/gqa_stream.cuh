@@ -134,6 +134,7 @@ __device__ __forceinline__ void stream_producer(unsigned char* smem, int hd, int
       phase ^= 1;
     }
   }
+  griddep_launch_dependents();  // every load of this CTA is issued
   if (!ok && lane == 0) {
     // Let the copies already issued land before this CTA can exit.
     const int64_t first = issued > stages ? issued - stages : 0;
@@ -145,6 +146,7 @@ __device__ __forceinline__ void stream_producer(unsigned char* smem, int hd, int
 
 template <int HD, bool SECTIONED, bool ROPE, bool SAVE, bool POOL, int NCW, int CPS>
 __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_fwd_stream_kernel(const FwdArgs a) {
+  griddep_wait();
   using G = Geom<HD>;
   constexpr int CPH = G::CPH, HALF = G::HALF, NCT = NCW * 32, MAXM = kStreamMaxSteps;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -289,6 +291,7 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_fwd_stream_kernel(co
 
 template <int HD, bool SECTIONED, bool ROPE, int NCW, int CPS>
 __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(const BwdArgs a) {
+  griddep_wait();
   using G = Geom<HD>;
   constexpr int CPH = G::CPH, HALF = G::HALF, NCT = NCW * 32, MAXM = kStreamMaxSteps;
   extern __shared__ __align__(128) unsigned char smem[];

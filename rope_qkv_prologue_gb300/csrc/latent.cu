@@ -14,6 +14,7 @@ namespace qkvp {
 
 template <bool POOL, bool ROPE, int NCL>
 __global__ void __launch_bounds__(kLatentWarps * 32) qkvp_latent_kernel(const LatentArgs a) {
+  griddep_wait();
   constexpr int TPW = kLatentTokensPerWarp;
   const int lane = threadIdx.x & 31;
   const int64_t warp_id = (int64_t)blockIdx.x * kLatentWarps + (threadIdx.x >> 5);
@@ -100,6 +101,7 @@ __global__ void __launch_bounds__(kLatentWarps * 32) qkvp_latent_kernel(const La
 
 // Staged write: copy contiguous rows [T, row_chunks] into pool slots.
 __global__ void __launch_bounds__(256) qkvp_scatter_kernel(const ScatterArgs a) {
+  griddep_wait();
   const int64_t total = a.T * a.row_chunks;
   for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < total; i += (int64_t)gridDim.x * 256) {
     const int64_t t = i / a.row_chunks;

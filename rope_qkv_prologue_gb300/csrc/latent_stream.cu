@@ -16,6 +16,7 @@ namespace qkvp {
 
 template <bool POOL, bool ROPE, int NCL, int NCW, int CPS>
 __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_latent_stream_kernel(const LatentArgs a) {
+  griddep_wait();
   constexpr int HD = 2;  // table layout: positions in the "cos" slots, pool slots after them
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + StreamSmem::kBarriers);

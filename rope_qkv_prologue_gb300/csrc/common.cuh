@@ -307,6 +307,38 @@ __device__ __forceinline__ float latent_sum_sq(const uint4 (&xr)[NCL], float2 (&
   return ss;
 }
 
+// r = 1 / sqrt(ss / n + eps) for R = 1, 2 or 4 rows at once; s[j] is this
+// lane's partial sum of squares of row j, r[j] comes back in every lane.
+// The reduction is latent_sum_sq's xor butterfly (partners 16, 8, 4, 2, 1)
+// with rows traded instead of copied: at partner 16 a lane keeps the rows of
+// its half (h = lane bit 4) and sends the others, at partner 8 (R = 4) it
+// keeps one row of the two (g = lane bit 3). Every addition adds the same two
+// values as the butterfly does, so each row's sum and r have the bits
+// latent_sum_sq gives, with 2 + 1 + 3 shuffles for four rows instead of 20.
+template <int R>
+__device__ __forceinline__ void latent_rsqrt_rows(const float (&s)[R], float inv_n, float eps, float (&r)[R]) {
+  static_assert(R == 1 || R == 2 || R == 4, "1, 2 or 4 rows");
+  const int lane = threadIdx.x & 31;
+  const bool h = (lane & 16) != 0, g = (lane & 8) != 0;
+  float u;
+  if constexpr (R == 4) {
+    const float t0 = (h ? s[2] : s[0]) + __shfl_xor_sync(0xffffffffu, h ? s[0] : s[2], 16);
+    const float t1 = (h ? s[3] : s[1]) + __shfl_xor_sync(0xffffffffu, h ? s[1] : s[3], 16);
+    u = (g ? t1 : t0) + __shfl_xor_sync(0xffffffffu, g ? t0 : t1, 8);  // row 2h + g
+  } else if constexpr (R == 2) {
+    u = (h ? s[1] : s[0]) + __shfl_xor_sync(0xffffffffu, h ? s[0] : s[1], 16);  // row h
+    u += __shfl_xor_sync(0xffffffffu, u, 8);
+  } else {
+    u = s[0] + __shfl_xor_sync(0xffffffffu, s[0], 16);
+    u += __shfl_xor_sync(0xffffffffu, u, 8);
+  }
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+  const float rr = rsqrtf(fmaf(u, inv_n, eps));
+#pragma unroll
+  for (int j = 0; j < R; ++j) r[j] = R == 1 ? rr : __shfl_sync(0xffffffffu, rr, j * (32 / R));
+}
+
 __device__ __forceinline__ uint4 latent_norm_chunk(const float2 (&x)[4], float r, const float2 (&w)[4]) {
   const float2 rr = f2(r, r);
   float2 y[4];
@@ -330,6 +362,25 @@ __device__ __forceinline__ void latent_rope_pair(const uint4& rlo, const uint4& 
   }
   olo = pack8(yl);
   ohi = pack8(yh);
+}
+
+// The same rotation for half a chunk pair: lo = values 8e + 4h .. 8e + 4h + 3
+// of the rope part, hi = their partners 32 further on (c, sn: cos / sin of
+// those four frequencies).
+__device__ __forceinline__ void latent_rope_quad(const uint2& rlo, const uint2& rhi, const float (&c)[4],
+                                                 const float (&sn)[4], uint2& olo, uint2& ohi) {
+  const float xl[4] = {__uint_as_float(rlo.x << 16), __uint_as_float(rlo.x & 0xffff0000u),
+                       __uint_as_float(rlo.y << 16), __uint_as_float(rlo.y & 0xffff0000u)};
+  const float xh[4] = {__uint_as_float(rhi.x << 16), __uint_as_float(rhi.x & 0xffff0000u),
+                       __uint_as_float(rhi.y << 16), __uint_as_float(rhi.y & 0xffff0000u)};
+  float yl[4], yh[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    yl[i] = fmaf(xl[i], c[i], xh[i] * -sn[i]);
+    yh[i] = fmaf(xh[i], c[i], xl[i] * sn[i]);
+  }
+  olo = make_uint2(pack2(yl[0], yl[1]), pack2(yl[2], yl[3]));
+  ohi = make_uint2(pack2(yh[0], yh[1]), pack2(yh[2], yh[3]));
 }
 
 // ---------------------------------------------------------- division ----

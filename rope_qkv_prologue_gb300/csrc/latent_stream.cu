@@ -4,12 +4,14 @@
 //
 // A tile is kLatentTileTokens consecutive rows. The producer warp bulk-copies
 // the tile's rows into a stage and writes the tile's positions and checked
-// pool slots beside it. Each consumer warp takes groups of 8 consecutive rows:
-//   * norm part, row by row: lane l holds norm chunks l, l + 32, ... of the
-//     row, the whole warp reduces its sum of squares;
-//   * rope part, all 8 rows at once: lane l takes row l / 4 and its rope chunk
-//     pair (e, e + 4), e = l % 4 (values 8e .. 8e+7 and their rotate-half
-//     partners), and computes the 8 angles it needs itself.
+// pool slots beside it. Each consumer warp takes groups of 4 consecutive rows:
+//   * norm part, 4 / NCL rows at a time (32 values per lane, NCL = norm chunks
+//     per lane): lane l holds norm chunks l, l + 32, ... of each row, and one
+//     row-trading butterfly reduces the rows' sums of squares together;
+//   * rope part, all four rows at once: lane l takes row l / 8, rope chunk pair
+//     (e, e + 4) with e = (l / 2) % 4, and half h = l % 2 of it (values
+//     8e + 4h .. 8e + 4h + 3 and their rotate-half partners), and computes the
+//     4 angles it needs itself.
 #include "gqa_stream.cuh"
 
 namespace qkvp {
@@ -18,6 +20,7 @@ template <bool POOL, bool ROPE, int NCL, int NCW, int CPS>
 __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_latent_stream_kernel(const LatentArgs a) {
   griddep_wait();
   constexpr int HD = 2;  // table layout: positions in the "cos" slots, pool slots after them
+  constexpr int RB = 4 / NCL;  // norm rows per reduction: 32 values per lane in flight (register budget)
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + StreamSmem::kBarriers);
   uint64_t* empty = full + kMaxStages;
@@ -51,7 +54,7 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_latent_stream_kernel
   }
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int kr = lane >> 2, e = lane & 3;  // rope part: row of the group, chunk pair
+  const int kr = lane >> 3, e = (lane >> 1) & 3, hh = lane & 1;  // rope part: row of the group, pair, half
   float2 w[NCL][4];
 #pragma unroll
   for (int m = 0; m < NCL; ++m) {
@@ -61,6 +64,9 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_latent_stream_kernel
       w[m][i] = chunk < a.norm_chunks ? f2(__ldg(a.w + chunk * 8 + 2 * i), __ldg(a.w + chunk * 8 + 2 * i + 1))
                                       : f2(0.f, 0.f);
   }
+  uint64_t turns[4];  // this lane's four rope frequencies (fixed for the whole kernel)
+#pragma unroll
+  for (int i = 0; i < 4; ++i) turns[i] = ROPE ? a.rope.turns[8 * e + 4 * hh + i] : 0;
   const unsigned char* data = smem + StreamSmem::data(HD, tpt, stages);
 
   int s = 0;
@@ -74,62 +80,70 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_latent_stream_kernel
                                                            s * StreamSmem::table_stride(HD, tpt));
     const int32_t* slots = spos + 2 * tpt * (HD / 2);
 
-    for (int g0 = 8 * warp; g0 < tpt; g0 += 8 * NCW) {
-      // norm part, row by row (two rows interleaved)
-#pragma unroll 2
-      for (int k = 0; k < 8; ++k) {
-        const int tl = g0 + k;
-        const int64_t t = t0 + tl;
-        const uint4* row = sx + tl * a.row_chunks;
-        uint4 xr[NCL];
+    for (int g0 = 4 * warp; g0 < tpt; g0 += 4 * NCW) {
+      // norm part: the group's rows, RB at a time (one shared reduction for all of them)
+#pragma unroll 1
+      for (int k0 = 0; k0 < 4; k0 += RB) {
+        float2 x[RB][NCL][4];
+        float ss[RB], r[RB];
 #pragma unroll
-        for (int m = 0; m < NCL; ++m) {
-          const int chunk = lane + 32 * m;
-          xr[m] = chunk < a.norm_chunks ? row[chunk] : make_uint4(0u, 0u, 0u, 0u);
-        }
-        float2 x[NCL][4];
-        const float r = rsqrtf(fmaf(latent_sum_sq<NCL>(xr, x), a.inv_norm_dim, a.eps));
-        if (t >= a.T) continue;  // warp-uniform
-        uint4* dst;
-        if (POOL) {
-          const int32_t slot = slots[tl];
-          if (slot < 0) continue;  // bad page / offset: reported by the producer, store skipped
-          dst = a.pool + (int64_t)slot * a.row_chunks;
-        } else {
-          dst = a.out + t * a.row_chunks;
-        }
+        for (int j = 0; j < RB; ++j) {
+          const uint4* row = sx + (g0 + k0 + j) * a.row_chunks;
+          ss[j] = 0.f;
 #pragma unroll
-        for (int m = 0; m < NCL; ++m) {
-          const int chunk = lane + 32 * m;
-          if (chunk < a.norm_chunks) st_keep(dst + chunk, latent_norm_chunk(x[m], r, w[m]));
+          for (int m = 0; m < NCL; ++m) {
+            const int chunk = lane + 32 * m;
+            unpack_pairs(chunk < a.norm_chunks ? row[chunk] : make_uint4(0u, 0u, 0u, 0u), x[j][m]);
+            ss[j] += chunk_partial_sq(x[j][m]);  // the per-lane partial of latent_sum_sq
+          }
         }
-      }
-      // rope part: lane -> (row g0 + kr, chunk pair e)
-      {
-        const int tl = g0 + kr;
-        const int64_t t = t0 + tl;
-        const uint4* row = sx + tl * a.row_chunks;
-        const uint4 rlo = row[a.norm_chunks + e], rhi = row[a.norm_chunks + e + 4];
-        uint4 olo = rlo, ohi = rhi;
-        if (ROPE) {
-          float c[8], sn[8];
-          const int32_t p = spos[tl];
+        latent_rsqrt_rows<RB>(ss, a.inv_norm_dim, a.eps, r);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) rope_cos_sin(p, a.rope.turns[8 * e + i], &c[i], &sn[i]);
-          latent_rope_pair(rlo, rhi, c, sn, olo, ohi);
-        }
-        uint4* dst = nullptr;
-        if (t < a.T) {
+        for (int j = 0; j < RB; ++j) {
+          const int tl = g0 + k0 + j;
+          const int64_t t = t0 + tl;
+          if (t >= a.T) break;  // warp-uniform; the rows after it are past the end too
+          uint4* dst;
           if (POOL) {
             const int32_t slot = slots[tl];
-            if (slot >= 0) dst = a.pool + (int64_t)slot * a.row_chunks;
+            if (slot < 0) continue;  // bad page / offset: reported by the producer, store skipped
+            dst = a.pool + (int64_t)slot * a.row_chunks;
           } else {
             dst = a.out + t * a.row_chunks;
           }
+#pragma unroll
+          for (int m = 0; m < NCL; ++m) {
+            const int chunk = lane + 32 * m;
+            if (chunk < a.norm_chunks) st_keep(dst + chunk, latent_norm_chunk(x[j][m], r[j], w[m]));
+          }
+        }
+      }
+      // rope part: lane -> (row g0 + kr, chunk pair e, half hh)
+      {
+        const int tl = g0 + kr;
+        const int64_t t = t0 + tl;
+        const uint2* row = reinterpret_cast<const uint2*>(sx + tl * a.row_chunks + a.norm_chunks);
+        const uint2 rlo = row[2 * e + hh], rhi = row[2 * (e + 4) + hh];
+        uint2 olo = rlo, ohi = rhi;
+        if (ROPE) {
+          float c[4], sn[4];
+          const int32_t p = spos[tl];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) rope_cos_sin(p, turns[i], &c[i], &sn[i]);
+          latent_rope_quad(rlo, rhi, c, sn, olo, ohi);
+        }
+        uint2* dst = nullptr;
+        if (t < a.T) {
+          if (POOL) {
+            const int32_t slot = slots[tl];
+            if (slot >= 0) dst = reinterpret_cast<uint2*>(a.pool + (int64_t)slot * a.row_chunks + a.norm_chunks);
+          } else {
+            dst = reinterpret_cast<uint2*>(a.out + t * a.row_chunks + a.norm_chunks);
+          }
         }
         if (dst) {
-          st_keep(dst + a.norm_chunks + e, olo);
-          st_keep(dst + a.norm_chunks + e + 4, ohi);
+          dst[2 * e + hh] = olo;
+          dst[2 * (e + 4) + hh] = ohi;
         }
       }
     }

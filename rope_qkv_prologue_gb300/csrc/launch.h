@@ -206,8 +206,8 @@ constexpr int kFinalizeThreads = 256;
 
 constexpr int kLatentWarps = 8;        // warps per CTA of the latent kernel
 constexpr int kLatentTokensPerWarp = 2;
-constexpr int kLatentTileTokens = 32;     // rows per tile of the pipelined latent kernel
-constexpr int kLatentStreamWarps = 4;     // its consumer warps (+1 producer); tile = 8 rows per warp
-constexpr int kLatentStreamCtasPerSm = 2;
+constexpr int kLatentTileTokens = 16;     // rows per tile of the pipelined latent kernel
+constexpr int kLatentStreamWarps = 4;     // its consumer warps (+1 producer); 4 rows per warp per tile
+constexpr int kLatentStreamCtasPerSm = 4; // small tiles and many CTAs: the first rows arrive early
 
 }  // namespace qkvp

@@ -14,7 +14,13 @@ reason, in the design notes of this repository):
   theta = pos * inv_freq_i,
       o_i       = y_i cos(theta) - y_{i+D/2} sin(theta)
       o_{i+D/2} = y_{i+D/2} cos(theta) + y_i sin(theta).
-  No frequency scaling. NoPE layers skip it.
+  No frequency scaling of its own. NoPE layers skip it.
+* The GQAttention variant (the follow-up the pages name for Llama 3, Qwen3
+  and GPT-OSS: "split -> norm -> RoPE" in GQAttention, GPT-OSS with a qkv
+  bias): the norm can be off (split -> RoPE); a bias in the packed row's
+  order is added first (before the norm); a caller-given inv_freq table and a
+  cos/sin factor stand for those models' frequency scalings. Training saves
+  the input heads before the bias; the backward adds it back.
 * Norm first, then RoPE ("split -> norm -> RoPE" in the after-diagram of
   "[muse_spark][perf] Split the packed qkv inside the q/k region", Solution).
 * One rounding to bf16 at the very end; nothing is rounded between the norm
@@ -158,64 +164,94 @@ def rope_inv_freq(head_dim, base):
     return np.power(float(base), -2.0 * i / head_dim)
 
 
-def rope_angles(pos, head_dim, base):
-    """theta[t, i] = pos[t] * inv_freq_i, float64."""
+def rope_angles(pos, head_dim, base, inv_freq=None):
+    """theta[t, i] = pos[t] * inv_freq_i, float64. A caller-given inv_freq
+    (D/2 values) replaces base**(-2 i / D): the frequency scalings of the
+    GQAttention users (Llama 3's, YaRN's) only change this table."""
     pos = np.asarray(pos, dtype=np.float64).reshape(-1, 1)
-    return pos * rope_inv_freq(head_dim, base)[None, :]
+    f = rope_inv_freq(head_dim, base) if inv_freq is None else np.asarray(inv_freq, dtype=np.float64)
+    assert f.shape == (head_dim // 2,)
+    return pos * f[None, :]
 
 
-def rope_rotate_half(y, pos, base):
-    """Rotate each head of y [T, h, D] by the angles of its token's position."""
+def rope_rotate_half(y, pos, base, inv_freq=None, scale=1.0):
+    """Rotate each head of y [T, h, D] by the angles of its token's position.
+    cos and sin are both multiplied by `scale` (YaRN's attention factor; 1 for
+    plain RoPE)."""
     y = np.asarray(y, dtype=np.float64)
     D = y.shape[-1]
     half = D // 2
-    th = rope_angles(pos, D, base)[:, None, :]
-    c, s = np.cos(th), np.sin(th)
+    th = rope_angles(pos, D, base, inv_freq)[:, None, :]
+    c, s = np.cos(th) * scale, np.sin(th) * scale
     a, b = y[..., :half], y[..., half:]
     return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
 
 
-def rope_rotate_half_transpose(d, pos, base):
-    """Apply R(theta)^T = R(-theta): the backward of rope_rotate_half."""
+def rope_rotate_half_transpose(d, pos, base, inv_freq=None, scale=1.0):
+    """Apply (scale R(theta))^T = scale R(-theta): the backward of rope_rotate_half."""
     d = np.asarray(d, dtype=np.float64)
     D = d.shape[-1]
     half = D // 2
-    th = rope_angles(pos, D, base)[:, None, :]
-    c, s = np.cos(th), np.sin(th)
+    th = rope_angles(pos, D, base, inv_freq)[:, None, :]
+    c, s = np.cos(th) * scale, np.sin(th) * scale
     a, b = d[..., :half], d[..., half:]
     return np.concatenate([a * c + b * s, b * c - a * s], axis=-1)
+
+
+# --------------------------------------------------------------------------
+# The GQAttention variant (Llama 3, Qwen3, GPT-OSS): a qkv bias and no norm
+# --------------------------------------------------------------------------
+
+def add_bias(packed, bias):
+    """packed [T, row_width] + bias [row_width]: the fused linear's bias, given
+    in the packed row's own order, added to every token before the split."""
+    x = np.asarray(packed, dtype=np.float64)
+    if bias is None:
+        return x
+    b = np.asarray(bias, dtype=np.float64)
+    assert b.shape == (x.shape[-1],)
+    return x + b[None, :]
 
 
 # --------------------------------------------------------------------------
 # S1-S4: the forward
 # --------------------------------------------------------------------------
 
-def prologue_fwd_f64(layout, packed, pos, w_q, w_k, eps, rope_base, nope=False):
-    """Forward on float64 packed rows [T, row_width]: returns exact q, k, v."""
-    x = np.asarray(packed, dtype=np.float64)
+def prologue_fwd_f64(layout, packed, pos, w_q, w_k, eps, rope_base, nope=False,
+                     norm=True, bias=None, inv_freq=None, rope_scale=1.0):
+    """Forward on float64 packed rows [T, row_width]: returns exact q, k, v.
+
+    The variant options: `bias` is added to the whole row first; `norm=False`
+    skips the RMSNorm (split -> RoPE only); `inv_freq` / `rope_scale` as in
+    rope_rotate_half."""
+    x = add_bias(packed, bias)
     xq, xk, xv = split_heads(layout, x)
-    q = rms_norm(xq, w_q, eps)
-    k = rms_norm(xk, w_k, eps)
+    q = rms_norm(xq, w_q, eps) if norm else xq
+    k = rms_norm(xk, w_k, eps) if norm else xk
     if not nope:
-        q = rope_rotate_half(q, pos, rope_base)
-        k = rope_rotate_half(k, pos, rope_base)
+        q = rope_rotate_half(q, pos, rope_base, inv_freq, rope_scale)
+        k = rope_rotate_half(k, pos, rope_base, inv_freq, rope_scale)
     return q, k, xv
 
 
-def prologue_fwd(layout, packed_bits, pos, w_q, w_k, eps, rope_base, nope=False):
+def prologue_fwd(layout, packed_bits, pos, w_q, w_k, eps, rope_base, nope=False,
+                 norm=True, bias=None, inv_freq=None, rope_scale=1.0):
     """Forward on bf16 packed rows (uint16 bits [T, row_width]).
 
     Returns a dict:
-      q, k     exact float64 outputs [T, n_q, D], [T, n_kv, D] (round with
+      q, k, v  exact float64 outputs [T, n_q, D], [T, n_kv, D] (round with
                to_bf16_rne to get the bf16 bits a kernel should store);
-      v_bits   the v heads' input bits (v is a pure copy);
-      q_pre_bits, k_pre_bits   the split pre-norm heads' input bits (what
-               training saves for the backward).
+      v_bits   the v heads' output bits: the input bits when there is no bias
+               (v is a pure copy), else v rounded once;
+      q_pre_bits, k_pre_bits   the split input heads' bits, before any bias
+               (what training saves for the backward).
     """
     bits = np.asarray(packed_bits, dtype=np.uint16).reshape(-1, layout.row_width)
-    q, k, _ = prologue_fwd_f64(layout, bf16_bits_to_f64(bits), pos, w_q, w_k, eps, rope_base, nope)
+    q, k, v = prologue_fwd_f64(layout, bf16_bits_to_f64(bits), pos, w_q, w_k, eps, rope_base, nope,
+                               norm, bias, inv_freq, rope_scale)
     qb, kb, vb = split_heads(layout, bits)
-    return {"q": q, "k": k, "v_bits": vb, "q_pre_bits": qb, "k_pre_bits": kb}
+    return {"q": q, "k": k, "v": v, "v_bits": vb if bias is None else to_bf16_rne(v),
+            "q_pre_bits": qb, "k_pre_bits": kb}
 
 
 # --------------------------------------------------------------------------
@@ -236,13 +272,14 @@ def pool_scatter(pool_bits, rows_bits, page, offset):
 
 
 def pool_write(layout, packed_bits, pos, w_q, w_k, eps, rope_base, nope,
-               page, offset, k_pool_bits, v_pool_bits):
+               page, offset, k_pool_bits, v_pool_bits, **variant):
     """GQA decode write: q contiguous, normed(+roped) k and raw v into the pools.
 
     Defined as the contiguous forward followed by the staged scatter.
+    `variant` takes prologue_fwd's norm / bias / inv_freq / rope_scale.
     Returns (q exact float64, k exact float64, new k pool bits, new v pool bits).
     """
-    out = prologue_fwd(layout, packed_bits, pos, w_q, w_k, eps, rope_base, nope)
+    out = prologue_fwd(layout, packed_bits, pos, w_q, w_k, eps, rope_base, nope, **variant)
     k_pool = pool_scatter(k_pool_bits, to_bf16_rne(out["k"]), page, offset)
     v_pool = pool_scatter(v_pool_bits, out["v_bits"], page, offset)
     return out["q"], out["k"], k_pool, v_pool
@@ -276,32 +313,42 @@ def mla_pool_write(rows_bits, pos, w, eps, rope_base, page, offset, pool_bits,
 # S7 / S8: the backward
 # --------------------------------------------------------------------------
 
-def prologue_bwd_f64(layout, dq, dk, dv, q_pre, k_pre, pos, w_q, w_k, eps, rope_base, nope=False):
+def prologue_bwd_f64(layout, dq, dk, dv, q_pre, k_pre, pos, w_q, w_k, eps, rope_base, nope=False,
+                     norm=True, bias=None, inv_freq=None, rope_scale=1.0):
     """Backward on float64 arrays.
 
     dq [T,n_q,D], dk/dv [T,n_kv,D] are the gradients of the forward's outputs;
-    q_pre/k_pre are the split pre-norm heads. Returns
+    q_pre/k_pre are the split input heads (before any bias). Returns
       dpacked [T, row_width]  gradient w.r.t. the packed input, in the input
                               layout (v slots hold dv unchanged);
       dw_q, dw_k [D]          gradients of the two RMSNorm weights, summed over
-                              every token and head.
+                              every token and head (zero without the norm);
+      db [row_width] or None  gradient of the bias: dpacked summed over tokens.
     """
     dq = np.asarray(dq, dtype=np.float64)
     dk = np.asarray(dk, dtype=np.float64)
     if nope:
         gq, gk = dq, dk
     else:
-        gq = rope_rotate_half_transpose(dq, pos, rope_base)
-        gk = rope_rotate_half_transpose(dk, pos, rope_base)
-    dxq, tq = rms_norm_backward(q_pre, w_q, gq, eps)
-    dxk, tk = rms_norm_backward(k_pre, w_k, gk, eps)
+        gq = rope_rotate_half_transpose(dq, pos, rope_base, inv_freq, rope_scale)
+        gk = rope_rotate_half_transpose(dk, pos, rope_base, inv_freq, rope_scale)
+    if norm:
+        # the norm saw the biased input: put the bias back on the saved heads
+        bq, bk, _ = split_heads(layout, add_bias(np.zeros((1, layout.row_width)), bias))
+        dxq, tq = rms_norm_backward(np.asarray(q_pre, dtype=np.float64) + bq, w_q, gq, eps)
+        dxk, tk = rms_norm_backward(np.asarray(k_pre, dtype=np.float64) + bk, w_k, gk, eps)
+        dw_q, dw_k = tq.sum(axis=(0, 1)), tk.sum(axis=(0, 1))
+    else:
+        dxq, dxk = gq, gk
+        dw_q = dw_k = np.zeros(layout.head_dim)
     dpacked = merge_heads(layout, dxq, dxk, np.asarray(dv, dtype=np.float64))
-    return {"dpacked": dpacked, "dw_q": tq.sum(axis=(0, 1)), "dw_k": tk.sum(axis=(0, 1))}
+    db = None if bias is None else dpacked.sum(axis=0)
+    return {"dpacked": dpacked, "dw_q": dw_q, "dw_k": dw_k, "db": db}
 
 
 def prologue_bwd(layout, dq_bits, dk_bits, dv_bits, q_pre_bits, k_pre_bits,
-                 pos, w_q, w_k, eps, rope_base, nope=False):
+                 pos, w_q, w_k, eps, rope_base, nope=False, **variant):
     """prologue_bwd_f64 on bf16 bit inputs; results stay exact float64."""
     f = bf16_bits_to_f64
     return prologue_bwd_f64(layout, f(dq_bits), f(dk_bits), f(dv_bits), f(q_pre_bits),
-                            f(k_pre_bits), pos, w_q, w_k, eps, rope_base, nope)
+                            f(k_pre_bits), pos, w_q, w_k, eps, rope_base, nope, **variant)

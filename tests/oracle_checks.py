@@ -17,6 +17,10 @@ What pins what:
   backward          central finite differences of the forward, eps=0
                     orthogonality, R^T as the adjoint of R, dv passthrough
   pool writes       exact placement and untouched bytes
+  variant options   norm off = pure split / pairwise-norm keeping rotation,
+                    bias order through the pinned split, bias before the norm
+                    (rms 1) and the rotation, one-hot frequency tables, the
+                    cos/sin factor at position 0, finite differences of all
 """
 
 import math
@@ -236,13 +240,16 @@ def check_nope_is_rope_at_zero(P, layout, rng, T=4):
 
 # ------------------------------------------------------------ backward ----
 
-def _loss(P, layout, x, wq, wk, pos, eps, base, nope, dq, dk, dv):
-    q, k, v = P.prologue_fwd_f64(layout, x, pos, wq, wk, eps, base, nope)
+def _loss(P, layout, x, wq, wk, pos, eps, base, nope, dq, dk, dv, variant):
+    q, k, v = P.prologue_fwd_f64(layout, x, pos, wq, wk, eps, base, nope, **variant)
     return np.sum(dq * q) + np.sum(dk * k) + np.sum(dv * v)
 
 
-def check_finite_differences(P, layout, rng, T=3, nope=False, n_probe=None, base=10000.0):
-    """Central differences of L = <dq,q> + <dk,k> + <dv,v> against prologue_bwd_f64."""
+def check_finite_differences(P, layout, rng, T=3, nope=False, n_probe=None, base=10000.0, **variant):
+    """Central differences of L = <dq,q> + <dk,k> + <dv,v> against prologue_bwd_f64.
+
+    `variant` (norm / bias / inv_freq / rope_scale) goes to both the forward and
+    the backward; with a bias the bias gradient is probed too."""
     D = layout.head_dim
     x = rng.standard_normal((T, layout.row_width))
     wq, wk = rng.uniform(0.5, 1.5, D), rng.uniform(0.5, 1.5, D)
@@ -252,9 +259,12 @@ def check_finite_differences(P, layout, rng, T=3, nope=False, n_probe=None, base
     dk = rng.standard_normal((T, layout.n_kv, D))
     dv = rng.standard_normal((T, layout.n_kv, D))
     xq, xk, _ = P.split_heads(layout, x)
-    got = P.prologue_bwd_f64(layout, dq, dk, dv, xq, xk, pos, wq, wk, eps, base, nope)
+    got = P.prologue_bwd_f64(layout, dq, dk, dv, xq, xk, pos, wq, wk, eps, base, nope, **variant)
     args = (pos, eps, base, nope, dq, dk, dv)
     h = 1e-6
+
+    def loss(xx, a, b, var):
+        return _loss(P, layout, xx, a, b, *args, var)
 
     idx = [(t, j) for t in range(T) for j in range(layout.row_width)]
     if n_probe is not None:
@@ -264,7 +274,7 @@ def check_finite_differences(P, layout, rng, T=3, nope=False, n_probe=None, base
         xp, xm = x.copy(), x.copy()
         xp[t, j] += h
         xm[t, j] -= h
-        fd = (_loss(P, layout, xp, wq, wk, *args) - _loss(P, layout, xm, wq, wk, *args)) / (2 * h)
+        fd = (loss(xp, wq, wk, variant) - loss(xm, wq, wk, variant)) / (2 * h)
         an = got["dpacked"][t, j]
         assert abs(fd - an) <= 1e-6 * (1 + abs(an)), (t, j, fd, an)
     for which, w in (("dw_q", wq), ("dw_k", wk)):
@@ -273,14 +283,24 @@ def check_finite_differences(P, layout, rng, T=3, nope=False, n_probe=None, base
             wp[d] += h
             wm[d] -= h
             if which == "dw_q":
-                lp = _loss(P, layout, x, wp, wk, *args)
-                lm = _loss(P, layout, x, wm, wk, *args)
+                lp, lm = loss(x, wp, wk, variant), loss(x, wm, wk, variant)
             else:
-                lp = _loss(P, layout, x, wq, wp, *args)
-                lm = _loss(P, layout, x, wq, wm, *args)
+                lp, lm = loss(x, wq, wp, variant), loss(x, wq, wm, variant)
             fd = (lp - lm) / (2 * h)
             an = got[which][d]
             assert abs(fd - an) <= 1e-6 * (1 + abs(an)), (which, d, fd, an)
+    if variant.get("bias") is not None:
+        b = np.asarray(variant["bias"], dtype=np.float64)
+        cols = range(layout.row_width) if n_probe is None else rng.choice(layout.row_width, n_probe, replace=False)
+        for j in cols:
+            bp, bm = b.copy(), b.copy()
+            bp[j] += h
+            bm[j] -= h
+            fd = (loss(x, wq, wk, dict(variant, bias=bp)) - loss(x, wq, wk, dict(variant, bias=bm))) / (2 * h)
+            an = got["db"][j]
+            assert abs(fd - an) <= 1e-6 * (1 + abs(an)), ("db", j, fd, an)
+    else:
+        assert got["db"] is None
 
 
 def check_backward_invariants(P, layout, rng, T=5):
@@ -348,3 +368,98 @@ def check_mla_rows(P, rng):
     # position 0 leaves the rope part unchanged
     o0 = P.mla_rows_f64(x, np.zeros(T, np.int64), w, 0.0, 1e4, 512, 64)
     assert np.array_equal(o0[:, 512:], x[:, 512:])
+
+
+# ------------------------------------------------ GQAttention variant ----
+
+def check_variant_forward(P, rng):
+    """Norm off, the qkv bias: what each option does, from facts outside the
+    oracle's own formulas (the pinned split, pairwise norms, closed values)."""
+    for kind in ("interleaved", "sectioned"):
+        layout = P.PackedLayout(kind, 8, 2, 64)
+        T, D, W, h = 4, layout.head_dim, layout.row_width, layout.head_dim // 2
+        x = rng.standard_normal((T, W))
+        pos = rng.integers(1, 131072, T)
+        ones = np.ones(D)
+        xq, xk, xv = P.split_heads(layout, x)
+        # norm off and NoPE: a pure split
+        q, k, v = P.prologue_fwd_f64(layout, x, pos, ones, ones, 1e-6, 5e5, nope=True, norm=False)
+        assert np.array_equal(q, xq) and np.array_equal(k, xk) and np.array_equal(v, xv)
+        # norm off with RoPE: the identity at position 0, and it keeps every
+        # rotate-half pair's norm elsewhere (with the norm on it would not)
+        q0, k0, _ = P.prologue_fwd_f64(layout, x, np.zeros(T, np.int64), ones, ones, 1e-6, 5e5, norm=False)
+        assert np.array_equal(q0, xq) and np.array_equal(k0, xk)
+        q, k, _ = P.prologue_fwd_f64(layout, x, pos, ones, ones, 1e-6, 5e5, norm=False)
+        for o, i in ((q, xq), (k, xk)):
+            assert np.allclose(o[..., :h] ** 2 + o[..., h:] ** 2, i[..., :h] ** 2 + i[..., h:] ** 2,
+                               rtol=1e-12, atol=1e-13)
+            assert not np.allclose(o, i)
+        # the bias is in the packed row's order: with x = 0 and nothing else
+        # applied the outputs are the bias split by the pinned head-block table
+        b = np.arange(W, dtype=np.float64) + 1.0
+        z = np.zeros((T, W))
+        q, k, v = P.prologue_fwd_f64(layout, z, pos, ones, ones, 1e-6, 5e5, nope=True, norm=False, bias=b)
+        bq, bk, bv = P.split_heads(layout, np.tile(b, (T, 1)))
+        assert np.array_equal(q, bq) and np.array_equal(k, bk) and np.array_equal(v, bv)
+        # the bias goes in before the norm: w = 1, eps = 0 gives every head of the
+        # normed bias an rms of exactly 1 (added after the norm it would keep b's)
+        q, k, _ = P.prologue_fwd_f64(layout, z, pos, ones, ones, 0.0, 5e5, bias=b)
+        for o in (q, k):
+            assert np.allclose(np.sqrt(np.mean(o * o, axis=-1)), 1.0, rtol=0, atol=1e-14)
+        # and before the rotation: norm off, the roped bias keeps its pairwise norms
+        q, k, _ = P.prologue_fwd_f64(layout, z, pos, ones, ones, 1e-6, 5e5, norm=False, bias=b)
+        for o, i in ((q, bq), (k, bk)):
+            assert np.allclose(o[..., :h] ** 2 + o[..., h:] ** 2, i[..., :h] ** 2 + i[..., h:] ** 2,
+                               rtol=1e-12, atol=1e-9)
+        # a bias that cancels the input zeroes every output (norm: 0 * r * w = 0)
+        q, k, v = P.prologue_fwd_f64(layout, x[:1], pos[:1], ones, ones, 1e-6, 5e5, bias=-x[0])
+        assert not np.any(q) and not np.any(k) and not np.any(v)
+
+
+def check_rope_extras(P, rng):
+    """A caller-given frequency table and the cos/sin factor."""
+    D, h = 64, 32
+    pos = rng.integers(1, 131072, 5)
+    y = rng.standard_normal((5, 3, D))
+    # the default table passed explicitly changes nothing
+    f = P.rope_inv_freq(D, 5e5)
+    assert np.array_equal(P.rope_rotate_half(y, pos, 5e5, inv_freq=f), P.rope_rotate_half(y, pos, 5e5))
+    # a one-hot table turns pair 0 by pos radians (the base is not used) and
+    # leaves every other pair alone
+    one = np.zeros(h)
+    one[0] = 1.0
+    o = P.rope_rotate_half(y, pos, 5e5, inv_freq=one)
+    assert np.array_equal(o[..., 1:h], y[..., 1:h]) and np.array_equal(o[..., h + 1:], y[..., h + 1:])
+    p = pos.astype(np.float64)[:, None]
+    assert np.allclose(o[..., 0], y[..., 0] * np.cos(p) - y[..., h] * np.sin(p), rtol=0, atol=1e-12)
+    assert np.allclose(o[..., h], y[..., h] * np.cos(p) + y[..., 0] * np.sin(p), rtol=0, atol=1e-12)
+    # cos and sin both carry the factor: position 0 gives factor * y, and every
+    # pair's norm is multiplied by factor**2
+    assert np.array_equal(P.rope_rotate_half(y, np.zeros(5, np.int64), 5e5, scale=2.0), 2.0 * y)
+    o = P.rope_rotate_half(y, pos, 5e5, scale=1.5)
+    assert np.allclose(o[..., :h] ** 2 + o[..., h:] ** 2, 2.25 * (y[..., :h] ** 2 + y[..., h:] ** 2),
+                       rtol=1e-12, atol=1e-12)
+    # the transpose with the same table and factor is the adjoint
+    g = rng.standard_normal((5, 3, D))
+    ff = rng.uniform(0.0, 1.0, h)
+    lhs = np.sum(P.rope_rotate_half(g, pos, 1.0, inv_freq=ff, scale=1.3) * y)
+    rhs = np.sum(g * P.rope_rotate_half_transpose(y, pos, 1.0, inv_freq=ff, scale=1.3))
+    assert abs(lhs - rhs) <= 1e-11 * (1 + abs(lhs))
+
+
+def check_variant_backward(P, rng):
+    """Finite differences of the forward with every option, on tiny shapes."""
+    layout = P.PackedLayout("interleaved", 2, 1, 8)
+    W = layout.row_width
+    b = rng.standard_normal(W)
+    ff = rng.uniform(0.0, 1.0, layout.head_dim // 2)
+    check_finite_differences(P, layout, rng, T=2, norm=False)
+    check_finite_differences(P, layout, rng, T=2, norm=False, bias=b, inv_freq=ff, rope_scale=1.25)
+    check_finite_differences(P, layout, rng, T=2, bias=b)
+    check_finite_differences(P, P.PackedLayout("sectioned", 2, 1, 8), rng, T=2, bias=b, rope_scale=0.75)
+    # without the norm there is nothing for the weights: dw is zero
+    x = rng.standard_normal((3, W))
+    xq, xk, _ = P.split_heads(layout, x)
+    d = [rng.standard_normal((3, n, 8)) for n in (layout.n_q, layout.n_kv, layout.n_kv)]
+    out = P.prologue_bwd_f64(layout, *d, xq, xk, [1, 2, 3], np.ones(8), np.ones(8), 1e-6, 1e4, norm=False)
+    assert not np.any(out["dw_q"]) and not np.any(out["dw_k"])

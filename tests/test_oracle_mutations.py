@@ -13,22 +13,46 @@ import oracle_checks as C
 import workloads
 
 
-def _rope_sign_flipped(y, pos, base):
+def _rope_sign_flipped(y, pos, base, inv_freq=None, scale=1.0):
     y = np.asarray(y, dtype=np.float64)
     half = y.shape[-1] // 2
-    th = P.rope_angles(pos, y.shape[-1], base)[:, None, :]
+    th = P.rope_angles(pos, y.shape[-1], base, inv_freq)[:, None, :]
+    c, s = np.cos(th) * scale, np.sin(th) * scale
     a, b = y[..., :half], y[..., half:]
-    return np.concatenate([a * np.cos(th) + b * np.sin(th), b * np.cos(th) - a * np.sin(th)], axis=-1)
+    return np.concatenate([a * c + b * s, b * c - a * s], axis=-1)
 
 
-def _rope_adjacent_pairs(y, pos, base):
+def _rope_adjacent_pairs(y, pos, base, inv_freq=None, scale=1.0):
     y = np.asarray(y, dtype=np.float64)
-    th = P.rope_angles(pos, y.shape[-1], base)[:, None, :]
+    th = P.rope_angles(pos, y.shape[-1], base, inv_freq)[:, None, :]
+    c, s = np.cos(th) * scale, np.sin(th) * scale
     a, b = y[..., 0::2], y[..., 1::2]
     out = np.empty_like(y)
-    out[..., 0::2] = a * np.cos(th) - b * np.sin(th)
-    out[..., 1::2] = b * np.cos(th) + a * np.sin(th)
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = b * c + a * s
     return out
+
+
+def _rope_factor_on_cos_only(y, pos, base, inv_freq=None, scale=1.0):
+    y = np.asarray(y, dtype=np.float64)
+    half = y.shape[-1] // 2
+    th = P.rope_angles(pos, y.shape[-1], base, inv_freq)[:, None, :]
+    c, s = np.cos(th) * scale, np.sin(th)
+    a, b = y[..., :half], y[..., half:]
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
+def _angles_ignore_table(pos, head_dim, base, inv_freq=None):
+    return np.asarray(pos, dtype=np.float64).reshape(-1, 1) * P.rope_inv_freq(head_dim, base)[None, :]
+
+
+def _bias_reversed(packed, bias):
+    x = np.asarray(packed, dtype=np.float64)
+    return x if bias is None else x + np.asarray(bias, dtype=np.float64)[::-1][None, :]
+
+
+def _bias_dropped(packed, bias):
+    return np.asarray(packed, dtype=np.float64)
 
 
 def _inv_freq_wrong_exponent(head_dim, base):
@@ -88,8 +112,8 @@ def _bf16_via_float32(x):
 _REAL_ROPE = P.rope_rotate_half
 
 
-def _rope_transpose_is_forward(d, pos, base):
-    return _REAL_ROPE(d, pos, base)
+def _rope_transpose_is_forward(d, pos, base, inv_freq=None, scale=1.0):
+    return _REAL_ROPE(d, pos, base, inv_freq, scale)
 
 
 def _checks_all(rng):
@@ -103,6 +127,9 @@ def _checks_all(rng):
     C.check_backward_invariants(P, P.PackedLayout("interleaved", 8, 2, 64), rng)
     C.check_pool_placement(P, B, rng)
     C.check_mla_rows(P, rng)
+    C.check_variant_forward(P, rng)
+    C.check_rope_extras(P, rng)
+    C.check_variant_backward(P, rng)
 
 
 def test_unmutated_oracle_passes_every_pin(rng):
@@ -121,6 +148,10 @@ MUTATIONS = [
     (P, "head_blocks", _blocks_k_v_swapped),
     (P, "head_blocks", _blocks_q_transposed),
     (B, "to_bf16_rne", _bf16_via_float32),
+    (P, "rope_rotate_half", _rope_factor_on_cos_only),
+    (P, "rope_angles", _angles_ignore_table),
+    (P, "add_bias", _bias_reversed),
+    (P, "add_bias", _bias_dropped),
 ]
 
 

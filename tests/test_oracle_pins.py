@@ -131,3 +131,15 @@ def test_workload_repack_matches_layout_definition():
     xs = workloads.bits_u16(wl.sectioned_rows())
     for u, v in zip(P.split_heads(L, xi), P.split_heads(Ls, xs)):
         assert np.array_equal(u, v)
+
+
+def test_variant_forward_options(rng):
+    C.check_variant_forward(P, rng)
+
+
+def test_rope_frequency_table_and_factor(rng):
+    C.check_rope_extras(P, rng)
+
+
+def test_variant_backward_finite_differences(rng):
+    C.check_variant_backward(P, rng)

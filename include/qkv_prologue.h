@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define QKVP_VERSION 1
+#define QKVP_VERSION 2
 
 /* Status codes (return values). */
 typedef enum {
@@ -101,11 +101,40 @@ enum {
   QKVP_NOPE = 1,           /* NoPE layer: RMSNorm only, no rotation            */
   QKVP_SAVE_PRE = 2,       /* forward also writes the split pre-norm q and k   */
   QKVP_ACCUMULATE_DW = 4,  /* backward adds into dw_q / dw_k instead of writing */
-  QKVP_FORCE_GENERIC = 8   /* use the general kernels even where the
+  QKVP_FORCE_GENERIC = 8,  /* use the general kernels even where the
                               shared-memory pipelined ones apply (same output
                               bits; for A/B checks). The backward's weight-grad
                               sums may differ in rounding. */
+  QKVP_NORM_OFF = 16       /* GQA layouts: no RMSNorm of q and k (split ->
+                              RoPE only, the GQAttention variant of Llama 3 and
+                              GPT-OSS). w_q / w_k may be NULL; the backward
+                              reads neither q_pre nor k_pre and has no weight
+                              gradients (dw_q / dw_k may be NULL, untouched). */
 };
+
+/* Options of the GQAttention variant (the *_ex entry points; NULL = none).
+ *
+ * "[muse_spark][perf] Split the packed qkv inside the q/k region" names the
+ * follow-up: a split -> norm -> RoPE region in GQAttention for Llama 3, Qwen3
+ * and GPT-OSS (GPT-OSS with a qkv bias). Those models scale their RoPE
+ * frequencies (Llama 3's and YaRN's scalings) and YaRN multiplies cos and sin
+ * by a factor; both only change the inputs below, the rotation is the same.
+ *
+ * inv_freq    HOST array of head_dim / 2 (LATENT: rope_dim / 2) float64
+ *             frequencies replacing rope_base^(-2 i / D), or NULL. Finite.
+ * rope_scale  factor on cos and sin (o = scale * R(theta) y); 0 means 1.
+ * bias        DEVICE float32 [(n_q + 2 n_kv) * head_dim], 16-byte aligned, in
+ *             the packed row's own order (the fused linear's output bias), or
+ *             NULL. Added to every token's row before anything else: the norm
+ *             (if on) sees x + b, and v becomes round(x + b) instead of a bit
+ *             copy. q_pre / k_pre stay the input heads WITHOUT the bias; the
+ *             backward adds it back. GQA layouts only.
+ */
+typedef struct {
+  const double* inv_freq;
+  double rope_scale;
+  const float* bias;
+} qkvp_variant;
 
 /* Device-side status bits (pool writes): set with an atomic OR in
  * *dev_status when a token's page or offset is out of range; that token's
@@ -242,6 +271,44 @@ QKVP_API int qkv_prologue_bwd_noalloc(const qkvp_layout* layout, int64_t T, cons
                                       const void* k_pre, const int32_t* pos, const float* w_q,
                                       const float* w_k, float eps, double rope_base, uint32_t flags,
                                       void* dpacked, float* dw_q, float* dw_k, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * The *_ex entry points: the calls above with a qkvp_variant (may be NULL,
+ * which gives exactly the plain call). Same arguments, errors and results
+ * otherwise; flags may also hold QKVP_NORM_OFF (GQA layouts).
+ *
+ * qkv_prologue_bwd_ex also takes
+ * dbias   float32 [(n_q + 2 n_kv) * head_dim] out, required when the variant
+ *         has a bias (else ignored): the bias gradient, dpacked's values (in
+ *         float32, before rounding to bf16) summed over tokens, in float64 in a
+ *         fixed order. Overwritten, or added to with QKVP_ACCUMULATE_DW.
+ *         With a bias the backward needs (n_q + 2 n_kv) * head_dim <= 12288
+ *         (QKVP_ERR_SHAPE beyond).
+ * Its workspace size is qkv_prologue_bwd_workspace_size_ex (larger with a
+ * bias: one float row of the bias length per CTA).
+ * ------------------------------------------------------------------------- */
+QKVP_API int qkv_prologue_fwd_ex(const qkvp_layout* layout, const qkvp_variant* variant, int64_t T,
+                                 const void* packed, const int32_t* pos, const float* w_q,
+                                 const float* w_k, float eps, double rope_base, uint32_t flags,
+                                 void* q, void* k, void* v, void* q_pre, void* k_pre, void* stream);
+
+QKVP_API int qkv_prologue_pool_write_ex(const qkvp_layout* layout, const qkvp_variant* variant,
+                                        int64_t T, const void* packed, const int32_t* pos,
+                                        const float* w_q, const float* w_k, float eps,
+                                        double rope_base, uint32_t flags, void* q,
+                                        const int32_t* page, const int32_t* offset, void* k_pool,
+                                        void* v_pool, int32_t num_pages, int32_t page_size,
+                                        int32_t* dev_status, void* stream);
+
+QKVP_API size_t qkv_prologue_bwd_workspace_size_ex(const qkvp_layout* layout,
+                                                   const qkvp_variant* variant, int64_t T);
+
+QKVP_API int qkv_prologue_bwd_ex(const qkvp_layout* layout, const qkvp_variant* variant, int64_t T,
+                                 const void* dq, const void* dk, const void* dv, const void* q_pre,
+                                 const void* k_pre, const int32_t* pos, const float* w_q,
+                                 const float* w_k, float eps, double rope_base, uint32_t flags,
+                                 void* dpacked, float* dw_q, float* dw_k, float* dbias,
+                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * qkv_prologue_device_error -- read (and with clear != 0, reset) the

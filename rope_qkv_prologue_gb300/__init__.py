@@ -19,5 +19,7 @@ __all__ = [
     "EXPORTED", "LIB_PATH", "QkvpError", "layout", "functional",
     "qkv_prologue_fwd", "qkv_prologue_pool_write", "qkv_prologue_pool_scatter",
     "qkv_prologue_bwd_workspace_size", "qkv_prologue_bwd", "qkv_prologue_status_string",
-    "qkv_prologue_version", "qkvp_layout",
+    "qkv_prologue_version", "qkvp_layout", "qkvp_variant", "variant",
+    "qkv_prologue_fwd_ex", "qkv_prologue_pool_write_ex", "qkv_prologue_bwd_workspace_size_ex",
+    "qkv_prologue_bwd_ex",
 ]

@@ -23,7 +23,7 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 # ---- constants (mirror include/qkv_prologue.h) ------------------------------
-QKVP_VERSION = 1
+QKVP_VERSION = 2
 QKVP_OK = 0
 QKVP_ERR_NULL = -1
 QKVP_ERR_SHAPE = -2
@@ -42,6 +42,7 @@ QKVP_NOPE = 1
 QKVP_SAVE_PRE = 2
 QKVP_ACCUMULATE_DW = 4
 QKVP_FORCE_GENERIC = 8
+QKVP_NORM_OFF = 16
 
 QKVP_DEV_BAD_PAGE = 1
 QKVP_DEV_BAD_OFFSET = 2
@@ -59,6 +60,14 @@ class qkvp_layout(ctypes.Structure):
     ]
 
 
+class qkvp_variant(ctypes.Structure):
+    _fields_ = [
+        ("inv_freq", ctypes.POINTER(ctypes.c_double)),
+        ("rope_scale", ctypes.c_double),
+        ("bias", ctypes.c_void_p),
+    ]
+
+
 class QkvpError(RuntimeError):
     def __init__(self, status, func):
         self.status = status
@@ -72,6 +81,7 @@ _u32 = ctypes.c_uint32
 _f32 = ctypes.c_float
 _f64 = ctypes.c_double
 _LP = ctypes.POINTER(qkvp_layout)
+_VP = ctypes.POINTER(qkvp_variant)
 
 _SIGS = {
     "qkv_prologue_fwd": ([_LP, _i64, _vp, _vp, _vp, _vp, _f32, _f64, _u32, _vp, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
@@ -83,6 +93,13 @@ _SIGS = {
                           _vp, ctypes.c_size_t, _vp], ctypes.c_int),
     "qkv_prologue_bwd_noalloc": ([_LP, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _f64, _u32, _vp, _vp,
                                   _vp, _vp], ctypes.c_int),
+    "qkv_prologue_fwd_ex": ([_LP, _VP, _i64, _vp, _vp, _vp, _vp, _f32, _f64, _u32, _vp, _vp, _vp, _vp, _vp, _vp],
+                            ctypes.c_int),
+    "qkv_prologue_pool_write_ex": ([_LP, _VP, _i64, _vp, _vp, _vp, _vp, _f32, _f64, _u32, _vp, _vp, _vp, _vp, _vp,
+                                    _i32, _i32, _vp, _vp], ctypes.c_int),
+    "qkv_prologue_bwd_workspace_size_ex": ([_LP, _VP, _i64], ctypes.c_size_t),
+    "qkv_prologue_bwd_ex": ([_LP, _VP, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _f64, _u32, _vp, _vp,
+                             _vp, _vp, _vp, ctypes.c_size_t, _vp], ctypes.c_int),
     "qkv_prologue_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "qkv_prologue_version": ([], ctypes.c_int),
     "qkv_prologue_device_error": ([ctypes.c_int, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
@@ -126,6 +143,24 @@ def _ret(status, func, check):
     if check and status != QKVP_OK:
         raise QkvpError(status, func)
     return status
+
+
+def variant(inv_freq=None, rope_scale=0.0, bias=None):
+    """A qkvp_variant (the GQAttention variant options). inv_freq: a sequence of
+    head_dim / 2 floats (kept alive with the struct); bias: a device tensor or
+    address, float32 [(n_q + 2 n_kv) * head_dim] in packed-row order."""
+    v = qkvp_variant()
+    if inv_freq is not None:
+        arr = (ctypes.c_double * len(inv_freq))(*[float(f) for f in inv_freq])
+        v._inv_freq_keepalive = arr
+        v.inv_freq = ctypes.cast(arr, ctypes.POINTER(ctypes.c_double))
+    v.rope_scale = float(rope_scale)
+    v.bias = _ptr(bias)
+    return v
+
+
+def _vref(v):
+    return None if v is None else ctypes.byref(v)
 
 
 def qkv_prologue_status_string(status):
@@ -191,3 +226,33 @@ def qkv_prologue_bwd_noalloc(L, T, dq, dk, dv, q_pre, k_pre, pos, w_q, w_k, eps,
                                        float(rope_base), int(flags), _ptr(dpacked), _ptr(dw_q), _ptr(dw_k),
                                        _stream(stream))
     return _ret(st, "qkv_prologue_bwd_noalloc", check)
+
+
+def qkv_prologue_fwd_ex(L, V, T, packed, pos, w_q, w_k, eps, rope_base, flags, q, k, v,
+                        q_pre=None, k_pre=None, stream=None, check=True):
+    st = _lib.qkv_prologue_fwd_ex(ctypes.byref(L), _vref(V), int(T), _ptr(packed), _ptr(pos), _ptr(w_q),
+                                  _ptr(w_k), float(eps), float(rope_base), int(flags), _ptr(q), _ptr(k), _ptr(v),
+                                  _ptr(q_pre), _ptr(k_pre), _stream(stream))
+    return _ret(st, "qkv_prologue_fwd_ex", check)
+
+
+def qkv_prologue_pool_write_ex(L, V, T, packed, pos, w_q, w_k, eps, rope_base, flags, q, page, offset,
+                               k_pool, v_pool, num_pages, page_size, dev_status=None, stream=None, check=True):
+    st = _lib.qkv_prologue_pool_write_ex(ctypes.byref(L), _vref(V), int(T), _ptr(packed), _ptr(pos), _ptr(w_q),
+                                         _ptr(w_k), float(eps), float(rope_base), int(flags), _ptr(q),
+                                         _ptr(page), _ptr(offset), _ptr(k_pool), _ptr(v_pool),
+                                         int(num_pages), int(page_size), _ptr(dev_status), _stream(stream))
+    return _ret(st, "qkv_prologue_pool_write_ex", check)
+
+
+def qkv_prologue_bwd_workspace_size_ex(L, V, T):
+    return int(_lib.qkv_prologue_bwd_workspace_size_ex(ctypes.byref(L), _vref(V), int(T)))
+
+
+def qkv_prologue_bwd_ex(L, V, T, dq, dk, dv, q_pre, k_pre, pos, w_q, w_k, eps, rope_base, flags, dpacked,
+                        dw_q, dw_k, dbias, workspace, workspace_bytes, stream=None, check=True):
+    st = _lib.qkv_prologue_bwd_ex(ctypes.byref(L), _vref(V), int(T), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(q_pre),
+                                  _ptr(k_pre), _ptr(pos), _ptr(w_q), _ptr(w_k), float(eps), float(rope_base),
+                                  int(flags), _ptr(dpacked), _ptr(dw_q), _ptr(dw_k), _ptr(dbias),
+                                  _ptr(workspace), int(workspace_bytes), _stream(stream))
+    return _ret(st, "qkv_prologue_bwd_ex", check)

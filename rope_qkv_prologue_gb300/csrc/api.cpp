@@ -124,16 +124,20 @@ bool allow_smem(const void* kernel, size_t smem) {
 // kMinStepFill full is taken, so a tile stays small and the ring deep; at
 // least two stages per CTA must fit in the shared memory left to each of the
 // shape.ctas_per_sm CTAs of an SM. token_bytes = bytes staged per token.
+// extra_dyn = dynamic shared memory after the ring (the bias copy);
+// one_token = one-token tiles only, with at most max_steps steps (the bias
+// gradient of the backward).
 bool stream_geometry(const StreamShape& shape, int upt, int lph, int hd, int64_t T, int64_t token_bytes,
-                     int smem_per_sm, int static_smem, StreamGeom* g, size_t* smem) {
+                     int smem_per_sm, int static_smem, int extra_dyn, bool one_token, int max_steps,
+                     StreamGeom* g, size_t* smem) {
   constexpr double kMinStepFill = 0.8;  // useful chunks / (steps * tpg)
   const int nct = shape.warps * 32;
-  const int budget = smem_per_sm / shape.ctas_per_sm - 1024 - static_smem;
+  const int budget = smem_per_sm / shape.ctas_per_sm - 1024 - static_smem - extra_dyn;
   for (int tpt = 1; nct / tpt >= lph && (nct / tpt) % lph == 0; tpt *= 2) {
     const int tpg = nct / tpt;
     const int steps = (upt + tpg - 1) / tpg;
-    if (steps > kStreamMaxSteps) return false;  // larger tiles only add steps
-    if ((double)upt / ((double)steps * tpg) < kMinStepFill) continue;
+    if (steps > max_steps) return false;  // larger tiles only add steps
+    if (!one_token && (double)upt / ((double)steps * tpg) < kMinStepFill) continue;
     const int64_t stage = (int64_t)tpt * token_bytes;
     const int fixed = StreamSmem::tables(hd) + 128;
     const int64_t per_stage = stage + StreamSmem::table_stride(hd, tpt);
@@ -146,7 +150,7 @@ bool stream_geometry(const StreamShape& shape, int upt, int lph, int hd, int64_t
     g->steps = steps;
     g->stage_bytes = (int32_t)stage;
     g->n_tiles = (T + tpt - 1) / tpt;
-    *smem = (size_t)StreamSmem::data(hd, tpt, (int)stages) + (size_t)stages * stage;
+    *smem = (size_t)StreamSmem::data(hd, tpt, (int)stages) + (size_t)stages * stage + (size_t)extra_dyn;
     return true;
   }
   return false;
@@ -179,28 +183,37 @@ int launch(const void* kernel, int64_t grid, int threads, size_t smem, cudaStrea
 
 // -------------------------------------------------------------- RoPE ----
 
-// turns_i = frac(inv_freq_i / 2pi) * 2^64 with inv_freq_i = base^(-2i/D):
-// the angle per unit position as a 0.64 fixed-point fraction of one turn.
-// The kernels multiply it by the position modulo 2^64, which reduces the
-// angle exactly. Double precision leaves < 2^-56 turn of error per unit
-// position (about 2^-37 turn at position 2^19).
-void rope_table(double base, int head_dim, RopeTable* out) {
+// turns_i = frac(inv_freq_i / 2pi) * 2^64 with inv_freq_i = base^(-2i/D), or
+// the caller's table: the angle per unit position as a 0.64 fixed-point
+// fraction of one turn. The kernels multiply it by the position modulo 2^64,
+// which reduces the angle exactly. Double precision leaves < 2^-56 turn of
+// error per unit position (about 2^-37 turn at position 2^19).
+uint64_t turns_of(double inv_freq) {
+  const double two_pi = 6.283185307179586476925286766559;
+  const double v = inv_freq / two_pi;
+  const double frac = v - std::floor(v);  // in [0, 1), exact
+  const double scaled = std::ldexp(frac, 64);
+  return scaled >= 18446744073709551616.0 ? 0 : (uint64_t)scaled;
+}
+
+void rope_table(double base, int dim, const double* inv_freq, float scale, RopeTable* out) {
+  if (inv_freq) {
+    std::memset(out, 0, sizeof(*out));
+    for (int i = 0; i < dim / 2; ++i) out->turns[i] = turns_of(inv_freq[i]);
+    out->scale = scale;
+    return;
+  }
   static thread_local double last_base = -1.0;
   static thread_local int last_dim = 0;
   static thread_local RopeTable last;
-  if (base != last_base || head_dim != last_dim) {
-    const double two_pi = 6.283185307179586476925286766559;
+  if (base != last_base || dim != last_dim) {
     std::memset(&last, 0, sizeof(last));
-    for (int i = 0; i < head_dim / 2; ++i) {
-      const double inv_freq = std::pow(base, -2.0 * i / head_dim);
-      const double frac = std::fmod(inv_freq / two_pi, 1.0);
-      const double scaled = std::ldexp(frac, 64);
-      last.turns[i] = scaled >= 18446744073709551616.0 ? 0 : (uint64_t)scaled;
-    }
+    for (int i = 0; i < dim / 2; ++i) last.turns[i] = turns_of(std::pow(base, -2.0 * i / dim));
     last_base = base;
-    last_dim = head_dim;
+    last_dim = dim;
   }
   *out = last;
+  out->scale = scale;
 }
 
 // ------------------------------------------------------------ checks ----
@@ -270,6 +283,36 @@ void gqa_items(int64_t T, int cpt, int chunks_per_thread, int64_t* item_chunks, 
 
 int64_t bwd_parts(int64_t n_items) { return n_items < kMaxBwdParts ? n_items : kMaxBwdParts; }
 
+// The GQAttention variant options of a call, checked.
+struct Variant {
+  const double* inv_freq = nullptr;
+  float scale = 1.f;
+  const float* bias = nullptr;
+};
+
+int check_variant(const qkvp_variant* v, int rope_dim, bool gqa, Variant* out) {
+  *out = Variant();
+  if (!v) return QKVP_OK;
+  if (v->inv_freq) {
+    for (int i = 0; i < rope_dim / 2; ++i)
+      if (!std::isfinite(v->inv_freq[i])) return QKVP_ERR_VALUE;
+    out->inv_freq = v->inv_freq;
+  }
+  if (!std::isfinite(v->rope_scale) || v->rope_scale < 0.0) return QKVP_ERR_VALUE;
+  out->scale = v->rope_scale == 0.0 ? 1.f : (float)v->rope_scale;
+  if (v->bias) {
+    if (!gqa) return QKVP_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(v->bias) & 15u) != 0) return QKVP_ERR_ALIGN;
+    out->bias = v->bias;
+  }
+  return QKVP_OK;
+}
+
+// Bias gradient limits: pipelined backward with one-token tiles of at most
+// kBiasMaxSteps chunk pairs per thread; the general backward with one-token
+// work items of at most kThreads * kBwdChunksPerThread chunks.
+constexpr int kBiasMaxChunks = kThreads * kBwdChunksPerThread;
+
 #define QKVP_TRY(expr)          \
   do {                          \
     const int _st = (expr);     \
@@ -302,8 +345,8 @@ const char* qkv_prologue_status_string(int status) {
 
 // ------------------------------------------------------------- forward ----
 
-static int gqa_forward(const qkvp_layout* L, int64_t T, const void* packed, const int32_t* pos,
-                       const float* w_q, const float* w_k, float eps, double rope_base,
+static int gqa_forward(const qkvp_layout* L, const qkvp_variant* variant, int64_t T, const void* packed,
+                       const int32_t* pos, const float* w_q, const float* w_k, float eps, double rope_base,
                        uint32_t flags, void* q, void* k, void* v, void* q_pre, void* k_pre,
                        const int32_t* page, const int32_t* offset, void* k_pool, void* v_pool,
                        int32_t num_pages, int32_t page_size, int32_t* dev_status, bool pool,
@@ -311,12 +354,15 @@ static int gqa_forward(const qkvp_layout* L, int64_t T, const void* packed, cons
   Gqa g;
   QKVP_TRY(check_gqa(L, T, &g));
   const uint32_t allowed = (pool ? (uint32_t)QKVP_NOPE : (uint32_t)(QKVP_NOPE | QKVP_SAVE_PRE)) |
-                           (uint32_t)QKVP_FORCE_GENERIC;
+                           (uint32_t)(QKVP_FORCE_GENERIC | QKVP_NORM_OFF);
   if (flags & ~allowed) return QKVP_ERR_FLAGS;
   const bool rope = !(flags & QKVP_NOPE);
   const bool save = (flags & QKVP_SAVE_PRE) != 0;
-  QKVP_TRY(check_scalars(eps, rope_base, rope));
-  if (!packed || !w_q || !w_k || !q || (rope && !pos)) return QKVP_ERR_NULL;
+  const bool norm = !(flags & QKVP_NORM_OFF);
+  Variant vr;
+  QKVP_TRY(check_variant(variant, L->head_dim, true, &vr));
+  QKVP_TRY(check_scalars(eps, rope_base, rope && !vr.inv_freq));
+  if (!packed || (norm && (!w_q || !w_k)) || !q || (rope && !pos)) return QKVP_ERR_NULL;
   if (pool) {
     if (!page || !offset || !k_pool || !v_pool) return QKVP_ERR_NULL;
     QKVP_TRY(check_pool(num_pages, page_size));
@@ -324,8 +370,8 @@ static int gqa_forward(const qkvp_layout* L, int64_t T, const void* packed, cons
     if (!k || !v) return QKVP_ERR_NULL;
     if (save && (!q_pre || !k_pre)) return QKVP_ERR_NULL;
   }
-  const void* vec[] = {packed, w_q, w_k, q, pool ? k_pool : k, pool ? v_pool : v,
-                       save ? q_pre : nullptr, save ? k_pre : nullptr};
+  const void* vec[] = {packed, norm ? w_q : nullptr, norm ? w_k : nullptr, q, pool ? k_pool : k,
+                       pool ? v_pool : v, save ? q_pre : nullptr, save ? k_pre : nullptr};
   for (const void* p : vec)
     if (p && !aligned16(p)) return QKVP_ERR_ALIGN;
   if ((pos && !aligned4(pos)) || (page && !aligned4(page)) || (offset && !aligned4(offset)) ||
@@ -364,16 +410,18 @@ static int gqa_forward(const qkvp_layout* L, int64_t T, const void* packed, cons
   a.num_pages = num_pages;
   a.page_size = page_size;
   a.dev_status = dev_status;
-  if (rope) rope_table(rope_base, L->head_dim, &a.rope);
+  a.bias = vr.bias;
+  if (rope) rope_table(rope_base, L->head_dim, vr.inv_freq, vr.scale, &a.rope);
 
-  const FwdVariant var{L->head_dim, L->kind == QKVP_SECTIONED, rope, save, pool};
+  const FwdVariant var{L->head_dim, L->kind == QKVP_SECTIONED, rope, save, pool, norm, vr.bias != nullptr};
+  const int bias_bytes = vr.bias ? a.cpt * 8 * (int)sizeof(float) : 0;
   size_t smem = 0;
   if (!(flags & QKVP_FORCE_GENERIC) &&
-      stream_geometry(fwd_stream_shape(save, rope), a.cpt / 2, L->head_dim / 16, L->head_dim, T,
-                      (int64_t)a.cpt * 16, smem_per_sm, 0, &a.sg, &smem) &&
+      stream_geometry(fwd_stream_shape(save, rope && norm), a.cpt / 2, L->head_dim / 16, L->head_dim, T,
+                      (int64_t)a.cpt * 16, smem_per_sm, 0, bias_bytes, false, kStreamMaxSteps, &a.sg, &smem) &&
       (a.err = device_error_word()) != nullptr) {
     a.sg.dense = g.stride == g.row;
-    const void* kern = L->head_dim == 64 ? fwd_stream_kernel_d64(var) : fwd_stream_kernel_d128(var);
+    const void* kern = fwd_stream_kernel(var);
     const int threads = (fwd_stream_shape(save).warps + 1) * 32;
     const int bps = allow_smem(kern, smem) ? blocks_per_sm(kern, threads, smem) : 0;
     if (bps > 0) {
@@ -381,23 +429,25 @@ static int gqa_forward(const qkvp_layout* L, int64_t T, const void* packed, cons
       return launch(kern, a.sg.n_tiles < cap ? a.sg.n_tiles : cap, threads, smem, stream, &a);
     }
   }
-  const void* kern = L->head_dim == 64 ? fwd_kernel_d64(var) : fwd_kernel_d128(var);
+  const void* kern = fwd_kernel(var);
   smem = (size_t)a.max_tok * (L->head_dim / 2) * 2 * sizeof(float) + (size_t)a.max_tok * sizeof(int32_t);
   const int64_t cap = (int64_t)sms * std::max(1, blocks_per_sm(kern, kThreads, smem));
   const int64_t grid = a.n_items < cap ? a.n_items : cap;
   return launch(kern, grid, kThreads, smem, stream, &a);
 }
 
-static int latent_forward(const qkvp_layout* L, int64_t T, const void* rows, const int32_t* pos,
-                          const float* w, float eps, double rope_base, uint32_t flags, void* out,
-                          const int32_t* page, const int32_t* offset, void* pool,
+static int latent_forward(const qkvp_layout* L, const qkvp_variant* variant, int64_t T, const void* rows,
+                          const int32_t* pos, const float* w, float eps, double rope_base, uint32_t flags,
+                          void* out, const int32_t* page, const int32_t* offset, void* pool,
                           int32_t num_pages, int32_t page_size, int32_t* dev_status,
                           bool to_pool, cudaStream_t stream) {
   Latent g;
   QKVP_TRY(check_latent(L, T, &g));
   if (flags & ~(uint32_t)(QKVP_NOPE | QKVP_FORCE_GENERIC)) return QKVP_ERR_FLAGS;
   const bool rope = !(flags & QKVP_NOPE);
-  QKVP_TRY(check_scalars(eps, rope_base, rope));
+  Variant vr;
+  QKVP_TRY(check_variant(variant, L->rope_dim, false, &vr));
+  QKVP_TRY(check_scalars(eps, rope_base, rope && !vr.inv_freq));
   if (!rows || !w || (rope && !pos)) return QKVP_ERR_NULL;
   if (to_pool) {
     if (!page || !offset || !pool) return QKVP_ERR_NULL;
@@ -432,7 +482,7 @@ static int latent_forward(const qkvp_layout* L, int64_t T, const void* rows, con
   a.num_pages = num_pages;
   a.page_size = page_size;
   a.dev_status = dev_status;
-  if (rope) rope_table(rope_base, L->rope_dim, &a.rope);
+  if (rope) rope_table(rope_base, L->rope_dim, vr.inv_freq, vr.scale, &a.rope);
   const int ncl = a.norm_chunks <= 32 ? 1 : (a.norm_chunks <= 64 ? 2 : 4);
 
   // Pipelined kernel: tiles of kLatentTileTokens rows, kLatentStreamCtasPerSm
@@ -471,16 +521,36 @@ static int latent_forward(const qkvp_layout* L, int64_t T, const void* rows, con
   return launch(kern, need < cap ? need : cap, threads, 0, stream, &a);
 }
 
+int qkv_prologue_fwd_ex(const qkvp_layout* layout, const qkvp_variant* variant, int64_t T, const void* packed,
+                        const int32_t* pos, const float* w_q, const float* w_k, float eps, double rope_base,
+                        uint32_t flags, void* q, void* k, void* v, void* q_pre, void* k_pre, void* stream) {
+  if (!layout) return QKVP_ERR_NULL;
+  if (layout->kind == QKVP_LATENT)
+    return latent_forward(layout, variant, T, packed, pos, w_k, eps, rope_base, flags, k, nullptr, nullptr,
+                          nullptr, 0, 0, nullptr, false, static_cast<cudaStream_t>(stream));
+  return gqa_forward(layout, variant, T, packed, pos, w_q, w_k, eps, rope_base, flags, q, k, v, q_pre, k_pre,
+                     nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, false, static_cast<cudaStream_t>(stream));
+}
+
 int qkv_prologue_fwd(const qkvp_layout* layout, int64_t T, const void* packed, const int32_t* pos,
                      const float* w_q, const float* w_k, float eps, double rope_base,
                      uint32_t flags, void* q, void* k, void* v, void* q_pre, void* k_pre,
                      void* stream) {
+  return qkv_prologue_fwd_ex(layout, nullptr, T, packed, pos, w_q, w_k, eps, rope_base, flags, q, k, v, q_pre,
+                             k_pre, stream);
+}
+
+int qkv_prologue_pool_write_ex(const qkvp_layout* layout, const qkvp_variant* variant, int64_t T,
+                               const void* packed, const int32_t* pos, const float* w_q, const float* w_k,
+                               float eps, double rope_base, uint32_t flags, void* q, const int32_t* page,
+                               const int32_t* offset, void* k_pool, void* v_pool, int32_t num_pages,
+                               int32_t page_size, int32_t* dev_status, void* stream) {
   if (!layout) return QKVP_ERR_NULL;
   if (layout->kind == QKVP_LATENT)
-    return latent_forward(layout, T, packed, pos, w_k, eps, rope_base, flags, k, nullptr, nullptr,
-                          nullptr, 0, 0, nullptr, false, static_cast<cudaStream_t>(stream));
-  return gqa_forward(layout, T, packed, pos, w_q, w_k, eps, rope_base, flags, q, k, v, q_pre,
-                     k_pre, nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, false,
+    return latent_forward(layout, variant, T, packed, pos, w_k, eps, rope_base, flags, nullptr, page, offset,
+                          k_pool, num_pages, page_size, dev_status, true, static_cast<cudaStream_t>(stream));
+  return gqa_forward(layout, variant, T, packed, pos, w_q, w_k, eps, rope_base, flags, q, nullptr, nullptr,
+                     nullptr, nullptr, page, offset, k_pool, v_pool, num_pages, page_size, dev_status, true,
                      static_cast<cudaStream_t>(stream));
 }
 
@@ -489,14 +559,8 @@ int qkv_prologue_pool_write(const qkvp_layout* layout, int64_t T, const void* pa
                             double rope_base, uint32_t flags, void* q, const int32_t* page,
                             const int32_t* offset, void* k_pool, void* v_pool, int32_t num_pages,
                             int32_t page_size, int32_t* dev_status, void* stream) {
-  if (!layout) return QKVP_ERR_NULL;
-  if (layout->kind == QKVP_LATENT)
-    return latent_forward(layout, T, packed, pos, w_k, eps, rope_base, flags, nullptr, page,
-                          offset, k_pool, num_pages, page_size, dev_status, true,
-                          static_cast<cudaStream_t>(stream));
-  return gqa_forward(layout, T, packed, pos, w_q, w_k, eps, rope_base, flags, q, nullptr, nullptr,
-                     nullptr, nullptr, page, offset, k_pool, v_pool, num_pages, page_size,
-                     dev_status, true, static_cast<cudaStream_t>(stream));
+  return qkv_prologue_pool_write_ex(layout, nullptr, T, packed, pos, w_q, w_k, eps, rope_base, flags, q, page,
+                                    offset, k_pool, v_pool, num_pages, page_size, dev_status, stream);
 }
 
 int qkv_prologue_pool_scatter(const qkvp_layout* layout, int64_t T, const void* k_rows,
@@ -546,46 +610,75 @@ int qkv_prologue_pool_scatter(const qkvp_layout* layout, int64_t T, const void* 
 
 // ------------------------------------------------------------ backward ----
 
-size_t qkv_prologue_bwd_workspace_size(const qkvp_layout* layout, int64_t T) {
+// Backward partial rows: one per CTA, at most max(work items, tokens), capped;
+// each row holds [dw_q | dw_k] (norm on) then the bias row (bias given).
+static int64_t bwd_row_floats(const qkvp_layout* layout, bool norm, bool bias) {
+  const int64_t heads = (int64_t)layout->n_q + 2 * (int64_t)layout->n_kv;
+  return (norm ? 2 * layout->head_dim : 0) + (bias ? heads * layout->head_dim : 0);
+}
+
+static size_t bwd_workspace(const qkvp_layout* layout, const Variant& vr, bool norm, int64_t T) {
   Gqa g;
   if (check_gqa(layout, T, &g) != QKVP_OK || T == 0) return 0;
   int64_t item_chunks = 0, n_items = 0;
   int max_tok = 0;
-  gqa_items(T, g.heads * (layout->head_dim / 8), kBwdChunksPerThread, &item_chunks, &n_items,
-            &max_tok);
-  // one partial row per CTA: at most max(work items, tokens), capped
-  return (size_t)bwd_parts(n_items > T ? n_items : T) * 2 * layout->head_dim * sizeof(float);
+  gqa_items(T, g.heads * (layout->head_dim / 8), kBwdChunksPerThread, &item_chunks, &n_items, &max_tok);
+  return (size_t)bwd_parts(n_items > T ? n_items : T) * (size_t)bwd_row_floats(layout, norm, vr.bias != nullptr) *
+         sizeof(float);
 }
 
-int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const void* dk,
-                     const void* dv, const void* q_pre, const void* k_pre, const int32_t* pos,
-                     const float* w_q, const float* w_k, float eps, double rope_base,
-                     uint32_t flags, void* dpacked, float* dw_q, float* dw_k, void* workspace,
-                     size_t workspace_bytes, void* stream) {
+size_t qkv_prologue_bwd_workspace_size(const qkvp_layout* layout, int64_t T) {
+  return bwd_workspace(layout, Variant(), true, T);
+}
+
+size_t qkv_prologue_bwd_workspace_size_ex(const qkvp_layout* layout, const qkvp_variant* variant, int64_t T) {
+  Variant vr;
+  if (!layout || check_variant(variant, layout->head_dim, true, &vr) != QKVP_OK) return 0;
+  // The size does not depend on the norm flag: a norm-off call needs less.
+  return bwd_workspace(layout, vr, true, T);
+}
+
+int qkv_prologue_bwd_ex(const qkvp_layout* layout, const qkvp_variant* variant, int64_t T, const void* dq,
+                        const void* dk, const void* dv, const void* q_pre, const void* k_pre, const int32_t* pos,
+                        const float* w_q, const float* w_k, float eps, double rope_base, uint32_t flags,
+                        void* dpacked, float* dw_q, float* dw_k, float* dbias, void* workspace,
+                        size_t workspace_bytes, void* stream) {
   Gqa g;
   QKVP_TRY(check_gqa(layout, T, &g));
-  if (flags & ~(uint32_t)(QKVP_NOPE | QKVP_ACCUMULATE_DW | QKVP_FORCE_GENERIC)) return QKVP_ERR_FLAGS;
+  if (flags & ~(uint32_t)(QKVP_NOPE | QKVP_ACCUMULATE_DW | QKVP_FORCE_GENERIC | QKVP_NORM_OFF))
+    return QKVP_ERR_FLAGS;
   const bool rope = !(flags & QKVP_NOPE);
   const bool accumulate = (flags & QKVP_ACCUMULATE_DW) != 0;
-  QKVP_TRY(check_scalars(eps, rope_base, rope));
-  if (!dq || !dk || !dv || !q_pre || !k_pre || !w_q || !w_k || !dpacked || !dw_q || !dw_k ||
-      (rope && !pos))
-    return QKVP_ERR_NULL;
-  const void* vec[] = {dq, dk, dv, q_pre, k_pre, w_q, w_k, dpacked, dw_q, dw_k};
+  const bool norm = !(flags & QKVP_NORM_OFF);
+  Variant vr;
+  QKVP_TRY(check_variant(variant, layout->head_dim, true, &vr));
+  const bool bias = vr.bias != nullptr;
+  QKVP_TRY(check_scalars(eps, rope_base, rope && !vr.inv_freq));
+  if (!dq || !dk || !dv || !dpacked || (rope && !pos)) return QKVP_ERR_NULL;
+  if (norm && (!q_pre || !k_pre || !w_q || !w_k || !dw_q || !dw_k)) return QKVP_ERR_NULL;
+  if (bias && !dbias) return QKVP_ERR_NULL;
+  const void* vec[] = {dq, dk, dv, dpacked, norm ? q_pre : nullptr, norm ? k_pre : nullptr,
+                       norm ? w_q : nullptr, norm ? w_k : nullptr, norm ? dw_q : nullptr,
+                       norm ? dw_k : nullptr, bias ? dbias : nullptr};
   for (const void* p : vec)
-    if (!aligned16(p)) return QKVP_ERR_ALIGN;
+    if (p && !aligned16(p)) return QKVP_ERR_ALIGN;
   if (pos && !aligned4(pos)) return QKVP_ERR_ALIGN;
-  const size_t need = qkv_prologue_bwd_workspace_size(layout, T);
-  if (T > 0 && (!workspace || workspace_bytes < need)) return workspace ? QKVP_ERR_WORKSPACE : QKVP_ERR_NULL;
+  const int hd = layout->head_dim;
+  const int cpt = g.heads * (hd / 8);
+  if (bias && cpt > kBiasMaxChunks) return QKVP_ERR_SHAPE;
+  const size_t need = bwd_workspace(layout, vr, norm, T);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return workspace ? QKVP_ERR_WORKSPACE : QKVP_ERR_NULL;
   if (workspace && !aligned16(workspace)) return QKVP_ERR_ALIGN;
 
   int sms = 0, smem_per_sm = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (T == 0) {
-    if (accumulate) return QKVP_OK;
+    if (accumulate || (!norm && !bias)) return QKVP_OK;
     QKVP_TRY(current_device(&sms));
-    const size_t bytes = (size_t)layout->head_dim * sizeof(float);
-    if (cudaMemsetAsync(dw_q, 0, bytes, s) != cudaSuccess || cudaMemsetAsync(dw_k, 0, bytes, s) != cudaSuccess) {
+    const size_t wbytes = (size_t)hd * sizeof(float), bbytes = (size_t)cpt * 8 * sizeof(float);
+    if ((norm && (cudaMemsetAsync(dw_q, 0, wbytes, s) != cudaSuccess ||
+                  cudaMemsetAsync(dw_k, 0, wbytes, s) != cudaSuccess)) ||
+        (bias && cudaMemsetAsync(dbias, 0, bbytes, s) != cudaSuccess)) {
       cudaGetLastError();
       return QKVP_ERR_LAUNCH;
     }
@@ -604,61 +697,91 @@ int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const
   a.w_q = w_q;
   a.w_k = w_k;
   a.eps = eps;
-  a.inv_head_dim = 1.0f / (float)layout->head_dim;
+  a.inv_head_dim = 1.0f / (float)hd;
   a.T = T;
   a.n_q = layout->n_q;
   a.n_kv = layout->n_kv;
   a.group = layout->n_q / layout->n_kv;
-  a.cpt = g.heads * (layout->head_dim / 8);
+  a.cpt = cpt;
   a.cpt_magic = magic((uint32_t)a.cpt);
   a.gs_magic = magic((uint32_t)(a.group + 2));
   gqa_items(T, a.cpt, kBwdChunksPerThread, &a.item_chunks, &a.n_items, &a.max_tok);
   a.dpacked = static_cast<uint4*>(dpacked);
   a.row_stride16 = g.stride / 8;
-  a.partials = static_cast<float*>(workspace);
-  if (rope) rope_table(rope_base, layout->head_dim, &a.rope);
+  a.bias = vr.bias;
+  if (rope) rope_table(rope_base, hd, vr.inv_freq, vr.scale, &a.rope);
 
-  const bool sectioned = layout->kind == QKVP_SECTIONED;
-  const int hd = layout->head_dim;
-  const int64_t token_bytes = (int64_t)(2 * layout->n_q + 3 * layout->n_kv) * hd * 2;
+  const BwdVariant var{hd, layout->kind == QKVP_SECTIONED, rope, norm, bias};
+  const int64_t heads_qkv = norm ? (2 * layout->n_q + 3 * layout->n_kv) : (layout->n_q + 2 * layout->n_kv);
+  const int64_t token_bytes = heads_qkv * hd * 2;
   const StreamShape shape = bwd_stream_shape();
-  const int static_smem = shape.warps * 2 * hd * (int)sizeof(float);
+  const int static_smem = (norm ? shape.warps : 1) * 2 * hd * (int)sizeof(float);
+  const int bias_bytes = (norm && bias) ? cpt * 8 * (int)sizeof(float) : 0;
   size_t smem = 0;
   int64_t grid = 0;
   bool streamed = false;
   if (!(flags & QKVP_FORCE_GENERIC) &&
-      stream_geometry(shape, a.cpt / 2, hd / 16, hd, T, token_bytes, smem_per_sm, static_smem, &a.sg, &smem) &&
+      stream_geometry(shape, a.cpt / 2, hd / 16, hd, T, token_bytes, smem_per_sm, static_smem, bias_bytes, bias,
+                      bias ? kBiasMaxSteps : kStreamMaxSteps, &a.sg, &smem) &&
       (a.err = device_error_word()) != nullptr) {
     a.sg.dense = 1;
-    const void* kern = bwd_stream_kernel(hd, sectioned, rope);
+    const void* kern = bwd_stream_kernel(var);
     const int threads = (shape.warps + 1) * 32;
     const int bps = allow_smem(kern, smem) ? blocks_per_sm(kern, threads, smem) : 0;
     if (bps > 0) {
       grid = (int64_t)sms * bps;
       if (grid > a.sg.n_tiles) grid = a.sg.n_tiles;
       if (grid > kMaxBwdParts) grid = kMaxBwdParts;
-      QKVP_TRY(launch(kern, grid, threads, smem, s, &a));
       streamed = true;
     }
   }
-  if (!streamed) {
-    const void* kern = bwd_kernel(hd, sectioned, rope);
-    smem = (size_t)a.max_tok * (hd / 2) * 2 * sizeof(float);
+  const void* kern = nullptr;
+  int threads = kThreads;
+  if (streamed) {
+    kern = bwd_stream_kernel(var);
+    threads = (shape.warps + 1) * 32;
+  } else {
+    if (bias) {  // one token per work item: every thread keeps the same chunks
+      a.item_chunks = a.cpt;
+      a.n_items = T;
+      a.max_tok = 1;
+    }
+    kern = bwd_kernel(var);
+    smem = (size_t)a.max_tok * (hd / 2) * 2 * sizeof(float) + (bias ? (size_t)a.cpt * 8 * sizeof(float) : 0);
+    if (!allow_smem(kern, smem)) return QKVP_ERR_LAUNCH;
     grid = (int64_t)sms * std::max(1, blocks_per_sm(kern, kThreads, smem));
     if (grid > a.n_items) grid = a.n_items;
     if (grid > kMaxBwdParts) grid = kMaxBwdParts;
-    QKVP_TRY(launch(kern, grid, kThreads, smem, s, &a));
   }
+  float* ws = static_cast<float*>(workspace);
+  a.partials = ws;
+  a.db_partials = ws + (norm ? grid * 2 * hd : 0);
+  QKVP_TRY(launch(kern, grid, threads, smem, s, &a));
+  if (!norm && !bias) return QKVP_OK;
 
   FinalizeArgs f;
+  std::memset(&f, 0, sizeof(f));
   f.partials = a.partials;
+  f.db_partials = a.db_partials;
   f.nparts = (int32_t)grid;
-  f.head_dim = layout->head_dim;
-  f.dw_q = dw_q;
-  f.dw_k = dw_k;
+  f.head_dim = hd;
+  f.n_bias = bias ? cpt * 8 : 0;
+  f.dw_q = norm ? dw_q : nullptr;
+  f.dw_k = norm ? dw_k : nullptr;
+  f.db = bias ? dbias : nullptr;
   f.accumulate = accumulate ? 1 : 0;
-  const int fgrid = 2 * layout->head_dim / kFinalizeOutputsPerCta;
+  const int n_out = (norm ? 2 * hd : 0) + f.n_bias;
+  const int fgrid = (n_out + kFinalizeOutputsPerCta - 1) / kFinalizeOutputsPerCta;
   return launch(dw_finalize_kernel(), fgrid, kFinalizeThreads, 0, s, &f);
+}
+
+int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const void* dk,
+                     const void* dv, const void* q_pre, const void* k_pre, const int32_t* pos,
+                     const float* w_q, const float* w_k, float eps, double rope_base,
+                     uint32_t flags, void* dpacked, float* dw_q, float* dw_k, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  return qkv_prologue_bwd_ex(layout, nullptr, T, dq, dk, dv, q_pre, k_pre, pos, w_q, w_k, eps, rope_base, flags,
+                             dpacked, dw_q, dw_k, nullptr, workspace, workspace_bytes, stream);
 }
 
 int qkv_prologue_device_error(int clear, int* value) {

@@ -1,24 +1,30 @@
-// Backward kernel instances and the float64 weight-grad finalize kernel.
-#include "gqa_kernels.cuh"
+// General backward kernel instances with the norm, and the float64 finalize
+// kernel of the weight and bias gradients.
+#include "instances.cuh"
 
 namespace qkvp {
 
-// dw[j] = sum over partial rows b of partials[b][j], j over [dw_q | dw_k],
-// added in float64 in a fixed order (deterministic), then rounded to float32.
-// CTA x owns kFinalizeOutputsPerCta consecutive outputs; its threads split
-// the rows into kFinalizeThreads / kFinalizeOutputsPerCta interleaved slices
-// and a fixed-shape tree adds the slices.
+// Outputs: [dw_q | dw_k] (2 * head_dim, when dw_q is set), then db (n_bias,
+// when db is set). Output j = sum over partial rows b of its column, added in
+// float64 in a fixed order (deterministic), then rounded to float32. CTA x
+// owns kFinalizeOutputsPerCta consecutive outputs; its threads split the rows
+// into kFinalizeThreads / kFinalizeOutputsPerCta interleaved slices and a
+// fixed-shape tree adds the slices.
 __global__ void __launch_bounds__(kFinalizeThreads) qkvp_dw_finalize_kernel(const FinalizeArgs a) {
   griddep_wait();
   constexpr int K = kFinalizeOutputsPerCta, SLICES = kFinalizeThreads / K;
   __shared__ double s_sum[SLICES][K];
   const int jj = threadIdx.x % K, slice = threadIdx.x / K;
   const int j = blockIdx.x * K + jj;
-  const int n_out = 2 * a.head_dim;
+  const int n_dw = a.dw_q ? 2 * a.head_dim : 0;
+  const int n_out = n_dw + (a.db ? a.n_bias : 0);
+  const bool is_dw = j < n_dw;
+  const float* col = is_dw ? a.partials + j : a.db_partials + (j - n_dw);
+  const int64_t stride = is_dw ? 2 * a.head_dim : a.n_bias;
   double acc = 0.0;
   if (j < n_out) {
 #pragma unroll 4
-    for (int b = slice; b < a.nparts; b += SLICES) acc += (double)a.partials[(int64_t)b * n_out + j];
+    for (int b = slice; b < a.nparts; b += SLICES) acc += (double)col[(int64_t)b * stride];
   }
   s_sum[slice][jj] = acc;
   __syncthreads();
@@ -27,27 +33,13 @@ __global__ void __launch_bounds__(kFinalizeThreads) qkvp_dw_finalize_kernel(cons
     __syncthreads();
   }
   if (slice == 0 && j < n_out) {
-    float* dst = j < a.head_dim ? a.dw_q + j : a.dw_k + (j - a.head_dim);
+    float* dst = is_dw ? (j < a.head_dim ? a.dw_q + j : a.dw_k + (j - a.head_dim)) : a.db + (j - n_dw);
     const double total = s_sum[0][jj];
     *dst = a.accumulate ? (float)(total + (double)*dst) : (float)total;
   }
 }
 
-namespace {
-template <int HD, bool S, bool R>
-const void* bwd_ptr() {
-  return reinterpret_cast<const void*>(&qkvp_bwd_kernel<HD, S, R>);
-}
-template <int HD>
-const void* bwd_pick(bool sectioned, bool rope) {
-  if (sectioned) return rope ? bwd_ptr<HD, true, true>() : bwd_ptr<HD, true, false>();
-  return rope ? bwd_ptr<HD, false, true>() : bwd_ptr<HD, false, false>();
-}
-}  // namespace
-
-const void* bwd_kernel(int head_dim, bool sectioned, bool rope) {
-  return head_dim == 64 ? bwd_pick<64>(sectioned, rope) : bwd_pick<128>(sectioned, rope);
-}
+const void* bwd_kernel_norm(const BwdVariant& v) { return inst::BwdPick<true, false>::pick(v); }
 
 const void* dw_finalize_kernel() { return reinterpret_cast<const void*>(&qkvp_dw_finalize_kernel); }
 

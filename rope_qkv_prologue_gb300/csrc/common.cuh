@@ -92,20 +92,30 @@ __device__ __forceinline__ float head_sum_sq(const float2 (&x)[4]) {
   return ss;
 }
 
-// Forward of one chunk (8 values of one head; the head's CPH lanes call this
-// together): y = x * r * w with r = (mean(x^2) + eps)^-1/2, then rotate-half:
-// o = y * cos + y_partner * ssin, where the partner (element +- D/2) is in
-// lane ^ CPH/2 and ssin = -sin for the first half of the head, +sin for the
-// second.
-template <int CPH, bool ROPE>
-__device__ __forceinline__ void chunk_forward(const uint4& xr, const float2 (&w)[4], float eps, float inv_hd,
-                                              const float2 (&c)[4], const float2 (&ssin)[4], float2 (&y)[4]) {
-  float2 x[4];
-  unpack_pairs(xr, x);
-  const float r = rsqrtf(fmaf(head_sum_sq<CPH>(x), inv_hd, eps));
-  const float2 rr = f2(r, r);
+// x + b on pairs (the qkv bias of the GQAttention variant, added before
+// anything else).
+__device__ __forceinline__ void add_bias_pairs(float2 (&x)[4], const float2 (&b)[4]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) y[i] = __fmul2_rn(__fmul2_rn(x[i], rr), w[i]);
+  for (int i = 0; i < 4; ++i) x[i] = __fadd2_rn(x[i], b[i]);
+}
+
+// Forward of one chunk (8 values of one head, already widened; the head's CPH
+// lanes call this together): y = x * r * w with r = (mean(x^2) + eps)^-1/2
+// (y = x when NORM is off), then rotate-half: o = y * cos + y_partner * ssin,
+// where the partner (element +- D/2) is in lane ^ CPH/2 and ssin = -sin for
+// the first half of the head, +sin for the second.
+template <int CPH, bool ROPE, bool NORM>
+__device__ __forceinline__ void chunk_forward(const float2 (&x)[4], const float2 (&w)[4], float eps, float inv_hd,
+                                              const float2 (&c)[4], const float2 (&ssin)[4], float2 (&y)[4]) {
+  if (NORM) {
+    const float r = rsqrtf(fmaf(head_sum_sq<CPH>(x), inv_hd, eps));
+    const float2 rr = f2(r, r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y[i] = __fmul2_rn(__fmul2_rn(x[i], rr), w[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y[i] = x[i];
+  }
   if (ROPE) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -116,19 +126,19 @@ __device__ __forceinline__ void chunk_forward(const uint4& xr, const float2 (&w)
   }
 }
 
-// Backward of one chunk. d: gradient of the roped output; x: pre-norm input.
+// Backward of one chunk. d: gradient of the roped output; x: the norm's input.
 //   g  = R(theta)^T d = d * cos + d_partner * ssin   (ssin = +sin / -sin for
 //        the first / second half of the head: the transpose flips the sign)
 //   r  = (mean(x^2) + eps)^-1/2
 //   dx = r (w g) - x (r^3 / D) sum(x w g)
-// Also returns gx = g * x (the weight gradient is gx * r) and r.
-template <int CPH, bool ROPE>
-__device__ __forceinline__ void chunk_backward(const uint4& dr, const uint4& xr, const float2 (&w)[4], float eps,
-                                               float inv_hd, const float2 (&c)[4], const float2 (&ssin)[4],
-                                               float2 (&dx)[4], float2 (&gx)[4], float& r_out) {
-  float2 d[4], x[4], g[4], wg[4];
-  unpack_pairs(dr, d);
-  unpack_pairs(xr, x);
+// Also returns gx = g * x (the weight gradient is gx * r) and r. Without the
+// norm dx = g (x, w, gx and r unused).
+template <int CPH, bool ROPE, bool NORM>
+__device__ __forceinline__ void chunk_backward(const float2 (&d)[4], const float2 (&x)[4], const float2 (&w)[4],
+                                               float eps, float inv_hd, const float2 (&c)[4],
+                                               const float2 (&ssin)[4], float2 (&dx)[4], float2 (&gx)[4],
+                                               float& r_out) {
+  float2 g[4], wg[4];
   if (ROPE) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -139,6 +149,12 @@ __device__ __forceinline__ void chunk_backward(const uint4& dr, const uint4& xr,
   } else {
 #pragma unroll
     for (int i = 0; i < 4; ++i) g[i] = d[i];
+  }
+  if (!NORM) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dx[i] = gx[i] = g[i];
+    r_out = 0.f;
+    return;
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) wg[i] = __fmul2_rn(w[i], g[i]);
@@ -193,22 +209,28 @@ __device__ __forceinline__ float pair_head_sum(float lo, float hi) {
   return lo + hi;
 }
 
-// Forward of a chunk pair: y = x * r * w, then o_lo = y_lo cos - y_hi sin,
-// o_hi = y_hi cos + y_lo sin (c, sn: cos and sin of the lane's 8 frequencies).
-template <int CPH, bool ROPE>
-__device__ __forceinline__ void pair_forward(const uint4& xlo, const uint4& xhi, const float2 (&wlo)[4],
+// Forward of a chunk pair (widened, biased): y = x * r * w (y = x without the
+// norm), then o_lo = y_lo cos - y_hi sin, o_hi = y_hi cos + y_lo sin (c, sn:
+// cos and sin of the lane's 8 frequencies).
+template <int CPH, bool ROPE, bool NORM>
+__device__ __forceinline__ void pair_forward(const float2 (&lo)[4], const float2 (&hi)[4], const float2 (&wlo)[4],
                                              const float2 (&whi)[4], float eps, float inv_hd, const float2 (&c)[4],
                                              const float2 (&sn)[4], float2 (&ylo)[4], float2 (&yhi)[4]) {
-  float2 lo[4], hi[4];
-  unpack_pairs(xlo, lo);
-  unpack_pairs(xhi, hi);
-  const float ss = pair_head_sum<CPH>(chunk_partial_sq(lo), chunk_partial_sq(hi));
-  const float r = rsqrtf(fmaf(ss, inv_hd, eps));
-  const float2 rr = f2(r, r);
+  if (NORM) {
+    const float ss = pair_head_sum<CPH>(chunk_partial_sq(lo), chunk_partial_sq(hi));
+    const float r = rsqrtf(fmaf(ss, inv_hd, eps));
+    const float2 rr = f2(r, r);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    ylo[i] = __fmul2_rn(__fmul2_rn(lo[i], rr), wlo[i]);
-    yhi[i] = __fmul2_rn(__fmul2_rn(hi[i], rr), whi[i]);
+    for (int i = 0; i < 4; ++i) {
+      ylo[i] = __fmul2_rn(__fmul2_rn(lo[i], rr), wlo[i]);
+      yhi[i] = __fmul2_rn(__fmul2_rn(hi[i], rr), whi[i]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      ylo[i] = lo[i];
+      yhi[i] = hi[i];
+    }
   }
   if (ROPE) {
     const float2 neg = f2(-1.f, -1.f);
@@ -224,18 +246,15 @@ __device__ __forceinline__ void pair_forward(const uint4& xlo, const uint4& xhi,
 }
 
 // Backward of a chunk pair (see chunk_backward): g_lo = d_lo cos + d_hi sin,
-// g_hi = d_hi cos - d_lo sin, then the RMSNorm backward with the head's r.
-template <int CPH, bool ROPE>
-__device__ __forceinline__ void pair_backward(const uint4& dlo_r, const uint4& dhi_r, const uint4& xlo_r,
-                                              const uint4& xhi_r, const float2 (&wlo)[4], const float2 (&whi)[4],
+// g_hi = d_hi cos - d_lo sin, then the RMSNorm backward with the head's r
+// (x: the norm's input, widened and biased). Without the norm dx = g.
+template <int CPH, bool ROPE, bool NORM>
+__device__ __forceinline__ void pair_backward(const float2 (&dlo)[4], const float2 (&dhi)[4], const float2 (&xlo)[4],
+                                              const float2 (&xhi)[4], const float2 (&wlo)[4], const float2 (&whi)[4],
                                               float eps, float inv_hd, const float2 (&c)[4], const float2 (&sn)[4],
                                               float2 (&dxlo)[4], float2 (&dxhi)[4], float2 (&gxlo)[4],
                                               float2 (&gxhi)[4], float& r_out) {
-  float2 dlo[4], dhi[4], xlo[4], xhi[4], glo[4], ghi[4];
-  unpack_pairs(dlo_r, dlo);
-  unpack_pairs(dhi_r, dhi);
-  unpack_pairs(xlo_r, xlo);
-  unpack_pairs(xhi_r, xhi);
+  float2 glo[4], ghi[4];
   if (ROPE) {
     const float2 neg = f2(-1.f, -1.f);
 #pragma unroll
@@ -250,6 +269,15 @@ __device__ __forceinline__ void pair_backward(const uint4& dlo_r, const uint4& d
       glo[i] = dlo[i];
       ghi[i] = dhi[i];
     }
+  }
+  if (!NORM) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      dxlo[i] = gxlo[i] = glo[i];
+      dxhi[i] = gxhi[i] = ghi[i];
+    }
+    r_out = 0.f;
+    return;
   }
   float2 wglo[4], wghi[4];
 #pragma unroll
@@ -397,10 +425,14 @@ __device__ __forceinline__ uint32_t small_div(uint32_t n, uint32_t m) { return _
 // (turns = frac(inv_freq / 2pi) * 2^64). The product pos * turns modulo 2^64
 // is the angle reduced exactly to one turn; read as a signed number it is
 // the angle / pi scaled by 2^63, in [-1, 1).
-__device__ __forceinline__ void rope_cos_sin(int32_t pos, uint64_t turns, float* c, float* s) {
+// Both are then multiplied by `scale` (the cos/sin factor of YaRN-style
+// scalings; exactly 1 for plain RoPE, which leaves the values unchanged).
+__device__ __forceinline__ void rope_cos_sin(int32_t pos, uint64_t turns, float scale, float* c, float* s) {
   const uint64_t t = static_cast<uint64_t>(static_cast<int64_t>(pos)) * turns;
   const float x = static_cast<float>(static_cast<int64_t>(t)) * 1.0842021724855044e-19f;  // 2^-63
   sincospif(x, s, c);
+  *c *= scale;
+  *s *= scale;
 }
 
 }  // namespace qkvp

@@ -82,7 +82,7 @@ __device__ __forceinline__ void fill_rope_table(const int32_t* pos, const RopeTa
     const int tl = i / HALF;
     const int f = i % HALF;
     float c, s;
-    rope_cos_sin(pos[t_first + tl], rope.turns[f], &c, &s);
+    rope_cos_sin(pos[t_first + tl], rope.turns[f], rope.scale, &c, &s);
     s_cos[i] = c;
     s_sin[i] = s;
   }
@@ -90,7 +90,7 @@ __device__ __forceinline__ void fill_rope_table(const int32_t* pos, const RopeTa
 
 // ------------------------------------------------------------- forward ----
 
-template <int HD, bool SECTIONED, bool ROPE, bool SAVE, bool POOL>
+template <int HD, bool SECTIONED, bool ROPE, bool SAVE, bool POOL, bool NORM, bool BIAS>
 __global__ void __launch_bounds__(kThreads, 2) qkvp_fwd_kernel(const FwdArgs a) {
   griddep_wait();
   using G = Geom<HD>;
@@ -105,8 +105,10 @@ __global__ void __launch_bounds__(kThreads, 2) qkvp_fwd_kernel(const FwdArgs a) 
   const float sign = e < CPH / 2 ? -1.f : 1.f;
   const int f0 = (e & (CPH / 2 - 1)) * 8;
   float2 wq[4], wk[4];
-  load_pairs(a.w_q + 8 * e, wq);
-  load_pairs(a.w_k + 8 * e, wk);
+  if (NORM) {
+    load_pairs(a.w_q + 8 * e, wq);
+    load_pairs(a.w_k + 8 * e, wk);
+  }
 
   const int64_t total = a.T * a.cpt;
   for (int64_t item = blockIdx.x; item < a.n_items; item += gridDim.x) {
@@ -154,15 +156,22 @@ __global__ void __launch_bounds__(kThreads, 2) qkvp_fwd_kernel(const FwdArgs a) 
       uint32_t oh;
       classify<SECTIONED>(j >> G::LOG_CPH, a.n_q, a.n_kv, a.group, a.gs_magic, role, oh);
 
-      float2 w[4], c[4], ssin[4], y[4];
+      float2 x[4], w[4], c[4], ssin[4], y[4];
+      unpack_pairs(xv[u], x);
+      if (BIAS) {
+        float2 b[4];
+        load_pairs(a.bias + 8 * j, b);
+        add_bias_pairs(x, b);
+      }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) w[i] = role == kRoleQ ? wq[i] : wk[i];
+      for (int i = 0; i < 4; ++i) w[i] = NORM ? (role == kRoleQ ? wq[i] : wk[i]) : f2(1.f, 1.f);
       if (ROPE) read_cos_sin<HALF>(s_cos, s_sin, tl, f0, sign, c, ssin);
-      chunk_forward<CPH, ROPE>(xv[u], w, a.eps, a.inv_head_dim, c, ssin, y);
+      chunk_forward<CPH, ROPE, NORM>(x, w, a.eps, a.inv_head_dim, c, ssin, y);
       if (!valid) continue;
 
       const int64_t t = t_first + tl;
       const uint4 out = pack_pairs(y);
+      const uint4 vout = BIAS ? pack_pairs(x) : xv[u];  // v: the (biased) input
       if (role == kRoleQ) {
         const int64_t idx = (t * a.n_q + oh) * CPH + e;
         st_keep(a.q + idx, out);
@@ -172,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 2) qkvp_fwd_kernel(const FwdArgs a) 
         if (slot >= 0) {
           const int64_t idx = ((int64_t)slot * a.n_kv + oh) * CPH + e;
           if (role == kRoleK) st_keep(a.k_pool + idx, out);
-          else st_keep(a.v_pool + idx, xv[u]);
+          else st_keep(a.v_pool + idx, vout);
         }
       } else {
         const int64_t idx = (t * a.n_kv + oh) * CPH + e;
@@ -180,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 2) qkvp_fwd_kernel(const FwdArgs a) 
           st_keep(a.k + idx, out);
           if (SAVE) st_stream(a.k_pre + idx, xv[u]);
         } else {
-          st_keep(a.v + idx, xv[u]);
+          st_keep(a.v + idx, vout);
         }
       }
     }
@@ -198,8 +207,14 @@ __global__ void __launch_bounds__(kThreads, 2) qkvp_fwd_kernel(const FwdArgs a) 
 //   dw += g x r                             (per thread, fp32 registers)
 // The CTA reduces its dw partial sums in a fixed order and writes one row of
 // `partials`; qkvp_dw_finalize_kernel adds the rows in float64.
+// Without the norm: dx = g, no dw, and the saved inputs are not read. With a
+// qkv bias the norm's input is x + b, and the bias gradient db = sum over
+// tokens of dx: the host then makes every work item one whole token, so a
+// thread always holds the same packed chunks and adds them into the CTA's row
+// of float sums in shared memory (no two threads share a chunk; the order is
+// fixed), written out as one row of `db_partials`.
 
-template <int HD, bool SECTIONED, bool ROPE>
+template <int HD, bool SECTIONED, bool ROPE, bool NORM, bool BIAS>
 __global__ void __launch_bounds__(kThreads, 2) qkvp_bwd_kernel(const BwdArgs a) {
   griddep_wait();
   using G = Geom<HD>;
@@ -207,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 2) qkvp_bwd_kernel(const BwdArgs a) 
   extern __shared__ __align__(16) unsigned char smem[];
   float* s_cos = reinterpret_cast<float*>(smem);
   float* s_sin = s_cos + a.max_tok * HALF;
+  float* s_db = s_sin + a.max_tok * HALF;  // [cpt * 8] (BIAS)
   __shared__ float s_red[kThreads / 32][2][HD];
 
   const int tid = threadIdx.x;
@@ -214,10 +230,15 @@ __global__ void __launch_bounds__(kThreads, 2) qkvp_bwd_kernel(const BwdArgs a) 
   const float sign = e < CPH / 2 ? 1.f : -1.f;  // R(theta)^T: the partner term flips sign
   const int f0 = (e & (CPH / 2 - 1)) * 8;
   float2 wq[4], wk[4], accq[4], acck[4];
-  load_pairs(a.w_q + 8 * e, wq);
-  load_pairs(a.w_k + 8 * e, wk);
+  if (NORM) {
+    load_pairs(a.w_q + 8 * e, wq);
+    load_pairs(a.w_k + 8 * e, wk);
+  }
 #pragma unroll
   for (int i = 0; i < 4; ++i) accq[i] = acck[i] = f2(0.f, 0.f);
+  if (BIAS) {
+    for (int i = tid; i < a.cpt * 8; i += kThreads) s_db[i] = 0.f;
+  }
 
   const int64_t total = a.T * a.cpt;
   for (int64_t item = blockIdx.x; item < a.n_items; item += gridDim.x) {
@@ -243,12 +264,12 @@ __global__ void __launch_bounds__(kThreads, 2) qkvp_bwd_kernel(const BwdArgs a) 
         if (role == kRoleQ) {
           const int64_t idx = (t * a.n_q + oh) * CPH + e;
           dv[u] = ld_stream(a.dq + idx);
-          xv[u] = ld_stream(a.q_pre + idx);
+          if (NORM) xv[u] = ld_stream(a.q_pre + idx);
         } else {
           const int64_t idx = (t * a.n_kv + oh) * CPH + e;
           if (role == kRoleK) {
             dv[u] = ld_stream(a.dk + idx);
-            xv[u] = ld_stream(a.k_pre + idx);
+            if (NORM) xv[u] = ld_stream(a.k_pre + idx);
           } else {
             dv[u] = ld_stream(a.dv + idx);
           }
@@ -271,25 +292,49 @@ __global__ void __launch_bounds__(kThreads, 2) qkvp_bwd_kernel(const BwdArgs a) 
       uint32_t oh;
       classify<SECTIONED>(j >> G::LOG_CPH, a.n_q, a.n_kv, a.group, a.gs_magic, role, oh);
 
-      float2 w[4], c[4], ssin[4], dx[4], gx[4];
+      float2 d[4], x[4], w[4], c[4], ssin[4], dx[4], gx[4];
       float r;
+      unpack_pairs(dv[u], d);
+      unpack_pairs(xv[u], x);
+      if (NORM && BIAS) {
+        float2 b[4];
+        load_pairs(a.bias + 8 * j, b);
+        add_bias_pairs(x, b);
+      }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) w[i] = role == kRoleQ ? wq[i] : wk[i];
+      for (int i = 0; i < 4; ++i) w[i] = NORM ? (role == kRoleQ ? wq[i] : wk[i]) : f2(1.f, 1.f);
       if (ROPE) read_cos_sin<HALF>(s_cos, s_sin, tl, f0, sign, c, ssin);
-      chunk_backward<CPH, ROPE>(dv[u], xv[u], w, a.eps, a.inv_head_dim, c, ssin, dx, gx, r);
+      chunk_backward<CPH, ROPE, NORM>(d, x, w, a.eps, a.inv_head_dim, c, ssin, dx, gx, r);
       if (!valid) continue;
 
-      const float rq = role == kRoleQ ? r : 0.f, rk = role == kRoleK ? r : 0.f;
-      const float2 rq2 = f2(rq, rq), rk2 = f2(rk, rk);
+      if (NORM) {
+        const float rq = role == kRoleQ ? r : 0.f, rk = role == kRoleK ? r : 0.f;
+        const float2 rq2 = f2(rq, rq), rk2 = f2(rk, rk);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        accq[i] = __ffma2_rn(gx[i], rq2, accq[i]);
-        acck[i] = __ffma2_rn(gx[i], rk2, acck[i]);
+        for (int i = 0; i < 4; ++i) {
+          accq[i] = __ffma2_rn(gx[i], rq2, accq[i]);
+          acck[i] = __ffma2_rn(gx[i], rk2, acck[i]);
+        }
+      }
+      if (BIAS) {  // one token per item: chunk j is this thread's on every item
+        float* p = s_db + 8 * j;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 g = role == kRoleV ? d[i] : dx[i];
+          p[2 * i] += g.x;
+          p[2 * i + 1] += g.y;
+        }
       }
       const int64_t t = t_first + tl;
       st_keep(a.dpacked + t * a.row_stride16 + j, role == kRoleV ? dv[u] : pack_pairs(dx));
     }
   }
+
+  if (BIAS) {
+    __syncthreads();
+    for (int i = tid; i < a.cpt * 8; i += kThreads) a.db_partials[(int64_t)blockIdx.x * a.cpt * 8 + i] = s_db[i];
+  }
+  if (!NORM) return;
 
   // Weight-grad partials: lanes of a warp with the same e, then the warps.
   float aq[8], ak[8];

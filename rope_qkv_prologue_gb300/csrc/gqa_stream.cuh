@@ -106,7 +106,7 @@ __device__ __forceinline__ void stream_producer(unsigned char* smem, int hd, int
       for (int i = lane; i < ntok * HALF; i += 32) {
         const int tl = i / HALF, f = i - (i / HALF) * HALF;
         float c, sn;
-        rope_cos_sin(pos[t0 + tl], rope.turns[f], &c, &sn);
+        rope_cos_sin(pos[t0 + tl], rope.turns[f], rope.scale, &c, &sn);
         tab[i] = c;
         tab[tpt * HALF + i] = sn;
       }
@@ -144,7 +144,15 @@ __device__ __forceinline__ void stream_producer(unsigned char* smem, int hd, int
 
 // ------------------------------------------------------------- forward ----
 
-template <int HD, bool SECTIONED, bool ROPE, bool SAVE, bool POOL, int NCW, int CPS>
+// Copy of the qkv bias (packed-row order, fp32) into shared memory.
+__device__ __forceinline__ void fill_bias(const float* bias, int n, float* s_b) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) s_b[i] = bias[i];
+}
+
+// NORM: RMSNorm of q and k (off: split -> RoPE only). BIAS: the qkv bias,
+// staged in shared memory after the ring, is added to every input chunk first;
+// v then stores the rounded biased value instead of a copy of the input.
+template <int HD, bool SECTIONED, bool ROPE, bool SAVE, bool POOL, bool NORM, bool BIAS, int NCW, int CPS>
 __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_fwd_stream_kernel(const FwdArgs a) {
   griddep_wait();
   using G = Geom<HD>;
@@ -154,6 +162,7 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_fwd_stream_kernel(co
   uint64_t* empty = full + kMaxStages;
   float* s_w = reinterpret_cast<float*>(smem + StreamSmem::kWeights);
   const int tpt = a.sg.tpt, stages = a.sg.stages, steps = a.sg.steps, stage_bytes = a.sg.stage_bytes;
+  float* s_b = reinterpret_cast<float*>(smem + StreamSmem::bias(HD, tpt, stages, stage_bytes));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -162,7 +171,8 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_fwd_stream_kernel(co
     }
     mbar_init_fence();
   }
-  fill_split_weights<HD>(a.w_q, a.w_k, s_w);
+  if (NORM) fill_split_weights<HD>(a.w_q, a.w_k, s_w);
+  if (BIAS) fill_bias(a.bias, a.cpt * 8, s_b);
   __syncthreads();
 
   if (threadIdx.x >= NCT) {
@@ -244,10 +254,21 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_fwd_stream_kernel(co
       const uint4 xlo = odd ? second : first, xhi = odd ? first : second;
       const int role = (int)((info[m] >> 16) & 3u);
       const int olo = (int)(info[m] & 0xffffu) * CPH + e;
-      float2 wlo[4], whi[4], ylo[4], yhi[4];
-      load_split_weights<HD>(s_w, role, e, wlo);
-      load_split_weights<HD>(s_w, role, e + PPH, whi);
-      pair_forward<CPH, ROPE>(xlo, xhi, wlo, whi, a.eps, a.inv_head_dim, c2, s2, ylo, yhi);
+      float2 lo[4], hi[4], wlo[4], whi[4], ylo[4], yhi[4];
+      unpack_pairs(xlo, lo);
+      unpack_pairs(xhi, hi);
+      if (BIAS) {
+        float2 blo[4], bhi[4];
+        load_pairs(s_b + 8 * clo, blo);
+        load_pairs(s_b + 8 * (clo + PPH), bhi);
+        add_bias_pairs(lo, blo);
+        add_bias_pairs(hi, bhi);
+      }
+      if (NORM) {
+        load_split_weights<HD>(s_w, role, e, wlo);
+        load_split_weights<HD>(s_w, role, e + PPH, whi);
+      }
+      pair_forward<CPH, ROPE, NORM>(lo, hi, wlo, whi, a.eps, a.inv_head_dim, c2, s2, ylo, yhi);
       if (!valid || !in_row) continue;
       // Plain contiguous forward: cache-streaming stores (measured faster on GB300
       // at every size tried); with the pre-norm save, or into a pool that
@@ -274,8 +295,8 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_fwd_stream_kernel(co
           st_stream(kprow + olo + PPH, xhi);
         }
       } else if (!POOL || slot >= 0) {
-        put(vrow + olo, xlo);
-        put(vrow + olo + PPH, xhi);
+        put(vrow + olo, BIAS ? pack_pairs(lo) : xlo);
+        put(vrow + olo + PPH, BIAS ? pack_pairs(hi) : xhi);
       }
     }
     __syncwarp();
@@ -289,18 +310,27 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_fwd_stream_kernel(co
 
 // ------------------------------------------------------------ backward ----
 
-template <int HD, bool SECTIONED, bool ROPE, int NCW, int CPS>
+// NORM off: g = R^T d is the whole gradient, and the saved inputs are neither
+// staged nor read (three sections per stage instead of five). BIAS: the norm's
+// input is x + b (bias staged in shared memory after the ring), and db = sum
+// over tokens of the packed gradient. The host then uses one-token tiles, so
+// thread i owns the same chunk pairs of every token and keeps their running
+// sums in registers (at most kBiasMaxSteps pairs); at the end it writes them
+// to the CTA's row of db_partials (every chunk by exactly one thread).
+template <int HD, bool SECTIONED, bool ROPE, bool NORM, bool BIAS, int NCW, int CPS>
 __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(const BwdArgs a) {
   griddep_wait();
   using G = Geom<HD>;
-  constexpr int CPH = G::CPH, HALF = G::HALF, NCT = NCW * 32, MAXM = kStreamMaxSteps;
+  constexpr int CPH = G::CPH, HALF = G::HALF, NCT = NCW * 32;
+  constexpr int MAXM = BIAS ? kBiasMaxSteps : kStreamMaxSteps;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ float s_red[NCW][2][HD];
+  __shared__ float s_red[NORM ? NCW : 1][2][HD];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + StreamSmem::kBarriers);
   uint64_t* empty = full + kMaxStages;
   float* s_w = reinterpret_cast<float*>(smem + StreamSmem::kWeights);
   const int tpt = a.sg.tpt, stages = a.sg.stages, steps = a.sg.steps, stage_bytes = a.sg.stage_bytes;
-  // Stage sections (16-byte chunks): dq, dk, dv, q_pre, k_pre, each [tpt][heads][CPH].
+  float* s_b = reinterpret_cast<float*>(smem + StreamSmem::bias(HD, tpt, stages, stage_bytes));
+  // Stage sections (16-byte chunks): dq, dk, dv[, q_pre, k_pre], each [tpt][heads][CPH].
   const int qc = a.n_q * CPH, kc = a.n_kv * CPH;
   const int sec_dk = tpt * qc, sec_dv = sec_dk + tpt * kc, sec_qp = sec_dv + tpt * kc, sec_kp = sec_qp + tpt * qc;
 
@@ -311,7 +341,8 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(co
     }
     mbar_init_fence();
   }
-  fill_split_weights<HD>(a.w_q, a.w_k, s_w);
+  if (NORM) fill_split_weights<HD>(a.w_q, a.w_k, s_w);
+  if (NORM && BIAS) fill_bias(a.bias, a.cpt * 8, s_b);
   __syncthreads();
 
   if (threadIdx.x >= NCT) {
@@ -319,13 +350,15 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(co
         smem, HD, tpt, stages, stage_bytes, a.sg.n_tiles, a.T, a.pos, a.rope, nullptr, nullptr, 0, 0, nullptr, a.err,
         [&](unsigned char* dst, int64_t t0, int ntok, uint64_t* bar, uint64_t pol) {
           const uint32_t qb = (uint32_t)qc * 16u, kb = (uint32_t)kc * 16u;
-          mbar_expect_tx(bar, (uint32_t)ntok * (2 * qb + 3 * kb));
+          mbar_expect_tx(bar, (uint32_t)ntok * (NORM ? 2 * qb + 3 * kb : qb + 2 * kb));
           uint4* d = reinterpret_cast<uint4*>(dst);
           bulk_load(d, a.dq + t0 * qc, ntok * qb, bar, pol);
           bulk_load(d + sec_dk, a.dk + t0 * kc, ntok * kb, bar, pol);
           bulk_load(d + sec_dv, a.dv + t0 * kc, ntok * kb, bar, pol);
-          bulk_load(d + sec_qp, a.q_pre + t0 * qc, ntok * qb, bar, pol);
-          bulk_load(d + sec_kp, a.k_pre + t0 * kc, ntok * kb, bar, pol);
+          if (NORM) {
+            bulk_load(d + sec_qp, a.q_pre + t0 * qc, ntok * qb, bar, pol);
+            bulk_load(d + sec_kp, a.k_pre + t0 * kc, ntok * kb, bar, pol);
+          }
         });
     return;
   }
@@ -371,6 +404,11 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(co
   float2 aql[4], aqh[4], akl[4], akh[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) aql[i] = aqh[i] = akl[i] = akh[i] = f2(0.f, 0.f);
+  float2 dbl[BIAS ? MAXM : 1][4], dbh[BIAS ? MAXM : 1][4];  // bias-gradient sums (BIAS)
+#pragma unroll
+  for (int m = 0; m < (BIAS ? MAXM : 1); ++m)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dbl[m][i] = dbh[m][i] = f2(0.f, 0.f);
 
   int s = 0;
   uint32_t phase = 0;
@@ -397,26 +435,53 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(co
       const int dl = (int)(offs[m] & 0xffffu), xl = (int)(offs[m] >> 16);
       // odd output heads read hi first (different shared-memory banks)
       const uint4 d1 = sx[odd ? dl + PPH : dl], d2 = sx[odd ? dl : dl + PPH];
-      const uint4 x1 = sx[odd ? xl + PPH : xl], x2 = sx[odd ? xl : xl + PPH];
-      const uint4 dlo = odd ? d2 : d1, dhi = odd ? d1 : d2;
-      const uint4 xlo = odd ? x2 : x1, xhi = odd ? x1 : x2;
-      float2 wlo[4], whi[4], dxlo[4], dxhi[4], gxlo[4], gxhi[4];
-      float r;
-      load_split_weights<HD>(s_w, role, e, wlo);
-      load_split_weights<HD>(s_w, role, e + PPH, whi);
-      pair_backward<CPH, ROPE>(dlo, dhi, xlo, xhi, wlo, whi, a.eps, a.inv_head_dim, c2, s2, dxlo, dxhi, gxlo,
-                               gxhi, r);
-      if (!valid || j >= upt) continue;
-      const float rq = role == kRoleQ ? r : 0.f, rk = role == kRoleK ? r : 0.f;
-      const float2 rq2 = f2(rq, rq), rk2 = f2(rk, rk);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        aql[i] = __ffma2_rn(gxlo[i], rq2, aql[i]);
-        aqh[i] = __ffma2_rn(gxhi[i], rq2, aqh[i]);
-        akl[i] = __ffma2_rn(gxlo[i], rk2, akl[i]);
-        akh[i] = __ffma2_rn(gxhi[i], rk2, akh[i]);
+      uint4 x1 = d1, x2 = d2;
+      if (NORM) {
+        x1 = sx[odd ? xl + PPH : xl];
+        x2 = sx[odd ? xl : xl + PPH];
       }
+      const uint4 dlo = odd ? d2 : d1, dhi = odd ? d1 : d2;
+      float2 dl2[4], dh2[4], xl2[4], xh2[4], wlo[4], whi[4], dxlo[4], dxhi[4], gxlo[4], gxhi[4];
+      float r;
+      unpack_pairs(dlo, dl2);
+      unpack_pairs(dhi, dh2);
+      if (NORM) {
+        unpack_pairs(odd ? x2 : x1, xl2);
+        unpack_pairs(odd ? x1 : x2, xh2);
+        if (BIAS) {
+          const int blo_c = (j >> LOG_PPH) * CPH + e;
+          float2 blo[4], bhi[4];
+          load_pairs(s_b + 8 * blo_c, blo);
+          load_pairs(s_b + 8 * (blo_c + PPH), bhi);
+          add_bias_pairs(xl2, blo);
+          add_bias_pairs(xh2, bhi);
+        }
+        load_split_weights<HD>(s_w, role, e, wlo);
+        load_split_weights<HD>(s_w, role, e + PPH, whi);
+      }
+      pair_backward<CPH, ROPE, NORM>(dl2, dh2, xl2, xh2, wlo, whi, a.eps, a.inv_head_dim, c2, s2, dxlo, dxhi,
+                                     gxlo, gxhi, r);
+      if (!valid || j >= upt) continue;
       const int plo = (j >> LOG_PPH) * CPH + e;  // packed-row chunk of lo
+      if (NORM) {
+        const float rq = role == kRoleQ ? r : 0.f, rk = role == kRoleK ? r : 0.f;
+        const float2 rq2 = f2(rq, rq), rk2 = f2(rk, rk);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          aql[i] = __ffma2_rn(gxlo[i], rq2, aql[i]);
+          aqh[i] = __ffma2_rn(gxhi[i], rq2, aqh[i]);
+          akl[i] = __ffma2_rn(gxlo[i], rk2, akl[i]);
+          akh[i] = __ffma2_rn(gxhi[i], rk2, akh[i]);
+        }
+      }
+      if (BIAS) {
+        const int mb = BIAS ? m : 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          dbl[mb][i] = __fadd2_rn(dbl[mb][i], role == kRoleV ? dl2[i] : dxlo[i]);
+          dbh[mb][i] = __fadd2_rn(dbh[mb][i], role == kRoleV ? dh2[i] : dxhi[i]);
+        }
+      }
       st_keep(drow + plo, role == kRoleV ? dlo : pack_pairs(dxlo));
       st_keep(drow + plo + PPH, role == kRoleV ? dhi : pack_pairs(dxhi));
     }
@@ -427,6 +492,22 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(co
       phase ^= 1;
     }
   }
+
+  if (BIAS) {  // one-token tiles: this thread alone holds its chunk pairs' sums
+    float* row = a.db_partials + (int64_t)blockIdx.x * a.cpt * 8;
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+      const int j = ig + tpg * m;
+      if (m >= steps || j >= upt) break;
+      const int plo = (j >> LOG_PPH) * CPH + e;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        reinterpret_cast<float2*>(row + 8 * plo)[i] = dbl[m][i];
+        reinterpret_cast<float2*>(row + 8 * (plo + PPH))[i] = dbh[m][i];
+      }
+    }
+  }
+  if (!NORM) return;
 
   // Weight-grad partials: lanes of a warp with the same e (lane % PPH), then
   // the warps, in a fixed order (deterministic).

@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kLatentWarps * 32) qkvp_latent_kernel(const La
       unpack8(xr[k], xq);
       if (ROPE) {
         float cl, sl;
-        rope_cos_sin(p[k], a.rope.turns[lane], &cl, &sl);
+        rope_cos_sin(p[k], a.rope.turns[lane], a.rope.scale, &cl, &sl);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float c = __shfl_sync(0xffffffffu, cl, f0 + i);

@@ -129,7 +129,7 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_latent_stream_kernel
           float c[4], sn[4];
           const int32_t p = spos[tl];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) rope_cos_sin(p, turns[i], &c[i], &sn[i]);
+          for (int i = 0; i < 4; ++i) rope_cos_sin(p, turns[i], a.rope.scale, &c[i], &sn[i]);
           latent_rope_quad(rlo, rhi, c, sn, olo, ohi);
         }
         uint2* dst = nullptr;

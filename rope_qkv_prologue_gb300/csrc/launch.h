@@ -55,6 +55,10 @@ struct StreamSmem {
   QKVP_HD static int data(int hd, int tpt, int stages) {
     return (tables(hd) + stages * table_stride(hd, tpt) + 127) & ~127;
   }
+  // after the ring: float bias[row] of the GQAttention variant (when given)
+  QKVP_HD static int bias(int hd, int tpt, int stages, int stage_bytes) {
+    return data(hd, tpt, stages) + stages * stage_bytes;
+  }
 };
 
 struct StreamGeom {
@@ -69,7 +73,13 @@ struct StreamGeom {
 
 struct RopeTable {
   uint64_t turns[kMaxHalf];  // frac(inv_freq_i / 2pi) * 2^64
+  float scale;               // factor on cos and sin (1 for plain RoPE)
+  int32_t pad_;
 };
+
+// Bias gradient of the backward: at most this many chunk pairs per consumer
+// thread (its running sums stay in registers).
+constexpr int kBiasMaxSteps = 2;
 
 // Forward (contiguous or paged-pool destination), GQA layouts.
 struct FwdArgs {
@@ -100,6 +110,7 @@ struct FwdArgs {
   int32_t num_pages, page_size;
   int32_t* dev_status;
   int* err;               // library device error word
+  const float* bias;      // [cpt * 8] in packed-row order, or null
   StreamGeom sg;
   RopeTable rope;
 };
@@ -125,7 +136,9 @@ struct BwdArgs {
   int32_t max_tok;
   uint4* dpacked;
   int64_t row_stride16;
-  float* partials;        // [grid][2][head_dim]
+  float* partials;        // [grid][2][head_dim] (norm on)
+  float* db_partials;     // [grid][cpt * 8] (bias given)
+  const float* bias;      // [cpt * 8] in packed-row order, or null
   int* err;
   StreamGeom sg;
   RopeTable rope;
@@ -171,19 +184,49 @@ struct FwdVariant {
   bool rope;
   bool save_pre;
   bool pool;
+  bool norm;          // RMSNorm of q and k (off: split -> RoPE only)
+  bool bias;          // qkv bias added first
+};
+
+struct BwdVariant {
+  int head_dim;
+  bool sectioned;
+  bool rope;
+  bool norm;
+  bool bias;
 };
 
 // Kernel entry points (host stubs for cudaLaunchKernel / occupancy queries).
 // Each takes its argument struct by value as the only parameter.
-const void* fwd_kernel_d64(const FwdVariant& v);
-const void* fwd_kernel_d128(const FwdVariant& v);
-const void* bwd_kernel(int head_dim, bool sectioned, bool rope);
+// One getter per instance file (head_dim x norm on / off).
+const void* fwd_kernel_d64_norm(const FwdVariant& v);
+const void* fwd_kernel_d64_nonorm(const FwdVariant& v);
+const void* fwd_kernel_d128_norm(const FwdVariant& v);
+const void* fwd_kernel_d128_nonorm(const FwdVariant& v);
+const void* bwd_kernel_norm(const BwdVariant& v);
+const void* bwd_kernel_nonorm(const BwdVariant& v);
+const void* fwd_stream_kernel_d64_norm(const FwdVariant& v);
+const void* fwd_stream_kernel_d64_nonorm(const FwdVariant& v);
+const void* fwd_stream_kernel_d128_norm(const FwdVariant& v);
+const void* fwd_stream_kernel_d128_nonorm(const FwdVariant& v);
+const void* bwd_stream_kernel_norm(const BwdVariant& v);
+const void* bwd_stream_kernel_nonorm(const BwdVariant& v);
+
+inline const void* fwd_kernel(const FwdVariant& v) {
+  if (v.head_dim == 64) return v.norm ? fwd_kernel_d64_norm(v) : fwd_kernel_d64_nonorm(v);
+  return v.norm ? fwd_kernel_d128_norm(v) : fwd_kernel_d128_nonorm(v);
+}
+inline const void* fwd_stream_kernel(const FwdVariant& v) {
+  if (v.head_dim == 64) return v.norm ? fwd_stream_kernel_d64_norm(v) : fwd_stream_kernel_d64_nonorm(v);
+  return v.norm ? fwd_stream_kernel_d128_norm(v) : fwd_stream_kernel_d128_nonorm(v);
+}
+inline const void* bwd_kernel(const BwdVariant& v) { return v.norm ? bwd_kernel_norm(v) : bwd_kernel_nonorm(v); }
+inline const void* bwd_stream_kernel(const BwdVariant& v) {
+  return v.norm ? bwd_stream_kernel_norm(v) : bwd_stream_kernel_nonorm(v);
+}
 const void* dw_finalize_kernel();
 const void* latent_kernel(bool pool, bool rope, int norm_chunks_per_lane);
 const void* scatter_kernel();
-const void* fwd_stream_kernel_d64(const FwdVariant& v);
-const void* fwd_stream_kernel_d128(const FwdVariant& v);
-const void* bwd_stream_kernel(int head_dim, bool sectioned, bool rope);
 const void* latent_stream_kernel(bool pool, bool rope, int norm_chunks_per_lane);
 
 // Address of the library's device error word on the current device (nullptr
@@ -192,13 +235,17 @@ const void* latent_stream_kernel(bool pool, bool rope, int norm_chunks_per_lane)
 int* device_error_word();
 int read_device_error(bool clear, int* value);
 
-// qkvp_dw_finalize_kernel arguments.
+// qkvp_dw_finalize_kernel arguments: outputs [dw_q | dw_k] (when dw_q is set)
+// then db (when db is set), each the float64 sum of its column of partial rows.
 struct FinalizeArgs {
-  const float* partials;  // [nparts][2][head_dim]
+  const float* partials;     // [nparts][2][head_dim]
+  const float* db_partials;  // [nparts][n_bias]
   int32_t nparts;
   int32_t head_dim;
-  float* dw_q;
+  int32_t n_bias;            // bias length (cpt * 8), 0 without a bias
+  float* dw_q;               // null: no weight gradients (norm off)
   float* dw_k;
+  float* db;                 // null: no bias gradient
   int32_t accumulate;
 };
 constexpr int kFinalizeOutputsPerCta = 4;

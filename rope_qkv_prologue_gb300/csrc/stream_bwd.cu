@@ -1,7 +1,8 @@
-// Streaming backward kernel instances, and the library's device error word.
+// Pipelined backward kernel instances with the norm, and the library's device
+// error word.
 #include <mutex>
 
-#include "gqa_stream.cuh"
+#include "instances.cuh"
 
 namespace qkvp {
 
@@ -9,25 +10,12 @@ namespace qkvp {
 __device__ int g_qkvp_device_error = 0;
 
 namespace {
-template <int HD, bool S, bool R>
-const void* ptr() {
-  constexpr StreamShape sh = bwd_stream_shape();
-  return reinterpret_cast<const void*>(&qkvp_bwd_stream_kernel<HD, S, R, sh.warps, sh.ctas_per_sm>);
-}
-template <int HD>
-const void* pick(bool sectioned, bool rope) {
-  if (sectioned) return rope ? ptr<HD, true, true>() : ptr<HD, true, false>();
-  return rope ? ptr<HD, false, true>() : ptr<HD, false, false>();
-}
-
 constexpr int kMaxDev = 64;
 std::mutex g_err_mutex;
 int* g_err_ptr[kMaxDev] = {};
 }  // namespace
 
-const void* bwd_stream_kernel(int head_dim, bool sectioned, bool rope) {
-  return head_dim == 64 ? pick<64>(sectioned, rope) : pick<128>(sectioned, rope);
-}
+const void* bwd_stream_kernel_norm(const BwdVariant& v) { return inst::BwdPick<true, true>::pick(v); }
 
 int* device_error_word() {
   int dev = -1;

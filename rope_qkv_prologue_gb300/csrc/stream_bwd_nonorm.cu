@@ -1,0 +1,6 @@
+// Pipelined backward kernel instances without the norm (g = R^T d only).
+#include "instances.cuh"
+
+namespace qkvp {
+const void* bwd_stream_kernel_nonorm(const BwdVariant& v) { return inst::BwdPick<false, true>::pick(v); }
+}  // namespace qkvp

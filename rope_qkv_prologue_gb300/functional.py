@@ -31,9 +31,31 @@ def _check_dev(*ts):
             raise ValueError("all tensors must live on a CUDA device")
 
 
+def _variant(bias=None, inv_freq=None, rope_scale=1.0):
+    """The qkvp_variant of the GQAttention options, or None for the plain call."""
+    if bias is None and inv_freq is None and rope_scale in (None, 0.0, 1.0):
+        return None
+    if bias is not None:
+        _check_dev(bias)
+        if bias.dtype != torch.float32 or not bias.is_contiguous():
+            raise ValueError("bias must be a contiguous float32 tensor")
+    return C.variant(inv_freq=None if inv_freq is None else [float(f) for f in inv_freq],
+                     rope_scale=0.0 if rope_scale is None else float(rope_scale), bias=bias)
+
+
+def _flags(nope=False, save_pre=False, norm=True):
+    return (C.QKVP_NOPE if nope else 0) | (C.QKVP_SAVE_PRE if save_pre else 0) | (0 if norm else C.QKVP_NORM_OFF)
+
+
 def prologue_forward(packed, pos, w_q, w_k, n_q, n_kv, head_dim=64, kind="interleaved", eps=1e-6,
-                     rope_base=500000.0, nope=False, save_pre=False, stream=None):
-    """Split + per-head RMSNorm + RoPE. Returns (q, k, v) or (q, k, v, q_pre, k_pre)."""
+                     rope_base=500000.0, nope=False, save_pre=False, stream=None, norm=True, bias=None,
+                     inv_freq=None, rope_scale=1.0):
+    """Split + per-head RMSNorm + RoPE. Returns (q, k, v) or (q, k, v, q_pre, k_pre).
+
+    The GQAttention variant options: norm=False (split -> RoPE only; w_q, w_k
+    may be None), bias (float32 [(n_q + 2 n_kv) * head_dim] in the packed
+    row's order, added first), inv_freq (head_dim / 2 frequencies replacing
+    rope_base**(-2i/D)) and rope_scale (factor on cos and sin)."""
     _check_dev(packed, pos, w_q, w_k)
     L, T = _layout_of(packed, n_q, n_kv, head_dim, kind)
     dev = packed.device
@@ -42,63 +64,68 @@ def prologue_forward(packed, pos, w_q, w_k, n_q, n_kv, head_dim=64, kind="interl
     v = torch.empty(T, n_kv, head_dim, dtype=torch.bfloat16, device=dev)
     q_pre = torch.empty_like(q) if save_pre else None
     k_pre = torch.empty_like(k) if save_pre else None
-    flags = (C.QKVP_NOPE if nope else 0) | (C.QKVP_SAVE_PRE if save_pre else 0)
-    C.qkv_prologue_fwd(L, T, packed, pos, w_q, w_k, eps, rope_base, flags, q, k, v, q_pre, k_pre, stream)
+    C.qkv_prologue_fwd_ex(L, _variant(bias, inv_freq, rope_scale), T, packed, pos, w_q, w_k, eps, rope_base,
+                          _flags(nope, save_pre, norm), q, k, v, q_pre, k_pre, stream)
     return (q, k, v, q_pre, k_pre) if save_pre else (q, k, v)
 
 
 def prologue_backward(dq, dk, dv, q_pre, k_pre, pos, w_q, w_k, n_q, n_kv, head_dim=64,
                       kind="interleaved", eps=1e-6, rope_base=500000.0, nope=False, stream=None,
-                      workspace=None):
-    """Packed gradient [T, (n_q + 2 n_kv) * head_dim] and fp32 (dw_q, dw_k)."""
+                      workspace=None, norm=True, bias=None, inv_freq=None, rope_scale=1.0):
+    """Packed gradient [T, (n_q + 2 n_kv) * head_dim] and fp32 (dw_q, dw_k), plus
+    the fp32 bias gradient when a bias is given: (dpacked, dw_q, dw_k[, dbias]).
+    Without the norm dw_q, dw_k are None and q_pre, k_pre, w_q, w_k may be None."""
     _check_dev(dq, dk, dv, q_pre, k_pre, w_q, w_k)
     T = dq.shape[0]
     L = C.layout(kind, n_q, n_kv, head_dim)
     dev = dq.device
+    V = _variant(bias, inv_freq, rope_scale)
     dpacked = torch.empty(T, (n_q + 2 * n_kv) * head_dim, dtype=torch.bfloat16, device=dev)
-    dw_q = torch.empty(head_dim, dtype=torch.float32, device=dev)
-    dw_k = torch.empty(head_dim, dtype=torch.float32, device=dev)
-    need = C.qkv_prologue_bwd_workspace_size(L, T)
+    dw_q = torch.empty(head_dim, dtype=torch.float32, device=dev) if norm else None
+    dw_k = torch.empty(head_dim, dtype=torch.float32, device=dev) if norm else None
+    dbias = torch.empty((n_q + 2 * n_kv) * head_dim, dtype=torch.float32, device=dev) if bias is not None else None
+    need = C.qkv_prologue_bwd_workspace_size_ex(L, V, T)
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
-    C.qkv_prologue_bwd(L, T, dq, dk, dv, q_pre, k_pre, pos, w_q, w_k, eps, rope_base,
-                       C.QKVP_NOPE if nope else 0, dpacked, dw_q, dw_k, workspace, need, stream)
-    return dpacked, dw_q, dw_k
+    C.qkv_prologue_bwd_ex(L, V, T, dq, dk, dv, q_pre, k_pre, pos, w_q, w_k, eps, rope_base,
+                          _flags(nope, False, norm), dpacked, dw_q, dw_k, dbias, workspace, need, stream)
+    return (dpacked, dw_q, dw_k, dbias) if bias is not None else (dpacked, dw_q, dw_k)
 
 
 def prologue_pool_write(packed, pos, w_q, w_k, page, offset, k_pool, v_pool, n_q, n_kv, head_dim=64,
                         kind="interleaved", eps=1e-6, rope_base=500000.0, nope=False, dev_status=None,
-                        stream=None):
+                        stream=None, norm=True, bias=None, inv_freq=None, rope_scale=1.0):
     """q contiguous; normed(+roped) k and raw v into the paged pools. Returns q."""
     _check_dev(packed, pos, w_q, w_k, page, offset, k_pool, v_pool)
     L, T = _layout_of(packed, n_q, n_kv, head_dim, kind)
     q = torch.empty(T, n_q, head_dim, dtype=torch.bfloat16, device=packed.device)
-    C.qkv_prologue_pool_write(L, T, packed, pos, w_q, w_k, eps, rope_base, C.QKVP_NOPE if nope else 0, q,
-                              page, offset, k_pool, v_pool, k_pool.shape[0], k_pool.shape[1],
-                              dev_status, stream)
+    C.qkv_prologue_pool_write_ex(L, _variant(bias, inv_freq, rope_scale), T, packed, pos, w_q, w_k, eps,
+                                 rope_base, _flags(nope, False, norm), q, page, offset, k_pool, v_pool,
+                                 k_pool.shape[0], k_pool.shape[1], dev_status, stream)
     return q
 
 
 def latent_rows(rows, pos, w, eps=1e-6, rope_base=10000.0, norm_dim=512, rope_dim=64, nope=False,
-                stream=None):
+                stream=None, inv_freq=None, rope_scale=1.0):
     """MLA kv latent rows normed/roped into a new contiguous [T, norm_dim + rope_dim] tensor."""
     _check_dev(rows, pos, w)
     T = rows.shape[0]
     L = C.layout("latent", norm_dim=norm_dim, rope_dim=rope_dim)
     out = torch.empty(T, norm_dim + rope_dim, dtype=torch.bfloat16, device=rows.device)
-    C.qkv_prologue_fwd(L, T, rows, pos, None, w, eps, rope_base, C.QKVP_NOPE if nope else 0, None, out,
-                       None, None, None, stream)
+    C.qkv_prologue_fwd_ex(L, _variant(None, inv_freq, rope_scale), T, rows, pos, None, w, eps, rope_base,
+                          _flags(nope), None, out, None, None, None, stream)
     return out
 
 
 def latent_pool_write(rows, pos, w, page, offset, pool, eps=1e-6, rope_base=10000.0, norm_dim=512,
-                      rope_dim=64, nope=False, dev_status=None, stream=None):
+                      rope_dim=64, nope=False, dev_status=None, stream=None, inv_freq=None, rope_scale=1.0):
     """MLA kv latent rows normed/roped straight into pool [num_pages, page_size, 576]."""
     _check_dev(rows, pos, w, page, offset, pool)
     T = rows.shape[0]
     L = C.layout("latent", norm_dim=norm_dim, rope_dim=rope_dim)
-    C.qkv_prologue_pool_write(L, T, rows, pos, None, w, eps, rope_base, C.QKVP_NOPE if nope else 0, None,
-                              page, offset, pool, None, pool.shape[0], pool.shape[1], dev_status, stream)
+    C.qkv_prologue_pool_write_ex(L, _variant(None, inv_freq, rope_scale), T, rows, pos, None, w, eps, rope_base,
+                                 _flags(nope), None, page, offset, pool, None, pool.shape[0], pool.shape[1],
+                                 dev_status, stream)
 
 
 class QKVPrologue(torch.autograd.Function):
@@ -124,3 +151,35 @@ class QKVPrologue(torch.autograd.Function):
         dpacked, dw_q, dw_k = prologue_backward(dq, dk, dv, q_pre, k_pre, pos, w_q, w_k, n_q, n_kv,
                                                 head_dim, kind, eps, rope_base, nope)
         return dpacked.view(shape), None, dw_q, dw_k, None, None, None, None, None, None, None
+
+
+class GQAttentionPrologue(torch.autograd.Function):
+    """The GQAttention variant region (Llama 3, Qwen3, GPT-OSS): packed [T, row]
+    -> (q, k, v) with the norm optional, an optional qkv bias and a caller's
+    RoPE frequency table / cos-sin factor; the backward writes d(packed) in one
+    pass and returns the norm-weight and bias gradients where they exist.
+
+    apply(packed, pos, w_q, w_k, bias, n_q, n_kv, head_dim, kind, eps, rope_base,
+          nope, norm, inv_freq, rope_scale); w_q / w_k / bias may be None.
+    """
+
+    @staticmethod
+    def forward(ctx, packed, pos, w_q, w_k, bias, n_q, n_kv, head_dim, kind, eps, rope_base, nope, norm,
+                inv_freq, rope_scale):
+        out = prologue_forward(packed, pos, w_q, w_k, n_q, n_kv, head_dim, kind, eps, rope_base, nope,
+                               save_pre=norm, norm=norm, bias=bias, inv_freq=inv_freq, rope_scale=rope_scale)
+        q, k, v = out[:3]
+        q_pre, k_pre = (out[3], out[4]) if norm else (None, None)
+        ctx.save_for_backward(q_pre, k_pre, pos, w_q, w_k, bias)
+        ctx.cfg = (n_q, n_kv, head_dim, kind, eps, rope_base, nope, norm, inv_freq, rope_scale, packed.shape)
+        return q, k, v
+
+    @staticmethod
+    def backward(ctx, dq, dk, dv):
+        q_pre, k_pre, pos, w_q, w_k, bias = ctx.saved_tensors
+        n_q, n_kv, head_dim, kind, eps, rope_base, nope, norm, inv_freq, rope_scale, shape = ctx.cfg
+        dq, dk, dv = (g.contiguous() for g in (dq, dk, dv))
+        out = prologue_backward(dq, dk, dv, q_pre, k_pre, pos, w_q, w_k, n_q, n_kv, head_dim, kind, eps, rope_base,
+                                nope, norm=norm, bias=bias, inv_freq=inv_freq, rope_scale=rope_scale)
+        dbias = out[3] if bias is not None else None
+        return (out[0].view(shape), None, out[1], out[2], dbias) + (None,) * 10

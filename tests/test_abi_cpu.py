@@ -54,7 +54,7 @@ def test_binding_exposes_the_same_names(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.qkv_prologue_version() == lib.QKVP_VERSION == 1
+    assert lib.qkv_prologue_version() == lib.QKVP_VERSION == 2
     for code in range(-8, 1):
         s = lib.qkv_prologue_status_string(code)
         assert s and s != "unknown status"
@@ -66,10 +66,20 @@ def test_constants_match_header(lib):
     for name in ("QKVP_OK", "QKVP_ERR_NULL", "QKVP_ERR_SHAPE", "QKVP_ERR_ALIGN", "QKVP_ERR_ARCH",
                  "QKVP_ERR_WORKSPACE", "QKVP_ERR_LAUNCH", "QKVP_ERR_FLAGS", "QKVP_ERR_VALUE",
                  "QKVP_INTERLEAVED", "QKVP_SECTIONED", "QKVP_LATENT", "QKVP_NOPE", "QKVP_SAVE_PRE",
-                 "QKVP_ACCUMULATE_DW", "QKVP_FORCE_GENERIC", "QKVP_DEV_BAD_PAGE", "QKVP_DEV_BAD_OFFSET"):
+                 "QKVP_ACCUMULATE_DW", "QKVP_FORCE_GENERIC", "QKVP_NORM_OFF", "QKVP_DEV_BAD_PAGE",
+                 "QKVP_DEV_BAD_OFFSET"):
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", src)
         assert m, name
         assert int(m.group(1)) == getattr(lib, name), name
+
+
+def test_variant_struct_matches_c_layout(lib):
+    # double* inv_freq; double rope_scale; float* bias
+    V = lib.qkvp_variant
+    assert ctypes.sizeof(V) == 24
+    assert V.inv_freq.offset == 0 and V.rope_scale.offset == 8 and V.bias.offset == 16
+    v = lib.variant(inv_freq=[1.0, 0.5], rope_scale=1.25, bias=0x1000)
+    assert v.inv_freq[0] == 1.0 and v.inv_freq[1] == 0.5 and v.rope_scale == 1.25 and v.bias == 0x1000
 
 
 def test_layout_struct_matches_c_layout(lib):
@@ -134,7 +144,7 @@ def test_fwd_argument_checks(lib):
     assert _fwd(C, pos=None, flags=C.QKVP_NOPE) == C.QKVP_ERR_ARCH  # NoPE needs no positions
     assert _fwd(C, flags=C.QKVP_SAVE_PRE) == C.QKVP_ERR_NULL
     assert _fwd(C, flags=C.QKVP_SAVE_PRE, q_pre=A, k_pre=A) == C.QKVP_ERR_ARCH
-    assert _fwd(C, flags=16) == C.QKVP_ERR_FLAGS
+    assert _fwd(C, flags=32) == C.QKVP_ERR_FLAGS
     assert _fwd(C, flags=C.QKVP_FORCE_GENERIC) == C.QKVP_ERR_ARCH
     assert _fwd(C, flags=C.QKVP_ACCUMULATE_DW) == C.QKVP_ERR_FLAGS
     assert _fwd(C, packed=A + 8) == C.QKVP_ERR_ALIGN
@@ -223,6 +233,67 @@ def test_bwd_argument_checks(lib):
     assert bwd(T=0, flags=C.QKVP_ACCUMULATE_DW, ws=None, wsb=0) == C.QKVP_OK
     # T == 0 without ACCUMULATE_DW zeroes dw, which needs the device
     assert bwd(T=0, ws=None, wsb=0) == C.QKVP_ERR_ARCH
+
+
+@cpu_only
+def test_variant_argument_checks(lib):
+    C = lib
+    L = C.layout("interleaved", 8, 2, 64)
+    F = (8 + 2 * 2) * 64
+
+    def fwd(V, flags=0, wq=A, wk=A, base=1e4, L=L, **kw):
+        a = dict(T=4, packed=A, pos=A, q=A, k=A, v=A)
+        a.update(kw)
+        return C.qkv_prologue_fwd_ex(L, V, a["T"], a["packed"], a["pos"], wq, wk, 1e-6, base, flags, a["q"],
+                                     a["k"], a["v"], None, None, stream=0, check=False)
+
+    assert fwd(None) == C.QKVP_ERR_ARCH
+    assert fwd(C.variant(inv_freq=[0.5] * 32, rope_scale=1.3, bias=A)) == C.QKVP_ERR_ARCH
+    # norm off needs no weights; with it on they are required
+    assert fwd(None, flags=C.QKVP_NORM_OFF, wq=None, wk=None) == C.QKVP_ERR_ARCH
+    assert fwd(None, wq=None) == C.QKVP_ERR_NULL
+    # a frequency table replaces the base, which is then not checked
+    assert fwd(None, base=0.0) == C.QKVP_ERR_VALUE
+    assert fwd(C.variant(inv_freq=[1.0] * 32), base=0.0) == C.QKVP_ERR_ARCH
+    assert fwd(C.variant(inv_freq=[1.0] * 31 + [float("nan")])) == C.QKVP_ERR_VALUE
+    assert fwd(C.variant(rope_scale=-1.0)) == C.QKVP_ERR_VALUE
+    assert fwd(C.variant(rope_scale=float("inf"))) == C.QKVP_ERR_VALUE
+    assert fwd(C.variant(bias=A + 4)) == C.QKVP_ERR_ALIGN
+    # latent rows: frequency table and factor yes, bias and norm-off no
+    LL = C.layout("latent", norm_dim=512, rope_dim=64)
+    assert fwd(C.variant(inv_freq=[1.0] * 32, rope_scale=2.0), L=LL, wq=None, q=None, v=None) == C.QKVP_ERR_ARCH
+    assert fwd(C.variant(bias=A), L=LL, wq=None, q=None, v=None) == C.QKVP_ERR_SHAPE
+    assert fwd(None, flags=C.QKVP_NORM_OFF, L=LL, wq=None, q=None, v=None) == C.QKVP_ERR_FLAGS
+    pw = C.qkv_prologue_pool_write_ex(L, C.variant(bias=A), 4, A, A, None, None, 1e-6, 1e4, C.QKVP_NORM_OFF, A, A,
+                                      A, A, A, 4096, 64, None, stream=0, check=False)
+    assert pw == C.QKVP_ERR_ARCH
+
+    # backward
+    V = C.variant(bias=A)
+    need = C.qkv_prologue_bwd_workspace_size_ex(L, V, 100)
+    assert need > C.qkv_prologue_bwd_workspace_size(L, 100)
+    # one row per CTA now also holds the bias gradient's F floats
+    assert need == C.qkv_prologue_bwd_workspace_size(L, 100) // (2 * 64) * (2 * 64 + F)
+    assert C.qkv_prologue_bwd_workspace_size_ex(L, None, 100) == C.qkv_prologue_bwd_workspace_size(L, 100)
+
+    def bwd(V, flags=0, qp=A, kp=A, wq=A, wk=A, dwq=A, dwk=A, db=A, ws=A, wsb=need, L=L):
+        return C.qkv_prologue_bwd_ex(L, V, 100, A, A, A, qp, kp, A, wq, wk, 1e-6, 5e5, flags, A, dwq, dwk, db, ws,
+                                     wsb, stream=0, check=False)
+
+    assert bwd(V) == C.QKVP_ERR_ARCH
+    assert bwd(V, db=None) == C.QKVP_ERR_NULL
+    assert bwd(V, db=A + 4) == C.QKVP_ERR_ALIGN
+    assert bwd(V, wsb=need - 1) == C.QKVP_ERR_WORKSPACE
+    assert bwd(None, db=None) == C.QKVP_ERR_ARCH  # no bias: no dbias needed
+    # norm off: no saved inputs, weights or weight gradients needed
+    assert bwd(V, flags=C.QKVP_NORM_OFF, qp=None, kp=None, wq=None, wk=None, dwq=None, dwk=None) == C.QKVP_ERR_ARCH
+    assert bwd(V, qp=None) == C.QKVP_ERR_NULL
+    # norm off and no bias: nothing to reduce, no workspace needed
+    assert bwd(None, flags=C.QKVP_NORM_OFF, qp=None, kp=None, wq=None, wk=None, dwq=None, dwk=None, ws=None,
+               wsb=0) == C.QKVP_ERR_ARCH
+    # a bias gradient longer than one-token work items can hold
+    Lbig = C.layout("interleaved", 128, 16, 128)
+    assert bwd(V, L=Lbig, wsb=1 << 40) == C.QKVP_ERR_SHAPE
 
 
 @cpu_only

@@ -17,9 +17,11 @@ qkv inside the q/k region" (Problem 1), and the 576-wide MLA kv latent rows
 each drafter layer's kv path beside its q path". No dataset is involved.
 """
 
+import math
 from dataclasses import dataclass, field
 from typing import Optional
 
+import numpy as np
 import torch
 
 EPS = 1e-6
@@ -88,6 +90,11 @@ class GQAWorkload:
     offset: Optional[torch.Tensor] = None  # int32 [T]
     num_pages: int = 0
     page_size: int = 0
+    # the GQAttention variant options (Llama 3, Qwen3, GPT-OSS)
+    norm: bool = True
+    bias: Optional[torch.Tensor] = None   # float32 [row_width], interleaved packed order
+    inv_freq: Optional[np.ndarray] = None  # float64 [head_dim / 2], or None: base**(-2i/D)
+    rope_scale: float = 1.0
     extra: dict = field(default_factory=dict)
 
     @property
@@ -104,6 +111,20 @@ class GQAWorkload:
 
     def sectioned_rows(self):
         return sectioned_from_interleaved(self.packed, self.n_q, self.n_kv, self.head_dim)
+
+    def bias_for(self, kind):
+        """The bias in the packed order of `kind` (None without a bias)."""
+        if self.bias is None:
+            return None
+        if kind == "interleaved":
+            return self.bias
+        G = self.n_q // self.n_kv
+        b = self.bias.reshape(1, self.n_kv, G + 2, self.head_dim)
+        return sectioned_from_interleaved(b, self.n_q, self.n_kv, self.head_dim).reshape(-1).contiguous()
+
+    def variant(self, kind="interleaved"):
+        """Keyword options of the GQAttention variant (for oracle and library calls)."""
+        return dict(norm=self.norm, bias=self.bias_for(kind), inv_freq=self.inv_freq, rope_scale=self.rope_scale)
 
 
 @dataclass
@@ -147,6 +168,80 @@ def gqa_inputs(T, n_q, n_kv, head_dim, seed, rope_base, nope=False, pos_high=Non
         wl.dq = normal_bf16((T, n_q, head_dim), g)
         wl.dk = normal_bf16((T, n_kv, head_dim), g)
         wl.dv = normal_bf16((T, n_kv, head_dim), g)
+    return wl
+
+
+# --- the GQAttention variant (Llama 3, Qwen3, GPT-OSS) -------------------------
+#
+# Frequency tables and the bias are inputs of the library call (the library
+# never computes them); these build them the way those models do.
+
+def llama3_inv_freq(head_dim, base=500000.0, factor=8.0, low_freq_factor=1.0, high_freq_factor=4.0,
+                    original_max_position=8192):
+    """Llama 3.1-style frequency table: a frequency whose wavelength is shorter
+    than original_max_position / high_freq_factor keeps its value, one longer
+    than original_max_position / low_freq_factor is divided by factor, and the
+    ones between blend the two linearly in original_max_position / wavelength."""
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    f = base ** (-2.0 * i / head_dim)
+    wavelen = 2.0 * np.pi / f
+    smooth = (original_max_position / wavelen - low_freq_factor) / (high_freq_factor - low_freq_factor)
+    mid = (1.0 - smooth) * f / factor + smooth * f
+    out = np.where(wavelen > original_max_position / low_freq_factor, f / factor, mid)
+    return np.where(wavelen < original_max_position / high_freq_factor, f, out)
+
+
+def yarn_inv_freq(head_dim, base, factor, original_max_position, beta_fast=32.0, beta_slow=1.0):
+    """YaRN-style frequency table: frequencies that turn more than beta_fast
+    times over the original context keep their value, those turning fewer than
+    beta_slow times are divided by factor, with a linear ramp over the
+    dimensions between."""
+    def dim_of(turns):
+        return head_dim * math.log(original_max_position / (turns * 2.0 * math.pi)) / (2.0 * math.log(base))
+
+    lo = max(math.floor(dim_of(beta_fast)), 0)
+    hi = min(math.ceil(dim_of(beta_slow)), head_dim - 1)
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    keep = base ** (-2.0 * i / head_dim)
+    ramp = np.clip((i - lo) / max(hi - lo, 1e-3), 0.0, 1.0)  # 0: keep, 1: divide by factor
+    return keep * (1.0 - ramp) + keep / factor * ramp
+
+
+def yarn_attention_factor(factor):
+    """YaRN's factor on cos and sin: 0.1 ln(factor) + 1."""
+    return 0.1 * math.log(factor) + 1.0
+
+
+def qkv_bias(row_width, g):
+    """A fused linear's qkv bias: float32 N(0, 0.5^2) [row_width]."""
+    return (torch.randn(row_width, generator=g, dtype=torch.float32) * 0.5).contiguous()
+
+
+def llama3(T, seed=6, pos_high=None, with_grads=True):
+    """Llama 3 8B attention: 32 q heads over 8 kv heads, head_dim 128, no q/k
+    norm, RoPE base 5e5 with the Llama 3.1 frequency scaling."""
+    wl = gqa_inputs(T, 32, 8, 128, seed, 500000.0, pos_high=pos_high, name=f"llama3_T{T}", with_grads=with_grads)
+    wl.norm = False
+    wl.inv_freq = llama3_inv_freq(128)
+    return wl
+
+
+def qwen3(T, seed=7, pos_high=None, with_grads=True):
+    """Qwen3 8B attention: 32 q heads over 8 kv heads, head_dim 128, per-head
+    q/k RMSNorm, RoPE base 1e6."""
+    return gqa_inputs(T, 32, 8, 128, seed, 1000000.0, pos_high=pos_high, name=f"qwen3_T{T}",
+                      with_grads=with_grads)
+
+
+def gpt_oss(T, seed=8, pos_high=None, with_grads=True):
+    """GPT-OSS 20b attention: 64 q heads over 8 kv heads, head_dim 64, no q/k
+    norm, a qkv bias, RoPE base 150000 with a YaRN-style table (factor 32,
+    original context 4096) and its cos/sin factor."""
+    wl = gqa_inputs(T, 64, 8, 64, seed, 150000.0, pos_high=pos_high, name=f"gpt_oss_T{T}", with_grads=with_grads)
+    wl.norm = False
+    wl.bias = qkv_bias(wl.row_width, _gen(seed * 1000 + 11))
+    wl.inv_freq = yarn_inv_freq(64, 150000.0, 32.0, 4096)
+    wl.rope_scale = yarn_attention_factor(32.0)
     return wl
 
 

@@ -407,6 +407,79 @@ class MlaStep(_Step):
                                   self.stream)
 
 
+class VariantTrainStep(_Step):
+    """Training forward + backward of the GQAttention variant for one model's
+    attention shape (sectioned q | k | v rows, as a fused QKV linear gives)."""
+
+    kernels_per_step = 3
+
+    def __init__(self, dev, T, model):
+        import torch
+
+        import workloads
+
+        self._common(dev)
+        C = self.C
+        self.T, self.model = T, model
+        wl = {"llama3": workloads.llama3, "qwen3": workloads.qwen3, "gpt_oss": workloads.gpt_oss}[model](T)
+        self.wl = wl
+        n_q, n_kv, hd = wl.n_q, wl.n_kv, wl.head_dim
+        row = wl.row_width
+        self.L = C.layout("sectioned", n_q, n_kv, hd)
+        self.packed = wl.sectioned_rows().to(dev)
+        self.pos = wl.pos.to(dev)
+        self.w_q = wl.w_q.to(dev) if wl.norm else None
+        self.w_k = wl.w_k.to(dev) if wl.norm else None
+        self.bias = wl.bias_for("sectioned").to(dev) if wl.bias is not None else None
+        self.V = C.variant(inv_freq=None if wl.inv_freq is None else list(wl.inv_freq), rope_scale=wl.rope_scale,
+                           bias=self.bias)
+        self.dq, self.dk, self.dv = wl.dq.to(dev), wl.dk.to(dev), wl.dv.to(dev)
+        bf = self.bf
+        self.q, self.k, self.v = (torch.empty(T, n, hd, **bf) for n in (n_q, n_kv, n_kv))
+        self.q_pre = torch.empty(T, n_q, hd, **bf) if wl.norm else None
+        self.k_pre = torch.empty(T, n_kv, hd, **bf) if wl.norm else None
+        self.dpacked = torch.empty(T, row, **bf)
+        self.dw_q = torch.empty(hd, dtype=torch.float32, device=dev) if wl.norm else None
+        self.dw_k = torch.empty(hd, dtype=torch.float32, device=dev) if wl.norm else None
+        self.dbias = torch.empty(row, dtype=torch.float32, device=dev) if wl.bias is not None else None
+        self.ws_bytes = C.qkv_prologue_bwd_workspace_size_ex(self.L, self.V, T)
+        self.ws = torch.empty(max(16, self.ws_bytes), dtype=torch.uint8, device=dev)
+        self.flags = 0 if wl.norm else C.QKVP_NORM_OFF
+        bf2, saved = 2, (n_q + n_kv) * hd * 2
+        small = (2 * hd * 4 if wl.norm else 0) + (row * 4 if wl.bias is not None else 0)
+        fwd_b = T * (row * bf2 + 4 + row * bf2 + (saved if wl.norm else 0)) + small
+        bwd_b = T * (row * bf2 + (saved if wl.norm else 0) + 4 + row * bf2) + small
+        self.kernels_per_step = 3 if (wl.norm or wl.bias is not None) else 2
+        self.calls = [(f"qkv_prologue_fwd_ex (qkvp_fwd_stream_kernel, {model})", self.fwd, fwd_b),
+                      (f"qkv_prologue_bwd_ex (qkvp_bwd_stream_kernel{' + finalize' if self.kernels_per_step == 3 else ''},"
+                       f" {model})", self.bwd, bwd_b)]
+        self.h_in = {"packed": wl.sectioned_rows(), "pos": wl.pos, "dq": wl.dq, "dk": wl.dk, "dv": wl.dv}
+        self.out_names = ("q", "k", "v", "dpacked")
+        opts = []
+        if not wl.norm:
+            opts.append("no q/k norm")
+        if wl.bias is not None:
+            opts.append("qkv bias")
+        if wl.inv_freq is not None:
+            opts.append("scaled RoPE frequency table")
+        if wl.rope_scale != 1.0:
+            opts.append(f"cos/sin factor {wl.rope_scale:.4f}")
+        self.describe = (f"{model} attention train fwd+bwd, T={T}, sectioned [T, ({n_q} + 2*{n_kv}) * {hd}], "
+                         f"RoPE base {wl.rope_base:g}" + (", " + ", ".join(opts) if opts else ""))
+
+    def fwd(self):
+        C, wl = self.C, self.wl
+        C.qkv_prologue_fwd_ex(self.L, self.V, self.T, self.packed, self.pos, self.w_q, self.w_k, wl.eps, wl.rope_base,
+                              self.flags | (C.QKVP_SAVE_PRE if wl.norm else 0) | self.xflags, self.q, self.k, self.v,
+                              self.q_pre, self.k_pre, self.stream)
+
+    def bwd(self):
+        C, wl = self.C, self.wl
+        C.qkv_prologue_bwd_ex(self.L, self.V, self.T, self.dq, self.dk, self.dv, self.q_pre, self.k_pre, self.pos,
+                              self.w_q, self.w_k, wl.eps, wl.rope_base, self.flags | self.xflags, self.dpacked,
+                              self.dw_q, self.dw_k, self.dbias, self.ws, self.ws_bytes, self.stream)
+
+
 def make_workload(name, dev, tokens):
     if name == "train":
         return TrainStep(dev, tokens or 16384)
@@ -416,6 +489,8 @@ def make_workload(name, dev, tokens):
         return DecodeStep(dev, tokens or 256)
     if name == "mla":
         return MlaStep(dev, tokens or 32768)
+    if name in ("llama3_train", "qwen3_train", "gpt_oss_train"):
+        return VariantTrainStep(dev, tokens or 16384, name[:-len("_train")])
     raise ValueError(name)
 
 
@@ -626,7 +701,9 @@ def run_ours(args):
         "data": "synthetic (seeded N(0,1) bf16 rows and upstream grads, U(0.5,1.5) norm weights)",
         "config": {
             "workload": ws.describe,
-            "T": T, "n_q": N_Q, "n_kv": N_KV, "head_dim": D,
+            "T": T,
+            **({"n_q": ws.wl.n_q, "n_kv": ws.wl.n_kv, "head_dim": ws.wl.head_dim} if hasattr(ws.wl, "n_q") else
+               {"norm_dim": ws.wl.norm_dim, "rope_dim": ws.wl.rope_dim}),
             "bytes_per_step": step_bytes,
             "l2": (f"flushed before every step ({flush_buf.numel() >> 20} MiB write, then a {flush_buf.numel() >> 20} MiB "
                    "read so the write-back is done; both outside the timed calls)"
@@ -768,7 +845,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--workload", choices=["train", "prefill", "prefill_nope", "decode", "mla"], default="train",
+    ap.add_argument("--workload", choices=["train", "prefill", "prefill_nope", "decode", "mla", "llama3_train",
+                                           "qwen3_train", "gpt_oss_train"], default="train",
                     help="train (the headline) | prefill | prefill_nope | decode (pool write) | mla (latent pool write)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="T (0 = the workload's default: 16384 train/prefill, 256 decode, 32768 mla)")

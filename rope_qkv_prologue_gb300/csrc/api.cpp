@@ -120,40 +120,47 @@ bool allow_smem(const void* kernel, size_t smem) {
 // Tile geometry of the streaming kernels, or false when the layout does not
 // fit them. A tile holds tpt tokens; each token's upt units (chunk pairs) are
 // split over tpg = consumers / tpt threads taking steps = ceil(upt / tpg)
-// units each (steps <= kStreamMaxSteps); lph = lanes per head. The smallest tpt whose last step is at least
-// kMinStepFill full is taken, so a tile stays small and the ring deep; at
-// least two stages per CTA must fit in the shared memory left to each of the
-// shape.ctas_per_sm CTAs of an SM. token_bytes = bytes staged per token.
-// extra_dyn = dynamic shared memory after the ring (the bias copy);
-// one_token = one-token tiles only, with at most max_steps steps (the bias
-// gradient of the backward).
+// units each (steps <= max_steps); lph = lanes per head. Among the tile sizes
+// whose last step is at least kMinStepFill full, the smallest one of at least
+// shape.min_stage_bytes is taken (else the largest), so a tile stays small
+// and the ring deep; the ring holds up to shape.max_inflight bytes, at least
+// two stages, in the shared memory left to each of the shape.ctas_per_sm CTAs
+// of an SM. token_bytes = bytes staged per token. extra_dyn = dynamic shared
+// memory after the ring (the bias copy); any_fill = take tile sizes whatever
+// their last step's fill (the bias gradient, whose step cap is small).
 bool stream_geometry(const StreamShape& shape, int upt, int lph, int hd, int64_t T, int64_t token_bytes,
-                     int smem_per_sm, int static_smem, int extra_dyn, bool one_token, int max_steps,
+                     int smem_per_sm, int static_smem, int extra_dyn, bool any_fill, int max_steps,
                      StreamGeom* g, size_t* smem) {
   constexpr double kMinStepFill = 0.8;  // useful chunks / (steps * tpg)
   const int nct = shape.warps * 32;
   const int budget = smem_per_sm / shape.ctas_per_sm - 1024 - static_smem - extra_dyn;
+  int pick = 0;
   for (int tpt = 1; nct / tpt >= lph && (nct / tpt) % lph == 0; tpt *= 2) {
     const int tpg = nct / tpt;
     const int steps = (upt + tpg - 1) / tpg;
-    if (steps > max_steps) return false;  // larger tiles only add steps
-    if (!one_token && (double)upt / ((double)steps * tpg) < kMinStepFill) continue;
-    const int64_t stage = (int64_t)tpt * token_bytes;
-    const int fixed = StreamSmem::tables(hd) + 128;
-    const int64_t per_stage = stage + StreamSmem::table_stride(hd, tpt);
-    int64_t stages = (budget - fixed) / per_stage;
-    if (stages < 2) return false;
-    if (stages > shape.max_stages) stages = shape.max_stages;
-    if (stages > kMaxStages) stages = kMaxStages;
-    g->tpt = tpt;
-    g->stages = (int32_t)stages;
-    g->steps = steps;
-    g->stage_bytes = (int32_t)stage;
-    g->n_tiles = (T + tpt - 1) / tpt;
-    *smem = (size_t)StreamSmem::data(hd, tpt, (int)stages) + (size_t)stages * stage + (size_t)extra_dyn;
-    return true;
+    if (steps > max_steps) break;  // larger tiles only add steps
+    if (!any_fill && (double)upt / ((double)steps * tpg) < kMinStepFill) continue;
+    const int64_t per_stage = (int64_t)tpt * token_bytes + StreamSmem::table_stride(hd, tpt);
+    if ((budget - StreamSmem::tables(hd) - 128) / per_stage < 2) break;  // two stages no longer fit
+    pick = tpt;
+    if ((int64_t)tpt * token_bytes >= shape.min_stage_bytes) break;
   }
-  return false;
+  if (pick == 0) return false;
+  const int tpt = pick;
+  const int64_t stage = (int64_t)tpt * token_bytes;
+  const int64_t per_stage = stage + StreamSmem::table_stride(hd, tpt);
+  int64_t stages = (budget - StreamSmem::tables(hd) - 128) / per_stage;
+  int64_t by_bytes = shape.max_inflight / stage;
+  if (by_bytes < 2) by_bytes = 2;
+  if (stages > by_bytes) stages = by_bytes;
+  if (stages > kMaxStages) stages = kMaxStages;
+  g->tpt = tpt;
+  g->stages = (int32_t)stages;
+  g->steps = (upt + nct / tpt - 1) / (nct / tpt);
+  g->stage_bytes = (int32_t)stage;
+  g->n_tiles = (T + tpt - 1) / tpt;
+  *smem = (size_t)StreamSmem::data(hd, tpt, (int)stages) + (size_t)stages * stage + (size_t)extra_dyn;
+  return true;
 }
 
 // Launch with programmatic stream serialization: the kernel may be launched
@@ -308,9 +315,9 @@ int check_variant(const qkvp_variant* v, int rope_dim, bool gqa, Variant* out) {
   return QKVP_OK;
 }
 
-// Bias gradient limits: pipelined backward with one-token tiles of at most
-// kBiasMaxSteps chunk pairs per thread; the general backward with one-token
-// work items of at most kThreads * kBwdChunksPerThread chunks.
+// Bias gradient limits: the pipelined backward keeps at most kBiasMaxSteps
+// chunk pairs per thread; the general backward takes one-token work items of
+// at most kThreads * kBwdChunksPerThread chunks.
 constexpr int kBiasMaxChunks = kThreads * kBwdChunksPerThread;
 
 #define QKVP_TRY(expr)          \
@@ -417,7 +424,7 @@ static int gqa_forward(const qkvp_layout* L, const qkvp_variant* variant, int64_
   const int bias_bytes = vr.bias ? a.cpt * 8 * (int)sizeof(float) : 0;
   size_t smem = 0;
   if (!(flags & QKVP_FORCE_GENERIC) &&
-      stream_geometry(fwd_stream_shape(save, rope && norm), a.cpt / 2, L->head_dim / 16, L->head_dim, T,
+      stream_geometry(fwd_stream_shape(save, rope), a.cpt / 2, L->head_dim / 16, L->head_dim, T,
                       (int64_t)a.cpt * 16, smem_per_sm, 0, bias_bytes, false, kStreamMaxSteps, &a.sg, &smem) &&
       (a.err = device_error_word()) != nullptr) {
     a.sg.dense = g.stride == g.row;

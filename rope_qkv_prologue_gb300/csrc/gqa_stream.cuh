@@ -74,7 +74,7 @@ constexpr int stream_max_regs(int ncw, int cps) {
 // wait that timed out) drains the copies it issued before returning.
 // `load(stage_ptr, t0, ntok, bar, policy)` (run by lane 0 only) announces the
 // tile's byte count on `bar` and issues its bulk copies.
-template <int HALF, bool ROPE, bool POOL, class LoadTile, bool STAGE_POS = false>
+template <int HALF, bool ROPE, bool POOL, bool STAGE_POS = false, class LoadTile>
 __device__ __forceinline__ void stream_producer(unsigned char* smem, int hd, int tpt, int stages,
                                                 int stage_bytes, int64_t n_tiles, int64_t T,
                                                 const int32_t* pos, const RopeTable& rope,
@@ -103,6 +103,10 @@ __device__ __forceinline__ void stream_producer(unsigned char* smem, int hd, int
     if (lane == 0) load(data + (size_t)s * stage_bytes, t0, ntok, &full[s], policy);
     float* tab = reinterpret_cast<float*>(smem + StreamSmem::tables(hd) + s * StreamSmem::table_stride(hd, tpt));
     if (ROPE) {
+      // Unrolled: the position loads and sincospif chains of several entries
+      // are in flight together (for head_dim 128 a tile's 64 frequencies per
+      // token otherwise hold the ring back; measured on GB300).
+#pragma unroll 4
       for (int i = lane; i < ntok * HALF; i += 32) {
         const int tl = i / HALF, f = i - (i / HALF) * HALF;
         float c, sn;
@@ -313,10 +317,10 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_fwd_stream_kernel(co
 // NORM off: g = R^T d is the whole gradient, and the saved inputs are neither
 // staged nor read (three sections per stage instead of five). BIAS: the norm's
 // input is x + b (bias staged in shared memory after the ring), and db = sum
-// over tokens of the packed gradient. The host then uses one-token tiles, so
-// thread i owns the same chunk pairs of every token and keeps their running
-// sums in registers (at most kBiasMaxSteps pairs); at the end it writes them
-// to the CTA's row of db_partials (every chunk by exactly one thread).
+// over tokens of the packed gradient. A thread owns the same chunk pairs of
+// the same token slot in every tile and keeps their running sums in registers
+// (the host keeps steps <= kBiasMaxSteps); at the end the token slots' sums
+// are added in a fixed order into the CTA's row of db_partials.
 template <int HD, bool SECTIONED, bool ROPE, bool NORM, bool BIAS, int NCW, int CPS>
 __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(const BwdArgs a) {
   griddep_wait();
@@ -493,19 +497,34 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(co
     }
   }
 
-  if (BIAS) {  // one-token tiles: this thread alone holds its chunk pairs' sums
-    float* row = a.db_partials + (int64_t)blockIdx.x * a.cpt * 8;
+  if (BIAS) {
+    // Token group g of the tile (threads with tl == g) holds the sums of token
+    // slot g of every tile; the groups are added in order 0, 1, ... through the
+    // ring's shared memory, idle now (it holds at least two stages of dq, dk,
+    // dv, i.e. at least the bias row's cpt * 8 floats), then written as the
+    // CTA's row of db_partials.
+    float* red = reinterpret_cast<float*>(smem + StreamSmem::data(HD, tpt, stages));
+    asm volatile("bar.sync 1, %0;" ::"r"(NCT) : "memory");  // every consumer is done with the ring
+    for (int g = 0; g < tpt; ++g) {
+      if (tl == g) {
 #pragma unroll
-    for (int m = 0; m < MAXM; ++m) {
-      const int j = ig + tpg * m;
-      if (m >= steps || j >= upt) break;
-      const int plo = (j >> LOG_PPH) * CPH + e;
+        for (int m = 0; m < MAXM; ++m) {
+          const int j = ig + tpg * m;
+          if (m >= steps || j >= upt) break;
+          const int plo = (j >> LOG_PPH) * CPH + e;
+          float2* lo = reinterpret_cast<float2*>(red + 8 * plo);
+          float2* hi = reinterpret_cast<float2*>(red + 8 * (plo + PPH));
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        reinterpret_cast<float2*>(row + 8 * plo)[i] = dbl[m][i];
-        reinterpret_cast<float2*>(row + 8 * (plo + PPH))[i] = dbh[m][i];
+          for (int i = 0; i < 4; ++i) {
+            lo[i] = g == 0 ? dbl[m][i] : __fadd2_rn(lo[i], dbl[m][i]);
+            hi[i] = g == 0 ? dbh[m][i] : __fadd2_rn(hi[i], dbh[m][i]);
+          }
+        }
       }
+      asm volatile("bar.sync 1, %0;" ::"r"(NCT) : "memory");
     }
+    float* row = a.db_partials + (int64_t)blockIdx.x * a.cpt * 8;
+    for (int i = ct; i < a.cpt * 8; i += NCT) row[i] = red[i];
   }
   if (!NORM) return;
 

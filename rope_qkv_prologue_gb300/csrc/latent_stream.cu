@@ -47,7 +47,7 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_latent_stream_kernel
           bulk_load(dst + (size_t)i * row_bytes, a.rows + (t0 + i) * a.row_stride16, row_bytes, bar, pol);
       }
     };
-    stream_producer<HD / 2, false, POOL, decltype(load), ROPE>(smem, HD, tpt, stages, stage_bytes, a.sg.n_tiles,
+    stream_producer<HD / 2, false, POOL, ROPE>(smem, HD, tpt, stages, stage_bytes, a.sg.n_tiles,
                                                               a.T, a.pos, a.rope, a.page, a.offset, a.num_pages,
                                                               a.page_size, a.dev_status, a.err, load);
     return;

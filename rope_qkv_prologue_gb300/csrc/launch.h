@@ -17,24 +17,28 @@ enum Role : int { kRoleQ = 0, kRoleK = 1, kRoleV = 2 };
 
 // Streaming (shared-memory staged) kernels.
 // Shape of the pipelined kernels: consumer warps per CTA (+1 producer warp),
-// the CTAs per SM the shared-memory budget is cut for, and the deepest ring
-// to use. Measured on GB300 (T = 16384, Muse Spark packing): one CTA of 10
-// consumer warps per SM is best for the forward (with and without the
-// pre-norm save) and the backward (with 11 warps per SM the register cap is
-// 168 per thread, enough for the pair-per-lane backward without spills). The
-// ring depth paces the reads: the backward and the NoPE forward, whose
-// consumers finish a tile quickly, run faster with at most 4 stages in flight
-// than with 8 (deeper rings issue the reads in bursts that interleave worse
-// with the writes); the RoPE forwards run best with 8.
+// the CTAs per SM the shared-memory budget is cut for, the most bytes to keep
+// in flight in the ring, and the smallest stage worth a tile. Measured on
+// GB300 (T = 16384, Muse Spark packing): one CTA of 10 consumer warps per SM
+// is best for the forward (with and without the pre-norm save) and the
+// backward (with 11 warps per SM the register cap is 168 per thread, enough
+// for the pair-per-lane backward without spills). The bytes in flight pace
+// the reads: the RoPE forwards and the backward run best with about 160 KB in
+// flight per SM (8 stages of a 20 KB token, 4 of a 39 KB one), the NoPE
+// forward, whose consumers finish a tile quickly, with half of that (deeper
+// rings issue the reads in bursts that interleave worse with the writes).
+// Tiles of at least 16 KB keep rows of small models (10-12 KB per token)
+// from giving rings too shallow to cover the memory latency.
 struct StreamShape {
   int warps;
   int ctas_per_sm;
-  int max_stages;
+  int max_inflight;     // bytes of stage data in flight per CTA (cap)
+  int min_stage_bytes;  // smallest tile worth taking
 };
 constexpr StreamShape fwd_stream_shape(bool save_pre, bool rope = true) {
-  return StreamShape{10, 1, (save_pre || rope) ? 8 : 4};
+  return StreamShape{10, 1, (save_pre || rope) ? 160 * 1024 : 80 * 1024, 16 * 1024};
 }
-constexpr StreamShape bwd_stream_shape() { return StreamShape{10, 1, 4}; }
+constexpr StreamShape bwd_stream_shape() { return StreamShape{10, 1, 160 * 1024, 16 * 1024}; }
 constexpr int kMaxStages = 8;  // depth of the shared-memory ring (max)
 constexpr int kStreamMaxSteps = 6;       // 16-byte chunks per consumer thread per tile (max)
 

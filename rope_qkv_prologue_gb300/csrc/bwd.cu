@@ -9,7 +9,8 @@ namespace qkvp {
 // float64 in a fixed order (deterministic), then rounded to float32. CTA x
 // owns kFinalizeOutputsPerCta consecutive outputs; its threads split the rows
 // into kFinalizeThreads / kFinalizeOutputsPerCta interleaved slices and a
-// fixed-shape tree adds the slices.
+// fixed-shape tree adds the slices. (Many small CTAs: the float64 adds spread
+// over every SM; 32 outputs per CTA measured slower on GB300.)
 __global__ void __launch_bounds__(kFinalizeThreads) qkvp_dw_finalize_kernel(const FinalizeArgs a) {
   griddep_wait();
   constexpr int K = kFinalizeOutputsPerCta, SLICES = kFinalizeThreads / K;

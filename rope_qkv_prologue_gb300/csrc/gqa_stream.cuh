@@ -148,9 +148,27 @@ __device__ __forceinline__ void stream_producer(unsigned char* smem, int hd, int
 
 // ------------------------------------------------------------- forward ----
 
-// Copy of the qkv bias (packed-row order, fp32) into shared memory.
-__device__ __forceinline__ void fill_bias(const float* bias, int n, float* s_b) {
-  for (int i = threadIdx.x; i < n; i += blockDim.x) s_b[i] = bias[i];
+// The qkv bias in shared memory, laid out by unit: unit j (chunk pair lo =
+// chunk e of packed head h, hi = chunk e + PPH; j = h * PPH + e) has four
+// float4 pieces (lo values 0-3, lo 4-7, hi 0-3, hi 4-7), piece k at
+// s_b[k * upt + j]. A warp's lanes hold consecutive units, so each 16-byte
+// read covers consecutive words (no bank conflicts).
+template <int HD>
+__device__ __forceinline__ void fill_bias(const float* bias, int upt, float4* s_b) {
+  constexpr int CPH = HD / 8, PPH = CPH / 2;
+  for (int i = threadIdx.x; i < 4 * upt; i += blockDim.x) {
+    const int k = i / upt, j = i - k * upt;
+    const int chunk = (j / PPH) * CPH + (j % PPH) + (k >= 2 ? PPH : 0);
+    s_b[i] = reinterpret_cast<const float4*>(bias)[2 * chunk + (k & 1)];
+  }
+}
+
+// The bias pairs of unit j (lo and hi chunk).
+__device__ __forceinline__ void load_bias_unit(const float4* s_b, int upt, int j, float2 (&lo)[4],
+                                               float2 (&hi)[4]) {
+  const float4 a = s_b[j], b = s_b[upt + j], c = s_b[2 * upt + j], d = s_b[3 * upt + j];
+  lo[0] = f2(a.x, a.y); lo[1] = f2(a.z, a.w); lo[2] = f2(b.x, b.y); lo[3] = f2(b.z, b.w);
+  hi[0] = f2(c.x, c.y); hi[1] = f2(c.z, c.w); hi[2] = f2(d.x, d.y); hi[3] = f2(d.z, d.w);
 }
 
 // NORM: RMSNorm of q and k (off: split -> RoPE only). BIAS: the qkv bias,
@@ -166,7 +184,7 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_fwd_stream_kernel(co
   uint64_t* empty = full + kMaxStages;
   float* s_w = reinterpret_cast<float*>(smem + StreamSmem::kWeights);
   const int tpt = a.sg.tpt, stages = a.sg.stages, steps = a.sg.steps, stage_bytes = a.sg.stage_bytes;
-  float* s_b = reinterpret_cast<float*>(smem + StreamSmem::bias(HD, tpt, stages, stage_bytes));
+  float4* s_b = reinterpret_cast<float4*>(smem + StreamSmem::bias(HD, tpt, stages, stage_bytes));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -176,7 +194,7 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_fwd_stream_kernel(co
     mbar_init_fence();
   }
   if (NORM) fill_split_weights<HD>(a.w_q, a.w_k, s_w);
-  if (BIAS) fill_bias(a.bias, a.cpt * 8, s_b);
+  if (BIAS) fill_bias<HD>(a.bias, a.cpt / 2, s_b);
   __syncthreads();
 
   if (threadIdx.x >= NCT) {
@@ -263,8 +281,7 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_fwd_stream_kernel(co
       unpack_pairs(xhi, hi);
       if (BIAS) {
         float2 blo[4], bhi[4];
-        load_pairs(s_b + 8 * clo, blo);
-        load_pairs(s_b + 8 * (clo + PPH), bhi);
+        load_bias_unit(s_b, upt, in_row ? j : 0, blo, bhi);
         add_bias_pairs(lo, blo);
         add_bias_pairs(hi, bhi);
       }
@@ -333,7 +350,7 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(co
   uint64_t* empty = full + kMaxStages;
   float* s_w = reinterpret_cast<float*>(smem + StreamSmem::kWeights);
   const int tpt = a.sg.tpt, stages = a.sg.stages, steps = a.sg.steps, stage_bytes = a.sg.stage_bytes;
-  float* s_b = reinterpret_cast<float*>(smem + StreamSmem::bias(HD, tpt, stages, stage_bytes));
+  float4* s_b = reinterpret_cast<float4*>(smem + StreamSmem::bias(HD, tpt, stages, stage_bytes));
   // Stage sections (16-byte chunks): dq, dk, dv[, q_pre, k_pre], each [tpt][heads][CPH].
   const int qc = a.n_q * CPH, kc = a.n_kv * CPH;
   const int sec_dk = tpt * qc, sec_dv = sec_dk + tpt * kc, sec_qp = sec_dv + tpt * kc, sec_kp = sec_qp + tpt * qc;
@@ -346,7 +363,7 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(co
     mbar_init_fence();
   }
   if (NORM) fill_split_weights<HD>(a.w_q, a.w_k, s_w);
-  if (NORM && BIAS) fill_bias(a.bias, a.cpt * 8, s_b);
+  if (NORM && BIAS) fill_bias<HD>(a.bias, a.cpt / 2, s_b);
   __syncthreads();
 
   if (threadIdx.x >= NCT) {
@@ -453,10 +470,8 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(co
         unpack_pairs(odd ? x2 : x1, xl2);
         unpack_pairs(odd ? x1 : x2, xh2);
         if (BIAS) {
-          const int blo_c = (j >> LOG_PPH) * CPH + e;
           float2 blo[4], bhi[4];
-          load_pairs(s_b + 8 * blo_c, blo);
-          load_pairs(s_b + 8 * (blo_c + PPH), bhi);
+          load_bias_unit(s_b, upt, j < upt ? j : 0, blo, bhi);
           add_bias_pairs(xl2, blo);
           add_bias_pairs(xh2, bhi);
         }

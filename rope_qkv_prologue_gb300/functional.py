@@ -128,6 +128,29 @@ def latent_pool_write(rows, pos, w, page, offset, pool, eps=1e-6, rope_base=1000
                                  dev_status, stream)
 
 
+def on_side_stream(side, fn, *args, **kwargs):
+    """Run fn(*args, **kwargs) on CUDA stream `side`, forked from the current
+    stream: `side` first waits for everything already queued on the current
+    stream, and the returned event is recorded on `side` after fn's work. The
+    caller joins with ``torch.cuda.current_stream().wait_event(event)`` before
+    anything that reads fn's results.
+
+    This is the drafter-layer pattern of "MLA DSpark: run each drafter layer's
+    kv path beside its q path" (Description): the kv path (kv projection ->
+    latent norm/RoPE -> direct pool write) forks to an aux stream after the input
+    layernorm, the q path runs on the main stream, and attention joins. Works
+    under CUDA graph capture (the fork and join become graph edges). Tensors made
+    on the current stream and used on `side` must stay alive until the join.
+    """
+    main = torch.cuda.current_stream()
+    side.wait_stream(main)
+    with torch.cuda.stream(side):
+        out = fn(*args, **kwargs)
+        done = torch.cuda.Event()
+        done.record(side)
+    return out, done
+
+
 class QKVPrologue(torch.autograd.Function):
     """packed [T, row] -> (q, k, v); backward writes d(packed) in one pass.
 

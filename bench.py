@@ -89,6 +89,15 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_bf16_tflops():
+    """The measured dense bf16 peak (burst: a kernel timed alone), or the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def kernel_sources_digest():
     csrc = os.path.join(ROOT, "rope_qkv_prologue_gb300", "csrc")
     h = hashlib.sha256()
@@ -480,6 +489,71 @@ class VariantTrainStep(_Step):
                               self.dw_q, self.dw_k, self.dbias, self.ws, self.ws_bytes, self.stream)
 
 
+class GemmStep(_Step):
+    """The wqkv projection with the prologue in its epilogue (tcgen05 tensor
+    cores): x [T, hidden] . W^T -> q, k, v (+ the pre-norm save), Muse Spark
+    packing; hidden 5120 stands in for the model's (the pages give none)."""
+
+    def __init__(self, dev, T, hidden=5120):
+        import torch
+
+        import workloads
+
+        self._common(dev)
+        self.T, self.hidden = T, hidden
+        wl = workloads.train(T)
+        self.wl = wl
+        x, w = workloads.gemm_inputs(T, hidden, N_Q, N_KV, D, seed=9, exact=False)
+        self.x, self.w = x.to(dev), w.to(dev)
+        self.pos, self.w_q, self.w_k = wl.pos.to(dev), wl.w_q.to(dev), wl.w_k.to(dev)
+        bf = self.bf
+        self.q, self.k, self.v = (torch.empty(T, n, D, **bf) for n in (N_Q, N_KV, N_KV))
+        self.q_pre, self.k_pre = torch.empty(T, N_Q, D, **bf), torch.empty(T, N_KV, D, **bf)
+        self.L = self.C.layout("interleaved", N_Q, N_KV, D)
+        self.flops = 2 * T * hidden * ROW
+        io = T * hidden * 2 + ROW * hidden * 2 + T * 4 + T * (ROW + (N_Q + N_KV) * D) * 2
+        self.calls = [("qkv_prologue_gemm_fwd (qkvp_gemm_fwd_kernel: tcgen05 projection + prologue epilogue)",
+                       self.fwd, io)]
+        self.h_in = {"x": x, "pos": wl.pos}
+        self.out_names = ("q", "k", "v")
+        self.describe = (f"wqkv projection + prologue fused, T={T}, x [T, {hidden}] . W [{ROW}, {hidden}]^T, "
+                         "Muse Spark packing [T,16,10,64] interleaved, RoPE base 5e5, pre-norm save")
+
+    def fwd(self):
+        C, wl = self.C, self.wl
+        C.qkv_prologue_gemm_fwd(self.L, self.T, self.hidden, self.x, self.w, self.pos, self.w_q, self.w_k, wl.eps,
+                                wl.rope_base, C.QKVP_SAVE_PRE, self.q, self.k, self.v, self.q_pre, self.k_pre,
+                                self.stream)
+
+    def unfused_us(self, reps=20):
+        """cuBLAS projection into a packed tensor + qkv_prologue_fwd, per call."""
+        import torch
+
+        C, wl = self.C, self.wl
+        packed = torch.empty(self.T, ROW, **self.bf)
+
+        def run():
+            torch.matmul(self.x, self.w.T, out=packed)
+            C.qkv_prologue_fwd(self.L, self.T, packed, self.pos, self.w_q, self.w_k, wl.eps, wl.rope_base,
+                               C.QKVP_SAVE_PRE, self.q, self.k, self.v, self.q_pre, self.k_pre)
+
+        for _ in range(3):
+            run()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            run()
+        b.record()
+        torch.cuda.synchronize()
+        t = a.elapsed_time(b) * 1e3 / reps
+        a.record()
+        for _ in range(reps):
+            torch.matmul(self.x, self.w.T, out=packed)
+        b.record()
+        torch.cuda.synchronize()
+        return t, a.elapsed_time(b) * 1e3 / reps
+
+
 def mla_two_stream_overlap(dev, T, layers=3, reps=20):
     """The drafter-layer scheduling of "MLA DSpark: run each drafter layer's kv
     path beside its q path": per layer, the kv path (kv_a projection -> latent
@@ -578,6 +652,8 @@ def make_workload(name, dev, tokens):
         return MlaStep(dev, tokens or 32768)
     if name in ("llama3_train", "qwen3_train", "gpt_oss_train"):
         return VariantTrainStep(dev, tokens or 16384, name[:-len("_train")])
+    if name == "gemm_fwd":
+        return GemmStep(dev, tokens or 16384)
     raise ValueError(name)
 
 
@@ -837,6 +913,16 @@ def run_ours(args):
         rot["pct_of_peak"] = round(100.0 * rot["GBps"] / peak, 1)
     if args.workload == "mla" and T <= 64:
         out["mla_two_stream_overlap"] = mla_two_stream_overlap(dev, T)
+    if getattr(ws, "flops", None):
+        # a contraction: the roofline is the tensor cores' measured bf16 peak
+        tflops = ws.flops / (call_ms[dom] * 1e-3) / 1e12
+        tpeak, tsrc = measured_bf16_tflops()
+        out["roofline"] = {"kernel": dom_name, "bound": "tensor", "achieved": round(tflops, 1), "peak": tpeak,
+                           "peak_source": f"{tsrc} (MEASURED_PEAKS.json bf16_tflops, burst: the call is timed alone)",
+                           "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4), "traffic": None}
+        unf, gemm_only = ws.unfused_us()
+        out["unfused_cublas_projection_plus_prologue_us"] = round(unf, 2)
+        out["cublas_projection_alone_us"] = round(gemm_only, 2)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "train":
         out["cpu_baseline"] = cpu_baseline(args.cpu_tokens)
     if rank == 0:
@@ -935,7 +1021,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--workload", choices=["train", "prefill", "prefill_nope", "decode", "mla", "llama3_train",
-                                           "qwen3_train", "gpt_oss_train"], default="train",
+                                           "qwen3_train", "gpt_oss_train", "gemm_fwd"], default="train",
                     help="train (the headline) | prefill | prefill_nope | decode (pool write) | mla (latent pool write)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="T (0 = the workload's default: 16384 train/prefill, 256 decode, 32768 mla)")

@@ -311,6 +311,36 @@ QKVP_API int qkv_prologue_bwd_ex(const qkvp_layout* layout, const qkvp_variant* 
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * qkv_prologue_gemm_fwd -- the wqkv projection with the prologue fused into its
+ * epilogue: packed = x . w_qkv^T (bf16 inputs, fp32 accumulation on the tensor
+ * cores), rounded to bf16 exactly as the packed tensor of the unfused path,
+ * then split, normed and roped into q, k, v (and q_pre, k_pre) as
+ * qkv_prologue_fwd does; the packed tensor itself is never written.
+ *
+ * Defines: the survey's next step to the left of the path: "[muse_spark][perf]
+ * Split the packed qkv inside the q/k region", Problem 1 (the packed tensor is
+ * the wqkv projection's output) and Solution 1 (the region starts at that
+ * output).
+ *
+ * layout   GQA layout (INTERLEAVED or SECTIONED), row_stride 0 (dense). Its
+ *          packed row order is the row order of w_qkv.
+ * hidden   K: columns of x and of w_qkv, a multiple of 8.
+ * x        bf16 [T, hidden] row-major (the input of the projection).
+ * w_qkv    bf16 [(n_q + 2 n_kv) * head_dim, hidden] row-major (nn.Linear's
+ *          weight layout).
+ * pos, w_q, w_k, eps, rope_base: as qkv_prologue_fwd.
+ * flags    QKVP_NOPE, QKVP_SAVE_PRE (q_pre, k_pre = the bf16 packed heads).
+ * q, k, v, q_pre, k_pre: as qkv_prologue_fwd (contiguous outputs).
+ * The summation order of the projection differs from other GEMM libraries,
+ * so a packed value sitting on a bf16 rounding boundary can round the other
+ * way than in an unfused cuBLAS + qkv_prologue_fwd pair.
+ * ------------------------------------------------------------------------- */
+QKVP_API int qkv_prologue_gemm_fwd(const qkvp_layout* layout, int64_t T, int32_t hidden, const void* x,
+                                   const void* w_qkv, const int32_t* pos, const float* w_q, const float* w_k,
+                                   float eps, double rope_base, uint32_t flags, void* q, void* k, void* v,
+                                   void* q_pre, void* k_pre, void* stream);
+
+/* ---------------------------------------------------------------------------
  * qkv_prologue_device_error -- read (and with clear != 0, reset) the
  * library's device error word on the current device. Bit 1 means a
  * pipelined kernel's bounded wait on its shared-memory pipeline gave up

@@ -54,4 +54,5 @@ from .prologue import (  # noqa: F401
     mla_rows_f64,
     mla_rows,
     mla_pool_write,
+    gemm_prologue_fwd,
 )

@@ -352,3 +352,18 @@ def prologue_bwd(layout, dq_bits, dk_bits, dv_bits, q_pre_bits, k_pre_bits,
     f = bf16_bits_to_f64
     return prologue_bwd_f64(layout, f(dq_bits), f(dk_bits), f(dv_bits), f(q_pre_bits),
                             f(k_pre_bits), pos, w_q, w_k, eps, rope_base, nope, **variant)
+
+
+# --------------------------------------------------------------------------
+# The projection to the left of the path, with the prologue after it
+# --------------------------------------------------------------------------
+
+def gemm_prologue_fwd(layout, x_bits, w_bits, pos, w_q, w_k, eps, rope_base, nope=False, **variant):
+    """packed = x . W^T (x [T, hidden], W [row_width, hidden], both bf16 bits),
+    the float64 product rounded once to bf16 (the packed tensor the projection
+    hands to the prologue), then prologue_fwd. Returns (prologue_fwd's dict,
+    packed bits)."""
+    x = bf16_bits_to_f64(np.asarray(x_bits, dtype=np.uint16))
+    w = bf16_bits_to_f64(np.asarray(w_bits, dtype=np.uint16))
+    packed = to_bf16_rne(x @ w.T)
+    return prologue_fwd(layout, packed, pos, w_q, w_k, eps, rope_base, nope, **variant), packed

@@ -21,5 +21,5 @@ __all__ = [
     "qkv_prologue_bwd_workspace_size", "qkv_prologue_bwd", "qkv_prologue_status_string",
     "qkv_prologue_version", "qkvp_layout", "qkvp_variant", "variant",
     "qkv_prologue_fwd_ex", "qkv_prologue_pool_write_ex", "qkv_prologue_bwd_workspace_size_ex",
-    "qkv_prologue_bwd_ex",
+    "qkv_prologue_bwd_ex", "qkv_prologue_gemm_fwd",
 ]

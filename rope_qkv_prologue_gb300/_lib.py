@@ -100,6 +100,8 @@ _SIGS = {
     "qkv_prologue_bwd_workspace_size_ex": ([_LP, _VP, _i64], ctypes.c_size_t),
     "qkv_prologue_bwd_ex": ([_LP, _VP, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _f64, _u32, _vp, _vp,
                              _vp, _vp, _vp, ctypes.c_size_t, _vp], ctypes.c_int),
+    "qkv_prologue_gemm_fwd": ([_LP, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _f32, _f64, _u32, _vp, _vp, _vp, _vp, _vp,
+                               _vp], ctypes.c_int),
     "qkv_prologue_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "qkv_prologue_version": ([], ctypes.c_int),
     "qkv_prologue_device_error": ([ctypes.c_int, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
@@ -256,3 +258,11 @@ def qkv_prologue_bwd_ex(L, V, T, dq, dk, dv, q_pre, k_pre, pos, w_q, w_k, eps, r
                                   int(flags), _ptr(dpacked), _ptr(dw_q), _ptr(dw_k), _ptr(dbias),
                                   _ptr(workspace), int(workspace_bytes), _stream(stream))
     return _ret(st, "qkv_prologue_bwd_ex", check)
+
+
+def qkv_prologue_gemm_fwd(L, T, hidden, x, w_qkv, pos, w_q, w_k, eps, rope_base, flags, q, k, v, q_pre=None,
+                          k_pre=None, stream=None, check=True):
+    st = _lib.qkv_prologue_gemm_fwd(ctypes.byref(L), int(T), int(hidden), _ptr(x), _ptr(w_qkv), _ptr(pos), _ptr(w_q),
+                                    _ptr(w_k), float(eps), float(rope_base), int(flags), _ptr(q), _ptr(k), _ptr(v),
+                                    _ptr(q_pre), _ptr(k_pre), _stream(stream))
+    return _ret(st, "qkv_prologue_gemm_fwd", check)

@@ -1,6 +1,7 @@
 // Host side of the C ABI: argument checks, RoPE frequency tables, launch
 // geometry and dispatch to the kernels. Nothing here allocates device memory
 // or synchronises; every launch goes to the caller's stream.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -186,6 +187,109 @@ int launch(const void* kernel, int64_t grid, int threads, size_t smem, cudaStrea
                : QKVP_ERR_LAUNCH;
   }
   return QKVP_OK;
+}
+
+// Launch with several kernel parameters (same attributes as launch()), in
+// clusters of `cluster` CTAs along x when cluster > 1.
+int launch_args(const void* kernel, int64_t grid, int threads, size_t smem, cudaStream_t s, void** args,
+                int cluster = 1) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cluster > 1 ? 2 : 1;
+  const cudaError_t err = cudaLaunchKernelExC(&cfg, kernel, args);
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return err == cudaErrorNoKernelImageForDevice || err == cudaErrorInvalidDeviceFunction ? QKVP_ERR_ARCH
+                                                                                            : QKVP_ERR_LAUNCH;
+  }
+  return QKVP_OK;
+}
+
+// Clusters of two CTAs of (kernel, threads, smem) that can be resident at
+// once on the current device (cached per device and kernel), or 0.
+int max_clusters_of_2(const void* kernel, int threads, size_t smem) {
+  struct Entry {
+    int dev;
+    const void* kernel;
+    size_t smem;
+    int n;
+  };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int n_cached = 0;
+  int dev = -1;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_cached; ++i)
+      if (cache[i].dev == dev && cache[i].kernel == kernel && cache[i].smem == smem) return cache[i].n;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (n_cached < 64) cache[n_cached++] = Entry{dev, kernel, smem, n};
+  return n;
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver once (the library does not
+// link libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// Tensor map of a row-major bf16 matrix [rows, cols] (cols contiguous, a
+// multiple of 8) read in boxes of 64 columns x box_rows rows with the 128-byte
+// swizzle the tcgen05 descriptors expect; outside the matrix a box reads 0.
+bool bf16_tile_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t elem[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // -------------------------------------------------------------- RoPE ----
@@ -789,6 +893,68 @@ int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const
                      size_t workspace_bytes, void* stream) {
   return qkv_prologue_bwd_ex(layout, nullptr, T, dq, dk, dv, q_pre, k_pre, pos, w_q, w_k, eps, rope_base, flags,
                              dpacked, dw_q, dw_k, nullptr, workspace, workspace_bytes, stream);
+}
+
+// ------------------------------------------- projection + prologue ----
+
+int qkv_prologue_gemm_fwd(const qkvp_layout* layout, int64_t T, int32_t hidden, const void* x, const void* w_qkv,
+                          const int32_t* pos, const float* w_q, const float* w_k, float eps, double rope_base,
+                          uint32_t flags, void* q, void* k, void* v, void* q_pre, void* k_pre, void* stream) {
+  Gqa g;
+  QKVP_TRY(check_gqa(layout, T, &g));
+  if (g.stride != g.row) return QKVP_ERR_SHAPE;  // W is [row width, hidden], dense
+  if (hidden < 8 || hidden % 8 != 0 || T > INT32_MAX) return QKVP_ERR_SHAPE;
+  if (flags & ~(uint32_t)(QKVP_NOPE | QKVP_SAVE_PRE)) return QKVP_ERR_FLAGS;
+  const bool rope = !(flags & QKVP_NOPE), save = (flags & QKVP_SAVE_PRE) != 0;
+  QKVP_TRY(check_scalars(eps, rope_base, rope));
+  if (!x || !w_qkv || !w_q || !w_k || !q || !k || !v || (rope && !pos) || (save && (!q_pre || !k_pre)))
+    return QKVP_ERR_NULL;
+  const void* vec[] = {x, w_qkv, w_q, w_k, q, k, v, save ? q_pre : nullptr, save ? k_pre : nullptr};
+  for (const void* p : vec)
+    if (p && !aligned16(p)) return QKVP_ERR_ALIGN;
+  if (pos && !aligned4(pos)) return QKVP_ERR_ALIGN;
+  if (T == 0) return QKVP_OK;
+
+  int sms = 0;
+  QKVP_TRY(current_device(&sms));
+  CUtensorMap tx, tw;
+  if (!bf16_tile_map(&tx, x, T, hidden, kGemmBM) || !bf16_tile_map(&tw, w_qkv, g.heads * (int64_t)layout->head_dim,
+                                                                    hidden, kGemmBN / 2))
+    return QKVP_ERR_LAUNCH;
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.T = T;
+  a.hidden = hidden;
+  a.n_q = layout->n_q;
+  a.n_kv = layout->n_kv;
+  a.group = layout->n_q / layout->n_kv;
+  a.n_blocks = g.heads;
+  a.gs_magic = magic((uint32_t)(a.group + 2));
+  a.m_tiles = (int32_t)((T + kGemmBM - 1) / kGemmBM);
+  a.n_tiles = (int32_t)((g.row + kGemmBN - 1) / kGemmBN);
+  a.m_pairs = (a.m_tiles + 1) / 2;
+  a.n_work = (int64_t)a.m_pairs * a.n_tiles;
+  a.pos = pos;
+  a.w_q = w_q;
+  a.w_k = w_k;
+  a.eps = eps;
+  a.inv_head_dim = 1.0f / (float)layout->head_dim;
+  a.q = static_cast<uint4*>(q);
+  a.k = static_cast<uint4*>(k);
+  a.v = static_cast<uint4*>(v);
+  a.q_pre = static_cast<uint4*>(q_pre);
+  a.k_pre = static_cast<uint4*>(k_pre);
+  if ((a.err = device_error_word()) == nullptr) return QKVP_ERR_LAUNCH;
+  if (rope) rope_table(rope_base, layout->head_dim, nullptr, 1.f, &a.rope);
+  const void* kern = gemm_fwd_kernel(layout->head_dim, layout->kind == QKVP_SECTIONED, rope, save);
+  const size_t smem = (size_t)gemm_fwd_smem_bytes();
+  if (!allow_smem(kern, smem)) return QKVP_ERR_LAUNCH;
+  const int threads = gemm_fwd_threads();
+  const int clusters = max_clusters_of_2(kern, threads, smem);
+  if (clusters < 1) return QKVP_ERR_LAUNCH;
+  const int64_t grid = 2 * (a.n_work < clusters ? a.n_work : clusters);
+  void* args[] = {&tx, &tw, &a};
+  return launch_args(kern, grid, threads, smem, static_cast<cudaStream_t>(stream), args, 2);
 }
 
 int qkv_prologue_device_error(int clear, int* value) {

@@ -255,6 +255,33 @@ struct FinalizeArgs {
 constexpr int kFinalizeOutputsPerCta = 4;
 constexpr int kFinalizeThreads = 256;
 
+// The wqkv projection with the prologue in its epilogue (tcgen05): tile of
+// kGemmBM tokens x kGemmBN packed columns, kGemmBK per pipeline stage.
+constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64;
+struct GemmArgs {
+  int64_t T;              // tokens (rows of x)
+  int32_t hidden;         // K: columns of x and W
+  int32_t n_q, n_kv, group, n_blocks;  // n_blocks = n_q + 2 n_kv head blocks of the packed row
+  uint32_t gs_magic;      // floor(2^32 / (group + 2)) + 1
+  int32_t m_tiles, n_tiles, m_pairs;  // m_pairs = ceil(m_tiles / 2): work items pair two M tiles
+  int64_t n_work;         // m_pairs * n_tiles
+  const int32_t* pos;
+  const float* w_q;
+  const float* w_k;
+  float eps;
+  float inv_head_dim;
+  uint4* q;
+  uint4* k;
+  uint4* v;
+  uint4* q_pre;
+  uint4* k_pre;
+  int* err;
+  RopeTable rope;
+};
+const void* gemm_fwd_kernel(int head_dim, bool sectioned, bool rope, bool save);
+int gemm_fwd_smem_bytes();
+int gemm_fwd_threads();
+
 constexpr int kLatentWarps = 8;        // warps per CTA of the latent kernel
 constexpr int kLatentTokensPerWarp = 2;
 constexpr int kLatentTileTokens = 16;     // rows per tile of the pipelined latent kernel

@@ -128,6 +128,30 @@ def latent_pool_write(rows, pos, w, page, offset, pool, eps=1e-6, rope_base=1000
                                  dev_status, stream)
 
 
+def gemm_prologue_forward(x, w_qkv, pos, w_q, w_k, n_q, n_kv, head_dim=64, kind="interleaved", eps=1e-6,
+                          rope_base=500000.0, nope=False, save_pre=False, stream=None):
+    """The wqkv projection with the prologue in its epilogue: x [T, hidden] bf16,
+    w_qkv [(n_q + 2 n_kv) * head_dim, hidden] bf16 (rows in the layout's packed
+    order) -> (q, k, v) or (q, k, v, q_pre, k_pre); the packed tensor is never
+    materialised."""
+    _check_dev(x, w_qkv, pos, w_q, w_k)
+    if x.dim() != 2 or w_qkv.dim() != 2 or x.shape[1] != w_qkv.shape[1]:
+        raise ValueError("x must be [T, hidden] and w_qkv [rows, hidden]")
+    if w_qkv.shape[0] != (n_q + 2 * n_kv) * head_dim:
+        raise ValueError("w_qkv must have (n_q + 2 n_kv) * head_dim rows")
+    T, hidden = x.shape
+    L = C.layout(kind, n_q, n_kv, head_dim)
+    dev = x.device
+    q = torch.empty(T, n_q, head_dim, dtype=torch.bfloat16, device=dev)
+    k = torch.empty(T, n_kv, head_dim, dtype=torch.bfloat16, device=dev)
+    v = torch.empty(T, n_kv, head_dim, dtype=torch.bfloat16, device=dev)
+    q_pre = torch.empty_like(q) if save_pre else None
+    k_pre = torch.empty_like(k) if save_pre else None
+    C.qkv_prologue_gemm_fwd(L, T, hidden, x.contiguous(), w_qkv.contiguous(), pos, w_q, w_k, eps, rope_base,
+                            _flags(nope, save_pre), q, k, v, q_pre, k_pre, stream)
+    return (q, k, v, q_pre, k_pre) if save_pre else (q, k, v)
+
+
 def on_side_stream(side, fn, *args, **kwargs):
     """Run fn(*args, **kwargs) on CUDA stream `side`, forked from the current
     stream: `side` first waits for everything already queued on the current

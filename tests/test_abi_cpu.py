@@ -297,6 +297,30 @@ def test_variant_argument_checks(lib):
 
 
 @cpu_only
+def test_gemm_fwd_argument_checks(lib):
+    C = lib
+    L = C.layout("interleaved", 128, 16, 64)
+
+    def g(T=256, hidden=5120, x=A, w=A, pos=A, wq=A, wk=A, flags=0, q=A, k=A, v=A, qp=None, kp=None, L=L):
+        return C.qkv_prologue_gemm_fwd(L, T, hidden, x, w, pos, wq, wk, 1e-6, 5e5, flags, q, k, v, qp, kp, stream=0,
+                                       check=False)
+
+    assert g() == C.QKVP_ERR_ARCH  # valid: reaches the device check
+    assert g(T=0) == C.QKVP_OK
+    assert g(hidden=5121) == C.QKVP_ERR_SHAPE  # rows of x and W must be 16-byte multiples
+    assert g(hidden=4) == C.QKVP_ERR_SHAPE
+    assert g(L=C.layout("interleaved", 128, 16, 64, row_stride=10248)) == C.QKVP_ERR_SHAPE  # W is dense
+    assert g(L=C.layout("latent", norm_dim=512, rope_dim=64)) == C.QKVP_ERR_SHAPE
+    assert g(x=None) == C.QKVP_ERR_NULL
+    assert g(w=A + 8) == C.QKVP_ERR_ALIGN
+    assert g(flags=C.QKVP_SAVE_PRE) == C.QKVP_ERR_NULL
+    assert g(flags=C.QKVP_SAVE_PRE, qp=A, kp=A) == C.QKVP_ERR_ARCH
+    assert g(flags=C.QKVP_FORCE_GENERIC) == C.QKVP_ERR_FLAGS
+    assert g(pos=None) == C.QKVP_ERR_NULL
+    assert g(pos=None, flags=C.QKVP_NOPE) == C.QKVP_ERR_ARCH
+
+
+@cpu_only
 def test_noalloc_backward_argument_checks(lib):
     C = lib
 

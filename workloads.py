@@ -245,6 +245,25 @@ def gpt_oss(T, seed=8, pos_high=None, with_grads=True):
     return wl
 
 
+# --- the projection to the left of the path -------------------------------------
+
+def gemm_inputs(T, hidden, n_q, n_kv, head_dim, seed, exact=True):
+    """x [T, hidden] and the fused weight W [(n_q + 2 n_kv) * head_dim, hidden],
+    bf16. exact: x = k / 8 (|k| <= 16) and W = k / 64 (|k| <= 32), so every
+    product and every partial sum of up to 4096 terms is exact in float32 and a
+    GEMM gives the exact product whatever its summation order; else x N(0,1)
+    and W N(0, 1/hidden) (the scale of a trained projection)."""
+    g = _gen(seed)
+    rows = (n_q + 2 * n_kv) * head_dim
+    if exact:
+        x = torch.clamp(torch.round(torch.randn(T, hidden, generator=g) * 4), -16, 16) / 8
+        w = torch.clamp(torch.round(torch.randn(rows, hidden, generator=g) * 8), -32, 32) / 64
+    else:
+        x = torch.randn(T, hidden, generator=g)
+        w = torch.randn(rows, hidden, generator=g) / math.sqrt(hidden)
+    return x.to(torch.bfloat16), w.to(torch.bfloat16)
+
+
 # --- the five workloads ------------------------------------------------------
 
 def tiny(seed=1):

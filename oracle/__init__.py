@@ -18,7 +18,10 @@ Sources (page title, then section):
 * "[muon] Per-head Newton-Schulz for fused QKV projections" (DeepSpeed)
   - What this PR does: the sectioned (q | k | v) and the interleaved-per-KV-
     group packings are the same partition into head_dim blocks in two orders;
-    a fused row holds exactly (n_q + 2 n_kv) * head_dim values.
+    a fused row holds exactly (n_q + 2 n_kv) * head_dim values. The same
+    partition of a fused weight's dim 0 is what per-head Newton-Schulz works
+    on, one block at a time, with the factor max(1, head_dim / in_features)
+    ** 0.5 (newton_schulz.py; the iteration itself is Muon's published one).
 * "MLA DSpark: run each drafter layer's kv path beside its q path"
   (TensorRT-LLM #20552)
   - Description: the RMSNorm/RoPE kernel stores the latent rows straight into
@@ -26,11 +29,12 @@ Sources (page title, then section):
   - Test Coverage: the direct pool write equals the staged path plus the
     scatter write.
 
-Parity status: the pages print no numeric example, so no function here is
-pinned by printed values. Every function is pinned by closed forms,
-invariants, brute force on tiny inputs, finite differences or the pages'
-stated layout facts (see tests/test_oracle_pins.py). None is "parity
-unpinned".
+Parity status: the pages print no numeric example (only the block counts and
+the split / no-split cases of the Newton-Schulz page, kept in tests/golden/),
+so no function here is pinned by printed values. Every function is pinned by
+closed forms, invariants, brute force on tiny inputs, finite differences or
+the pages' stated layout facts (see tests/test_oracle_pins.py). None is
+"parity unpinned".
 """
 
 from .bf16 import bf16_bits_to_f64, f64_to_f32_rne, to_bf16_rne  # noqa: F401
@@ -55,4 +59,17 @@ from .prologue import (  # noqa: F401
     mla_rows,
     mla_pool_write,
     gemm_prologue_fwd,
+)
+from .newton_schulz import (  # noqa: F401
+    NS_COEFFS,
+    NS_STEPS,
+    NS_EPS,
+    newton_schulz5,
+    fused_head_blocks,
+    per_head_scale,
+    full_matrix_scale,
+    per_head_newton_schulz,
+    full_matrix_newton_schulz,
+    muon_orthogonalize,
+    qkv_newton_schulz,
 )

@@ -21,6 +21,12 @@ What pins what:
                     bias order through the pinned split, bias before the norm
                     (rms 1) and the rotation, one-hot frequency tables, the
                     cos/sin factor at position 0, finite differences of all
+  per-head Newton-  known-SVD closed forms through a scalar recursion on the
+  Schulz            singular values (Muon's published constants, typed here
+                    on their own), the 1e-7 on a tiny matrix, orthogonal
+                    equivariance, block independence, the tall-block factor,
+                    sectioned == interleaved up to the block permutation, the
+                    page's split / no-split cases and scales (tests/golden/)
 """
 
 import math
@@ -463,3 +469,132 @@ def check_variant_backward(P, rng):
     d = [rng.standard_normal((3, n, 8)) for n in (layout.n_q, layout.n_kv, layout.n_kv)]
     out = P.prologue_bwd_f64(layout, *d, xq, xk, [1, 2, 3], np.ones(8), np.ones(8), 1e-6, 1e4, norm=False)
     assert not np.any(out["dw_q"]) and not np.any(out["dw_k"])
+
+
+# ---------------------------------------------- per-head Newton-Schulz ----
+
+# Muon's quintic constants and step count as published with the optimizer
+# (Jordan et al., 2024), typed here independently of the oracle's copy.
+_MUON_ABC = (3.4445, -4.7750, 2.0315)
+_MUON_STEPS = 5
+
+
+def _phi5(sigma):
+    """What five Newton-Schulz steps do to one singular value."""
+    a, b, c = _MUON_ABC
+    s = np.asarray(sigma, dtype=np.float64)
+    for _ in range(_MUON_STEPS):
+        s = a * s + b * s ** 3 + c * s ** 5
+    return s
+
+
+def _orthonormal_columns(rng, n, k):
+    q, r = np.linalg.qr(rng.standard_normal((n, k)))
+    return q * np.sign(np.diag(r))
+
+
+def _ns_by_svd(g):
+    """Newton-Schulz of g through its SVD: U phi5(s / (||g||_F + 1e-7)) V^T."""
+    U, s, Vt = np.linalg.svd(np.asarray(g, dtype=np.float64), full_matrices=False)
+    return (U * _phi5(s / (np.sqrt(np.sum(s * s)) + 1e-7))) @ Vt
+
+
+def check_ns_svd_closed_form(N, rng):
+    """A matrix built from a known SVD: the iteration acts on each singular value
+    alone. Wide, square and tall shapes; a tiny matrix shows the 1e-7."""
+    for m, n in [(8, 24), (16, 16), (24, 8), (64, 512)]:
+        k = min(m, n)
+        U, V = _orthonormal_columns(rng, m, k), _orthonormal_columns(rng, n, k)
+        s = np.sort(rng.uniform(0.05, 3.0, k))[::-1]
+        for mag in (1.0, 1e-7):
+            sm = s * mag
+            want = (U * _phi5(sm / (np.sqrt(np.sum(sm * sm)) + 1e-7))) @ V.T
+            got = N.newton_schulz5((U * sm) @ V.T)
+            err = np.abs(got - want).max()
+            assert err <= 1e-9 * max(1.0, np.abs(want).max()), f"svd closed form {m}x{n} mag {mag}: {err}"
+    # equal singular values: s Q with orthonormal rows maps to phi5(1/(sqrt(k) + 1e-7/s)) Q
+    Q = _orthonormal_columns(rng, 40, 8).T
+    got = N.newton_schulz5(3.0 * Q)
+    assert np.allclose(got, _phi5(3.0 / (3.0 * np.sqrt(8) + 1e-7)) * Q, rtol=0, atol=1e-12)
+
+
+def check_ns_equivariance(N, rng):
+    """NS(P G Q^T) = P NS(G) Q^T for orthogonal P, Q (order of the products)."""
+    for m, n in [(6, 10), (10, 6), (7, 7)]:
+        g = rng.standard_normal((m, n))
+        Pm, Qm = _orthonormal_columns(rng, m, m), _orthonormal_columns(rng, n, n)
+        lhs = N.newton_schulz5(Pm @ g @ Qm.T)
+        rhs = Pm @ N.newton_schulz5(g) @ Qm.T
+        assert np.abs(lhs - rhs).max() <= 1e-10, f"equivariance {m}x{n}"
+
+
+def check_ns_per_head(N, rng):
+    """Blocks are independent, each normalised on its own, scaled by
+    max(1, head_dim / in_features) ** 0.5 (wide: 1; tall: sqrt(D / in))."""
+    D, cols = 8, 24
+    m = rng.standard_normal((4 * D, cols)) * np.repeat([1e-3, 1.0, 1e3, 7.0], D)[:, None]
+    out = N.per_head_newton_schulz(m, D)
+    for blk in range(4):
+        sl = slice(blk * D, (blk + 1) * D)
+        assert np.abs(out[sl] - _ns_by_svd(m[sl])).max() <= 1e-9, f"block {blk}"
+    m2 = m.copy()
+    m2[:D] = rng.standard_normal((D, cols))
+    out2 = N.per_head_newton_schulz(m2, D)
+    assert np.array_equal(out2[D:], out[D:]), "a block's result depends on another block"
+    # tall blocks (head_dim 16 over 8 inputs): factor sqrt(2)
+    t = rng.standard_normal((3 * 16, 8))
+    out = N.per_head_newton_schulz(t, 16)
+    for blk in range(3):
+        sl = slice(blk * 16, (blk + 1) * 16)
+        assert np.abs(out[sl] - np.sqrt(2.0) * _ns_by_svd(t[sl])).max() <= 1e-9, f"tall block {blk}"
+
+
+def check_ns_layout_equivalence(N, P, rng):
+    """The same heads packed sectioned and interleaved (block orders pinned by
+    the golden head-block fixtures) give the same per-head results, permuted."""
+    n_q, n_kv, D, cols = 8, 2, 8, 24
+    heads = {("q", h): rng.standard_normal((D, cols)) for h in range(n_q)}
+    heads.update({(r, h): rng.standard_normal((D, cols)) for r in "kv" for h in range(n_kv)})
+    res = {}
+    for kind in ("sectioned", "interleaved"):
+        order = P.head_blocks(P.PackedLayout(kind, n_q, n_kv, D))
+        w = np.concatenate([heads[b] for b in order], axis=0)
+        assert N.fused_head_blocks(w.shape[0], n_q, n_kv, D) == len(order)
+        out = N.per_head_newton_schulz(w, D)
+        res[kind] = {b: out[i * D:(i + 1) * D] for i, b in enumerate(order)}
+    for b in heads:
+        assert np.array_equal(res["sectioned"][b], res["interleaved"][b]), f"head {b}"
+    # and the per-head update is not the whole-matrix one
+    w = np.concatenate([heads[b] for b in P.head_blocks(P.PackedLayout("sectioned", n_q, n_kv, D))])
+    assert np.abs(N.per_head_newton_schulz(w, D) - N.full_matrix_newton_schulz(w)).max() > 1e-2
+
+
+def read_muon_fixture():
+    cands, full, head = [], [], []
+    with open(os.path.join(GOLDEN, "muon_fused_candidates.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *rest = line.split()
+            if key == "candidate":
+                name, rows, cols, nq, nkv, d, blocks = rest
+                cands.append((name, int(rows), int(cols), int(nq), int(nkv), int(d),
+                              None if blocks == "-" else int(blocks)))
+            elif key == "full_scale":
+                full.append((int(rest[0]), int(rest[1]), float(rest[2])))
+            elif key == "head_scale":
+                head.append((int(rest[0]), int(rest[1]), float(rest[2])))
+    return cands, full, head
+
+
+def check_ns_page_facts(N):
+    """The page's split / no-split cases and the scales the review compares."""
+    cands, full, head = read_muon_fixture()
+    assert cands and full and head
+    for name, rows, cols, nq, nkv, d, blocks in cands:
+        assert N.fused_head_blocks(rows, nq, nkv, d) == blocks, name
+    for rows, cols, f in full:
+        assert abs(N.full_matrix_scale(rows, cols) - f) <= 1e-15, (rows, cols)
+    for d, cin, f in head:
+        assert abs(N.per_head_scale(d, cin) - f) <= 1e-15, (d, cin)

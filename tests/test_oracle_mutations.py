@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 
 import oracle.bf16 as B
+import oracle.newton_schulz as N
 import oracle.prologue as P
 import oracle_checks as C
 import workloads
@@ -116,6 +117,59 @@ def _rope_transpose_is_forward(d, pos, base, inv_freq=None, scale=1.0):
     return _REAL_ROPE(d, pos, base, inv_freq, scale)
 
 
+def _ns_variant(g, norm=lambda x: np.linalg.norm(x) + 1e-7, steps=5, coeffs=(3.4445, -4.7750, 2.0315),
+                square=True):
+    """Newton-Schulz written out with one planted change at a time."""
+    x = np.asarray(g, dtype=np.float64)
+    tall = x.shape[0] > x.shape[1]
+    x = x.T if tall else x
+    x = x / norm(x)
+    a, b, c = coeffs
+    for _ in range(steps):
+        A = x @ x.T
+        x = a * x + (b * A + c * (A @ A if square else A)) @ x
+    return x.T if tall else x
+
+
+def _ns_b_sign_flipped(g, **kw):
+    return _ns_variant(g, coeffs=(3.4445, 4.7750, 2.0315))
+
+
+def _ns_four_steps(g, **kw):
+    return _ns_variant(g, steps=4)
+
+
+def _ns_spectral_norm(g, **kw):
+    return _ns_variant(g, norm=lambda x: np.linalg.norm(x, 2) + 1e-7)
+
+
+def _ns_square_dropped(g, **kw):
+    return _ns_variant(g, square=False)
+
+
+def _ns_no_eps(g, **kw):
+    return _ns_variant(g, norm=np.linalg.norm)
+
+
+def _head_scale_whole_matrix(head_dim, in_features):
+    return max(1.0, 3.0 * head_dim / in_features) ** 0.5
+
+
+def _per_head_global_norm(m, head_dim, **kw):
+    # the whole fused weight normalised once, no per-block normalisation
+    m = np.asarray(m, dtype=np.float64)
+    m = m / (np.linalg.norm(m) + 1e-7)
+    out = np.empty_like(m)
+    for blk in range(m.shape[0] // head_dim):
+        sl = slice(blk * head_dim, (blk + 1) * head_dim)
+        out[sl] = _ns_variant(m[sl], norm=lambda x: 1.0) * N.per_head_scale(head_dim, m.shape[1])
+    return out
+
+
+def _blocks_any_multiple(rows, n_q, n_kv, head_dim):
+    return rows // head_dim if head_dim and rows % head_dim == 0 else None
+
+
 def _checks_all(rng):
     """Every pin, run in turn; raises AssertionError at the first that fails."""
     C.check_to_bf16_rne(B, rng)
@@ -130,6 +184,11 @@ def _checks_all(rng):
     C.check_variant_forward(P, rng)
     C.check_rope_extras(P, rng)
     C.check_variant_backward(P, rng)
+    C.check_ns_svd_closed_form(N, rng)
+    C.check_ns_equivariance(N, rng)
+    C.check_ns_per_head(N, rng)
+    C.check_ns_layout_equivalence(N, P, rng)
+    C.check_ns_page_facts(N)
 
 
 def test_unmutated_oracle_passes_every_pin(rng):
@@ -152,6 +211,14 @@ MUTATIONS = [
     (P, "rope_angles", _angles_ignore_table),
     (P, "add_bias", _bias_reversed),
     (P, "add_bias", _bias_dropped),
+    (N, "newton_schulz5", _ns_b_sign_flipped),
+    (N, "newton_schulz5", _ns_four_steps),
+    (N, "newton_schulz5", _ns_spectral_norm),
+    (N, "newton_schulz5", _ns_square_dropped),
+    (N, "newton_schulz5", _ns_no_eps),
+    (N, "per_head_scale", _head_scale_whole_matrix),
+    (N, "per_head_newton_schulz", _per_head_global_norm),
+    (N, "fused_head_blocks", _blocks_any_multiple),
 ]
 
 

@@ -143,3 +143,42 @@ def test_rope_frequency_table_and_factor(rng):
 
 def test_variant_backward_finite_differences(rng):
     C.check_variant_backward(P, rng)
+
+
+# ---------------------------------------------- per-head Newton-Schulz ----
+
+import oracle.newton_schulz as N  # noqa: E402
+
+
+def test_ns_known_svd_closed_forms(rng):
+    C.check_ns_svd_closed_form(N, rng)
+
+
+def test_ns_orthogonal_equivariance(rng):
+    C.check_ns_equivariance(N, rng)
+
+
+def test_ns_blocks_independent_and_scaled(rng):
+    C.check_ns_per_head(N, rng)
+
+
+def test_ns_sectioned_equals_interleaved(rng):
+    C.check_ns_layout_equivalence(N, P, rng)
+
+
+def test_ns_page_split_cases_and_scales():
+    C.check_ns_page_facts(N)
+
+
+def test_ns_constants_are_muons_published_defaults():
+    assert N.NS_COEFFS == (3.4445, -4.7750, 2.0315) and N.NS_STEPS == 5 and N.NS_EPS == 1e-7
+
+
+def test_ns_bits_entry_checks_the_fused_total(rng):
+    L = P.PackedLayout("interleaved", 8, 2, 16)
+    m = B.to_bf16_rne(rng.standard_normal((12 * 16, 32)))
+    out = N.qkv_newton_schulz(L, m)
+    assert out.shape == (192, 32)
+    assert np.array_equal(out, N.per_head_newton_schulz(B.bf16_bits_to_f64(m), 16))
+    with pytest.raises(ValueError):
+        N.qkv_newton_schulz(L, m[:-16])

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define QKVP_VERSION 2
+#define QKVP_VERSION 3
 
 /* Status codes (return values). */
 typedef enum {
@@ -339,6 +339,46 @@ QKVP_API int qkv_prologue_gemm_fwd(const qkvp_layout* layout, int64_t T, int32_t
                                    const void* w_qkv, const int32_t* pos, const float* w_q, const float* w_k,
                                    float eps, double rope_base, uint32_t flags, void* q, void* k, void* v,
                                    void* q_pre, void* k_pre, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * qkv_newton_schulz -- per-head Newton-Schulz of a fused QKV weight's update.
+ *
+ * Defines: "[muon] Per-head Newton-Schulz for fused QKV projections"
+ * (DeepSpeed), What this PR does: dim 0 of a fused weight
+ * [(n_q + 2 n_kv) * head_dim, in_features] is cut into head_dim-row blocks,
+ * which are the same blocks in the sectioned and the interleaved packing (so
+ * `layout->kind` does not change the result, only the row count is taken from
+ * it); every block G is replaced by NS(G) * max(1, head_dim / in_features)^0.5,
+ * where NS is Muon's published quintic Newton-Schulz iteration:
+ *     X = G / (||G||_F + 1e-7);  5 times:  A = X X^T,  X = a X + (b A + c A A) X
+ * with (a, b, c) = (3.4445, -4.7750, 2.0315).
+ *
+ * Arithmetic: bf16 operands on the tensor cores with fp32 accumulation; X, A
+ * and b A + c A A are held in bf16 between the products (as in the published
+ * bf16 iteration), norms and sums in fp32. The result differs from an exact
+ * evaluation by about 1-2 % (relative Frobenius norm per block), as any bf16
+ * evaluation of the iteration does. Deterministic.
+ *
+ * layout   INTERLEAVED or SECTIONED; n_q, n_kv, head_dim (64 or 128) give the
+ *          rows; row_stride is not used.
+ * cols     in_features: a multiple of 64, at most 8192.
+ * m        bf16 [rows, cols] row-major (the update: gradient or momentum).
+ * out      bf16 [rows, cols] row-major; must not overlap m (QKVP_ERR_VALUE).
+ * cluster  0: the library picks how many CTAs share one 128-row unit (a
+ *          thread-block cluster splitting its columns); else that number
+ *          (it must divide cols / 64 with cols / cluster <= 512, and be at
+ *          most 16), for tests. A size the device cannot co-schedule gives
+ *          QKVP_ERR_SHAPE.
+ * A wait that times out inside the kernel sets bit 1 of the device error
+ * word (qkv_prologue_device_error); the launch's output is then invalid.
+ * ------------------------------------------------------------------------- */
+QKVP_API int qkv_newton_schulz(const qkvp_layout* layout, int64_t cols, const void* m, void* out,
+                               int32_t cluster, void* stream);
+
+/* The cluster size and grid qkv_newton_schulz would use for these arguments
+ * (host only, nothing is launched). */
+QKVP_API int qkv_newton_schulz_plan(const qkvp_layout* layout, int64_t cols, int32_t cluster,
+                                    int32_t* cluster_out, int32_t* grid_out);
 
 /* ---------------------------------------------------------------------------
  * qkv_prologue_device_error -- read (and with clear != 0, reset) the

@@ -23,7 +23,7 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 # ---- constants (mirror include/qkv_prologue.h) ------------------------------
-QKVP_VERSION = 2
+QKVP_VERSION = 3
 QKVP_OK = 0
 QKVP_ERR_NULL = -1
 QKVP_ERR_SHAPE = -2
@@ -102,6 +102,9 @@ _SIGS = {
                              _vp, _vp, _vp, ctypes.c_size_t, _vp], ctypes.c_int),
     "qkv_prologue_gemm_fwd": ([_LP, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _f32, _f64, _u32, _vp, _vp, _vp, _vp, _vp,
                                _vp], ctypes.c_int),
+    "qkv_newton_schulz": ([_LP, _i64, _vp, _vp, _i32, _vp], ctypes.c_int),
+    "qkv_newton_schulz_plan": ([_LP, _i64, _i32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
+                               ctypes.c_int),
     "qkv_prologue_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "qkv_prologue_version": ([], ctypes.c_int),
     "qkv_prologue_device_error": ([ctypes.c_int, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
@@ -266,3 +269,16 @@ def qkv_prologue_gemm_fwd(L, T, hidden, x, w_qkv, pos, w_q, w_k, eps, rope_base,
                                     _ptr(w_k), float(eps), float(rope_base), int(flags), _ptr(q), _ptr(k), _ptr(v),
                                     _ptr(q_pre), _ptr(k_pre), _stream(stream))
     return _ret(st, "qkv_prologue_gemm_fwd", check)
+
+
+def qkv_newton_schulz(L, cols, m, out, cluster=0, stream=None, check=True):
+    st = _lib.qkv_newton_schulz(ctypes.byref(L), int(cols), _ptr(m), _ptr(out), int(cluster), _stream(stream))
+    return _ret(st, "qkv_newton_schulz", check)
+
+
+def qkv_newton_schulz_plan(L, cols, cluster=0):
+    """(cluster size, grid) the library would launch for these arguments."""
+    c, g = ctypes.c_int32(0), ctypes.c_int32(0)
+    st = _lib.qkv_newton_schulz_plan(ctypes.byref(L), int(cols), int(cluster), ctypes.byref(c), ctypes.byref(g))
+    _ret(st, "qkv_newton_schulz_plan", True)
+    return c.value, g.value

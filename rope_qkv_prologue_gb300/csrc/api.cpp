@@ -192,21 +192,26 @@ int launch(const void* kernel, int64_t grid, int threads, size_t smem, cudaStrea
 // Launch with several kernel parameters (same attributes as launch()), in
 // clusters of `cluster` CTAs along x when cluster > 1.
 int launch_args(const void* kernel, int64_t grid, int threads, size_t smem, cudaStream_t s, void** args,
-                int cluster = 1) {
+                int cluster = 1, bool pdl = true) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = (unsigned)cluster;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
+  int n_attr = 0;
+  if (pdl) {
+    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n_attr++].val.programmaticStreamSerializationAllowed = 1;
+  }
+  if (cluster > 1) {
+    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+    attr[n_attr].val.clusterDim.x = (unsigned)cluster;
+    attr[n_attr].val.clusterDim.y = 1;
+    attr[n_attr++].val.clusterDim.z = 1;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = cluster > 1 ? 2 : 1;
+  cfg.numAttrs = n_attr;
   const cudaError_t err = cudaLaunchKernelExC(&cfg, kernel, args);
   if (err != cudaSuccess) {
     cudaGetLastError();
@@ -429,6 +434,106 @@ constexpr int kBiasMaxChunks = kThreads * kBwdChunksPerThread;
     const int _st = (expr);     \
     if (_st != QKVP_OK) return _st; \
   } while (0)
+
+// ------------------------------------------- per-head Newton-Schulz ----
+
+// Clusters of `nc` Newton-Schulz CTAs (smem bytes each) that can be resident
+// at once on the current device, cached per device; 0 if none.
+int ns_active_clusters(int nc, size_t smem) {
+  struct Entry {
+    int dev, nc;
+    size_t smem;
+    int n;
+  };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int n_cached = 0;
+  int dev = -1;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_cached; ++i)
+      if (cache[i].dev == dev && cache[i].nc == nc && cache[i].smem == smem) return cache[i].n;
+  }
+  const void* kern = ns_kernel();
+  int n = 0;
+  if (nc > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nc);
+    cfg.blockDim = dim3((unsigned)ns_threads());
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)nc;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (n_cached < 64) cache[n_cached++] = Entry{dev, nc, smem, n};
+  return n;
+}
+
+// A step costs about as much as kNsStepColumns more columns per CTA would
+// (the Gram exchange, the A A product and the epilogues; measured on GB300).
+constexpr int kNsStepColumns = 600;
+
+
+// Cluster size for a fused weight of `units` 128-row units and `cols` columns:
+// the one with the lowest cost waves * (columns per CTA + kNsStepColumns)
+// among the sizes that divide the 64-column boxes, keep a slice within
+// kNsMaxSliceCols and can be resident; `want` > 0 forces that size.
+// Returns 0 when none fits.
+int ns_plan(int64_t units, int64_t cols, int want, size_t* smem) {
+  const void* kern = ns_kernel();
+  const int boxes = (int)(cols / 64);
+  int nc = 0;
+  int64_t best = -1;
+  for (int c = 1; c <= kNsMaxCluster; ++c) {
+    if (boxes % c != 0 || boxes / c > kNsMaxSliceCols / 64 || (want > 0 && c != want)) continue;
+    const size_t sm = (size_t)ns_smem_bytes((int)(cols / c));
+    if (!allow_smem(kern, sm)) continue;
+    int per_sm = 0;  // resident CTAs per SM must not ask for more than 512 TMEM columns together
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, ns_threads(), sm) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    if (per_sm < 1 || per_sm * ns_tmem_cols((int)(cols / c)) > 512) continue;
+    const int act = ns_active_clusters(c, sm);
+    if (act < 1) continue;
+    const int64_t waves = (units + act - 1) / act;
+    const int64_t cost = waves * (cols / c + kNsStepColumns);
+    if (best < 0 || cost < best) {
+      best = cost;
+      nc = c;
+      *smem = sm;
+    }
+  }
+  return nc;
+}
+
+// Shape checks shared by qkv_newton_schulz and qkv_newton_schulz_plan.
+int check_ns(const qkvp_layout* layout, int64_t cols, int32_t cluster, int64_t* rows) {
+  if (!layout) return QKVP_ERR_NULL;
+  if (layout->kind != QKVP_INTERLEAVED && layout->kind != QKVP_SECTIONED) return QKVP_ERR_SHAPE;
+  if (layout->n_q <= 0 || layout->n_kv <= 0 || layout->n_q % layout->n_kv) return QKVP_ERR_SHAPE;
+  if (layout->head_dim != 64 && layout->head_dim != 128) return QKVP_ERR_SHAPE;
+  *rows = ((int64_t)layout->n_q + 2 * (int64_t)layout->n_kv) * layout->head_dim;
+  if (*rows > (1 << 30)) return QKVP_ERR_SHAPE;
+  if (cols < 64 || cols % 64 != 0 || cols > (int64_t)kNsMaxCluster * kNsMaxSliceCols) return QKVP_ERR_SHAPE;
+  const int boxes = (int)(cols / 64);
+  if (cluster < 0 || cluster > kNsMaxCluster ||
+      (cluster > 0 && (boxes % cluster != 0 || boxes / cluster > kNsMaxSliceCols / 64)))
+    return QKVP_ERR_SHAPE;
+  return QKVP_OK;
+}
 
 }  // namespace
 }  // namespace qkvp
@@ -955,6 +1060,59 @@ int qkv_prologue_gemm_fwd(const qkvp_layout* layout, int64_t T, int32_t hidden, 
   const int64_t grid = 2 * (a.n_work < clusters ? a.n_work : clusters);
   void* args[] = {&tx, &tw, &a};
   return launch_args(kern, grid, threads, smem, static_cast<cudaStream_t>(stream), args, 2);
+}
+
+int qkv_newton_schulz(const qkvp_layout* layout, int64_t cols, const void* m, void* out, int32_t cluster,
+                      void* stream) {
+  using namespace qkvp;
+  int64_t rows = 0;
+  QKVP_TRY(check_ns(layout, cols, cluster, &rows));
+  if (!m || !out) return QKVP_ERR_NULL;
+  if (!aligned16(m) || !aligned16(out)) return QKVP_ERR_ALIGN;
+  const uintptr_t bytes = (uintptr_t)(rows * cols * 2), pm = (uintptr_t)m, po = (uintptr_t)out;
+  if (pm < po + bytes && po < pm + bytes) return QKVP_ERR_VALUE;  // out overlaps m
+
+  int sms = 0;
+  QKVP_TRY(current_device(&sms));
+  const int64_t units = (rows + kNsUnitRows - 1) / kNsUnitRows;
+  size_t smem = 0;
+  const int nc = ns_plan(units, cols, cluster, &smem);
+  if (nc == 0) return cluster > 0 ? QKVP_ERR_SHAPE : QKVP_ERR_LAUNCH;
+
+  CUtensorMap tm, to;
+  if (!bf16_tile_map(&tm, m, rows, cols, kNsUnitRows) || !bf16_tile_map(&to, out, rows, cols, kNsUnitRows))
+    return QKVP_ERR_LAUNCH;
+  NsArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.rows = (int32_t)rows;
+  a.cols = (int32_t)cols;
+  a.head_dim = layout->head_dim;
+  a.nc = nc;
+  a.cs = (int32_t)(cols / nc);
+  a.tmem_cols = ns_tmem_cols(a.cs);
+  a.scale = (float)std::sqrt(std::max(1.0, (double)layout->head_dim / (double)cols));
+  a.eps = 1e-7f;
+  if ((a.err = device_error_word()) == nullptr) return QKVP_ERR_LAUNCH;
+  void* args[] = {&tm, &to, &a};
+  return launch_args(ns_kernel(), units * nc, ns_threads(), smem, static_cast<cudaStream_t>(stream), args, nc,
+                     false);
+}
+
+int qkv_newton_schulz_plan(const qkvp_layout* layout, int64_t cols, int32_t cluster, int32_t* cluster_out,
+                           int32_t* grid_out) {
+  using namespace qkvp;
+  int64_t rows = 0;
+  QKVP_TRY(check_ns(layout, cols, cluster, &rows));
+  if (!cluster_out || !grid_out) return QKVP_ERR_NULL;
+  int sms = 0;
+  QKVP_TRY(current_device(&sms));
+  const int64_t units = (rows + kNsUnitRows - 1) / kNsUnitRows;
+  size_t smem = 0;
+  const int nc = ns_plan(units, cols, cluster, &smem);
+  if (nc == 0) return cluster > 0 ? QKVP_ERR_SHAPE : QKVP_ERR_LAUNCH;
+  *cluster_out = nc;
+  *grid_out = (int32_t)(units * nc);
+  return QKVP_OK;
 }
 
 int qkv_prologue_device_error(int clear, int* value) {

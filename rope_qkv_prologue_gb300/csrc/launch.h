@@ -282,6 +282,31 @@ const void* gemm_fwd_kernel(int head_dim, bool sectioned, bool rope, bool save);
 int gemm_fwd_smem_bytes();
 int gemm_fwd_threads();
 
+// Per-head Newton-Schulz of a fused QKV update: one cluster of `nc` CTAs per
+// unit of 128 weight rows (two 64-row heads or one 128-row head), CTA r of the
+// cluster holding columns [r cs, (r + 1) cs) of the unit in shared memory.
+constexpr int kNsUnitRows = 128;
+constexpr int kNsMaxSliceCols = 512;   // cs limit: the slice, A/B and the exchange fit one SM
+constexpr int kNsMaxCluster = 16;      // non-portable cluster size limit
+struct NsArgs {
+  int32_t rows;      // (n_q + 2 n_kv) head_dim
+  int32_t cols;      // in_features
+  int32_t head_dim;  // 64 or 128
+  int32_t nc;        // CTAs per cluster (column slices of a unit)
+  int32_t cs;        // columns per CTA, a multiple of 64, at most kNsMaxSliceCols
+  int32_t tmem_cols; // 256 (cs <= 256) or 512: B X needs cs columns, the Gram and A A 128 each
+  float scale;       // max(1, head_dim / cols) ** 0.5
+  float eps;         // added to each block's Frobenius norm
+  int* err;
+};
+const void* ns_kernel();
+// Dynamic shared memory per CTA for a slice of cs columns, padded so that no
+// more CTAs fit on one SM than its 512 TMEM columns can serve at once (a CTA
+// waiting in tcgen05.alloc for another cluster's CTA could deadlock both).
+int ns_smem_bytes(int cs);
+inline int ns_tmem_cols(int cs) { return cs <= 256 ? 256 : 512; }
+int ns_threads();
+
 constexpr int kLatentWarps = 8;        // warps per CTA of the latent kernel
 constexpr int kLatentTokensPerWarp = 2;
 constexpr int kLatentTileTokens = 16;     // rows per tile of the pipelined latent kernel

@@ -1,0 +1,451 @@
+// Per-head Newton-Schulz of a fused QKV update on the tensor cores (sm_103a).
+//
+// "[muon] Per-head Newton-Schulz for fused QKV projections" (DeepSpeed), What
+// this PR does: a fused weight's dim 0 is cut into head_dim-row blocks (the
+// same blocks in the sectioned and the interleaved packing, so the packing
+// never enters), each block is orthogonalised on its own and multiplied by
+// max(1, head_dim / in_features) ** 0.5. The iteration is Muon's published
+// quintic Newton-Schulz: X = G / (||G||_F + eps), then five times
+//     A = X X^T,   B = b A + c A A,   X = a X + B X,
+// with (a, b, c) = (3.4445, -4.7750, 2.0315). (The published code transposes a
+// tall block first only to work on the smaller Gram matrix; a X + B X with
+// A = X X^T is the same polynomial in X either way.)
+//
+// Work split. A unit is 128 consecutive weight rows, two 64-row heads or one
+// 128-row head (the tensor cores' M = 128). One cluster of nc CTAs takes one
+// unit; CTA r keeps columns [r cs, (r + 1) cs) of it resident in shared memory
+// for the whole iteration (bf16, 128-byte-swizzled boxes of 64 columns, loaded
+// once by TMA). Each step:
+//   1. Gram partial P_r = X_r X_r^T: tcgen05, K = cs, into TMEM columns 0-127.
+//   2. A = sum over the cluster of P_r: every CTA copies 64 columns of its
+//      partial to an fp32 exchange buffer; CTA r sums rows
+//      [128 r / nc, 128 (r + 1) / nc) of all buffers through distributed
+//      shared memory, rounds them to bf16 and writes them into the A tile of
+//      every CTA of the cluster.
+//   3. A A: tcgen05, K = 128, into TMEM columns 128-255 (TMEM: 256 columns
+//      when cs <= 256, else 512; the three products reuse the same columns
+//      one after the other).
+//   4. B = b A + c A A, rounded to bf16, in place of A.
+//   5. B X_r with X_r as the MN-major B operand: tcgen05, N = cs, into TMEM
+//      columns 0 .. cs-1.
+//   6. X_r = a X_r + B X_r, rounded to bf16, in place; after the last step
+//      times the scale, then TMA-stored to the output.
+// With 64-row heads only the two diagonal 64 x 64 blocks of A are reduced and
+// written; the rest of the A tile stays 0, so B is block diagonal and the two
+// heads of a unit never mix. Before the first step each block's squared norm
+// is summed the same way (row sums, then over the cluster) and X is scaled in
+// place to X / (norm + eps).
+//
+// Roles: warp 0 issues the TMA load; warp 1 owns TMEM and one of its threads
+// issues every MMA; warps 2-9 are the epilogue: warp w reads TMEM lanes
+// 32 (w % 4) .. 32 (w % 4) + 31 (= weight rows of the unit) and one half of
+// the columns. Every wait is bounded (2 s); after a timeout the device error
+// word is set and every thread still passes every barrier, without waiting.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "pipeline.cuh"
+#include "tcgen05.cuh"
+
+namespace qkvp {
+namespace {
+
+constexpr int kNsThreads = 320, kNsEpiThreads = 256, kNsEpiBar = 1;
+constexpr int kBox = kNsUnitRows * 128;  // bytes of one 128-row x 64-column bf16 box
+constexpr int kEStride = 68;             // floats per exchange row: 64 + 4 (conflict-free float4 rows)
+constexpr int kEBytes = kNsUnitRows * kEStride * 4;
+constexpr float kNsA = 3.4445f, kNsB = -4.7750f, kNsC = 2.0315f;
+constexpr int kNsSteps = 5;
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a swizzled box.
+__device__ __forceinline__ int swz(int row, int chunk) { return row * 128 + ((chunk ^ (row & 7)) << 4); }
+
+// Bounded wait that gives up at once when another thread of the CTA already
+// gave up (*fail): after one timeout the rest of the kernel runs through its
+// barriers without waiting.
+template <bool CLUSTER>
+__device__ __forceinline__ bool ns_wait(uint64_t* bar, uint32_t parity, int* err, volatile int* fail) {
+  auto test = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (test()) return true;
+  const uint64_t t0 = global_ns();
+  while (!test()) {
+    if (*fail) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *fail = 1;
+      atomicOr(err, kErrWaitTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Step 2 of the exchange, run by every epilogue thread of CTA `rank`: the rows
+// [128 rank / nc, 128 (rank + 1) / nc) of the Gram, 64 columns (pass p), as
+// float4 items; each item is summed over the exchange buffers of all CTAs in
+// rank order (the same sums in every CTA) and written, rounded to bf16, into
+// the A tile of every CTA of the cluster. NC > 0 fixes the cluster size at
+// compile time so that all of a thread's remote loads are in flight together
+// (2048 / NC items over 256 threads: 8 loads per thread); NC = 0 takes nc at
+// run time, one item at a time.
+template <int NC>
+__device__ __forceinline__ void reduce_rows(const float* E, unsigned char* ab, int hd, int p, uint32_t nc,
+                                            uint32_t rank, int et) {
+  const int r0 = (int)(kNsUnitRows * rank / nc), r1 = (int)(kNsUnitRows * (rank + 1) / nc);
+  const int n = (r1 - r0) * 16;
+  auto item_src = [&](int idx) { return E + (r0 + (idx >> 4)) * kEStride + 4 * (idx & 15); };
+  auto put = [&](int idx, const float4& s) {
+    const int i = r0 + (idx >> 4);
+    const int col = (hd == 64 ? 64 * (i >> 6) : 64 * p) + 4 * (idx & 15);
+    unsigned char* d = ab + (col >> 6) * kBox + swz(i, (col & 63) >> 3) + (col & 7) * 2;
+    const uint32_t lo = pack2(s.x, s.y), hi = pack2(s.z, s.w);
+    if (NC == 1) {
+      *reinterpret_cast<uint2*>(d) = make_uint2(lo, hi);
+    } else {
+      for (uint32_t r = 0; r < nc; ++r) st_cluster_u2(cluster_map(smem_addr(d), r), lo, hi);
+    }
+  };
+  auto add = [](float4& s, const float4& t) {
+    s.x += t.x;
+    s.y += t.y;
+    s.z += t.z;
+    s.w += t.w;
+  };
+  if constexpr (NC > 0) {
+    constexpr int kItems = 8 / NC;
+    float4 t[kItems][NC];
+#pragma unroll
+    for (int j = 0; j < kItems; ++j) {
+      const int idx = et + kNsEpiThreads * j;
+      if (idx < n) {
+        if (NC == 1) {
+          t[j][0] = *reinterpret_cast<const float4*>(item_src(idx));
+        } else {
+          const uint32_t src = smem_addr(item_src(idx));
+#pragma unroll
+          for (int r = 0; r < NC; ++r) t[j][r] = ld_cluster_f4(cluster_map(src, (uint32_t)r));
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kItems; ++j) {
+      const int idx = et + kNsEpiThreads * j;
+      if (idx < n) {
+        float4 s = t[j][0];
+#pragma unroll
+        for (int r = 1; r < NC; ++r) add(s, t[j][r]);
+        put(idx, s);
+      }
+    }
+  } else {
+    for (int idx = et; idx < n; idx += kNsEpiThreads) {
+      const uint32_t src = smem_addr(item_src(idx));
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (uint32_t rb = 0; rb < nc; rb += 8) {  // eight remote loads in flight at a time
+        float4 t[8];
+#pragma unroll
+        for (uint32_t k = 0; k < 8; ++k)
+          if (rb + k < nc) t[k] = ld_cluster_f4(cluster_map(src, rb + k));
+#pragma unroll
+        for (uint32_t k = 0; k < 8; ++k) {
+          if (rb + k < nc) {
+            if (rb + k == 0)
+              s = t[k];
+            else
+              add(s, t[k]);
+          }
+        }
+      }
+      put(idx, s);
+    }
+  }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kNsThreads, 1)
+    qkvp_newton_schulz_kernel(const __grid_constant__ CUtensorMap tmap_m, const __grid_constant__ CUtensorMap tmap_out,
+                              const NsArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ __align__(8) uint64_t bar_load, bar_xready, bar_gram, bar_aready, bar_sq, bar_bready, bar_bx, bar_fin;
+  __shared__ __align__(8) uint64_t bar_efull, bar_afull;  // completed by arrivals from every CTA of the cluster
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_fail;
+  __shared__ float s_red[8], s_inv[2];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t nc = (uint32_t)a.nc, rank = cluster_ctarank();
+  const int unit = blockIdx.x / a.nc;
+  const int cs = a.cs, nbox = cs >> 6, hd = a.head_dim;
+  const int npass = hd == 64 ? 1 : 2;  // exchange passes per Gram (64 columns each)
+  // Phases: every waiter below waits each phase of a barrier in order and can
+  // never be more than one phase behind it, so a parity names one phase.
+  unsigned char* xs = smem;                 // nbox boxes: this CTA's columns of the unit
+  unsigned char* ab = smem + nbox * kBox;   // 2 boxes: A, then B in place (128 x 128)
+  float* E = reinterpret_cast<float*>(ab + 2 * kBox);  // fp32 exchange, 128 rows x kEStride
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_load, 1);
+    mbar_init(&bar_xready, 1);
+    mbar_init(&bar_gram, 1);
+    mbar_init(&bar_aready, 1);
+    mbar_init(&bar_sq, 1);
+    mbar_init(&bar_bready, 1);
+    mbar_init(&bar_bx, 1);
+    mbar_init(&bar_fin, 1);
+    mbar_init(&bar_efull, nc);
+    mbar_init(&bar_afull, nc);
+    s_fail = 0;
+    mbar_init_fence();
+  }
+  // The A tile starts at 0: with 64-row heads its off-diagonal blocks stay 0.
+  for (int i = threadIdx.x; i < 2 * kBox / 16; i += kNsThreads) reinterpret_cast<uint4*>(ab)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_cta();
+  if (warp == 1) tmem_alloc(&s_tmem, (uint32_t)a.tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // every CTA's barriers are initialised before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ loads
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar_load, (uint32_t)(nbox * kBox));
+      for (int j = 0; j < nbox; ++j)
+        tma_load_2d(xs + j * kBox, &tmap_m, (int)rank * cs + 64 * j, unit * kNsUnitRows, &bar_load);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMAs
+    if (lane == 0) {
+      const uint32_t id_sq = umma_idesc_bf16(128, 128);
+      for (int it = 0; it < kNsSteps; ++it) {
+        if (!ns_wait<false>(&bar_xready, it & 1, a.err, &s_fail)) break;
+        tc_fence_after();
+        for (int j = 0; j < nbox; ++j) {  // P = X_r X_r^T
+          const uint64_t d = umma_desc_sw128(xs + j * kBox);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) umma_bf16(tmem, d + 2 * k, d + 2 * k, id_sq, (j | k) != 0);
+        }
+        umma_commit(&bar_gram);
+        // A is complete in this CTA (the epilogue has seen every exchange pass
+        // of this step finish; waiting on the cluster barrier here could skip
+        // a phase when a step has two passes)
+        if (!ns_wait<false>(&bar_aready, it & 1, a.err, &s_fail)) break;
+        tc_fence_after();
+        for (int j = 0; j < 2; ++j) {  // A A (A is symmetric: both operands are its rows)
+          const uint64_t d = umma_desc_sw128(ab + j * kBox);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) umma_bf16(tmem + 128, d + 2 * k, d + 2 * k, id_sq, (j | k) != 0);
+        }
+        umma_commit(&bar_sq);
+        if (!ns_wait<false>(&bar_bready, it & 1, a.err, &s_fail)) break;
+        tc_fence_after();
+        for (int n0 = 0; n0 < cs; n0 += 256) {  // B X_r
+          const int n = cs - n0 < 256 ? cs - n0 : 256;
+          const uint32_t id = umma_idesc_bf16_bmn(128, n);
+          const uint64_t bd = umma_desc_sw128_mn(xs + (n0 >> 6) * kBox, kBox);
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            const uint64_t ad = umma_desc_sw128(ab + (s >> 2) * kBox) + 2 * (s & 3);
+            umma_bf16(tmem + n0, ad, bd + (uint64_t)(128 * s), id, s != 0);  // +2048 B: 16 rows of X
+          }
+        }
+        umma_commit(&bar_bx);
+      }
+      umma_commit(&bar_fin);  // arrives once everything issued above has completed
+      mbar_wait(&bar_fin, 0, a.err);
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int et = threadIdx.x - 64, q = warp & 3, h = (warp - 2) >> 2, row = 32 * q + lane;
+    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+    const uint32_t efull = smem_addr(&bar_efull), afull = smem_addr(&bar_afull);
+    uint32_t pass = 0;
+
+    // ---- block norms: row sums of squares, then over the cluster
+    ns_wait<false>(&bar_load, 0, a.err, &s_fail);
+    const int half_ch = nbox * 4;  // 16-byte chunks per row in one column half
+    float ss = 0.f;
+    for (int ch = h * half_ch; ch < (h + 1) * half_ch; ++ch) {
+      float f[8];
+      unpack8(*reinterpret_cast<const uint4*>(xs + (ch >> 3) * kBox + swz(row, ch & 7)), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) s_red[warp - 2] = ss;
+    named_sync(kNsEpiBar, kNsEpiThreads);
+    if (warp == 2) {  // the cluster exchange of the block norms: lane r talks to CTA r
+      if (lane == 0) {
+        float lo = 0.f, hi = 0.f;  // rows 0-63, rows 64-127 of this CTA's columns
+        for (int i = 0; i < 8; ++i) {
+          if (((i + 2) & 3) < 2)
+            lo += s_red[i];
+          else
+            hi += s_red[i];
+        }
+        E[0] = lo;
+        E[1] = hi;
+        fence_acq_rel_cluster();
+      }
+      __syncwarp();
+      if ((uint32_t)lane < nc) mbar_arrive_cluster(cluster_map(efull, lane));
+      float tlo = 0.f, thi = 0.f;
+      if (ns_wait<true>(&bar_efull, pass & 1, a.err, &s_fail) && (uint32_t)lane < nc) {
+        const float4 v = ld_cluster_f4(cluster_map(smem_addr(E), lane));
+        tlo = v.x;
+        thi = v.y;
+      }
+      tlo = warp_sum(tlo);  // the same order in every CTA of the cluster
+      thi = warp_sum(thi);
+      fence_acq_rel_cluster();
+      __syncwarp();
+      if ((uint32_t)lane < nc) mbar_arrive_cluster(cluster_map(afull, lane));
+      if (lane == 0) {
+        if (hd == 64) {
+          s_inv[0] = 1.f / (sqrtf(tlo) + a.eps);
+          s_inv[1] = 1.f / (sqrtf(thi) + a.eps);
+        } else {
+          s_inv[0] = s_inv[1] = 1.f / (sqrtf(tlo + thi) + a.eps);
+        }
+      }
+      ns_wait<true>(&bar_afull, pass & 1, a.err, &s_fail);  // every CTA has read this E
+    }
+    ++pass;
+    named_sync(kNsEpiBar, kNsEpiThreads);
+    {
+      const float inv = s_inv[row >> 6];
+      for (int ch = h * half_ch; ch < (h + 1) * half_ch; ++ch) {
+        uint4* p = reinterpret_cast<uint4*>(xs + (ch >> 3) * kBox + swz(row, ch & 7));
+        float f[8];
+        unpack8(*p, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] *= inv;
+        *p = pack8(f);
+      }
+    }
+    fence_proxy_async_cta();
+    named_sync(kNsEpiBar, kNsEpiThreads);
+    if (et == 0) mbar_arrive(&bar_xready);
+
+    for (int it = 0; it < kNsSteps; ++it) {
+      // ---- 1-2: Gram partial -> exchange -> A (bf16) in every CTA
+      ns_wait<false>(&bar_gram, it & 1, a.err, &s_fail);
+      tc_fence_after();
+      for (int p = 0; p < npass; ++p) {
+        {
+          float v[32];
+          tmem_ld32(trow + (uint32_t)((hd == 64 ? 64 * (q >> 1) : 64 * p) + 32 * h), v);
+          float4* er = reinterpret_cast<float4*>(E + row * kEStride + 32 * h);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) er[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+        fence_acq_rel_cluster();
+        named_sync(kNsEpiBar, kNsEpiThreads);
+        if (et < (int)nc) mbar_arrive_cluster(cluster_map(efull, (uint32_t)et));  // one lane per CTA
+        ns_wait<true>(&bar_efull, pass & 1, a.err, &s_fail);
+        switch (nc) {  // all the remote loads of a thread in flight at once
+          case 1: reduce_rows<1>(E, ab, hd, p, nc, rank, et); break;
+          case 2: reduce_rows<2>(E, ab, hd, p, nc, rank, et); break;
+          case 4: reduce_rows<4>(E, ab, hd, p, nc, rank, et); break;
+          default: reduce_rows<0>(E, ab, hd, p, nc, rank, et); break;
+        }
+        fence_proxy_async_cluster();
+        fence_acq_rel_cluster();
+        named_sync(kNsEpiBar, kNsEpiThreads);
+        if (et < (int)nc) mbar_arrive_cluster(cluster_map(afull, (uint32_t)et));
+        ns_wait<true>(&bar_afull, pass & 1, a.err, &s_fail);  // A complete; every CTA has read this E
+        ++pass;
+      }
+      if (et == 0) mbar_arrive(&bar_aready);
+
+      // ---- 3-4: B = b A + c A A, in place of A
+      ns_wait<false>(&bar_sq, it & 1, a.err, &s_fail);
+      tc_fence_after();
+      {
+        float sq[64];
+        tmem_ld32(trow + (uint32_t)(128 + 64 * h), sq);
+        tmem_ld32(trow + (uint32_t)(128 + 64 * h + 32), sq + 32);
+        unsigned char* arow = ab + h * kBox;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          uint4* pch = reinterpret_cast<uint4*>(arow + swz(row, k));
+          float f[8];
+          unpack8(*pch, f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) f[i] = fmaf(kNsC, sq[8 * k + i], kNsB * f[i]);
+          *pch = pack8(f);
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async_cta();
+      named_sync(kNsEpiBar, kNsEpiThreads);
+      if (et == 0) mbar_arrive(&bar_bready);
+
+      // ---- 5-6: X = a X + B X (after the last step: times the scale, then stored)
+      ns_wait<false>(&bar_bx, it & 1, a.err, &s_fail);
+      tc_fence_after();
+      const bool last = it == kNsSteps - 1;
+      const float fa = last ? a.scale * kNsA : kNsA, fd = last ? a.scale : 1.f;
+      auto update = [&](int c, const float* d) {  // 32 columns from c: a X + B X
+        unsigned char* xb = xs + (c >> 6) * kBox;
+        const int k0 = (c & 63) >> 3;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          uint4* pch = reinterpret_cast<uint4*>(xb + swz(row, k0 + kk));
+          float f[8];
+          unpack8(*pch, f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) f[i] = fmaf(fa, f[i], fd * d[8 * kk + i]);
+          *pch = pack8(f);
+        }
+      };
+      for (int c = h * (cs >> 1); c < (h + 1) * (cs >> 1); c += 32) {
+        float d[32];
+        tmem_ld32(trow + (uint32_t)c, d);
+        update(c, d);
+      }
+      tc_fence_before();
+      fence_proxy_async_cta();
+      named_sync(kNsEpiBar, kNsEpiThreads);
+      if (et == 0) {
+        if (!last) {
+          mbar_arrive(&bar_xready);
+        } else {
+          for (int j = 0; j < nbox; ++j)
+            tma_store_2d(&tmap_out, xs + j * kBox, (int)rank * cs + 64 * j, unit * kNsUnitRows);
+          bulk_commit();
+          bulk_wait_all();
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no CTA leaves while another may still touch its shared memory
+  if (warp == 1) tmem_dealloc(tmem, (uint32_t)a.tmem_cols);
+}
+
+const void* ns_kernel() { return reinterpret_cast<const void*>(&qkvp_newton_schulz_kernel); }
+int ns_smem_bytes(int cs) {
+  const int need = (cs / 64) * kBox + 2 * kBox + kEBytes + 1024;
+  // 228 KiB per SM, 1 KiB reserved per CTA: 118 KiB admits one CTA per SM,
+  // 78 KiB at most two
+  const int floor = ns_tmem_cols(cs) == 512 ? 118 * 1024 : 78 * 1024;
+  return need > floor ? need : floor;
+}
+int ns_threads() { return kNsThreads; }
+
+}  // namespace qkvp

@@ -152,6 +152,25 @@ def gemm_prologue_forward(x, w_qkv, pos, w_q, w_k, n_q, n_kv, head_dim=64, kind=
     return (q, k, v, q_pre, k_pre) if save_pre else (q, k, v)
 
 
+def per_head_newton_schulz(m, n_q, n_kv, head_dim=64, kind="interleaved", cluster=0, out=None, stream=None):
+    """Per-head Newton-Schulz of a fused QKV weight's update m
+    [(n_q + 2 n_kv) * head_dim, in_features] bf16: every head_dim-row block
+    orthogonalised on its own (Muon's quintic iteration, five steps) and scaled
+    by max(1, head_dim / in_features) ** 0.5 ("[muon] Per-head Newton-Schulz for
+    fused QKV projections", What this PR does). `kind` names the packing of the
+    rows; the result does not depend on it."""
+    _check_dev(m)
+    if m.dim() != 2 or m.dtype != torch.bfloat16:
+        raise ValueError("m must be a 2-D bf16 tensor")
+    if m.shape[0] != (n_q + 2 * n_kv) * head_dim:
+        raise ValueError("m must have (n_q + 2 n_kv) * head_dim rows")
+    m = m.contiguous()
+    if out is None:
+        out = torch.empty_like(m)
+    C.qkv_newton_schulz(C.layout(kind, n_q, n_kv, head_dim), m.shape[1], m, out, cluster, stream)
+    return out
+
+
 def on_side_stream(side, fn, *args, **kwargs):
     """Run fn(*args, **kwargs) on CUDA stream `side`, forked from the current
     stream: `side` first waits for everything already queued on the current

@@ -23,7 +23,7 @@ def _declared_functions():
         if f.endswith(".h"):
             src = open(os.path.join(HEADER_DIR, f)).read()
             src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-            names |= set(re.findall(r"QKVP_API\s+[\w\s\*]+?\b(qkv_prologue_\w+)\s*\(", src))
+            names |= set(re.findall(r"QKVP_API\s+[\w\s\*]+?\b(qkv_\w+)\s*\(", src))
     return names
 
 
@@ -31,7 +31,8 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     assert {"qkv_prologue_fwd", "qkv_prologue_bwd", "qkv_prologue_pool_write",
             "qkv_prologue_pool_scatter", "qkv_prologue_bwd_workspace_size",
-            "qkv_prologue_status_string", "qkv_prologue_version", "qkv_prologue_device_error"} <= names
+            "qkv_prologue_status_string", "qkv_prologue_version", "qkv_prologue_device_error",
+            "qkv_newton_schulz", "qkv_newton_schulz_plan"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -41,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
     missing = _declared_functions() - exported
     assert not missing, missing
     # and nothing else of ours leaks out of the library
-    ours = {s for s in exported if "qkvp" in s.lower() or "qkv_prologue" in s}
+    ours = {s for s in exported if "qkvp" in s.lower() or s.startswith("qkv_")}
     assert ours == _declared_functions()
     dl = ctypes.CDLL(lib.LIB_PATH)
     for name in _declared_functions():
@@ -54,7 +55,7 @@ def test_binding_exposes_the_same_names(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.qkv_prologue_version() == lib.QKVP_VERSION == 2
+    assert lib.qkv_prologue_version() == lib.QKVP_VERSION == 3
     for code in range(-8, 1):
         s = lib.qkv_prologue_status_string(code)
         assert s and s != "unknown status"
@@ -346,3 +347,34 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
     code = "import rope_qkv_prologue_gb300"
     res = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True)
     assert res.returncode != 0 and "libqkv_prologue.so is missing" in res.stderr
+
+
+@cpu_only
+def test_newton_schulz_argument_checks(lib):
+    C = lib
+    L = C.layout("interleaved", 128, 16, 64)
+    rows = 160 * 64
+
+    def ns(L=L, cols=5120, m=A, out=A + rows * 5120 * 2, cluster=0):
+        return C.qkv_newton_schulz(L, cols, m, out, cluster, stream=0, check=False)
+
+    assert ns() == C.QKVP_ERR_ARCH  # valid: reaches the device check
+    assert ns(cluster=10) == C.QKVP_ERR_ARCH
+    assert ns(L=C.layout("sectioned", 8, 2, 128), cols=1024, out=A + 1536 * 1024 * 2) == C.QKVP_ERR_ARCH
+    assert ns(cols=5121) == C.QKVP_ERR_SHAPE    # a multiple of 64
+    assert ns(cols=32) == C.QKVP_ERR_SHAPE
+    assert ns(cols=16384) == C.QKVP_ERR_SHAPE   # more than 16 slices of 512
+    assert ns(cluster=3) == C.QKVP_ERR_SHAPE    # must divide the 80 boxes of 64 columns
+    assert ns(cluster=2) == C.QKVP_ERR_SHAPE    # 2560 columns per CTA is more than 512
+    assert ns(cluster=17) == C.QKVP_ERR_SHAPE
+    assert ns(cluster=-1) == C.QKVP_ERR_SHAPE
+    assert ns(L=C.layout("interleaved", 8, 2, 96)) == C.QKVP_ERR_SHAPE
+    assert ns(L=C.layout("interleaved", 8, 3, 64)) == C.QKVP_ERR_SHAPE
+    assert ns(L=C.layout("latent", norm_dim=512, rope_dim=64)) == C.QKVP_ERR_SHAPE
+    assert ns(m=None) == C.QKVP_ERR_NULL
+    assert ns(out=None) == C.QKVP_ERR_NULL
+    assert ns(m=A + 8) == C.QKVP_ERR_ALIGN
+    assert ns(out=A + 16) == C.QKVP_ERR_VALUE   # the output overlaps the input
+    assert ns(out=A - rows * 5120 * 2) == C.QKVP_ERR_ARCH  # just below: no overlap
+    with pytest.raises(C.QkvpError):
+        C.qkv_newton_schulz_plan(L, 5120)      # planning needs the device

@@ -264,6 +264,34 @@ def gemm_inputs(T, hidden, n_q, n_kv, head_dim, seed, exact=True):
     return x.to(torch.bfloat16), w.to(torch.bfloat16)
 
 
+def fused_qkv_update(n_q, n_kv, head_dim, cols, seed, scale=1.0):
+    """A fused QKV weight's update (a gradient or a momentum)
+    [(n_q + 2 n_kv) * head_dim, cols] bf16, N(0, scale^2), rows in the
+    interleaved-per-KV-group order. The whole tensor is one draw, so every
+    head block looks like any other."""
+    g = _gen(seed)
+    rows = (n_q + 2 * n_kv) * head_dim
+    return (torch.randn(rows, cols, generator=g) * scale).to(torch.bfloat16)
+
+
+def sectioned_weight_from_interleaved(w, n_q, n_kv, head_dim):
+    """The same fused weight with its dim-0 head blocks in sectioned order
+    (q heads, then k heads, then v heads): a row permutation of w."""
+    return sectioned_from_interleaved(w.t().contiguous(), n_q, n_kv, head_dim).t().contiguous()
+
+
+# Fused QKV weights the per-head Newton-Schulz path runs on:
+#  - the page's model ("[muon] Per-head Newton-Schulz for fused QKV
+#    projections", End-to-end training): a LLaMA-shaped model, 6 layers,
+#    hidden 512, 8 query heads over 2 KV heads of 64, so a [768, 512] fused
+#    weight per layer;
+#  - the Muse Spark packing of the prologue ([T, 16 kv heads, 10, 64]): a
+#    [10240, hidden] fused weight; hidden 5120 stands in for the model's
+#    (the pages give none).
+NS_PAGE_MODEL = dict(n_q=8, n_kv=2, head_dim=64, cols=512, layers=6)
+NS_MUSE_SPARK = dict(n_q=128, n_kv=16, head_dim=64, cols=5120, layers=1)
+
+
 # --- the five workloads ------------------------------------------------------
 
 def tiny(seed=1):

@@ -554,6 +554,79 @@ class GemmStep(_Step):
         return t, a.elapsed_time(b) * 1e3 / reps
 
 
+class NewtonSchulzStep(_Step):
+    """Per-head Newton-Schulz of fused QKV weight updates (tcgen05 tensor cores),
+    one C-ABI call per layer ("[muon] Per-head Newton-Schulz for fused QKV
+    projections"). `newton_schulz`: the Muse Spark fused weight [10240, 5120]
+    (16 kv groups x (8 q + k + v) heads of 64; hidden 5120 stands in for the
+    model's); `newton_schulz_page`: the page's 17M-parameter model, 6 layers of
+    [768, 512] (8 q heads over 2 kv heads of 64, hidden 512)."""
+
+    def __init__(self, dev, name):
+        import types
+
+        import torch
+
+        import workloads
+
+        self._common(dev)
+        c = workloads.NS_PAGE_MODEL if name == "newton_schulz_page" else workloads.NS_MUSE_SPARK
+        self.c, self.layers = c, c["layers"]
+        self.n_q, self.n_kv, self.hd, self.cols = c["n_q"], c["n_kv"], c["head_dim"], c["cols"]
+        self.rows = (self.n_q + 2 * self.n_kv) * self.hd
+        self.T = self.rows
+        self.wl = types.SimpleNamespace(n_q=self.n_q, n_kv=self.n_kv, head_dim=self.hd)
+        self.L = self.C.layout("interleaved", self.n_q, self.n_kv, self.hd)
+        h_in = {}
+        for layer in range(self.layers):
+            m = workloads.fused_qkv_update(self.n_q, self.n_kv, self.hd, self.cols, seed=200 + layer)
+            h_in[f"m{layer}"] = m
+            setattr(self, f"m{layer}", m.to(dev))
+            setattr(self, f"o{layer}", torch.empty(self.rows, self.cols, **self.bf))
+        self.h_in = h_in
+        self.out_names = tuple(f"o{layer}" for layer in range(self.layers))
+        blocks = self.rows // self.hd
+        # per call: 5 steps of X X^T, A A and B X on every head block
+        self.flops = blocks * 5 * (4 * self.hd * self.hd * self.cols + 2 * self.hd ** 3)
+        io = 2 * self.rows * self.cols * 2
+        self.calls = [(f"qkv_newton_schulz layer {layer} (qkvp_newton_schulz_kernel: tcgen05, cluster-split columns)",
+                       (lambda layer=layer: self.ns(layer)), io) for layer in range(self.layers)]
+        self.kernels_per_step = self.layers
+        nc, grid = self.C.qkv_newton_schulz_plan(self.L, self.cols)
+        self.describe = (f"per-head Newton-Schulz (Muon quintic, 5 steps) of {self.layers} fused QKV update(s) "
+                         f"[{self.rows}, {self.cols}] bf16, {blocks} head blocks of {self.hd} rows each; "
+                         f"clusters of {nc} CTAs, grid {grid}")
+
+    def ns(self, layer):
+        self.C.qkv_newton_schulz(self.L, self.cols, getattr(self, f"m{layer}"), getattr(self, f"o{layer}"), 0,
+                                 self.stream)
+
+    def comparison(self, reps=10):
+        """The published bf16 iteration in plain PyTorch, batched over the head
+        blocks of one layer (cuBLAS batched GEMMs + element-wise kernels)."""
+        import torch
+
+        X0 = self.m0.view(-1, self.hd, self.cols)
+
+        def run():
+            X = X0 / (X0.norm(dim=(-2, -1), keepdim=True) + 1e-7)
+            for _ in range(5):
+                A = X @ X.mT
+                B = -4.7750 * A + 2.0315 * (A @ A)
+                X = 3.4445 * X + B @ X
+            return X
+
+        for _ in range(3):
+            run()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            run()
+        b.record()
+        torch.cuda.synchronize()
+        return {"torch_bf16_batched_iteration_us_per_layer": round(a.elapsed_time(b) * 1e3 / reps, 2)}
+
+
 def mla_two_stream_overlap(dev, T, layers=3, reps=20):
     """The drafter-layer scheduling of "MLA DSpark: run each drafter layer's kv
     path beside its q path": per layer, the kv path (kv_a projection -> latent
@@ -654,6 +727,8 @@ def make_workload(name, dev, tokens):
         return VariantTrainStep(dev, tokens or 16384, name[:-len("_train")])
     if name == "gemm_fwd":
         return GemmStep(dev, tokens or 16384)
+    if name in ("newton_schulz", "newton_schulz_page"):
+        return NewtonSchulzStep(dev, name)
     raise ValueError(name)
 
 
@@ -920,11 +995,16 @@ def run_ours(args):
         out["roofline"] = {"kernel": dom_name, "bound": "tensor", "achieved": round(tflops, 1), "peak": tpeak,
                            "peak_source": f"{tsrc} (MEASURED_PEAKS.json bf16_tflops, burst: the call is timed alone)",
                            "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4), "traffic": None}
-        unf, gemm_only = ws.unfused_us()
-        out["unfused_cublas_projection_plus_prologue_us"] = round(unf, 2)
-        out["cublas_projection_alone_us"] = round(gemm_only, 2)
+        if hasattr(ws, "unfused_us"):
+            unf, gemm_only = ws.unfused_us()
+            out["unfused_cublas_projection_plus_prologue_us"] = round(unf, 2)
+            out["cublas_projection_alone_us"] = round(gemm_only, 2)
+        if hasattr(ws, "comparison"):
+            out.update(ws.comparison())
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "train":
         out["cpu_baseline"] = cpu_baseline(args.cpu_tokens)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload.startswith("newton_schulz"):
+        out["cpu_baseline"] = ns_cpu_baseline(args.workload)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -975,11 +1055,56 @@ def cpu_baseline(n_tokens):
     }
 
 
+class NsOracleSample:
+    """The fp64 oracle's per-head Newton-Schulz on the first n head blocks of
+    the workload's first layer (inputs drawn once; only the oracle is timed)."""
+
+    def __init__(self, name, n_blocks):
+        import oracle.newton_schulz as N
+        import workloads
+        from oracle.bf16 import bf16_bits_to_f64
+        from workloads import bits_u16 as u16
+
+        c = workloads.NS_PAGE_MODEL if name == "newton_schulz_page" else workloads.NS_MUSE_SPARK
+        m = workloads.fused_qkv_update(c["n_q"], c["n_kv"], c["head_dim"], c["cols"], seed=200)
+        self.N, self.c, self.n = N, c, n_blocks
+        self.m = bf16_bits_to_f64(u16(m[: n_blocks * c["head_dim"]]))
+
+    def run(self):
+        t0 = time.perf_counter()
+        self.N.per_head_newton_schulz(self.m, self.c["head_dim"])
+        return time.perf_counter() - t0
+
+    def bytes(self):
+        return 2 * self.m.size * 2  # the bf16 update in and the result out
+
+
+def ns_cpu_baseline(name, target_s=10.0):
+    probe = NsOracleSample(name, 1)
+    per_block = max(probe.run(), 1e-4)
+    blocks = (probe.c["n_q"] + 2 * probe.c["n_kv"])
+    n = int(max(1, min(blocks, target_s / per_block)))
+    sample = NsOracleSample(name, n)
+    secs = sample.run()
+    return {
+        "value": round(sample.bytes() / secs / 1e9, 6),
+        "unit": "GB/s",
+        "cores": len(os.sched_getaffinity(0)),
+        "kind": "oracle",
+        "sample": f"fp64 NumPy oracle per-head Newton-Schulz of the first {n} of {blocks} head blocks of layer 0 "
+                  f"({probe.c['head_dim']} x {probe.c['cols']} each), {secs:.1f} s; its matrix products run on "
+                  "NumPy's BLAS with its default threads (all host cores listed)",
+        "seconds": round(secs, 2),
+    }
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
     K, W = args.steps, args.warmup
+    if args.workload.startswith("newton_schulz"):
+        return run_reference_ns(args, world)
     per_token_s = 0.0025
     n = int(max(1, min(512, 120.0 / max(1, K + W) / per_token_s)))
     sample = OracleSample(n)
@@ -1013,6 +1138,40 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_reference_ns(args, world):
+    K, W = args.steps, args.warmup
+    probe = NsOracleSample(args.workload, 1)
+    per_block = max(probe.run(), 1e-4)
+    blocks = probe.c["n_q"] + 2 * probe.c["n_kv"]
+    n = int(max(1, min(blocks, 120.0 / max(1, K + W) / per_block)))
+    sample = NsOracleSample(args.workload, n)
+    for _ in range(W):
+        sample.run()
+    step_s = statistics.fmean(sample.run() for _ in range(K))
+    value = sample.bytes() / step_s / 1e9
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(step_s * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (same seeded workload as the CUDA arm)",
+        "config": {"workload": f"per-head Newton-Schulz, {args.workload}", "sample_blocks_per_step": n},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": len(os.sched_getaffinity(0)),
+                         "kind": "oracle",
+                         "sample": f"fp64 NumPy oracle per-head Newton-Schulz of {n} head blocks per step"},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -1021,7 +1180,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--workload", choices=["train", "prefill", "prefill_nope", "decode", "mla", "llama3_train",
-                                           "qwen3_train", "gpt_oss_train", "gemm_fwd"], default="train",
+                                           "qwen3_train", "gpt_oss_train", "gemm_fwd", "newton_schulz",
+                                           "newton_schulz_page"], default="train",
                     help="train (the headline) | prefill | prefill_nope | decode (pool write) | mla (latent pool write)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="T (0 = the workload's default: 16384 train/prefill, 256 decode, 32768 mla)")

@@ -29,7 +29,9 @@
 //   5. B X_r with X_r as the MN-major B operand: tcgen05, N = cs, into TMEM
 //      columns 0 .. cs-1.
 //   6. X_r = a X_r + B X_r, rounded to bf16, in place; after the last step
-//      times the scale, then TMA-stored to the output.
+//      times the scale, then TMA-stored to the output. (a stays an fp32
+//      factor: folded into B's diagonal it would be rounded to bf16 too,
+//      0.2 % off, which is what X gets when B is small.)
 // With 64-row heads only the two diagonal 64 x 64 blocks of A are reduced and
 // written; the rest of the A tile stays 0, so B is block diagonal and the two
 // heads of a unit never mix. Before the first step each block's squared norm
@@ -176,7 +178,11 @@ __global__ void __launch_bounds__(kNsThreads, 1)
                               const NsArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t bar_load, bar_xready, bar_gram, bar_aready, bar_sq, bar_bready, bar_bx, bar_fin;
+  __shared__ __align__(8) uint64_t bar_load, bar_gram, bar_aready, bar_sq, bar_bready, bar_fin;
+  // Section s of the slice written (one arrive per epilogue warp; the Gram of
+  // the next step starts on section 0 while section 1 is being written) and
+  // B X of section s done
+  __shared__ __align__(8) uint64_t bar_xsec[2], bar_bx[2];
   __shared__ __align__(8) uint64_t bar_efull, bar_afull;  // completed by arrivals from every CTA of the cluster
   __shared__ uint32_t s_tmem;
   __shared__ int s_fail;
@@ -187,20 +193,28 @@ __global__ void __launch_bounds__(kNsThreads, 1)
   const int unit = blockIdx.x / a.nc;
   const int cs = a.cs, nbox = cs >> 6, hd = a.head_dim;
   const int npass = hd == 64 ? 1 : 2;  // exchange passes per Gram (64 columns each)
+  // Sections: boxes [0, sb) and [sb, nbox) when the slice has 4 boxes or more
+  // (the Gram accumulator, TMEM columns 0-127, then lies in section 0's part
+  // of the last B X), else one section.
+  const int nsec = nbox >= 4 ? 2 : 1, sb = nsec == 2 ? nbox >> 1 : nbox;
   // Phases: every waiter below waits each phase of a barrier in order and can
   // never be more than one phase behind it, so a parity names one phase.
+  // bar_xsec[s] completes once for the normalised input (phase 0) and once per
+  // step's update (phase it + 1); the Gram of step it waits phase it.
   unsigned char* xs = smem;                 // nbox boxes: this CTA's columns of the unit
   unsigned char* ab = smem + nbox * kBox;   // 2 boxes: A, then B in place (128 x 128)
   float* E = reinterpret_cast<float*>(ab + 2 * kBox);  // fp32 exchange, 128 rows x kEStride
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_load, 1);
-    mbar_init(&bar_xready, 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&bar_xsec[k], kNsEpiThreads / 32);
+      mbar_init(&bar_bx[k], 1);
+    }
     mbar_init(&bar_gram, 1);
     mbar_init(&bar_aready, 1);
     mbar_init(&bar_sq, 1);
     mbar_init(&bar_bready, 1);
-    mbar_init(&bar_bx, 1);
     mbar_init(&bar_fin, 1);
     mbar_init(&bar_efull, nc);
     mbar_init(&bar_afull, nc);
@@ -229,13 +243,18 @@ __global__ void __launch_bounds__(kNsThreads, 1)
     if (lane == 0) {
       const uint32_t id_sq = umma_idesc_bf16(128, 128);
       for (int it = 0; it < kNsSteps; ++it) {
-        if (!ns_wait<false>(&bar_xready, it & 1, a.err, &s_fail)) break;
-        tc_fence_after();
-        for (int j = 0; j < nbox; ++j) {  // P = X_r X_r^T
-          const uint64_t d = umma_desc_sw128(xs + j * kBox);
+        // P = X_r X_r^T, section by section as the epilogue finishes them
+        bool ok = true;
+        for (int sec = 0; sec < nsec && ok; ++sec) {
+          ok = ns_wait<false>(&bar_xsec[sec], it & 1, a.err, &s_fail);
+          tc_fence_after();
+          for (int j = sec * sb; j < (sec == 0 ? sb : nbox); ++j) {
+            const uint64_t d = umma_desc_sw128(xs + j * kBox);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) umma_bf16(tmem, d + 2 * k, d + 2 * k, id_sq, (j | k) != 0);
+            for (int k = 0; k < 4; ++k) umma_bf16(tmem, d + 2 * k, d + 2 * k, id_sq, (j | k) != 0);
+          }
         }
+        if (!ok) break;
         umma_commit(&bar_gram);
         // A is complete in this CTA (the epilogue has seen every exchange pass
         // of this step finish; waiting on the cluster barrier here could skip
@@ -250,8 +269,8 @@ __global__ void __launch_bounds__(kNsThreads, 1)
         umma_commit(&bar_sq);
         if (!ns_wait<false>(&bar_bready, it & 1, a.err, &s_fail)) break;
         tc_fence_after();
-        for (int n0 = 0; n0 < cs; n0 += 256) {  // B X_r
-          const int n = cs - n0 < 256 ? cs - n0 : 256;
+        for (int sec = 0; sec < nsec; ++sec) {  // B X_r, one section (at most 256 columns) at a time
+          const int n0 = 64 * sec * sb, n = 64 * (sec == 0 ? sb : nbox - sb);
           const uint32_t id = umma_idesc_bf16_bmn(128, n);
           const uint64_t bd = umma_desc_sw128_mn(xs + (n0 >> 6) * kBox, kBox);
 #pragma unroll
@@ -259,8 +278,8 @@ __global__ void __launch_bounds__(kNsThreads, 1)
             const uint64_t ad = umma_desc_sw128(ab + (s >> 2) * kBox) + 2 * (s & 3);
             umma_bf16(tmem + n0, ad, bd + (uint64_t)(128 * s), id, s != 0);  // +2048 B: 16 rows of X
           }
+          umma_commit(&bar_bx[sec]);
         }
-        umma_commit(&bar_bx);
       }
       umma_commit(&bar_fin);  // arrives once everything issued above has completed
       mbar_wait(&bar_fin, 0, a.err);
@@ -325,18 +344,29 @@ __global__ void __launch_bounds__(kNsThreads, 1)
     named_sync(kNsEpiBar, kNsEpiThreads);
     {
       const float inv = s_inv[row >> 6];
-      for (int ch = h * half_ch; ch < (h + 1) * half_ch; ++ch) {
-        uint4* p = reinterpret_cast<uint4*>(xs + (ch >> 3) * kBox + swz(row, ch & 7));
-        float f[8];
-        unpack8(*p, f);
+      for (int j = 0; j < nbox; ++j) {  // box j: this warp's rows, 32 columns
+        uint4* pch[4];
+        uint4 xv[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] *= inv;
-        *p = pack8(f);
+        for (int kk = 0; kk < 4; ++kk) {
+          pch[kk] = reinterpret_cast<uint4*>(xs + j * kBox + swz(row, 4 * h + kk));
+          xv[kk] = *pch[kk];
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          float f[8];
+          unpack8(xv[kk], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) f[i] *= inv;
+          *pch[kk] = pack8(f);
+        }
+        if (j == sb - 1 || j == nbox - 1) {  // end of a section
+          fence_proxy_async_cta();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_xsec[j == nbox - 1 ? nsec - 1 : 0]);
+        }
       }
     }
-    fence_proxy_async_cta();
-    named_sync(kNsEpiBar, kNsEpiThreads);
-    if (et == 0) mbar_arrive(&bar_xready);
 
     for (int it = 0; it < kNsSteps; ++it) {
       // ---- 1-2: Gram partial -> exchange -> A (bf16) in every CTA
@@ -344,11 +374,12 @@ __global__ void __launch_bounds__(kNsThreads, 1)
       tc_fence_after();
       for (int p = 0; p < npass; ++p) {
         {
-          float v[32];
-          tmem_ld32(trow + (uint32_t)((hd == 64 ? 64 * (q >> 1) : 64 * p) + 32 * h), v);
-          float4* er = reinterpret_cast<float4*>(E + row * kEStride + 32 * h);
+          uint32_t v[32];
+          tmem_ld32_issue(trow + (uint32_t)((hd == 64 ? 64 * (q >> 1) : 64 * p) + 32 * h), v);
+          tmem_wait_ld32(v);
+          uint4* er = reinterpret_cast<uint4*>(E + row * kEStride + 32 * h);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) er[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          for (int i = 0; i < 8; ++i) er[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
         fence_acq_rel_cluster();
         named_sync(kNsEpiBar, kNsEpiThreads);
@@ -372,19 +403,25 @@ __global__ void __launch_bounds__(kNsThreads, 1)
       // ---- 3-4: B = b A + c A A, in place of A
       ns_wait<false>(&bar_sq, it & 1, a.err, &s_fail);
       tc_fence_after();
-      {
-        float sq[64];
-        tmem_ld32(trow + (uint32_t)(128 + 64 * h), sq);
-        tmem_ld32(trow + (uint32_t)(128 + 64 * h + 32), sq + 32);
-        unsigned char* arow = ab + h * kBox;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {  // 32 columns of A A, and of A, at a time
+        uint32_t sq[32];
+        tmem_ld32_issue(trow + (uint32_t)(128 + 64 * h + 32 * half), sq);
+        uint4* pch[4];
+        uint4 av[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          uint4* pch = reinterpret_cast<uint4*>(arow + swz(row, k));
+        for (int k = 0; k < 4; ++k) {
+          pch[k] = reinterpret_cast<uint4*>(ab + h * kBox + swz(row, 4 * half + k));
+          av[k] = *pch[k];
+        }
+        tmem_wait_ld32(sq);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
           float f[8];
-          unpack8(*pch, f);
+          unpack8(av[k], f);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) f[i] = fmaf(kNsC, sq[8 * k + i], kNsB * f[i]);
-          *pch = pack8(f);
+          for (int i = 0; i < 8; ++i) f[i] = fmaf(kNsC, __uint_as_float(sq[8 * k + i]), kNsB * f[i]);
+          *pch[k] = pack8(f);
         }
       }
       tc_fence_before();
@@ -393,40 +430,52 @@ __global__ void __launch_bounds__(kNsThreads, 1)
       if (et == 0) mbar_arrive(&bar_bready);
 
       // ---- 5-6: X = a X + B X (after the last step: times the scale, then stored)
-      ns_wait<false>(&bar_bx, it & 1, a.err, &s_fail);
-      tc_fence_after();
       const bool last = it == kNsSteps - 1;
       const float fa = last ? a.scale * kNsA : kNsA, fd = last ? a.scale : 1.f;
-      auto update = [&](int c, const float* d) {  // 32 columns from c: a X + B X
+      // 32 columns from c: X = a X + B X. The TMEM load is issued first, the
+      // four shared-memory loads of X go out while it is in flight, and only
+      // then are the new values computed and stored.
+      auto update = [&](int c) {
+        uint32_t d[32];
+        tmem_ld32_issue(trow + (uint32_t)c, d);
+        uint4* pch[4];
+        uint4 xv[4];
         unsigned char* xb = xs + (c >> 6) * kBox;
         const int k0 = (c & 63) >> 3;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          uint4* pch = reinterpret_cast<uint4*>(xb + swz(row, k0 + kk));
-          float f[8];
-          unpack8(*pch, f);
+          pch[kk] = reinterpret_cast<uint4*>(xb + swz(row, k0 + kk));
+          xv[kk] = *pch[kk];
+        }
+        tmem_wait_ld32(d);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) f[i] = fmaf(fa, f[i], fd * d[8 * kk + i]);
-          *pch = pack8(f);
+        for (int kk = 0; kk < 4; ++kk) {
+          float f[8];
+          unpack8(xv[kk], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) f[i] = fmaf(fa, f[i], fd * __uint_as_float(d[8 * kk + i]));
+          *pch[kk] = pack8(f);
         }
       };
-      for (int c = h * (cs >> 1); c < (h + 1) * (cs >> 1); c += 32) {
-        float d[32];
-        tmem_ld32(trow + (uint32_t)c, d);
-        update(c, d);
-      }
-      tc_fence_before();
-      fence_proxy_async_cta();
-      named_sync(kNsEpiBar, kNsEpiThreads);
-      if (et == 0) {
-        if (!last) {
-          mbar_arrive(&bar_xready);
-        } else {
-          for (int j = 0; j < nbox; ++j)
-            tma_store_2d(&tmap_out, xs + j * kBox, (int)rank * cs + 64 * j, unit * kNsUnitRows);
-          bulk_commit();
-          bulk_wait_all();
+      for (int sec = 0; sec < nsec; ++sec) {
+        ns_wait<false>(&bar_bx[sec], it & 1, a.err, &s_fail);
+        tc_fence_after();
+        for (int j = sec * sb; j < (sec == 0 ? sb : nbox); ++j) {  // box j: this warp's rows, 32 columns
+          update(64 * j + 32 * h);
         }
+        tc_fence_before();
+        fence_proxy_async_cta();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_xsec[sec]);
+      }
+      if (last && et == 0) {  // store each section of the result as soon as every warp has written it
+        for (int sec = 0; sec < nsec; ++sec) {
+          ns_wait<false>(&bar_xsec[sec], kNsSteps & 1, a.err, &s_fail);
+          for (int j = sec * sb; j < (sec == 0 ? sb : nbox); ++j)
+            tma_store_2d(&tmap_out, xs + j * kBox, (int)rank * cs + 64 * j, unit * kNsUnitRows);
+        }
+        bulk_commit();
+        bulk_wait_all();
       }
     }
   }

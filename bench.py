@@ -601,9 +601,11 @@ class NewtonSchulzStep(_Step):
         self.C.qkv_newton_schulz(self.L, self.cols, getattr(self, f"m{layer}"), getattr(self, f"o{layer}"), 0,
                                  self.stream)
 
-    def comparison(self, reps=10):
+    def comparison(self, reps=20):
         """The published bf16 iteration in plain PyTorch, batched over the head
-        blocks of one layer (cuBLAS batched GEMMs + element-wise kernels)."""
+        blocks of one layer (cuBLAS batched GEMMs + element-wise kernels),
+        captured in a CUDA graph so that the host's launch rate does not enter
+        (eager, each of its ~25 launches costs ~30 us of host time here)."""
         import torch
 
         X0 = self.m0.view(-1, self.hd, self.cols)
@@ -616,15 +618,24 @@ class NewtonSchulzStep(_Step):
                 X = 3.4445 * X + B @ X
             return X
 
-        for _ in range(3):
+        side = torch.cuda.Stream(self.dev)
+        side.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                run()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
             run()
+        for _ in range(3):
+            g.replay()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         for _ in range(reps):
-            run()
+            g.replay()
         b.record()
         torch.cuda.synchronize()
-        return {"torch_bf16_batched_iteration_us_per_layer": round(a.elapsed_time(b) * 1e3 / reps, 2)}
+        return {"torch_bf16_batched_iteration_graph_us_per_layer": round(a.elapsed_time(b) * 1e3 / reps, 2)}
 
 
 def mla_two_stream_overlap(dev, T, layers=3, reps=20):
@@ -994,7 +1005,8 @@ def run_ours(args):
         tpeak, tsrc = measured_bf16_tflops()
         out["roofline"] = {"kernel": dom_name, "bound": "tensor", "achieved": round(tflops, 1), "peak": tpeak,
                            "peak_source": f"{tsrc} (MEASURED_PEAKS.json bf16_tflops, burst: the call is timed alone)",
-                           "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4), "traffic": None}
+                           "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
+                           "traffic": traffic_from_profile(f"{args.workload}:{dom}")}
         if hasattr(ws, "unfused_us"):
             unf, gemm_only = ws.unfused_us()
             out["unfused_cublas_projection_plus_prologue_us"] = round(unf, 2)

@@ -385,7 +385,9 @@ QKVP_API int qkv_newton_schulz_plan(const qkvp_layout* layout, int64_t cols, int
  * library's device error word on the current device. Bit 1 means a
  * pipelined kernel's bounded wait on its shared-memory pipeline gave up
  * (after 2 s) and the kernel returned early: the results of that launch are
- * invalid. Synchronises with the device (it copies the word to the host).
+ * invalid. Bit 2 means a kernel that needs an explicit thread-block cluster
+ * launch (qkv_newton_schulz) found none and did nothing. Synchronises with the
+ * device (it copies the word to the host).
  * ------------------------------------------------------------------------- */
 QKVP_API int qkv_prologue_device_error(int clear, int* value);
 

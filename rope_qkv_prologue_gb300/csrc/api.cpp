@@ -190,9 +190,11 @@ int launch(const void* kernel, int64_t grid, int threads, size_t smem, cudaStrea
 }
 
 // Launch with several kernel parameters (same attributes as launch()), in
-// clusters of `cluster` CTAs along x when cluster > 1.
+// clusters of `cluster` CTAs along x when cluster > 1, or always when
+// explicit_cluster (a kernel that uses cluster-only instructions such as
+// st.async needs an explicit cluster launch even for one CTA).
 int launch_args(const void* kernel, int64_t grid, int threads, size_t smem, cudaStream_t s, void** args,
-                int cluster = 1, bool pdl = true) {
+                int cluster = 1, bool pdl = true, bool explicit_cluster = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(threads);
@@ -204,7 +206,7 @@ int launch_args(const void* kernel, int64_t grid, int threads, size_t smem, cuda
     attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n_attr++].val.programmaticStreamSerializationAllowed = 1;
   }
-  if (cluster > 1) {
+  if (cluster > 1 || explicit_cluster) {
     attr[n_attr].id = cudaLaunchAttributeClusterDimension;
     attr[n_attr].val.clusterDim.x = (unsigned)cluster;
     attr[n_attr].val.clusterDim.y = 1;
@@ -1095,7 +1097,7 @@ int qkv_newton_schulz(const qkvp_layout* layout, int64_t cols, const void* m, vo
   if ((a.err = device_error_word()) == nullptr) return QKVP_ERR_LAUNCH;
   void* args[] = {&tm, &to, &a};
   return launch_args(ns_kernel(), units * nc, ns_threads(), smem, static_cast<cudaStream_t>(stream), args, nc,
-                     false);
+                     false, true);
 }
 
 int qkv_newton_schulz_plan(const qkvp_layout* layout, int64_t cols, int32_t cluster, int32_t* cluster_out,

@@ -17,11 +17,14 @@
 // for the whole iteration (bf16, 128-byte-swizzled boxes of 64 columns, loaded
 // once by TMA). Each step:
 //   1. Gram partial P_r = X_r X_r^T: tcgen05, K = cs, into TMEM columns 0-127.
-//   2. A = sum over the cluster of P_r: every CTA copies 64 columns of its
-//      partial to an fp32 exchange buffer; CTA r sums rows
-//      [128 r / nc, 128 (r + 1) / nc) of all buffers through distributed
-//      shared memory, rounds them to bf16 and writes them into the A tile of
-//      every CTA of the cluster.
+//   2. A = sum over the cluster of P_r: every thread pushes its row's 64
+//      columns of the partial (straight from TMEM via registers) to the CTA
+//      that owns the row (CTA r owns rows [128 r / nc, 128 (r + 1) / nc)),
+//      with st.async into that CTA's receive buffer, counted in bytes on its
+//      mbarrier; the owner sums the nc partials of its rows in rank order,
+//      rounds them to bf16 and pushes them the same way into the A tile of
+//      every CTA of the cluster. No remote loads, no fences, no barrier
+//      round trips: each CTA arms its two barriers with the bytes it expects.
 //   3. A A: tcgen05, K = 128, into TMEM columns 128-255 (TMEM: 256 columns
 //      when cs <= 256, else 512; the three products reuse the same columns
 //      one after the other).
@@ -57,8 +60,9 @@ namespace {
 
 constexpr int kNsThreads = 320, kNsEpiThreads = 256, kNsEpiBar = 1;
 constexpr int kBox = kNsUnitRows * 128;  // bytes of one 128-row x 64-column bf16 box
-constexpr int kEStride = 68;             // floats per exchange row: 64 + 4 (conflict-free float4 rows)
-constexpr int kEBytes = kNsUnitRows * kEStride * 4;
+// Receive buffer of a row owner: nc slots of ceil(128 / nc) rows x 64 fp32
+// columns; nc ceil(128 / nc) is at most 140 (nc = 14) for nc <= 16.
+constexpr int kRecvBytes = 140 * 64 * 4;
 constexpr float kNsA = 3.4445f, kNsB = -4.7750f, kNsC = 2.0315f;
 constexpr int kNsSteps = 5;
 
@@ -90,87 +94,6 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Step 2 of the exchange, run by every epilogue thread of CTA `rank`: the rows
-// [128 rank / nc, 128 (rank + 1) / nc) of the Gram, 64 columns (pass p), as
-// float4 items; each item is summed over the exchange buffers of all CTAs in
-// rank order (the same sums in every CTA) and written, rounded to bf16, into
-// the A tile of every CTA of the cluster. NC > 0 fixes the cluster size at
-// compile time so that all of a thread's remote loads are in flight together
-// (2048 / NC items over 256 threads: 8 loads per thread); NC = 0 takes nc at
-// run time, one item at a time.
-template <int NC>
-__device__ __forceinline__ void reduce_rows(const float* E, unsigned char* ab, int hd, int p, uint32_t nc,
-                                            uint32_t rank, int et) {
-  const int r0 = (int)(kNsUnitRows * rank / nc), r1 = (int)(kNsUnitRows * (rank + 1) / nc);
-  const int n = (r1 - r0) * 16;
-  auto item_src = [&](int idx) { return E + (r0 + (idx >> 4)) * kEStride + 4 * (idx & 15); };
-  auto put = [&](int idx, const float4& s) {
-    const int i = r0 + (idx >> 4);
-    const int col = (hd == 64 ? 64 * (i >> 6) : 64 * p) + 4 * (idx & 15);
-    unsigned char* d = ab + (col >> 6) * kBox + swz(i, (col & 63) >> 3) + (col & 7) * 2;
-    const uint32_t lo = pack2(s.x, s.y), hi = pack2(s.z, s.w);
-    if (NC == 1) {
-      *reinterpret_cast<uint2*>(d) = make_uint2(lo, hi);
-    } else {
-      for (uint32_t r = 0; r < nc; ++r) st_cluster_u2(cluster_map(smem_addr(d), r), lo, hi);
-    }
-  };
-  auto add = [](float4& s, const float4& t) {
-    s.x += t.x;
-    s.y += t.y;
-    s.z += t.z;
-    s.w += t.w;
-  };
-  if constexpr (NC > 0) {
-    constexpr int kItems = 8 / NC;
-    float4 t[kItems][NC];
-#pragma unroll
-    for (int j = 0; j < kItems; ++j) {
-      const int idx = et + kNsEpiThreads * j;
-      if (idx < n) {
-        if (NC == 1) {
-          t[j][0] = *reinterpret_cast<const float4*>(item_src(idx));
-        } else {
-          const uint32_t src = smem_addr(item_src(idx));
-#pragma unroll
-          for (int r = 0; r < NC; ++r) t[j][r] = ld_cluster_f4(cluster_map(src, (uint32_t)r));
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kItems; ++j) {
-      const int idx = et + kNsEpiThreads * j;
-      if (idx < n) {
-        float4 s = t[j][0];
-#pragma unroll
-        for (int r = 1; r < NC; ++r) add(s, t[j][r]);
-        put(idx, s);
-      }
-    }
-  } else {
-    for (int idx = et; idx < n; idx += kNsEpiThreads) {
-      const uint32_t src = smem_addr(item_src(idx));
-      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (uint32_t rb = 0; rb < nc; rb += 8) {  // eight remote loads in flight at a time
-        float4 t[8];
-#pragma unroll
-        for (uint32_t k = 0; k < 8; ++k)
-          if (rb + k < nc) t[k] = ld_cluster_f4(cluster_map(src, rb + k));
-#pragma unroll
-        for (uint32_t k = 0; k < 8; ++k) {
-          if (rb + k < nc) {
-            if (rb + k == 0)
-              s = t[k];
-            else
-              add(s, t[k]);
-          }
-        }
-      }
-      put(idx, s);
-    }
-  }
-}
-
 }  // namespace
 
 __global__ void __launch_bounds__(kNsThreads, 1)
@@ -187,7 +110,12 @@ __global__ void __launch_bounds__(kNsThreads, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_fail;
   __shared__ float s_red[8], s_inv[2];
+  __shared__ __align__(16) float2 s_nrecv[kNsMaxCluster];  // the cluster's block-norm partials
 
+  if (!is_explicit_cluster()) {  // the exchange needs a cluster launch (the host always makes one)
+    if (threadIdx.x == 0) atomicOr(a.err, kErrNotCluster);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t nc = (uint32_t)a.nc, rank = cluster_ctarank();
   const int unit = blockIdx.x / a.nc;
@@ -203,7 +131,9 @@ __global__ void __launch_bounds__(kNsThreads, 1)
   // step's update (phase it + 1); the Gram of step it waits phase it.
   unsigned char* xs = smem;                 // nbox boxes: this CTA's columns of the unit
   unsigned char* ab = smem + nbox * kBox;   // 2 boxes: A, then B in place (128 x 128)
-  float* E = reinterpret_cast<float*>(ab + 2 * kBox);  // fp32 exchange, 128 rows x kEStride
+  float* R = reinterpret_cast<float*>(ab + 2 * kBox);  // receive buffer: [nc][rmax][64] fp32
+  const int rmax = (kNsUnitRows + a.nc - 1) / a.nc;
+  const int r0 = (int)(kNsUnitRows * rank / nc), r1 = (int)(kNsUnitRows * (rank + 1) / nc);  // rows owned
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_load, 1);
@@ -216,8 +146,8 @@ __global__ void __launch_bounds__(kNsThreads, 1)
     mbar_init(&bar_sq, 1);
     mbar_init(&bar_bready, 1);
     mbar_init(&bar_fin, 1);
-    mbar_init(&bar_efull, nc);
-    mbar_init(&bar_afull, nc);
+    mbar_init(&bar_efull, 1);  // armed once per phase by this CTA, completed by bytes from the cluster
+    mbar_init(&bar_afull, 1);
     s_fail = 0;
     mbar_init_fence();
   }
@@ -261,6 +191,7 @@ __global__ void __launch_bounds__(kNsThreads, 1)
         // a phase when a step has two passes)
         if (!ns_wait<false>(&bar_aready, it & 1, a.err, &s_fail)) break;
         tc_fence_after();
+        fence_proxy_async_cta();  // A arrived by st.async (generic proxy); the MMA reads it
         for (int j = 0; j < 2; ++j) {  // A A (A is symmetric: both operands are its rows)
           const uint64_t d = umma_desc_sw128(ab + j * kBox);
 #pragma unroll
@@ -305,31 +236,24 @@ __global__ void __launch_bounds__(kNsThreads, 1)
     if (lane == 0) s_red[warp - 2] = ss;
     named_sync(kNsEpiBar, kNsEpiThreads);
     if (warp == 2) {  // the cluster exchange of the block norms: lane r talks to CTA r
-      if (lane == 0) {
-        float lo = 0.f, hi = 0.f;  // rows 0-63, rows 64-127 of this CTA's columns
-        for (int i = 0; i < 8; ++i) {
-          if (((i + 2) & 3) < 2)
-            lo += s_red[i];
-          else
-            hi += s_red[i];
-        }
-        E[0] = lo;
-        E[1] = hi;
-        fence_acq_rel_cluster();
+      float lo = 0.f, hi = 0.f;  // rows 0-63, rows 64-127 of this CTA's columns
+      for (int i = 0; i < 8; ++i) {
+        if (((i + 2) & 3) < 2)
+          lo += s_red[i];
+        else
+          hi += s_red[i];
       }
-      __syncwarp();
-      if ((uint32_t)lane < nc) mbar_arrive_cluster(cluster_map(efull, lane));
+      if (lane == 0) mbar_arrive_expect_tx(&bar_efull, 8u * nc);
+      if ((uint32_t)lane < nc)
+        st_async_u2(cluster_map(smem_addr(&s_nrecv[rank]), lane), __float_as_uint(lo), __float_as_uint(hi),
+                    cluster_map(efull, lane));
       float tlo = 0.f, thi = 0.f;
       if (ns_wait<true>(&bar_efull, pass & 1, a.err, &s_fail) && (uint32_t)lane < nc) {
-        const float4 v = ld_cluster_f4(cluster_map(smem_addr(E), lane));
-        tlo = v.x;
-        thi = v.y;
+        tlo = s_nrecv[lane].x;
+        thi = s_nrecv[lane].y;
       }
       tlo = warp_sum(tlo);  // the same order in every CTA of the cluster
       thi = warp_sum(thi);
-      fence_acq_rel_cluster();
-      __syncwarp();
-      if ((uint32_t)lane < nc) mbar_arrive_cluster(cluster_map(afull, lane));
       if (lane == 0) {
         if (hd == 64) {
           s_inv[0] = 1.f / (sqrtf(tlo) + a.eps);
@@ -338,9 +262,9 @@ __global__ void __launch_bounds__(kNsThreads, 1)
           s_inv[0] = s_inv[1] = 1.f / (sqrtf(tlo + thi) + a.eps);
         }
       }
-      ns_wait<true>(&bar_afull, pass & 1, a.err, &s_fail);  // every CTA has read this E
     }
-    ++pass;
+    ++pass;  // bar_efull: phase 0 was the norms; bar_afull starts with the first Gram
+    uint32_t apass = 0;
     named_sync(kNsEpiBar, kNsEpiThreads);
     {
       const float inv = s_inv[row >> 6];
@@ -373,30 +297,47 @@ __global__ void __launch_bounds__(kNsThreads, 1)
       ns_wait<false>(&bar_gram, it & 1, a.err, &s_fail);
       tc_fence_after();
       for (int p = 0; p < npass; ++p) {
-        {
+        if (et == 0) {  // the bytes this CTA receives in this pass
+          mbar_arrive_expect_tx(&bar_efull, (uint32_t)(nc * (r1 - r0) * 256));
+          mbar_arrive_expect_tx(&bar_afull, (uint32_t)(kNsUnitRows * 64 * 2));
+        }
+        {  // push this row's 32 columns of the partial to the row's owner
           uint32_t v[32];
           tmem_ld32_issue(trow + (uint32_t)((hd == 64 ? 64 * (q >> 1) : 64 * p) + 32 * h), v);
+          const uint32_t o = (uint32_t)(((row + 1) * (int)nc - 1) / kNsUnitRows);  // owner of this row
+          const int lo_row = (int)(kNsUnitRows * o / nc);
+          const uint32_t dst = cluster_map(smem_addr(R + ((int)rank * rmax + row - lo_row) * 64 + 32 * h), o);
+          const uint32_t bar = cluster_map(efull, o);
           tmem_wait_ld32(v);
-          uint4* er = reinterpret_cast<uint4*>(E + row * kEStride + 32 * h);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) er[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          for (int i = 0; i < 8; ++i)
+            st_async_f4(dst + 16 * i,
+                        make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                    __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])),
+                        bar);
         }
-        fence_acq_rel_cluster();
-        named_sync(kNsEpiBar, kNsEpiThreads);
-        if (et < (int)nc) mbar_arrive_cluster(cluster_map(efull, (uint32_t)et));  // one lane per CTA
         ns_wait<true>(&bar_efull, pass & 1, a.err, &s_fail);
-        switch (nc) {  // all the remote loads of a thread in flight at once
-          case 1: reduce_rows<1>(E, ab, hd, p, nc, rank, et); break;
-          case 2: reduce_rows<2>(E, ab, hd, p, nc, rank, et); break;
-          case 4: reduce_rows<4>(E, ab, hd, p, nc, rank, et); break;
-          default: reduce_rows<0>(E, ab, hd, p, nc, rank, et); break;
+        // this CTA's rows: the nc partials summed in rank order, then pushed as
+        // bf16 into the A tile of every CTA of the cluster
+        for (int idx = et; idx < (r1 - r0) * 16; idx += kNsEpiThreads) {
+          const int li = idx >> 4, c4 = idx & 15, i = r0 + li;
+          const float* src = R + li * 64 + 4 * c4;
+          float4 s4 = *reinterpret_cast<const float4*>(src);
+          for (uint32_t r = 1; r < nc; ++r) {
+            const float4 t = *reinterpret_cast<const float4*>(src + (int)r * rmax * 64);
+            s4.x += t.x;
+            s4.y += t.y;
+            s4.z += t.z;
+            s4.w += t.w;
+          }
+          const int col = (hd == 64 ? 64 * (i >> 6) : 64 * p) + 4 * c4;
+          const uint32_t d = smem_addr(ab + (col >> 6) * kBox + swz(i, (col & 63) >> 3) + (col & 7) * 2);
+          const uint32_t lo = pack2(s4.x, s4.y), hi2 = pack2(s4.z, s4.w);
+          for (uint32_t r = 0; r < nc; ++r) st_async_u2(cluster_map(d, r), lo, hi2, cluster_map(afull, r));
         }
-        fence_proxy_async_cluster();
-        fence_acq_rel_cluster();
-        named_sync(kNsEpiBar, kNsEpiThreads);
-        if (et < (int)nc) mbar_arrive_cluster(cluster_map(afull, (uint32_t)et));
-        ns_wait<true>(&bar_afull, pass & 1, a.err, &s_fail);  // A complete; every CTA has read this E
+        ns_wait<true>(&bar_afull, apass & 1, a.err, &s_fail);  // A complete in this CTA
         ++pass;
+        ++apass;
       }
       if (et == 0) mbar_arrive(&bar_aready);
 
@@ -489,7 +430,7 @@ __global__ void __launch_bounds__(kNsThreads, 1)
 
 const void* ns_kernel() { return reinterpret_cast<const void*>(&qkvp_newton_schulz_kernel); }
 int ns_smem_bytes(int cs) {
-  const int need = (cs / 64) * kBox + 2 * kBox + kEBytes + 1024;
+  const int need = (cs / 64) * kBox + 2 * kBox + kRecvBytes + 1024;
   // 228 KiB per SM, 1 KiB reserved per CTA: 118 KiB admits one CTA per SM,
   // 78 KiB at most two
   const int floor = ns_tmem_cols(cs) == 512 ? 118 * 1024 : 78 * 1024;

@@ -40,6 +40,14 @@ __device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorM
       : "memory");
 }
 
+// True when the grid was launched with an explicit thread-block cluster
+// (required by st.async, even for a cluster of one CTA).
+__device__ __forceinline__ bool is_explicit_cluster() {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred p;\n\tmov.pred p, %%is_explicit_cluster;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(r));
+  return r != 0;
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -262,6 +270,22 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
       : "r"(smem_addr(bar)), "r"(parity)
       : "memory");
   return done != 0;
+}
+
+// Asynchronous store into shared memory of a CTA of this cluster (cluster
+// address `addr`), its bytes counted on that CTA's mbarrier at cluster address
+// `bar` (complete_tx: the receiver arms the barrier with the bytes it expects
+// and waits; the data is visible to it once the phase completes).
+__device__ __forceinline__ void st_async_f4(uint32_t addr, const float4& v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_async_u2(uint32_t addr, uint32_t lo, uint32_t hi, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+               "r"(lo), "r"(hi), "r"(bar)
+               : "memory");
 }
 
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }

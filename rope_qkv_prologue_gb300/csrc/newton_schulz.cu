@@ -276,13 +276,14 @@ __global__ void __launch_bounds__(kNsThreads, 1)
           pch[kk] = reinterpret_cast<uint4*>(xs + j * kBox + swz(row, 4 * h + kk));
           xv[kk] = *pch[kk];
         }
+        const float2 inv2 = f2(inv, inv);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          float f[8];
-          unpack8(xv[kk], f);
+          float2 x2[4];
+          unpack_pairs(xv[kk], x2);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) f[i] *= inv;
-          *pch[kk] = pack8(f);
+          for (int i = 0; i < 4; ++i) x2[i] = __fmul2_rn(x2[i], inv2);
+          *pch[kk] = pack_pairs(x2);
         }
         if (j == sb - 1 || j == nbox - 1) {  // end of a section
           fence_proxy_async_cta();
@@ -356,13 +357,16 @@ __global__ void __launch_bounds__(kNsThreads, 1)
           av[k] = *pch[k];
         }
         tmem_wait_ld32(sq);
+        const float2 b2 = f2(kNsB, kNsB), c2 = f2(kNsC, kNsC);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float f[8];
-          unpack8(av[k], f);
+        for (int k = 0; k < 4; ++k) {  // on pairs: c (A A) + b A
+          float2 a2[4];
+          unpack_pairs(av[k], a2);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) f[i] = fmaf(kNsC, __uint_as_float(sq[8 * k + i]), kNsB * f[i]);
-          *pch[k] = pack8(f);
+          for (int i = 0; i < 4; ++i)
+            a2[i] = __ffma2_rn(c2, f2(__uint_as_float(sq[8 * k + 2 * i]), __uint_as_float(sq[8 * k + 2 * i + 1])),
+                               __fmul2_rn(b2, a2[i]));
+          *pch[k] = pack_pairs(a2);
         }
       }
       tc_fence_before();
@@ -373,6 +377,7 @@ __global__ void __launch_bounds__(kNsThreads, 1)
       // ---- 5-6: X = a X + B X (after the last step: times the scale, then stored)
       const bool last = it == kNsSteps - 1;
       const float fa = last ? a.scale * kNsA : kNsA, fd = last ? a.scale : 1.f;
+      const float2 fa2 = f2(fa, fa), fd2 = f2(fd, fd);
       // 32 columns from c: X = a X + B X. The TMEM load is issued first, the
       // four shared-memory loads of X go out while it is in flight, and only
       // then are the new values computed and stored.
@@ -390,12 +395,16 @@ __global__ void __launch_bounds__(kNsThreads, 1)
         }
         tmem_wait_ld32(d);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          float f[8];
-          unpack8(xv[kk], f);
+        for (int kk = 0; kk < 4; ++kk) {  // on pairs: a x + d (a x + s d after the last step)
+          float2 x2[4];
+          unpack_pairs(xv[kk], x2);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) f[i] = fmaf(fa, f[i], fd * __uint_as_float(d[8 * kk + i]));
-          *pch[kk] = pack8(f);
+          for (int i = 0; i < 4; ++i) {
+            float2 d2 = f2(__uint_as_float(d[8 * kk + 2 * i]), __uint_as_float(d[8 * kk + 2 * i + 1]));
+            if (last) d2 = __fmul2_rn(fd2, d2);
+            x2[i] = __ffma2_rn(fa2, x2[i], d2);
+          }
+          *pch[kk] = pack_pairs(x2);
         }
       };
       for (int sec = 0; sec < nsec; ++sec) {

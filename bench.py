@@ -555,12 +555,13 @@ class GemmStep(_Step):
 
 
 class NewtonSchulzStep(_Step):
-    """Per-head Newton-Schulz of fused QKV weight updates (tcgen05 tensor cores),
-    one C-ABI call per layer ("[muon] Per-head Newton-Schulz for fused QKV
-    projections"). `newton_schulz`: the Muse Spark fused weight [10240, 5120]
-    (16 kv groups x (8 q + k + v) heads of 64; hidden 5120 stands in for the
-    model's); `newton_schulz_page`: the page's 17M-parameter model, 6 layers of
-    [768, 512] (8 q heads over 2 kv heads of 64, hidden 512)."""
+    """Per-head Newton-Schulz of fused QKV weight updates (tcgen05 tensor cores)
+    ("[muon] Per-head Newton-Schulz for fused QKV projections"). `newton_schulz`:
+    the Muse Spark fused weight [10240, 5120] (16 kv groups x (8 q + k + v) heads
+    of 64; hidden 5120 stands in for the model's); `newton_schulz_page`: the
+    page's 17M-parameter model, 6 layers of [768, 512] (8 q heads over 2 kv heads
+    of 64, hidden 512), all layers' updates stacked and done in one launch, as an
+    optimizer step does them."""
 
     def __init__(self, dev, name):
         import types
@@ -574,41 +575,37 @@ class NewtonSchulzStep(_Step):
         self.c, self.layers = c, c["layers"]
         self.n_q, self.n_kv, self.hd, self.cols = c["n_q"], c["n_kv"], c["head_dim"], c["cols"]
         self.rows = (self.n_q + 2 * self.n_kv) * self.hd
-        self.T = self.rows
+        self.T = self.rows * self.layers
         self.wl = types.SimpleNamespace(n_q=self.n_q, n_kv=self.n_kv, head_dim=self.hd)
         self.L = self.C.layout("interleaved", self.n_q, self.n_kv, self.hd)
-        h_in = {}
-        for layer in range(self.layers):
-            m = workloads.fused_qkv_update(self.n_q, self.n_kv, self.hd, self.cols, seed=200 + layer)
-            h_in[f"m{layer}"] = m
-            setattr(self, f"m{layer}", m.to(dev))
-            setattr(self, f"o{layer}", torch.empty(self.rows, self.cols, **self.bf))
-        self.h_in = h_in
-        self.out_names = tuple(f"o{layer}" for layer in range(self.layers))
-        blocks = self.rows // self.hd
-        # per call: 5 steps of X X^T, A A and B X on every head block
+        m = torch.stack([workloads.fused_qkv_update(self.n_q, self.n_kv, self.hd, self.cols, seed=200 + layer)
+                         for layer in range(self.layers)])
+        self.h_in = {"m": m}
+        self.m = m.to(dev)
+        self.o = torch.empty_like(self.m)
+        self.out_names = ("o",)
+        blocks = self.rows // self.hd * self.layers
+        # per call: 5 steps of X X^T, A A and B X on every head block of every layer
         self.flops = blocks * 5 * (4 * self.hd * self.hd * self.cols + 2 * self.hd ** 3)
-        io = 2 * self.rows * self.cols * 2
-        self.calls = [(f"qkv_newton_schulz layer {layer} (qkvp_newton_schulz_kernel: tcgen05, cluster-split columns)",
-                       (lambda layer=layer: self.ns(layer)), io) for layer in range(self.layers)]
-        self.kernels_per_step = self.layers
-        nc, grid = self.C.qkv_newton_schulz_plan(self.L, self.cols)
+        io = 2 * self.layers * self.rows * self.cols * 2
+        what = "qkv_newton_schulz_batch" if self.layers > 1 else "qkv_newton_schulz"
+        self.calls = [(f"{what} (qkvp_newton_schulz_kernel: tcgen05, cluster-split columns)", self.ns, io)]
+        nc, grid = self.C.qkv_newton_schulz_plan(self.L, self.cols, count=self.layers)
         self.describe = (f"per-head Newton-Schulz (Muon quintic, 5 steps) of {self.layers} fused QKV update(s) "
-                         f"[{self.rows}, {self.cols}] bf16, {blocks} head blocks of {self.hd} rows each; "
+                         f"[{self.rows}, {self.cols}] bf16 in one launch, {blocks} head blocks of {self.hd} rows; "
                          f"clusters of {nc} CTAs, grid {grid}")
 
-    def ns(self, layer):
-        self.C.qkv_newton_schulz(self.L, self.cols, getattr(self, f"m{layer}"), getattr(self, f"o{layer}"), 0,
-                                 self.stream)
+    def ns(self):
+        self.C.qkv_newton_schulz_batch(self.L, self.layers, self.cols, self.m, self.o, 0, self.stream)
 
     def comparison(self, reps=20):
         """The published bf16 iteration in plain PyTorch, batched over the head
-        blocks of one layer (cuBLAS batched GEMMs + element-wise kernels),
+        blocks of all layers (cuBLAS batched GEMMs + element-wise kernels),
         captured in a CUDA graph so that the host's launch rate does not enter
         (eager, each of its ~25 launches costs ~30 us of host time here)."""
         import torch
 
-        X0 = self.m0.view(-1, self.hd, self.cols)
+        X0 = self.m.view(-1, self.hd, self.cols)  # every head block of every layer in one batch
 
         def run():
             X = X0 / (X0.norm(dim=(-2, -1), keepdim=True) + 1e-7)
@@ -635,7 +632,7 @@ class NewtonSchulzStep(_Step):
             g.replay()
         b.record()
         torch.cuda.synchronize()
-        return {"torch_bf16_batched_iteration_graph_us_per_layer": round(a.elapsed_time(b) * 1e3 / reps, 2)}
+        return {"torch_bf16_batched_iteration_graph_us_per_step": round(a.elapsed_time(b) * 1e3 / reps, 2)}
 
 
 def mla_two_stream_overlap(dev, T, layers=3, reps=20):

@@ -375,9 +375,18 @@ QKVP_API int qkv_prologue_gemm_fwd(const qkvp_layout* layout, int64_t T, int32_t
 QKVP_API int qkv_newton_schulz(const qkvp_layout* layout, int64_t cols, const void* m, void* out,
                                int32_t cluster, void* stream);
 
-/* The cluster size and grid qkv_newton_schulz would use for these arguments
- * (host only, nothing is launched). */
-QKVP_API int qkv_newton_schulz_plan(const qkvp_layout* layout, int64_t cols, int32_t cluster,
+/* The same for `count` fused updates of one shape stacked along dim 0
+ * (m and out: bf16 [count, rows, cols], contiguous), in one launch: the
+ * optimizer step of every layer at once. Head blocks are independent and the
+ * factor depends only on head_dim and cols, so the stack is one taller weight
+ * of count * (n_q + 2 n_kv) blocks. count 0 enqueues nothing; otherwise as
+ * qkv_newton_schulz (count * rows at most 2^30). */
+QKVP_API int qkv_newton_schulz_batch(const qkvp_layout* layout, int64_t count, int64_t cols, const void* m,
+                                     void* out, int32_t cluster, void* stream);
+
+/* The cluster size and grid qkv_newton_schulz_batch would use for these
+ * arguments (host only, nothing is launched; count 0 gives 0, 0). */
+QKVP_API int qkv_newton_schulz_plan(const qkvp_layout* layout, int64_t count, int64_t cols, int32_t cluster,
                                     int32_t* cluster_out, int32_t* grid_out);
 
 /* ---------------------------------------------------------------------------

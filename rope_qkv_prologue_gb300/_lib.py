@@ -103,8 +103,9 @@ _SIGS = {
     "qkv_prologue_gemm_fwd": ([_LP, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _f32, _f64, _u32, _vp, _vp, _vp, _vp, _vp,
                                _vp], ctypes.c_int),
     "qkv_newton_schulz": ([_LP, _i64, _vp, _vp, _i32, _vp], ctypes.c_int),
-    "qkv_newton_schulz_plan": ([_LP, _i64, _i32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
-                               ctypes.c_int),
+    "qkv_newton_schulz_batch": ([_LP, _i64, _i64, _vp, _vp, _i32, _vp], ctypes.c_int),
+    "qkv_newton_schulz_plan": ([_LP, _i64, _i64, _i32, ctypes.POINTER(ctypes.c_int32),
+                                ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
     "qkv_prologue_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "qkv_prologue_version": ([], ctypes.c_int),
     "qkv_prologue_device_error": ([ctypes.c_int, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
@@ -276,9 +277,16 @@ def qkv_newton_schulz(L, cols, m, out, cluster=0, stream=None, check=True):
     return _ret(st, "qkv_newton_schulz", check)
 
 
-def qkv_newton_schulz_plan(L, cols, cluster=0):
+def qkv_newton_schulz_batch(L, count, cols, m, out, cluster=0, stream=None, check=True):
+    st = _lib.qkv_newton_schulz_batch(ctypes.byref(L), int(count), int(cols), _ptr(m), _ptr(out), int(cluster),
+                                      _stream(stream))
+    return _ret(st, "qkv_newton_schulz_batch", check)
+
+
+def qkv_newton_schulz_plan(L, cols, cluster=0, count=1):
     """(cluster size, grid) the library would launch for these arguments."""
     c, g = ctypes.c_int32(0), ctypes.c_int32(0)
-    st = _lib.qkv_newton_schulz_plan(ctypes.byref(L), int(cols), int(cluster), ctypes.byref(c), ctypes.byref(g))
+    st = _lib.qkv_newton_schulz_plan(ctypes.byref(L), int(count), int(cols), int(cluster), ctypes.byref(c),
+                                     ctypes.byref(g))
     _ret(st, "qkv_newton_schulz_plan", True)
     return c.value, g.value

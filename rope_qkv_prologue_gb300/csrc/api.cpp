@@ -521,13 +521,15 @@ int ns_plan(int64_t units, int64_t cols, int want, size_t* smem) {
   return nc;
 }
 
-// Shape checks shared by qkv_newton_schulz and qkv_newton_schulz_plan.
-int check_ns(const qkvp_layout* layout, int64_t cols, int32_t cluster, int64_t* rows) {
+// Shape checks shared by the Newton-Schulz entry points; *rows = the rows of
+// `count` fused weights stacked along dim 0.
+int check_ns(const qkvp_layout* layout, int64_t count, int64_t cols, int32_t cluster, int64_t* rows) {
   if (!layout) return QKVP_ERR_NULL;
   if (layout->kind != QKVP_INTERLEAVED && layout->kind != QKVP_SECTIONED) return QKVP_ERR_SHAPE;
   if (layout->n_q <= 0 || layout->n_kv <= 0 || layout->n_q % layout->n_kv) return QKVP_ERR_SHAPE;
   if (layout->head_dim != 64 && layout->head_dim != 128) return QKVP_ERR_SHAPE;
-  *rows = ((int64_t)layout->n_q + 2 * (int64_t)layout->n_kv) * layout->head_dim;
+  if (count < 0 || count > (1 << 20)) return QKVP_ERR_SHAPE;
+  *rows = ((int64_t)layout->n_q + 2 * (int64_t)layout->n_kv) * layout->head_dim * count;
   if (*rows > (1 << 30)) return QKVP_ERR_SHAPE;
   if (cols < 64 || cols % 64 != 0 || cols > (int64_t)kNsMaxCluster * kNsMaxSliceCols) return QKVP_ERR_SHAPE;
   const int boxes = (int)(cols / 64);
@@ -1064,16 +1066,17 @@ int qkv_prologue_gemm_fwd(const qkvp_layout* layout, int64_t T, int32_t hidden, 
   return launch_args(kern, grid, threads, smem, static_cast<cudaStream_t>(stream), args, 2);
 }
 
-int qkv_newton_schulz(const qkvp_layout* layout, int64_t cols, const void* m, void* out, int32_t cluster,
-                      void* stream) {
+int qkv_newton_schulz_batch(const qkvp_layout* layout, int64_t count, int64_t cols, const void* m, void* out,
+                            int32_t cluster, void* stream) {
   using namespace qkvp;
   int64_t rows = 0;
-  QKVP_TRY(check_ns(layout, cols, cluster, &rows));
+  QKVP_TRY(check_ns(layout, count, cols, cluster, &rows));
   if (!m || !out) return QKVP_ERR_NULL;
   if (!aligned16(m) || !aligned16(out)) return QKVP_ERR_ALIGN;
   const uintptr_t bytes = (uintptr_t)(rows * cols * 2), pm = (uintptr_t)m, po = (uintptr_t)out;
   if (pm < po + bytes && po < pm + bytes) return QKVP_ERR_VALUE;  // out overlaps m
 
+  if (count == 0) return QKVP_OK;
   int sms = 0;
   QKVP_TRY(current_device(&sms));
   const int64_t units = (rows + kNsUnitRows - 1) / kNsUnitRows;
@@ -1100,12 +1103,21 @@ int qkv_newton_schulz(const qkvp_layout* layout, int64_t cols, const void* m, vo
                      false, true);
 }
 
-int qkv_newton_schulz_plan(const qkvp_layout* layout, int64_t cols, int32_t cluster, int32_t* cluster_out,
-                           int32_t* grid_out) {
+int qkv_newton_schulz(const qkvp_layout* layout, int64_t cols, const void* m, void* out, int32_t cluster,
+                      void* stream) {
+  return qkv_newton_schulz_batch(layout, 1, cols, m, out, cluster, stream);
+}
+
+int qkv_newton_schulz_plan(const qkvp_layout* layout, int64_t count, int64_t cols, int32_t cluster,
+                           int32_t* cluster_out, int32_t* grid_out) {
   using namespace qkvp;
   int64_t rows = 0;
-  QKVP_TRY(check_ns(layout, cols, cluster, &rows));
+  QKVP_TRY(check_ns(layout, count, cols, cluster, &rows));
   if (!cluster_out || !grid_out) return QKVP_ERR_NULL;
+  if (count == 0) {
+    *cluster_out = *grid_out = 0;
+    return QKVP_OK;
+  }
   int sms = 0;
   QKVP_TRY(current_device(&sms));
   const int64_t units = (rows + kNsUnitRows - 1) / kNsUnitRows;

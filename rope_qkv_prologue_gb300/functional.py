@@ -158,16 +158,21 @@ def per_head_newton_schulz(m, n_q, n_kv, head_dim=64, kind="interleaved", cluste
     orthogonalised on its own (Muon's quintic iteration, five steps) and scaled
     by max(1, head_dim / in_features) ** 0.5 ("[muon] Per-head Newton-Schulz for
     fused QKV projections", What this PR does). `kind` names the packing of the
-    rows; the result does not depend on it."""
+    rows; the result does not depend on it. A 3-D m [count, rows, cols] (one
+    update per layer) is done in a single launch."""
     _check_dev(m)
-    if m.dim() != 2 or m.dtype != torch.bfloat16:
-        raise ValueError("m must be a 2-D bf16 tensor")
-    if m.shape[0] != (n_q + 2 * n_kv) * head_dim:
+    if m.dim() not in (2, 3) or m.dtype != torch.bfloat16:
+        raise ValueError("m must be a bf16 [rows, cols] or [count, rows, cols] tensor")
+    if m.shape[-2] != (n_q + 2 * n_kv) * head_dim:
         raise ValueError("m must have (n_q + 2 n_kv) * head_dim rows")
     m = m.contiguous()
     if out is None:
         out = torch.empty_like(m)
-    C.qkv_newton_schulz(C.layout(kind, n_q, n_kv, head_dim), m.shape[1], m, out, cluster, stream)
+    L = C.layout(kind, n_q, n_kv, head_dim)
+    if m.dim() == 2:
+        C.qkv_newton_schulz(L, m.shape[1], m, out, cluster, stream)
+    else:  # every weight of the stack in one launch
+        C.qkv_newton_schulz_batch(L, m.shape[0], m.shape[2], m, out, cluster, stream)
     return out
 
 

@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
     assert {"qkv_prologue_fwd", "qkv_prologue_bwd", "qkv_prologue_pool_write",
             "qkv_prologue_pool_scatter", "qkv_prologue_bwd_workspace_size",
             "qkv_prologue_status_string", "qkv_prologue_version", "qkv_prologue_device_error",
-            "qkv_newton_schulz", "qkv_newton_schulz_plan"} <= names
+            "qkv_newton_schulz", "qkv_newton_schulz_batch", "qkv_newton_schulz_plan"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -378,3 +378,21 @@ def test_newton_schulz_argument_checks(lib):
     assert ns(out=A - rows * 5120 * 2) == C.QKVP_ERR_ARCH  # just below: no overlap
     with pytest.raises(C.QkvpError):
         C.qkv_newton_schulz_plan(L, 5120)      # planning needs the device
+
+
+@cpu_only
+def test_newton_schulz_batch_argument_checks(lib):
+    C = lib
+    L = C.layout("interleaved", 8, 2, 64)
+    one = 768 * 512 * 2
+
+    def nb(count=6, cols=512, m=A, out=A + 6 * one, cluster=0):
+        return C.qkv_newton_schulz_batch(L, count, cols, m, out, cluster, stream=0, check=False)
+
+    assert nb() == C.QKVP_ERR_ARCH            # valid: reaches the device check
+    assert nb(count=0) == C.QKVP_OK           # nothing to do
+    assert nb(count=-1) == C.QKVP_ERR_SHAPE
+    assert nb(count=(1 << 30) // 768 + 1) == C.QKVP_ERR_SHAPE  # more than 2^30 rows
+    assert nb(out=A + 5 * one) == C.QKVP_ERR_VALUE  # overlaps the last weight of the stack
+    assert nb(out=A + 6 * one, m=None) == C.QKVP_ERR_NULL
+    assert nb(cols=500) == C.QKVP_ERR_SHAPE

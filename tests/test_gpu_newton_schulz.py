@@ -154,3 +154,33 @@ def test_full_size_muse_spark_weight_sampled(lib, cuda):
     rng = np.random.default_rng(5)
     sample = sorted(set([0, 1, n_blocks - 1] + list(rng.choice(n_blocks, 5, replace=False))))
     check_blocks(got, w, c["head_dim"], blocks=sample, what="full size")
+
+
+def test_batch_of_layers_in_one_launch(lib, cuda):
+    # the page's model: six layers' updates stacked, one launch; each layer
+    # against the oracle, and the same bits as six single calls with the same
+    # cluster size (the 128-row units line up with the layers)
+    c = workloads.NS_PAGE_MODEL
+    ws = [workloads.fused_qkv_update(c["n_q"], c["n_kv"], c["head_dim"], c["cols"], seed=300 + i) for i in range(6)]
+    m = torch.stack(ws).to(cuda)
+    got = lib.functional.per_head_newton_schulz(m, c["n_q"], c["n_kv"], c["head_dim"], cluster=4)
+    torch.cuda.synchronize()
+    assert lib.qkv_prologue_device_error(clear=True) == 0
+    for i in range(6):
+        one = run(lib, m[i], c["n_q"], c["n_kv"], c["head_dim"], cluster=4)
+        assert torch.equal(one.view(torch.int16), got[i].view(torch.int16)), f"layer {i}"
+        check_blocks(got[i].cpu(), ws[i], c["head_dim"], what=f"layer {i}")
+
+
+def test_batch_with_units_across_layers(lib, cuda):
+    # 3 blocks per layer (1 q + 1 k + 1 v): the 128-row units straddle layers
+    n_q, n_kv, D, cols = 1, 1, 64, 256
+    ws = [workloads.fused_qkv_update(n_q, n_kv, D, cols, seed=400 + i) for i in range(3)]
+    buf = torch.full((4, 3 * D, cols), 5.0, dtype=torch.bfloat16, device=cuda)
+    out = buf[:3]
+    lib.functional.per_head_newton_schulz(torch.stack(ws).to(cuda), n_q, n_kv, D, out=out)
+    torch.cuda.synchronize()
+    assert lib.qkv_prologue_device_error(clear=True) == 0
+    assert torch.all(buf[3] == 5.0), "rows past the stack were written"
+    for i in range(3):
+        check_blocks(out[i].cpu(), ws[i], D, what=f"layer {i}")

@@ -41,10 +41,15 @@
 // is summed the same way (row sums, then over the cluster) and X is scaled in
 // place to X / (norm + eps).
 //
+// B X is committed in two sections of the slice's columns, and the next
+// step's Gram starts on section 0 while the epilogue still updates section 1.
+//
 // Roles: warp 0 issues the TMA load; warp 1 owns TMEM and one of its threads
 // issues every MMA; warps 2-9 are the epilogue: warp w reads TMEM lanes
 // 32 (w % 4) .. 32 (w % 4) + 31 (= weight rows of the unit) and one half of
-// the columns. Every wait is bounded (2 s); after a timeout the device error
+// the columns. The grid is always launched as an explicit cluster (st.async
+// needs one, even for one CTA); without one the kernel does nothing and sets
+// an error bit. Every wait is bounded (2 s); after a timeout the device error
 // word is set and every thread still passes every barrier, without waiting.
 #include <cuda.h>
 #include <cuda_bf16.h>

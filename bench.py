@@ -401,10 +401,15 @@ class MlaStep(_Step):
         self.rows, self.pos, self.w = wl.rows.to(dev), wl.pos.to(dev), wl.w.to(dev)
         self.page, self.offset = wl.page.to(dev), wl.offset.to(dev)
         self.pool = workloads.random_pool_bits((wl.num_pages, wl.page_size, 576), 51, dev)
+        import torch
+
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)  # bad page / offset bits of the writes
         self.calls = [("qkv_prologue_pool_write (qkvp_latent_kernel, pool)", self.fwd,
                        T * (1152 + 4 + 1152 + 8) + 512 * 4)]
         self.h_in = {"rows": wl.rows, "pos": wl.pos, "w": wl.w, "page": wl.page, "offset": wl.offset}
-        self.out_names = ()
+        # the rows stay in the device-resident pool (the KV cache); what the caller
+        # reads back is the write's status word
+        self.out_names = ("status",)
         self.describe = (f"MLA latent rows [T,576] -> pool 8192 x [64,576], T={T}, 512 normed + 64 roped "
                          "(base 1e4), positions U[0,393216)")
 
@@ -412,7 +417,7 @@ class MlaStep(_Step):
         C, wl = self.C, self.wl
         C.qkv_prologue_pool_write(self.L, self.T, self.rows, self.pos, None, self.w, wl.eps, wl.rope_base, self.xflags,
                                   None,
-                                  self.page, self.offset, self.pool, None, wl.num_pages, wl.page_size, None,
+                                  self.page, self.offset, self.pool, None, wl.num_pages, wl.page_size, self.status,
                                   self.stream)
 
 
@@ -633,6 +638,60 @@ class NewtonSchulzStep(_Step):
         b.record()
         torch.cuda.synchronize()
         return {"torch_bf16_batched_iteration_graph_us_per_step": round(a.elapsed_time(b) * 1e3 / reps, 2)}
+
+
+def e2e_pipelined(ws, steps):
+    """The e2e step run as a pipeline over two sets of device buffers: the
+    inputs of step k + 1 go host -> device on one stream while step k runs the
+    C-ABI calls on the library's stream and step k - 1's outputs go device ->
+    host on a third. Every step still copies its own inputs in from pinned
+    host memory and its outputs out to it. Returns ms per step."""
+    import torch
+
+    names_in, names_out = list(ws.h_in), list(ws.out_names)
+    orig = {n: getattr(ws, n) for n in names_in + names_out}
+    sets = [orig, ws.rotated_copy(1)]
+    comp = torch.cuda.current_stream(ws.dev)
+    s_in, s_out = torch.cuda.Stream(ws.dev), torch.cuda.Stream(ws.dev)
+    ev_in, ev_done, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+
+    def run(n):
+        s_in.wait_stream(comp)
+        s_out.wait_stream(comp)
+        for k in range(n):
+            b = k % 2
+            st = sets[b]
+            with torch.cuda.stream(s_in):
+                if k >= 2:
+                    s_in.wait_event(ev_done[b])  # step k - 2 has read this set's inputs
+                for name in names_in:
+                    st[name].copy_(ws.h_in_pinned[name], non_blocking=True)
+                ev_in[b].record(s_in)
+            comp.wait_event(ev_in[b])
+            if k >= 2:
+                comp.wait_event(ev_out[b])  # step k - 2's outputs in this set are on the host
+            for name, t in st.items():
+                setattr(ws, name, t)
+            ws.step()
+            ev_done[b].record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[b])
+                for name in names_out:
+                    ws.h_out[name].copy_(st[name], non_blocking=True)
+                ev_out[b].record(s_out)
+        comp.wait_stream(s_in)
+        comp.wait_stream(s_out)
+
+    run(2)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(comp)
+    run(steps)
+    e1.record(comp)
+    torch.cuda.synchronize()
+    for name, t in orig.items():
+        setattr(ws, name, t)
+    return e0.elapsed_time(e1) / steps
 
 
 def mla_two_stream_overlap(dev, T, layers=3, reps=20):
@@ -918,10 +977,11 @@ def run_ours(args):
         ws.e2e_step()
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_serial_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = e2e_pipelined(ws, e2e_steps)
 
     if world > 1:
-        elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], dev)
+        elapsed_ms, e2e_ms, e2e_serial_ms = max_over_ranks([elapsed_ms, e2e_ms, e2e_serial_ms], dev)
 
     ms_per_step = elapsed_ms / K
     value = whole_job_gbs(step_bytes, world, ms_per_step)
@@ -983,7 +1043,10 @@ def run_ours(args):
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "path": "pinned host -> device copies of the inputs, the C-ABI calls, device -> pinned host copies "
-                    "of the outputs, every step",
+                    "of the outputs, every step; pipelined over two buffer sets (the next step's inputs in "
+                    "and the last step's outputs out on their own streams while a step computes)",
+            "serial_ms_per_step": round(e2e_serial_ms, 4),
+            "serial_value": round(whole_job_gbs(step_bytes, world, e2e_serial_ms), 1),
         },
         "gpu_launches": ws.kernels_per_step * K,
         "gpu_launches_note": f"{ws.kernels_per_step} library kernel(s) per step",

@@ -483,9 +483,10 @@ int ns_active_clusters(int nc, size_t smem) {
   return n;
 }
 
-// A step costs about as much as kNsStepColumns more columns per CTA would
-// (the Gram exchange, the A A product and the epilogues; measured on GB300).
-constexpr int kNsStepColumns = 600;
+// A step costs about as much as kNsStepColumns more columns per CTA would:
+// on GB300 the exchange, A A and the epilogues take ~5 us of a step, the Gram
+// and B X products ~0.5 us per 100 columns of the slice.
+constexpr int kNsStepColumns = 1000;
 
 
 // Cluster size for a fused weight of `units` 128-row units and `cols` columns:

@@ -317,10 +317,9 @@ QKVP_API int qkv_prologue_bwd_ex(const qkvp_layout* layout, const qkvp_variant* 
  * then split, normed and roped into q, k, v (and q_pre, k_pre) as
  * qkv_prologue_fwd does; the packed tensor itself is never written.
  *
- * Defines: the survey's next step to the left of the path: "[muse_spark][perf]
- * Split the packed qkv inside the q/k region", Problem 1 (the packed tensor is
- * the wqkv projection's output) and Solution 1 (the region starts at that
- * output).
+ * Defines: the step just before the prologue, "[muse_spark][perf] Split the
+ * packed qkv inside the q/k region", Problem 1 (the packed tensor is the wqkv
+ * projection's output) and Solution 1 (the region starts at that output).
  *
  * layout   GQA layout (INTERLEAVED or SECTIONED), row_stride 0 (dense). Its
  *          packed row order is the row order of w_qkv.

@@ -184,3 +184,34 @@ def test_batch_with_units_across_layers(lib, cuda):
     assert torch.all(buf[3] == 5.0), "rows past the stack were written"
     for i in range(3):
         check_blocks(out[i].cpu(), ws[i], D, what=f"layer {i}")
+
+
+@pytest.mark.parametrize("cluster", [14, 16])
+def test_wide_in_features_large_clusters(lib, cuda, cluster):
+    # in_features 7168 (112 boxes of 64 columns): clusters of 14 (512 columns per
+    # CTA, the fullest receive buffer: 14 slots of 10 rows) and of 16 (448)
+    n_q, n_kv, D, cols = 4, 2, 128, 7168
+    L = lib.layout("interleaved", n_q, n_kv, D)
+    try:
+        nc, _ = lib.qkv_newton_schulz_plan(L, cols, cluster)
+    except lib.QkvpError:
+        pytest.skip(f"the device does not co-schedule clusters of {cluster} of these CTAs")
+    assert nc == cluster
+    w = workloads.fused_qkv_update(n_q, n_kv, D, cols, seed=500 + cluster)
+    got = run(lib, w.to(cuda), n_q, n_kv, D, cluster=cluster).cpu()
+    check_blocks(got, w, D, what=f"7168 columns, cluster {cluster}")
+
+
+def test_llama70b_shaped_weight_sampled(lib, cuda):
+    # 64 q heads over 8 kv heads of 128, in_features 8192: [10240, 8192], the
+    # widest update the kernel takes (16 CTAs of 512 columns per unit)
+    n_q, n_kv, D, cols = 64, 8, 128, 8192
+    L = lib.layout("interleaved", n_q, n_kv, D)
+    try:
+        lib.qkv_newton_schulz_plan(L, cols)
+    except lib.QkvpError:
+        pytest.skip("the device does not co-schedule clusters of 16 of these CTAs")
+    w = workloads.fused_qkv_update(n_q, n_kv, D, cols, seed=601)
+    got = run(lib, w.to(cuda), n_q, n_kv, D).cpu()
+    assert torch.isfinite(got.float()).all()
+    check_blocks(got, w, D, blocks=[0, 1, 37, 79], what="[10240, 8192]")

@@ -598,3 +598,21 @@ def check_ns_page_facts(N):
         assert abs(N.full_matrix_scale(rows, cols) - f) <= 1e-15, (rows, cols)
     for d, cin, f in head:
         assert abs(N.per_head_scale(d, cin) - f) <= 1e-15, (d, cin)
+
+
+def check_ns_dispatch(N, rng):
+    """The update a fused weight gets: per head when dim 0 is the exact fused
+    total, else the whole matrix with max(1, rows / cols) ** 0.5 (sqrt(3) for a
+    [3h, h] weight), each against the SVD closed form."""
+    h = 16
+    w = rng.standard_normal((3 * h, h))
+    # 1 q head of 16 over 1 kv head: 3 blocks of 16 rows, the exact total
+    got = N.muon_orthogonalize(w, n_q=1, n_kv=1, head_dim=16)
+    for blk in range(3):
+        sl = slice(16 * blk, 16 * blk + 16)
+        assert np.abs(got[sl] - _ns_by_svd(w[sl])).max() <= 1e-9, f"per-head block {blk}"
+    # a config whose total (4 + 2 * 2) * 16 = 128 is not 48: the whole matrix
+    got = N.muon_orthogonalize(w, n_q=4, n_kv=2, head_dim=16)
+    assert np.abs(got - np.sqrt(3.0) * _ns_by_svd(w)).max() <= 1e-9, "whole-matrix path"
+    got = N.muon_orthogonalize(w)
+    assert np.abs(got - np.sqrt(3.0) * _ns_by_svd(w)).max() <= 1e-9, "no head tag: whole matrix"

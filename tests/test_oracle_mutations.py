@@ -166,6 +166,10 @@ def _per_head_global_norm(m, head_dim, **kw):
     return out
 
 
+def _full_scale_cols_over_rows(rows, cols):
+    return max(1.0, cols / rows) ** 0.5
+
+
 def _blocks_any_multiple(rows, n_q, n_kv, head_dim):
     return rows // head_dim if head_dim and rows % head_dim == 0 else None
 
@@ -189,6 +193,7 @@ def _checks_all(rng):
     C.check_ns_per_head(N, rng)
     C.check_ns_layout_equivalence(N, P, rng)
     C.check_ns_page_facts(N)
+    C.check_ns_dispatch(N, rng)
 
 
 def test_unmutated_oracle_passes_every_pin(rng):
@@ -219,6 +224,7 @@ MUTATIONS = [
     (N, "per_head_scale", _head_scale_whole_matrix),
     (N, "per_head_newton_schulz", _per_head_global_norm),
     (N, "fused_head_blocks", _blocks_any_multiple),
+    (N, "full_matrix_scale", _full_scale_cols_over_rows),
 ]
 
 

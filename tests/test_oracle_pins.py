@@ -182,3 +182,7 @@ def test_ns_bits_entry_checks_the_fused_total(rng):
     assert np.array_equal(out, N.per_head_newton_schulz(B.bf16_bits_to_f64(m), 16))
     with pytest.raises(ValueError):
         N.qkv_newton_schulz(L, m[:-16])
+
+
+def test_ns_dispatch_per_head_or_whole(rng):
+    C.check_ns_dispatch(N, rng)

@@ -1158,7 +1158,7 @@ class NsOracleSample:
         return 2 * self.m.size * 2  # the bf16 update in and the result out
 
 
-def ns_cpu_baseline(name, target_s=10.0, max_passes=40):
+def ns_cpu_baseline(name, target_s=10.0, max_passes=100000):
     probe = NsOracleSample(name, 1)
     per_block = max(probe.run(), 1e-4)
     blocks = (probe.c["n_q"] + 2 * probe.c["n_kv"])

@@ -358,12 +358,19 @@ def prologue_bwd(layout, dq_bits, dk_bits, dv_bits, q_pre_bits, k_pre_bits,
 # The projection to the left of the path, with the prologue after it
 # --------------------------------------------------------------------------
 
-def gemm_prologue_fwd(layout, x_bits, w_bits, pos, w_q, w_k, eps, rope_base, nope=False, **variant):
-    """packed = x . W^T (x [T, hidden], W [row_width, hidden], both bf16 bits),
-    the float64 product rounded once to bf16 (the packed tensor the projection
-    hands to the prologue), then prologue_fwd. Returns (prologue_fwd's dict,
-    packed bits)."""
+def projection(x_bits, w_bits):
+    """The wqkv projection: packed = x . W^T for x [T, hidden] and W
+    [row_width, hidden] (nn.Linear's weight layout, rows in the layout's
+    packed order), both bf16 bits. Every product of two bf16 values is exact in
+    float64 and the float64 sum is rounded once to bf16: the packed tensor the
+    projection hands to the prologue ("[muse_spark][perf] ...", Problem 1)."""
     x = bf16_bits_to_f64(np.asarray(x_bits, dtype=np.uint16))
     w = bf16_bits_to_f64(np.asarray(w_bits, dtype=np.uint16))
-    packed = to_bf16_rne(x @ w.T)
+    return to_bf16_rne(x @ w.T)
+
+
+def gemm_prologue_fwd(layout, x_bits, w_bits, pos, w_q, w_k, eps, rope_base, nope=False, **variant):
+    """projection, then prologue_fwd on its packed bits. Returns (prologue_fwd's
+    dict, packed bits)."""
+    packed = projection(x_bits, w_bits)
     return prologue_fwd(layout, packed, pos, w_q, w_k, eps, rope_base, nope, **variant), packed

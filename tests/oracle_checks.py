@@ -21,6 +21,11 @@ What pins what:
                     bias order through the pinned split, bias before the norm
                     (rms 1) and the rotation, one-hot frequency tables, the
                     cos/sin factor at position 0, finite differences of all
+  projection       x . W^T against exact rational sums rounded by the exact
+                    nearest-even search (square and non-square weights, rows
+                    in packed order), a sum one 2**-30 past a bf16 tie (one
+                    rounding, not two), W = identity / a row permutation
+                    handing the prologue exactly x / x's columns permuted
   per-head Newton-  known-SVD closed forms through a scalar recursion on the
   Schulz            singular values (Muon's published constants, typed here
                     on their own), the 1e-7 on a tiny matrix, orthogonal
@@ -42,17 +47,23 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 # ---------------------------------------------------------------- bf16 ----
 
 def _exact_bf16_rne(x):
-    """Nearest bf16 to float x by exact rational comparison (ties -> even)."""
-    if math.isnan(x):
-        return 0x7FC0
-    sign = 0x8000 if math.copysign(1.0, x) < 0 else 0
-    ax = abs(x)
-    if math.isinf(ax):
-        return sign | 0x7F80
+    """Nearest bf16 to x (a float or an exact Fraction) by exact rational
+    comparison (ties -> even)."""
+    if isinstance(x, Fraction):
+        sign = 0x8000 if x < 0 else 0
+        X = abs(x)
+        ax = float(X)  # within one float64 ulp of X: the candidate window below covers it
+    else:
+        if math.isnan(x):
+            return 0x7FC0
+        sign = 0x8000 if math.copysign(1.0, x) < 0 else 0
+        ax = abs(x)
+        if math.isinf(ax):
+            return sign | 0x7F80
+        X = Fraction(ax)
     # Candidates: the bf16 patterns around the float32 truncation of |x|.
     f32 = struct.unpack("<I", struct.pack("<f", min(ax, 3.4e38)))[0] >> 16
     best, best_d = None, None
-    X = Fraction(ax)
     for b in range(max(0, f32 - 2), min(0x7F80, f32 + 3) + 1):
         if b == 0x7F80:
             val = Fraction(2) ** 128  # overflow rounds like a value at 2**128
@@ -616,3 +627,76 @@ def check_ns_dispatch(N, rng):
     assert np.abs(got - np.sqrt(3.0) * _ns_by_svd(w)).max() <= 1e-9, "whole-matrix path"
     got = N.muon_orthogonalize(w)
     assert np.abs(got - np.sqrt(3.0) * _ns_by_svd(w)).max() <= 1e-9, "no head tag: whole matrix"
+
+
+# ---------------------------------------------------------- projection ----
+
+def _bf16_bits_of(vals):
+    """bf16 bits of values that are exactly bf16 (checked)."""
+    out = np.array([_exact_bf16_rne(float(v)) for v in np.ravel(vals)], dtype=np.uint16).reshape(np.shape(vals))
+    back = np.array([struct.unpack("<f", struct.pack("<I", int(b) << 16))[0] for b in out.ravel()]).reshape(out.shape)
+    assert np.array_equal(back, np.asarray(vals, dtype=np.float64)), "test values must be bf16"
+    return out
+
+
+def _bf16_value(bits):
+    return Fraction(struct.unpack("<f", struct.pack("<I", int(bits) << 16))[0])
+
+
+def _exact_projection_bits(x_bits, w_bits):
+    """packed[t, c] = sum_k x[t, k] W[c, k], summed exactly in rationals and
+    rounded once to the nearest bf16 (ties to even)."""
+    T, K = x_bits.shape
+    R = w_bits.shape[0]
+    xf = [[_bf16_value(b) for b in row] for row in x_bits]
+    wf = [[_bf16_value(b) for b in row] for row in w_bits]
+    out = np.empty((T, R), dtype=np.uint16)
+    for t in range(T):
+        for c in range(R):
+            out[t, c] = _exact_bf16_rne(sum((xf[t][k] * wf[c][k] for k in range(K)), Fraction(0)))
+    return out
+
+
+def _random_bf16(rng, shape, spread=6):
+    v = rng.standard_normal(shape) * np.exp2(rng.integers(-spread, spread + 1, shape))
+    return _bf16_bits_of(np.vectorize(lambda a: float(struct.unpack("<f", struct.pack(
+        "<I", _exact_bf16_rne(float(a)) << 16))[0]))(v))
+
+
+def check_projection(P, rng):
+    """The projection step and its hand-over to the prologue."""
+    L = P.PackedLayout("interleaved", 2, 1, 8)          # packed row of 32 values
+    # 1. a square weight (hidden = row width = 32) with no symmetry: x . W^T,
+    #    not x . W, against exact rational sums
+    x = _random_bf16(rng, (3, L.row_width))
+    w = _random_bf16(rng, (L.row_width, L.row_width))
+    assert np.array_equal(P.projection(x, w), _exact_projection_bits(x, w)), "square projection"
+    # 2. non-square: 5 tokens, hidden 40, wide value spread
+    x = _random_bf16(rng, (5, 40), spread=12)
+    w = _random_bf16(rng, (L.row_width, 40), spread=12)
+    assert np.array_equal(P.projection(x, w), _exact_projection_bits(x, w)), "projection"
+    # 3. one rounding: 1 + 2**-8 + 2**-30 is just above the bf16 tie between 1
+    #    and 1 + 2**-7 and rounds up; rounded to float32 first it would land on
+    #    the tie and go to the even 1.0. Its mirror 1 + 2**-8 - 2**-30 goes to 1.
+    xv = np.zeros((2, 40))
+    xv[0, :3] = [1.0, 2.0 ** -8, 2.0 ** -30]
+    xv[1, :3] = [1.0, 2.0 ** -8, -(2.0 ** -30)]
+    wv = np.zeros((L.row_width, 40))
+    wv[5, :3] = 1.0
+    got = P.projection(_bf16_bits_of(xv), _bf16_bits_of(wv))
+    assert got[0, 5] == 0x3F81 and got[1, 5] == 0x3F80, "one rounding to bf16"
+    assert not got[:, [c for c in range(L.row_width) if c != 5]].any()
+    # 4. hand-over: W = identity gives the prologue exactly x; W = a row
+    #    permutation gives it x's columns in that order
+    x = _random_bf16(rng, (4, L.row_width), spread=2)
+    pos = np.array([0, 1, 7, 300])
+    wq, wk = 0.5 + rng.random(8), 0.5 + rng.random(8)
+    ident = _bf16_bits_of(np.eye(L.row_width))
+    got, packed = P.gemm_prologue_fwd(L, x, ident, pos, wq, wk, 1e-6, 1e4)
+    assert np.array_equal(packed, x)
+    want = P.prologue_fwd(L, x, pos, wq, wk, 1e-6, 1e4)
+    for key in ("q", "k", "v"):
+        assert np.array_equal(got[key], want[key]), key
+    perm = rng.permutation(L.row_width)
+    _, packed = P.gemm_prologue_fwd(L, x, ident[perm], pos, wq, wk, 1e-6, 1e4, nope=True)
+    assert np.array_equal(packed, x[:, perm]), "rows of W are the packed columns, in order"

@@ -174,6 +174,21 @@ def _blocks_any_multiple(rows, n_q, n_kv, head_dim):
     return rows // head_dim if head_dim and rows % head_dim == 0 else None
 
 
+def _projection_w_not_transposed(x_bits, w_bits):
+    x, w = B.bf16_bits_to_f64(x_bits), B.bf16_bits_to_f64(w_bits)
+    return B.to_bf16_rne(x @ w)
+
+
+def _projection_via_float32(x_bits, w_bits):
+    x, w = B.bf16_bits_to_f64(x_bits), B.bf16_bits_to_f64(w_bits)
+    return _bf16_via_float32((x @ w.T).astype(np.float32).astype(np.float64))
+
+
+def _projection_rows_reversed(x_bits, w_bits):
+    x, w = B.bf16_bits_to_f64(x_bits), B.bf16_bits_to_f64(w_bits)
+    return B.to_bf16_rne(x @ w[::-1].T)
+
+
 def _checks_all(rng):
     """Every pin, run in turn; raises AssertionError at the first that fails."""
     C.check_to_bf16_rne(B, rng)
@@ -194,6 +209,7 @@ def _checks_all(rng):
     C.check_ns_layout_equivalence(N, P, rng)
     C.check_ns_page_facts(N)
     C.check_ns_dispatch(N, rng)
+    C.check_projection(P, rng)
 
 
 def test_unmutated_oracle_passes_every_pin(rng):
@@ -225,6 +241,9 @@ MUTATIONS = [
     (N, "per_head_newton_schulz", _per_head_global_norm),
     (N, "fused_head_blocks", _blocks_any_multiple),
     (N, "full_matrix_scale", _full_scale_cols_over_rows),
+    (P, "projection", _projection_w_not_transposed),
+    (P, "projection", _projection_via_float32),
+    (P, "projection", _projection_rows_reversed),
 ]
 
 

@@ -186,3 +186,9 @@ def test_ns_bits_entry_checks_the_fused_total(rng):
 
 def test_ns_dispatch_per_head_or_whole(rng):
     C.check_ns_dispatch(N, rng)
+
+
+def test_projection_exact_sums_one_rounding_and_hand_over(rng):
+    # x . W^T against exact rational sums (square and non-square W), one
+    # rounding past a bf16 tie, and W = identity / permutation into the prologue
+    C.check_projection(P, rng)

@@ -255,12 +255,18 @@ QKVP_API int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* 
  * qkv_prologue_bwd, minus the workspace: the weight-gradient partial sums go
  * to a fixed 512 KiB array inside the library's device memory, which every
  * GPU that loads the library holds until the process exits.
- *  - Limit: qkv_prologue_bwd_workspace_size(layout, T) must be <= 512 KiB
- *    (always true for head_dim 64; head_dim 128 up to 512 tokens), otherwise
- *    QKVP_ERR_WORKSPACE is returned and nothing is enqueued.
+ *  - Limit: with the norm on, qkv_prologue_bwd_workspace_size(layout, T)
+ *    must be <= 512 KiB, otherwise QKVP_ERR_WORKSPACE is returned and nothing
+ *    is enqueued. That size is min(1024, max(T, n_items)) partial rows of
+ *    2 * head_dim floats, n_items = ceil(T * (n_q + 2 n_kv) * head_dim / 8 /
+ *    1536): head_dim 64 always fits (at most 1024 rows of 512 B); head_dim 128
+ *    fits while max(T, n_items) <= 512 (e.g. n_q 32, n_kv 8: 512 tokens;
+ *    n_q 128, n_kv 16: 307 tokens). With QKVP_NORM_OFF no scratch is needed
+ *    and every T is accepted.
  *  - The first call on each device looks up the array's device address (with
  *    that device current) and caches it; make that first call before any
- *    stream capture.
+ *    stream capture. The cache outlives a cudaDeviceReset: do not use this
+ *    call on a device after resetting it in the same process.
  *  - All calls share the array and it keeps the last call's contents (nothing
  *    in it needs to start at zero). Calls whose work can overlap on the GPU
  *    (different streams without ordering) race on it: order them.
@@ -330,6 +336,11 @@ QKVP_API int qkv_prologue_bwd_ex(const qkvp_layout* layout, const qkvp_variant* 
  * pos, w_q, w_k, eps, rope_base: as qkv_prologue_fwd.
  * flags    QKVP_NOPE, QKVP_SAVE_PRE (q_pre, k_pre = the bf16 packed heads).
  * q, k, v, q_pre, k_pre: as qkv_prologue_fwd (contiguous outputs).
+ * x and w_qkv must be device memory of the current device (cudaMalloc or a
+ * caching allocator on it): the kernel reads them through tensor maps of this
+ * GPU's memory, so another GPU's memory (peer access), host or managed memory
+ * gives QKVP_ERR_VALUE. The call is for one-GPU use: each GPU of a multi-GPU
+ * job calls it on its own data.
  * The summation order of the projection differs from other GEMM libraries,
  * so a packed value sitting on a bf16 rounding boundary can round the other
  * way than in an unfused cuBLAS + qkv_prologue_fwd pair.

@@ -337,6 +337,18 @@ void rope_table(double base, int dim, const double* inv_freq, float scale, RopeT
 // ------------------------------------------------------------ checks ----
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// True when p points into device memory of the current device (not host,
+// managed-on-host or another GPU's memory reached through peer access).
+bool on_current_device(const void* p) {
+  int dev = -1;
+  cudaPointerAttributes attr;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return attr.type == cudaMemoryTypeDevice && attr.device == dev;
+}
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 struct Gqa {
@@ -1027,6 +1039,9 @@ int qkv_prologue_gemm_fwd(const qkvp_layout* layout, int64_t T, int32_t hidden, 
 
   int sms = 0;
   QKVP_TRY(current_device(&sms));
+  // The tensor maps must cover this GPU's own memory: x and w_qkv are read by
+  // the tensor-memory copy engine of the current device only.
+  if (!on_current_device(x) || !on_current_device(w_qkv)) return QKVP_ERR_VALUE;
   CUtensorMap tx, tw;
   if (!bf16_tile_map(&tx, x, T, hidden, kGemmBM) || !bf16_tile_map(&tw, w_qkv, g.heads * (int64_t)layout->head_dim,
                                                                     hidden, kGemmBN / 2))

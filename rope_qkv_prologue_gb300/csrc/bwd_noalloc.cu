@@ -16,7 +16,11 @@
 //    (different streams, no ordering between them) race on it and give wrong
 //    weight gradients; calls on one stream, or otherwise ordered, are fine;
 //  * the array keeps whatever the last call left in it. Nothing has to start
-//    at zero: the backward writes every partial row before it reads it.
+//    at zero: the backward writes every partial row before it reads it;
+//  * the array's device address is cached per device index for the life of
+//    the process, so the call must not be used on a device after a
+//    cudaDeviceReset in the same process (the module, and the array with it,
+//    is then reloaded at another address).
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -64,7 +68,8 @@ extern "C" int qkv_prologue_bwd_noalloc(const qkvp_layout* layout, int64_t T, co
                                         const float* w_q, const float* w_k, float eps, double rope_base,
                                         uint32_t flags, void* dpacked, float* dw_q, float* dw_k, void* stream) {
   if (!layout) return QKVP_ERR_NULL;
-  const size_t need = qkv_prologue_bwd_workspace_size(layout, T);
+  // Without the norm there are no weight-gradient partial sums: no scratch.
+  const size_t need = (flags & QKVP_NORM_OFF) ? 0 : qkv_prologue_bwd_workspace_size(layout, T);
   if (need > kScratchBytes) return QKVP_ERR_WORKSPACE;  // too many partial rows for the fixed array
   if (T == 0 || need == 0) {
     // an empty batch needs no scratch; an invalid layout gets the regular checks' answer

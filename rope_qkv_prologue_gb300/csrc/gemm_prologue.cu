@@ -5,12 +5,12 @@
 // the packed tensor never goes to HBM.
 //
 // Persistent CTAs, one per SM, in clusters of two that work on the same W
-// tile for two neighbouring 128-token tiles; 10 warps per CTA:
-//   warp 0       TMA producer: its own x tile [128 x 64] and one half of the
-//                shared W tile [256 x 64] per K step, the W half multicast to
-//                both CTAs of the cluster (so each W byte leaves L2 once per
-//                pair), into a ring of 128B-swizzled shared-memory stages; a
-//                stage is reused only after both CTAs' MMAs have read it;
+// tile for two neighbouring 128-token tiles at the same time (the second read
+// of each W tile is an L2 hit); 10 warps per CTA:
+//   warp 0       TMA producer: its own x tile [128 x 64] and the W tile
+//                [256 x 64] per K step into a ring of 128B-swizzled
+//                shared-memory stages; a stage is reused once this CTA's MMAs
+//                have read it;
 //   warp 1       MMA issuer: four 128x256x16 MMAs per stage into one of two
 //                TMEM accumulators (2 x 256 columns), then a commit that frees
 //                the stage; a commit after the tile's last K step hands the
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGemmStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 2);  // the MMA commits of both CTAs of the cluster
+      mbar_init(&empty[s], 1);  // this CTA's MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync_all();  // the peer's barriers exist before anything is multicast to them
+  cluster_sync_all();  // both CTAs of the pair start together
   const uint32_t tmem = s_tmem;
   const uint32_t rank = cluster_ctarank();
   const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
@@ -156,10 +156,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           unsigned char* st = ring + (size_t)s * kGemmStageBytes;
-          mbar_arrive_expect_tx(&full[s], kGemmStageBytes);  // own x tile + both W halves
+          mbar_arrive_expect_tx(&full[s], kGemmStageBytes);  // x tile + both W halves
           tma_load_2d(st, &tmap_x, kb * kGemmBK, mt * kGemmBM, &full[s]);
-          tma_load_2d_multicast(st + kGemmBM * kGemmBK * 2 + rank * (kGemmBN / 2) * kGemmBK * 2, &tmap_w,
-                                kb * kGemmBK, nt * kGemmBN + (int)rank * (kGemmBN / 2), &full[s], 0x3);
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d(st + kGemmBM * kGemmBK * 2 + h * (kGemmBN / 2) * kGemmBK * 2, &tmap_w, kb * kGemmBK,
+                        nt * kGemmBN + h * (kGemmBN / 2), &full[s]);
         }
       }
     }
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint64_t ad = umma_desc_sw128(st), bd = umma_desc_sw128(st + kGemmBM * kGemmBK * 2);
 #pragma unroll
           for (int k = 0; k < kGemmBK / 16; ++k) umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
-          umma_commit_multicast(&empty[s], 0x3);  // frees the stage in both CTAs' eyes
+          umma_commit(&empty[s]);  // frees the stage once these MMAs have read it
         }
         if (ok) umma_commit(&tfull[b]);
       }
@@ -222,7 +223,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, 2 * kGemmBN);
-  cluster_sync_all();  // the peer's last multicasts and commit arrivals into this CTA are done
+  cluster_sync_all();
 }
 
 namespace {

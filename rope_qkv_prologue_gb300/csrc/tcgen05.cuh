@@ -30,17 +30,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// The same load delivered to every CTA of the cluster in `mask`, at the same
-// shared-memory offset, each completing on its own mbarrier at `bar`'s offset.
-__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map, int c0, int c1,
-                                                      uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "h"(mask)
-      : "memory");
-}
-
 // True when the grid was launched with an explicit thread-block cluster
 // (required by st.async, even for a cluster of one CTA).
 __device__ __forceinline__ bool is_explicit_cluster() {
@@ -110,15 +99,6 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
                : "memory");
-}
-
-// The same, arriving on the mbarrier at `bar`'s offset in every CTA of `mask`.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_addr(bar)),
-      "h"(mask)
-      : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }

@@ -36,19 +36,19 @@ def _outputs(wl, dev):
     return dp, torch.empty(D, device=dev), torch.empty(D, device=dev)
 
 
-def _regular(C, L, wl, a, dev):
+def _regular(C, L, wl, a, dev, flags=0):
     dp, dwq, dwk = _outputs(wl, dev)
     need = C.qkv_prologue_bwd_workspace_size(L, wl.T)
     ws = torch.empty(max(16, need), dtype=torch.uint8, device=dev)
     C.qkv_prologue_bwd(L, wl.T, a["dq"], a["dk"], a["dv"], a["q_pre"], a["k_pre"], a["pos"], a["w_q"], a["w_k"],
-                       wl.eps, wl.rope_base, 0, dp, dwq, dwk, ws, need)
+                       wl.eps, wl.rope_base, flags, dp, dwq, dwk, ws, need)
     return dp, dwq, dwk
 
 
-def _noalloc(C, L, wl, a, dev):
-    dp, dwq, dwk = _outputs(wl, dev)
+def _noalloc(C, L, wl, a, dev, flags=0, out=None):
+    dp, dwq, dwk = _outputs(wl, dev) if out is None else out
     C.qkv_prologue_bwd_noalloc(L, wl.T, a["dq"], a["dk"], a["dv"], a["q_pre"], a["k_pre"], a["pos"], a["w_q"],
-                               a["w_k"], wl.eps, wl.rope_base, 0, dp, dwq, dwk)
+                               a["w_k"], wl.eps, wl.rope_base, flags, dp, dwq, dwk)
     return dp, dwq, dwk
 
 
@@ -100,3 +100,44 @@ def test_noalloc_backward_rejects_work_beyond_its_array(lib, cuda):
     torch.cuda.synchronize()
     assert st == C.QKVP_ERR_WORKSPACE
     assert torch.all(dwq == 3.0)  # nothing was enqueued
+
+
+def test_noalloc_backward_nope_and_norm_off(lib, cuda):
+    # NoPE and norm-off calls give the regular entry point's bits too; without the
+    # norm there are no partial sums, so no scratch is needed and a size that the
+    # norm-on call refuses is accepted
+    C = lib
+    small = workloads.gqa_inputs(257, 16, 4, 64, seed=12, rope_base=5e5, pos_high=131072, with_grads=True)
+    big = workloads.gqa_inputs(2048, 32, 8, 128, seed=11, rope_base=5e5, with_grads=True)
+    for wl, flags in ((small, C.QKVP_NOPE), (small, C.QKVP_NORM_OFF), (big, C.QKVP_NORM_OFF),
+                      (big, C.QKVP_NORM_OFF | C.QKVP_NOPE)):
+        L, a = _inputs(C, wl, cuda)
+        want = _regular(C, L, wl, a, cuda, flags)
+        first = _noalloc(C, L, wl, a, cuda, flags)
+        second = _noalloc(C, L, wl, a, cuda, flags)
+        torch.cuda.synchronize()
+        for got in (first, second):
+            assert torch.equal(got[0].view(torch.int16), want[0].view(torch.int16))
+            if not flags & C.QKVP_NORM_OFF:
+                _same(got, want)
+    assert C.qkv_prologue_device_error(clear=False) == 0
+
+
+def test_noalloc_backward_allocates_no_device_memory(lib, cuda):
+    # one warm-up call (it looks up the array's address), then a loop of calls
+    # with preallocated outputs: neither the driver's free memory nor torch's
+    # allocator may move
+    C = lib
+    wl = workloads.gqa_inputs(1024, 32, 8, 64, seed=13, rope_base=5e5, pos_high=131072, with_grads=True)
+    L, a = _inputs(C, wl, cuda)
+    out = _outputs(wl, cuda)
+    _noalloc(C, L, wl, a, cuda, out=out)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info(cuda)
+    used0 = torch.cuda.memory_allocated(cuda)
+    for _ in range(20):
+        _noalloc(C, L, wl, a, cuda, out=out)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info(cuda)
+    assert torch.cuda.memory_allocated(cuda) == used0
+    assert free1 == free0

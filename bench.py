@@ -66,18 +66,16 @@ def dist_env():
 
 
 def max_over_ranks(values, device):
-    """Element-wise max of per-rank timings over the process group (any backend)."""
-    import torch
-    import torch.distributed as dist
+    """Element-wise max of per-rank timings (the package's replicas helper)."""
+    from rope_qkv_prologue_gb300 import replicas
 
-    t = torch.tensor(values, dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return [float(x) for x in t]
+    return replicas.max_over_ranks(values, device)
 
 
 def whole_job_gbs(bytes_per_rank_step, world, ms_per_step):
-    """Whole-job throughput: the bytes all ranks moved / the slowest rank's time."""
-    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+    from rope_qkv_prologue_gb300 import replicas
+
+    return replicas.whole_job_gbs(bytes_per_rank_step, world, ms_per_step)
 
 
 def measured_peak():
@@ -106,6 +104,11 @@ def kernel_sources_digest():
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()
+
+
+TRAFFIC_SOURCE = ("copied from the ncu capture summarised in profiles/dram_traffic_full_size.md "
+                  "(dram__bytes_read.sum + dram__bytes_write.sum per launch), not measured in this run; "
+                  "null when the kernel sources changed since that capture")
 
 
 def traffic_from_profile(kernel_key):
@@ -700,7 +703,7 @@ def mla_two_stream_overlap(dev, T, layers=3, reps=20):
     norm/RoPE written straight into the pool by the library) and the q path
     (q_a projection -> q_a norm -> q_b projection -> k absorption) from the same
     input, one after the other on one stream, or the kv path forked to a side
-    stream (functional.on_side_stream) and joined after the q path. Both are
+    stream (functional.mla_kv_path_beside) and joined after the q path. Both are
     captured in CUDA graphs and replayed; returns the two step times. The
     projections are cuBLAS GEMMs with random bf16 weights of DeepSeek-V3-style
     per-rank shapes (hidden 7168, q rank 1536, 16 heads of 128 + 64, latent
@@ -732,6 +735,10 @@ def mla_two_stream_overlap(dev, T, layers=3, reps=20):
         F.latent_pool_write(kv, pos, w, page, off, pool, wl.eps, wl.rope_base)
         return kv
 
+    def kv_path_beside(lw, pool):
+        return F.mla_kv_path_beside(side, pos, w, page, off, pool, kv_proj=lambda: h @ lw["wkva"], eps=wl.eps,
+                                    rope_base=wl.rope_base)
+
     def q_path(lw):
         qa = torch.nn.functional.rms_norm(h @ lw["wqa"], (q_rank,), lw["qa_w"], 1e-6)
         q = (qa @ lw["wqb"]).view(T, heads, nope + rope)
@@ -744,9 +751,9 @@ def mla_two_stream_overlap(dev, T, layers=3, reps=20):
                 kv_path(lw, pools["serial"])
                 outs.append(q_path(lw))
             else:
-                _, done = F.on_side_stream(side, kv_path, lw, pools["two"])
+                _, done = kv_path_beside(lw, pools["two"])
                 outs.append(q_path(lw))
-                torch.cuda.current_stream().wait_event(done)
+                F.join(done)
         return outs
 
     graphs, times = {}, {}
@@ -1033,6 +1040,7 @@ def run_ours(args):
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "traffic": traffic_from_profile(f"{args.workload}:{dom}"),
+            "traffic_source": TRAFFIC_SOURCE,
         },
         "clocks": clocks,
         "e2e": {
@@ -1066,7 +1074,8 @@ def run_ours(args):
         out["roofline"] = {"kernel": dom_name, "bound": "tensor", "achieved": round(tflops, 1), "peak": tpeak,
                            "peak_source": f"{tsrc} (MEASURED_PEAKS.json bf16_tflops, burst: the call is timed alone)",
                            "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
-                           "traffic": traffic_from_profile(f"{args.workload}:{dom}")}
+                           "traffic": traffic_from_profile(f"{args.workload}:{dom}"),
+                           "traffic_source": TRAFFIC_SOURCE}
         if hasattr(ws, "unfused_us"):
             unf, gemm_only = ws.unfused_us()
             out["unfused_cublas_projection_plus_prologue_us"] = round(unf, 2)

@@ -199,6 +199,45 @@ def on_side_stream(side, fn, *args, **kwargs):
     return out, done
 
 
+def join(event, stream=None):
+    """Make `stream` (default: the current stream) wait for `event`, the join of
+    a fork made with on_side_stream or mla_kv_path_beside. Under CUDA graph
+    capture this becomes a graph edge."""
+    (stream or torch.cuda.current_stream()).wait_event(event)
+
+
+def mla_kv_path_beside(side, pos, w, page, offset, pool, kv_rows=None, kv_proj=None, eps=1e-6,
+                       rope_base=10000.0, norm_dim=512, rope_dim=64, nope=False, dev_status=None,
+                       inv_freq=None, rope_scale=1.0):
+    """The kv path of one MLA drafter layer on the side stream `side`, beside
+    the q path on the current stream ("MLA DSpark: run each drafter layer's kv
+    path beside its q path", Description): fork after the layer's input norm,
+    run the kv path there, join before attention reads the pool.
+
+    The kv path is: the kv_a rows [T, norm_dim + rope_dim] bf16 (either
+    `kv_rows`, already computed, or `kv_proj()`, a callable run on `side` that
+    returns them, e.g. the kv_a projection of the layer input), then the
+    library's latent norm / RoPE written straight into `pool` [num_pages,
+    page_size, norm_dim + rope_dim] at (page, offset) (latent_pool_write).
+
+    Returns (kv_rows, join_event). Everything the caller queued on the current
+    stream before the call is visible to the kv path; nothing on the current
+    stream waits for it until the caller joins (join(join_event)) -- do that
+    before anything reads `pool` or the returned rows. Inputs made on the
+    current stream must stay alive until the join. Works under CUDA graph
+    capture: the fork and the join become graph edges."""
+    if (kv_rows is None) == (kv_proj is None):
+        raise ValueError("give exactly one of kv_rows and kv_proj")
+
+    def kv_path():
+        rows = kv_proj() if kv_proj is not None else kv_rows
+        latent_pool_write(rows, pos, w, page, offset, pool, eps, rope_base, norm_dim, rope_dim, nope,
+                          dev_status, None, inv_freq, rope_scale)
+        return rows
+
+    return on_side_stream(side, kv_path)
+
+
 class QKVPrologue(torch.autograd.Function):
     """packed [T, row] -> (q, k, v); backward writes d(packed) in one pass.
 

@@ -1,8 +1,18 @@
 """The wqkv projection with the prologue in its epilogue (tcgen05 tensor cores)
 against the fp64 oracle: packed = x . W^T rounded once to bf16, then the
-prologue. The inputs make every product and partial sum exact in float32, so
-the kernel's packed values are the oracle's bit for bit and the outputs are
-held to the prologue's tolerance."""
+prologue.
+
+Two kinds of inputs. With the exact generator every product and partial sum
+is exact in float32, so the kernel's packed values are the oracle's bit for
+bit and the outputs are held to the prologue's tolerance. With the bench's
+inputs (x N(0,1), W N(0, 1/hidden), hidden 5120) a float32 accumulation in
+any order can land on the other side of a bf16 rounding boundary, so the
+packed values the kernel hands its prologue (q_pre, k_pre and v) are held to
+one bf16 ulp of the exact product rounded once (and the share that differs
+is reported and bounded); q and k are held to the prologue's tolerance
+against the oracle on every head whose packed values match bit for bit, and
+against the oracle's prologue of the kernel's own packed values on every
+head."""
 
 import numpy as np
 import pytest
@@ -26,19 +36,20 @@ CASES = [
 
 
 @pytest.mark.parametrize("T,hidden,n_q,n_kv,D,kind", CASES)
-@pytest.mark.parametrize("save", [False, True])
-def test_gemm_prologue_matches_oracle(lib, cuda, T, hidden, n_q, n_kv, D, kind, save):
+@pytest.mark.parametrize("save,nope", [(False, False), (True, False), (True, True)])
+def test_gemm_prologue_matches_oracle(lib, cuda, T, hidden, n_q, n_kv, D, kind, save, nope):
     F = lib.functional
     x, w = workloads.gemm_inputs(T, hidden, n_q, n_kv, D, seed=T + hidden)
     g = workloads._gen(7)
     pos = torch.randint(0, 393216, (T,), generator=g, dtype=torch.int32)
     w_q, w_k = workloads.norm_weight(D, g), workloads.norm_weight(D, g)
     out = F.gemm_prologue_forward(x.to(cuda), w.to(cuda), pos.to(cuda), w_q.to(cuda), w_k.to(cuda), n_q, n_kv, D,
-                                  kind, 1e-6, 5e5, save_pre=save)
+                                  kind, 1e-6, 5e5, nope=nope, save_pre=save)
     torch.cuda.synchronize()
     assert lib.qkv_prologue_device_error(clear=False) == 0
     L = P.PackedLayout(kind, n_q, n_kv, D)
-    ref, packed = P.gemm_prologue_fwd(L, u16(x), u16(w), pos.numpy(), w_q.numpy(), w_k.numpy(), 1e-6, 5e5)
+    ref, packed = P.gemm_prologue_fwd(L, u16(x), u16(w), pos.numpy(), w_q.numpy(), w_k.numpy(), 1e-6, 5e5,
+                                      nope=nope)
     assert_bf16_close(u16(out[0]), ref["q"], "q")
     assert_bf16_close(u16(out[1]), ref["k"], "k")
     assert np.array_equal(u16(out[2]), ref["v_bits"]), "v is the rounded product"
@@ -63,3 +74,76 @@ def test_gemm_prologue_equals_projection_then_prologue(lib, cuda):
     torch.cuda.synchronize()
     for a, b in zip(fused, unfused):
         assert_bf16_close(u16(a), b.double().cpu().numpy(), "fused vs unfused")
+
+
+def _ulp_distance(a_bits, b_bits):
+    """Distance in bf16 steps between finite bf16 patterns (sign-magnitude)."""
+    def key(b):
+        b = b.astype(np.int32)
+        return np.where(b & 0x8000, -(b & 0x7FFF), b)
+    return np.abs(key(np.asarray(a_bits)) - key(np.asarray(b_bits)))
+
+
+def _check_general_inputs(L, got, x_bits, w_bits, pos, w_q, w_k, nope, tokens=None):
+    """got = (q, k, v, q_pre, k_pre) bits of the kernel for the rows `tokens` of x."""
+    q, k, v, qp, kp = got
+    xs = x_bits if tokens is None else x_bits[tokens]
+    ps = pos if tokens is None else pos[tokens]
+    ref, packed = P.gemm_prologue_fwd(L, xs, w_bits, ps, w_q, w_k, 1e-6, 5e5, nope=nope)
+    # 1. the packed values the kernel hands its prologue: one bf16 ulp at most
+    rq, rk, rv = P.split_heads(L, packed)
+    dist = [_ulp_distance(g, r) for g, r in ((qp, rq), (kp, rk), (v, rv))]
+    assert max(int(d.max()) for d in dist) <= 1, "packed values within one bf16 ulp of the exact product"
+    n_off = sum(int((d != 0).sum()) for d in dist)
+    n_all = sum(d.size for d in dist)
+    assert n_off <= 0.01 * n_all, f"{n_off} of {n_all} packed values one ulp off"
+    # 2. q and k on every head whose packed values match bit for bit
+    for name, g, r, d in (("q", q, ref["q"], dist[0]), ("k", k, ref["k"], dist[1])):
+        same = ~(d != 0).any(axis=-1)                        # [T, heads]
+        assert same.mean() > 0.5
+        assert_bf16_close(g[same], r[same], f"{name} (heads with exact packed values)")
+    # 3. every head: the oracle's prologue of the kernel's own packed values
+    own = P.merge_heads(L, qp, kp, v)
+    ref2 = P.prologue_fwd(L, own, ps, w_q, w_k, 1e-6, 5e5, nope)
+    assert_bf16_close(q, ref2["q"], "q (prologue of the kernel's packed values)")
+    assert_bf16_close(k, ref2["k"], "k (prologue of the kernel's packed values)")
+    return n_off, n_all
+
+
+@pytest.mark.parametrize("nope", [False, True])
+def test_gemm_prologue_bench_inputs(lib, cuda, nope):
+    # the bench's distribution and hidden size on a ragged token count
+    F = lib.functional
+    T, hidden, n_q, n_kv, D = 300, 5120, 128, 16, 64
+    x, w = workloads.gemm_inputs(T, hidden, n_q, n_kv, D, seed=21, exact=False)
+    g = workloads._gen(22)
+    pos = torch.randint(0, 131072, (T,), generator=g, dtype=torch.int32)
+    w_q, w_k = workloads.norm_weight(D, g), workloads.norm_weight(D, g)
+    out = F.gemm_prologue_forward(x.to(cuda), w.to(cuda), pos.to(cuda), w_q.to(cuda), w_k.to(cuda), n_q, n_kv, D,
+                                  "interleaved", 1e-6, 5e5, nope=nope, save_pre=True)
+    torch.cuda.synchronize()
+    assert lib.qkv_prologue_device_error(clear=False) == 0
+    L = P.PackedLayout("interleaved", n_q, n_kv, D)
+    n_off, n_all = _check_general_inputs(L, [u16(t) for t in out], u16(x), u16(w), pos.numpy(), w_q.numpy(),
+                                         w_k.numpy(), nope)
+    print(f"packed values one bf16 ulp from the exact product: {n_off} of {n_all}")
+
+
+def test_gemm_prologue_bench_workload_full_size(lib, cuda):
+    # the bench's own workload and launch (T = 16384, hidden 5120, seed 9, pre-norm
+    # save), sampled tokens against the oracle token by token
+    F = lib.functional
+    T, hidden, n_q, n_kv, D = 16384, 5120, 128, 16, 64
+    wl = workloads.train(T)
+    x, w = workloads.gemm_inputs(T, hidden, n_q, n_kv, D, seed=9, exact=False)
+    out = F.gemm_prologue_forward(x.to(cuda), w.to(cuda), wl.pos.to(cuda), wl.w_q.to(cuda), wl.w_k.to(cuda), n_q,
+                                  n_kv, D, "interleaved", wl.eps, wl.rope_base, save_pre=True)
+    torch.cuda.synchronize()
+    assert lib.qkv_prologue_device_error(clear=False) == 0
+    g = workloads._gen(23)
+    tokens = np.unique(np.concatenate([[0, 127, 128, 255, 8191, T - 129, T - 1],
+                                       torch.randint(0, T, (57,), generator=g).numpy()]))
+    got = [u16(t[torch.from_numpy(tokens).to(cuda)]) for t in out]
+    assert all(bool(torch.isfinite(t.float()).all()) for t in out[:3])
+    L = P.PackedLayout("interleaved", n_q, n_kv, D)
+    _check_general_inputs(L, got, u16(x), u16(w), wl.pos.numpy(), wl.w_q.numpy(), wl.w_k.numpy(), False, tokens)

@@ -3,8 +3,9 @@
 Tokens are independent, so N GPUs each take a token shard (or, in bench.py's weak
 scaling, a full per-GPU batch) and nothing is exchanged in the forward. The one
 cross-token quantity is the RMSNorm weight gradient: summed over the shards it
-must equal the gradient over all tokens. bench.py's rank aggregation (max of the
-per-rank times, total bytes over ranks) is checked here as well.
+must equal the gradient over all tokens. The rank bookkeeping of
+rope_qkv_prologue_gb300.replicas (token shards, the gradient sum, the max of
+the per-rank times, total bytes over ranks) is checked here as well.
 """
 
 import os
@@ -25,8 +26,8 @@ def _worker(rank, world, port, out):
     import torch
     import torch.distributed as dist
 
-    import bench
     import oracle.prologue as P
+    from rope_qkv_prologue_gb300 import replicas
     import workloads
     from workloads import bits_u16 as u16
 
@@ -37,15 +38,15 @@ def _worker(rank, world, port, out):
         wl = workloads.gqa_inputs(24, 8, 2, 64, seed=77, rope_base=5e5, pos_high=131072, with_grads=True)
         L = P.PackedLayout("interleaved", 8, 2, 64)
         xq, xk, _ = P.split_heads(L, u16(wl.packed_rows()))
-        sl = slice(rank * wl.T // world, (rank + 1) * wl.T // world)   # this rank's token shard
+        sl = slice(*replicas.token_shard(wl.T, rank, world))           # this rank's token shard
         r = P.prologue_bwd(L, u16(wl.dq)[sl], u16(wl.dk)[sl], u16(wl.dv)[sl], xq[sl], xk[sl], wl.pos.numpy()[sl],
                            wl.w_q.numpy(), wl.w_k.numpy(), wl.eps, wl.rope_base)
         dw = torch.from_numpy(np.concatenate([r["dw_q"], r["dw_k"]]))
-        dist.all_reduce(dw)  # the data-parallel gradient all-reduce
+        replicas.sum_over_ranks(dw)  # the data-parallel gradient all-reduce
         shard_dp = torch.from_numpy(r["dpacked"])
         gathered = [torch.empty_like(shard_dp) for _ in range(world)]
         dist.all_gather(gathered, shard_dp)
-        ms = bench.max_over_ranks([1.0 + rank, 10.0 - rank], "cpu")
+        ms = replicas.max_over_ranks([1.0 + rank, 10.0 - rank], "cpu")
         if rank == 0:
             out.put({"dw": dw.numpy(), "dpacked": torch.cat(gathered).numpy(), "ms": ms})
     finally:
@@ -80,7 +81,20 @@ def test_token_shards_and_dw_allreduce_match_the_whole_batch():
 
 
 def test_whole_job_throughput_counts_every_rank():
-    import bench
+    from rope_qkv_prologue_gb300 import replicas
 
-    assert bench.whole_job_gbs(1e9, 1, 1.0) == pytest.approx(1000.0)
-    assert bench.whole_job_gbs(1e9, 4, 2.0) == pytest.approx(2000.0)
+    assert replicas.whole_job_gbs(1e9, 1, 1.0) == pytest.approx(1000.0)
+    assert replicas.whole_job_gbs(1e9, 4, 2.0) == pytest.approx(2000.0)
+
+
+def test_token_shards_cover_the_batch_once():
+    from rope_qkv_prologue_gb300 import replicas
+
+    for T in (0, 1, 7, 16384, 16385):
+        for world in (1, 2, 3, 8):
+            spans = [replicas.token_shard(T, r, world) for r in range(world)]
+            assert spans[0][0] == 0 and spans[-1][1] == T
+            assert all(a[1] == b[0] for a, b in zip(spans, spans[1:]))
+            assert max(b - a for a, b in spans) - min(b - a for a, b in spans) <= 1
+    with pytest.raises(ValueError):
+        replicas.token_shard(10, 2, 2)

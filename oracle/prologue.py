@@ -358,15 +358,19 @@ def prologue_bwd(layout, dq_bits, dk_bits, dv_bits, q_pre_bits, k_pre_bits,
 # The projection to the left of the path, with the prologue after it
 # --------------------------------------------------------------------------
 
-def projection(x_bits, w_bits):
-    """The wqkv projection: packed = x . W^T for x [T, hidden] and W
-    [row_width, hidden] (nn.Linear's weight layout, rows in the layout's
-    packed order), both bf16 bits. Every product of two bf16 values is exact in
-    float64 and the float64 sum is rounded once to bf16: the packed tensor the
-    projection hands to the prologue ("[muse_spark][perf] ...", Problem 1)."""
+def projection_f64(x_bits, w_bits):
+    """The wqkv projection x . W^T for x [T, hidden] and W [row_width, hidden]
+    (nn.Linear's weight layout, rows in the layout's packed order), both bf16
+    bits, in float64: every product of two bf16 values is exact in float64."""
     x = bf16_bits_to_f64(np.asarray(x_bits, dtype=np.uint16))
     w = bf16_bits_to_f64(np.asarray(w_bits, dtype=np.uint16))
-    return to_bf16_rne(x @ w.T)
+    return x @ w.T
+
+
+def projection(x_bits, w_bits):
+    """projection_f64 rounded once to bf16: the packed tensor the projection
+    hands to the prologue ("[muse_spark][perf] ...", Problem 1)."""
+    return to_bf16_rne(projection_f64(x_bits, w_bits))
 
 
 def gemm_prologue_fwd(layout, x_bits, w_bits, pos, w_q, w_k, eps, rope_base, nope=False, **variant):

@@ -176,17 +176,16 @@ def _blocks_any_multiple(rows, n_q, n_kv, head_dim):
 
 def _projection_w_not_transposed(x_bits, w_bits):
     x, w = B.bf16_bits_to_f64(x_bits), B.bf16_bits_to_f64(w_bits)
-    return B.to_bf16_rne(x @ w)
+    return x @ w
 
 
 def _projection_via_float32(x_bits, w_bits):
-    x, w = B.bf16_bits_to_f64(x_bits), B.bf16_bits_to_f64(w_bits)
-    return _bf16_via_float32((x @ w.T).astype(np.float32).astype(np.float64))
+    return _bf16_via_float32(P.projection_f64(x_bits, w_bits).astype(np.float32).astype(np.float64))
 
 
 def _projection_rows_reversed(x_bits, w_bits):
     x, w = B.bf16_bits_to_f64(x_bits), B.bf16_bits_to_f64(w_bits)
-    return B.to_bf16_rne(x @ w[::-1].T)
+    return x @ w[::-1].T
 
 
 def _checks_all(rng):
@@ -241,9 +240,9 @@ MUTATIONS = [
     (N, "per_head_newton_schulz", _per_head_global_norm),
     (N, "fused_head_blocks", _blocks_any_multiple),
     (N, "full_matrix_scale", _full_scale_cols_over_rows),
-    (P, "projection", _projection_w_not_transposed),
+    (P, "projection_f64", _projection_w_not_transposed),
     (P, "projection", _projection_via_float32),
-    (P, "projection", _projection_rows_reversed),
+    (P, "projection_f64", _projection_rows_reversed),
 ]
 
 

@@ -275,7 +275,7 @@ class _Step:
 class TrainStep(_Step):
     """Training forward (with the pre-norm save) + backward, Muse Spark packing."""
 
-    kernels_per_step = 3  # forward, backward, dw finalize
+    kernels_per_step = 2  # forward, backward (the last CTA of the backward adds the weight-gradient rows)
 
     def __init__(self, dev, T):
         import torch
@@ -306,7 +306,7 @@ class TrainStep(_Step):
         self.eps, self.base = wl.eps, wl.rope_base
         self.calls = [("qkv_prologue_fwd (qkvp_fwd_stream_kernel, save_pre)", self.fwd,
                        T * fwd_bytes_per_token(True) + WEIGHT_BYTES),
-                      ("qkv_prologue_bwd (qkvp_bwd_stream_kernel + dw finalize)", self.bwd,
+                      ("qkv_prologue_bwd (qkvp_bwd_stream_kernel, weight-gradient fold in its last CTA)", self.bwd,
                        T * bwd_bytes_per_token() + 2 * WEIGHT_BYTES)]
         self.h_in = {"packed": wl.packed_rows(), "pos": wl.pos, "w_q": wl.w_q, "w_k": wl.w_k,
                      "dq": wl.dq, "dk": wl.dk, "dv": wl.dv}
@@ -466,7 +466,7 @@ class VariantTrainStep(_Step):
         small = (2 * hd * 4 if wl.norm else 0) + (row * 4 if wl.bias is not None else 0)
         fwd_b = T * (row * bf2 + 4 + row * bf2 + (saved if wl.norm else 0)) + small
         bwd_b = T * (row * bf2 + (saved if wl.norm else 0) + 4 + row * bf2) + small
-        self.kernels_per_step = 3 if (wl.norm or wl.bias is not None) else 2
+        self.kernels_per_step = 3 if wl.bias is not None else 2  # a bias gradient needs the finalize kernel
         self.calls = [(f"qkv_prologue_fwd_ex (qkvp_fwd_stream_kernel, {model})", self.fwd, fwd_b),
                       (f"qkv_prologue_bwd_ex (qkvp_bwd_stream_kernel{' + finalize' if self.kernels_per_step == 3 else ''},"
                        f" {model})", self.bwd, bwd_b)]

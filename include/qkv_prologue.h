@@ -236,6 +236,12 @@ QKVP_API size_t qkv_prologue_bwd_workspace_size(const qkvp_layout* layout, int64
  *         gradient. Overwritten, or added to with QKVP_ACCUMULATE_DW.
  * workspace   device scratch of at least qkv_prologue_bwd_workspace_size
  *         bytes (any contents; 16-byte aligned); QKVP_ERR_WORKSPACE if smaller.
+ *         It holds per-CTA partial sums of the weight gradients and, at its
+ *         end, one arrival word per CTA and an election word: the CTA of the
+ *         backward kernel that finishes last adds the partial rows (fixed
+ *         order: deterministic) into dw_q, dw_k itself. The words need no
+ *         clearing (each call tags them with its own generation). Two calls
+ *         whose work can overlap on the GPU must not share a workspace.
  * GQA layouts only.
  * ------------------------------------------------------------------------- */
 QKVP_API int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* dq, const void* dk,
@@ -253,16 +259,16 @@ QKVP_API int qkv_prologue_bwd(const qkvp_layout* layout, int64_t T, const void* 
  * pool, or a latency-critical loop where cudaMalloc (which can synchronise
  * the device) is not allowed. Same arguments, results and errors as
  * qkv_prologue_bwd, minus the workspace: the weight-gradient partial sums go
- * to a fixed 512 KiB array inside the library's device memory, which every
+ * to a fixed 520 KiB array inside the library's device memory, which every
  * GPU that loads the library holds until the process exits.
  *  - Limit: with the norm on, qkv_prologue_bwd_workspace_size(layout, T)
- *    must be <= 512 KiB, otherwise QKVP_ERR_WORKSPACE is returned and nothing
+ *    must be <= 520 KiB, otherwise QKVP_ERR_WORKSPACE is returned and nothing
  *    is enqueued. That size is min(1024, max(T, n_items)) partial rows of
- *    2 * head_dim floats, n_items = ceil(T * (n_q + 2 n_kv) * head_dim / 8 /
- *    1536): head_dim 64 always fits (at most 1024 rows of 512 B); head_dim 128
- *    fits while max(T, n_items) <= 512 (e.g. n_q 32, n_kv 8: 512 tokens;
- *    n_q 128, n_kv 16: 307 tokens). With QKVP_NORM_OFF no scratch is needed
- *    and every T is accepted.
+ *    2 * head_dim floats plus 4112 bytes of arrival words, n_items =
+ *    ceil(T * (n_q + 2 n_kv) * head_dim / 8 / 1536): head_dim 64 always fits
+ *    (at most 1024 rows of 512 B); head_dim 128 fits while max(T, n_items)
+ *    <= 515 (e.g. n_q 32, n_kv 8: 515 tokens; n_q 128, n_kv 16: 309 tokens).
+ *    With QKVP_NORM_OFF no scratch is needed and every T is accepted.
  *  - The first call on each device looks up the array's device address (with
  *    that device current) and caches it; make that first call before any
  *    stream capture. The cache outlives a cudaDeviceReset: do not use this

@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "launch.h"
@@ -850,7 +851,10 @@ static int64_t bwd_row_floats(const qkvp_layout* layout, bool norm, bool bias) {
   return (norm ? 2 * layout->head_dim : 0) + (bias ? heads * layout->head_dim : 0);
 }
 
-static size_t bwd_workspace(const qkvp_layout* layout, const Variant& vr, bool norm, int64_t T) {
+// Bytes of the partial rows; the workspace is these rows followed by
+// kFoldBytes for the weight-gradient fold's arrival words (one per CTA, at
+// most kMaxBwdParts) and its election word.
+static size_t bwd_rows_bytes(const qkvp_layout* layout, const Variant& vr, bool norm, int64_t T) {
   Gqa g;
   if (check_gqa(layout, T, &g) != QKVP_OK || T == 0) return 0;
   int64_t item_chunks = 0, n_items = 0;
@@ -858,6 +862,20 @@ static size_t bwd_workspace(const qkvp_layout* layout, const Variant& vr, bool n
   gqa_items(T, g.heads * (layout->head_dim / 8), kBwdChunksPerThread, &item_chunks, &n_items, &max_tok);
   return (size_t)bwd_parts(n_items > T ? n_items : T) * (size_t)bwd_row_floats(layout, norm, vr.bias != nullptr) *
          sizeof(float);
+}
+
+constexpr size_t kFoldBytes = 4 * (kMaxBwdParts + 4);
+
+static size_t bwd_workspace(const qkvp_layout* layout, const Variant& vr, bool norm, int64_t T) {
+  const size_t rows = bwd_rows_bytes(layout, vr, norm, T);
+  return rows ? rows + kFoldBytes : 0;
+}
+
+// A new generation for the fold's arrival word on every call (never 0).
+static uint32_t next_call_id() {
+  static std::atomic<uint32_t> counter{0x9e3779b9u};
+  uint32_t id = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  return id ? id : counter.fetch_add(1, std::memory_order_relaxed) + 1;
 }
 
 size_t qkv_prologue_bwd_workspace_size(const qkvp_layout* layout, int64_t T) {
@@ -989,8 +1007,18 @@ int qkv_prologue_bwd_ex(const qkvp_layout* layout, const qkvp_variant* variant, 
   float* ws = static_cast<float*>(workspace);
   a.partials = ws;
   a.db_partials = ws + (norm ? grid * 2 * hd : 0);
+  // The pipelined kernel with the norm and no bias adds its own partial rows
+  // (the last CTA to finish); otherwise the finalize kernel does.
+  const bool fold = streamed && norm && !bias;
+  if (fold) {
+    a.flags = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(workspace) + bwd_rows_bytes(layout, vr, norm, T));
+    a.call_id = next_call_id();
+    a.accumulate = accumulate ? 1 : 0;
+    a.dw_q = dw_q;
+    a.dw_k = dw_k;
+  }
   QKVP_TRY(launch(kern, grid, threads, smem, s, &a));
-  if (!norm && !bias) return QKVP_OK;
+  if (fold || (!norm && !bias)) return QKVP_OK;
 
   FinalizeArgs f;
   std::memset(&f, 0, sizeof(f));

@@ -30,7 +30,10 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = 512 * 1024;
+// 520 KiB: up to 512 KiB of partial rows (head_dim 64 always fits: at most
+// 1024 rows of 512 bytes) and, after them, the 4112 bytes of arrival and
+// election words of the weight-gradient fold.
+constexpr size_t kScratchBytes = 520 * 1024;
 constexpr int kMaxDevices = 64;
 
 // Weight-gradient partial sums of qkv_prologue_bwd_noalloc. In host code this

@@ -49,7 +49,7 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_latent_stream_kernel
     };
     stream_producer<HD / 2, false, POOL, ROPE>(smem, HD, tpt, stages, stage_bytes, a.sg.n_tiles,
                                                               a.T, a.pos, a.rope, a.page, a.offset, a.num_pages,
-                                                              a.page_size, a.dev_status, a.err, load);
+                                                              a.page_size, a.dev_status, a.err, true, load);
     return;
   }
 

@@ -142,6 +142,14 @@ struct BwdArgs {
   int64_t row_stride16;
   float* partials;        // [grid][2][head_dim] (norm on)
   float* db_partials;     // [grid][cpt * 8] (bias given)
+  // Weight-gradient fold of the pipelined kernel (norm on, no bias): the CTA
+  // that finishes last adds the partial rows (fixed order) into dw_q / dw_k
+  // itself, so no finalize kernel runs. null flags: the finalize kernel does it.
+  uint32_t* flags;             // [grid] per-CTA arrival words, then the election word
+  uint32_t call_id;            // this call's generation (never 0)
+  int32_t accumulate;          // add to dw_q / dw_k instead of overwriting
+  float* dw_q;
+  float* dw_k;
   const float* bias;      // [cpt * 8] in packed-row order, or null
   int* err;
   StreamGeom sg;

@@ -77,10 +77,53 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
   return true;
 }
 
+// Grid-wide "who finished last" without a counter that would need clearing:
+// CTA b publishes the call's generation in its own word flags[b]
+// (release: everything it wrote before is visible to a reader that sees the
+// flag), then an SC fence, then reads every CTA's word. The CTA whose fence
+// comes last in the fences' total order sees every flag, so at least one CTA
+// sees all of them; the first of those to swap the call's generation into
+// the election word wins. Words left by earlier calls (other generations) or
+// any initial contents count as "not arrived".
+__device__ __forceinline__ void fence_sc_gpu() { asm volatile("fence.sc.gpu;" ::: "memory"); }
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// One warp (all 32 lanes) of CTA `me` of `n`: publish, look, elect. Returns
+// true (in every lane) for exactly one CTA of the call. The caller orders
+// the data it publishes before this (a fence by every writer, then a barrier).
+__device__ __forceinline__ bool warp_publish_and_elect(uint32_t* flags, uint32_t* elect, uint32_t me, uint32_t n,
+                                                       uint32_t gen) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) st_relaxed_gpu(flags + me, gen);
+  __syncwarp();
+  fence_sc_gpu();
+  bool all = true;
+  for (uint32_t i = lane; i < n; i += 32) all &= ld_relaxed_gpu(flags + i) == gen;
+  all = __all_sync(0xffffffffu, all);
+  uint32_t won = 0;
+  if (all && lane == 0) won = atomicExch(elect, gen) != gen ? 1u : 0u;
+  return __shfl_sync(0xffffffffu, won, 0) != 0;
+}
+
 // L2 policy for data read exactly once.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// The default L2 policy (lines age like any other).
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 

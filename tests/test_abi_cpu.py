@@ -93,11 +93,14 @@ def test_layout_struct_matches_c_layout(lib):
 def test_workspace_size(lib):
     L = lib.layout("interleaved", 128, 16, 64)
     assert lib.qkv_prologue_bwd_workspace_size(L, 0) == 0
-    # one partial row [2, 64] fp32 per CTA, at most 1024 rows
-    assert lib.qkv_prologue_bwd_workspace_size(L, 1) == 512
+    # one partial row [2, 64] fp32 per CTA, at most 1024 rows, then the weight-
+    # gradient fold's words: one per possible CTA (1024) and the election word,
+    # padded to 16 bytes (4112 bytes)
+    fold = 4 * (1024 + 4)
+    assert lib.qkv_prologue_bwd_workspace_size(L, 1) == 512 + fold
     for T in range(1, 40):  # at least one row per token up to the cap
-        assert lib.qkv_prologue_bwd_workspace_size(L, T) >= 512 * T
-    assert lib.qkv_prologue_bwd_workspace_size(L, 16384) == 1024 * 512
+        assert lib.qkv_prologue_bwd_workspace_size(L, T) >= 512 * T + fold
+    assert lib.qkv_prologue_bwd_workspace_size(L, 16384) == 1024 * 512 + fold
     assert lib.qkv_prologue_bwd_workspace_size(lib.layout("interleaved", 8, 3, 64), 16) == 0
     assert lib.qkv_prologue_bwd_workspace_size(lib.layout("interleaved", 32, 8, 128), 100) > 0
 

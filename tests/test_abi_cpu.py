@@ -277,7 +277,9 @@ def test_variant_argument_checks(lib):
     need = C.qkv_prologue_bwd_workspace_size_ex(L, V, 100)
     assert need > C.qkv_prologue_bwd_workspace_size(L, 100)
     # one row per CTA now also holds the bias gradient's F floats
-    assert need == C.qkv_prologue_bwd_workspace_size(L, 100) // (2 * 64) * (2 * 64 + F)
+    fold = 4 * (1024 + 4)  # the fold's words after the rows
+    rows = (C.qkv_prologue_bwd_workspace_size(L, 100) - fold) // (4 * 2 * 64)
+    assert need == rows * 4 * (2 * 64 + F) + fold
     assert C.qkv_prologue_bwd_workspace_size_ex(L, None, 100) == C.qkv_prologue_bwd_workspace_size(L, 100)
 
     def bwd(V, flags=0, qp=A, kp=A, wq=A, wk=A, dwq=A, dwk=A, db=A, ws=A, wsb=need, L=L):

@@ -1067,12 +1067,20 @@ int qkv_prologue_gemm_fwd(const qkvp_layout* layout, int64_t T, int32_t hidden, 
 
   int sms = 0;
   QKVP_TRY(current_device(&sms));
-  // The tensor maps must cover this GPU's own memory: x and w_qkv are read by
-  // the tensor-memory copy engine of the current device only.
-  if (!on_current_device(x) || !on_current_device(w_qkv)) return QKVP_ERR_VALUE;
+  // The tensor maps must cover this GPU's own memory: x and w_qkv are read and
+  // the outputs written by this GPU's tensor-memory-access (TMA) unit only.
+  const void* dev_ptrs[] = {x, w_qkv, q, k, v, save ? q_pre : nullptr, save ? k_pre : nullptr};
+  for (const void* ptr : dev_ptrs)
+    if (ptr && !on_current_device(ptr)) return QKVP_ERR_VALUE;
   CUtensorMap tx, tw;
   if (!bf16_tile_map(&tx, x, T, hidden, kGemmBM) || !bf16_tile_map(&tw, w_qkv, g.heads * (int64_t)layout->head_dim,
                                                                     hidden, kGemmBN / 2))
+    return QKVP_ERR_LAUNCH;
+  GemmOutMaps om;
+  const int64_t qcols = (int64_t)layout->n_q * layout->head_dim, kcols = (int64_t)layout->n_kv * layout->head_dim;
+  if (!bf16_tile_map(&om.q, q, T, qcols, 32) || !bf16_tile_map(&om.k, k, T, kcols, 32) ||
+      !bf16_tile_map(&om.v, v, T, kcols, 32) || !bf16_tile_map(&om.q_pre, save ? q_pre : q, T, qcols, 32) ||
+      !bf16_tile_map(&om.k_pre, save ? k_pre : k, T, kcols, 32))
     return QKVP_ERR_LAUNCH;
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -1083,10 +1091,9 @@ int qkv_prologue_gemm_fwd(const qkvp_layout* layout, int64_t T, int32_t hidden, 
   a.group = layout->n_q / layout->n_kv;
   a.n_blocks = g.heads;
   a.gs_magic = magic((uint32_t)(a.group + 2));
-  a.m_tiles = (int32_t)((T + kGemmBM - 1) / kGemmBM);
+  a.m_tiles = (int32_t)((T + 2 * kGemmBM - 1) / (2 * kGemmBM));
   a.n_tiles = (int32_t)((g.row + kGemmBN - 1) / kGemmBN);
-  a.m_pairs = (a.m_tiles + 1) / 2;
-  a.n_work = (int64_t)a.m_pairs * a.n_tiles;
+  a.n_work = (int64_t)a.m_tiles * a.n_tiles;
   a.pos = pos;
   a.w_q = w_q;
   a.w_k = w_k;
@@ -1106,7 +1113,7 @@ int qkv_prologue_gemm_fwd(const qkvp_layout* layout, int64_t T, int32_t hidden, 
   const int clusters = max_clusters_of_2(kern, threads, smem);
   if (clusters < 1) return QKVP_ERR_LAUNCH;
   const int64_t grid = 2 * (a.n_work < clusters ? a.n_work : clusters);
-  void* args[] = {&tx, &tw, &a};
+  void* args[] = {&tx, &tw, &om, &a};
   return launch_args(kern, grid, threads, smem, static_cast<cudaStream_t>(stream), args, 2);
 }
 

@@ -2,6 +2,7 @@
 // Plain structs of device pointers and sizes, passed to the kernels by value.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -264,15 +265,16 @@ constexpr int kFinalizeOutputsPerCta = 4;
 constexpr int kFinalizeThreads = 256;
 
 // The wqkv projection with the prologue in its epilogue (tcgen05): tile of
-// kGemmBM tokens x kGemmBN packed columns, kGemmBK per pipeline stage.
+// a CTA pair computes 2 kGemmBM tokens x kGemmBN packed columns (each CTA
+// holds kGemmBM token rows of it), kGemmBK per pipeline stage.
 constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64;
 struct GemmArgs {
   int64_t T;              // tokens (rows of x)
   int32_t hidden;         // K: columns of x and W
   int32_t n_q, n_kv, group, n_blocks;  // n_blocks = n_q + 2 n_kv head blocks of the packed row
   uint32_t gs_magic;      // floor(2^32 / (group + 2)) + 1
-  int32_t m_tiles, n_tiles, m_pairs;  // m_pairs = ceil(m_tiles / 2): work items pair two M tiles
-  int64_t n_work;         // m_pairs * n_tiles
+  int32_t m_tiles, n_tiles;  // M tiles of 2 kGemmBM tokens (one per CTA pair), N tiles of kGemmBN columns
+  int64_t n_work;         // m_tiles * n_tiles
   const int32_t* pos;
   const float* w_q;
   const float* w_k;
@@ -285,6 +287,12 @@ struct GemmArgs {
   uint4* k_pre;
   int* err;
   RopeTable rope;
+};
+// Tensor maps of the projection kernel's outputs, each the 2-D view
+// [T, heads * head_dim] bf16 read in boxes of 64 columns x 32 tokens with the
+// 128-byte swizzle (the epilogue stores its tiles with TMA).
+struct GemmOutMaps {
+  CUtensorMap q, k, v, q_pre, k_pre;
 };
 const void* gemm_fwd_kernel(int head_dim, bool sectioned, bool rope, bool save);
 int gemm_fwd_smem_bytes();

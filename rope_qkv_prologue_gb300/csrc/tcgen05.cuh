@@ -30,6 +30,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// The same load for a CTA pair working on one 2-SM MMA (cta_group::2): the
+// data lands in this CTA's shared memory, the completed bytes are counted on
+// the mbarrier at cluster address `bar_cluster` (the leader CTA's barrier).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int c0, int c1,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(bar_cluster)
+      : "memory");
+}
+
 // True when the grid was launched with an explicit thread-block cluster
 // (required by st.async, even for a cluster of one CTA).
 __device__ __forceinline__ bool is_explicit_cluster() {
@@ -99,6 +111,50 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
                : "memory");
+}
+
+// The 2-SM forms (cta_group::2), issued by the pair's leader CTA: A is the
+// two CTAs' 128-row halves and B the two CTAs' N-halves at the same shared-
+// memory offsets; D is M = 256 rows, rows 0-127 in the leader's tensor memory
+// and 128-255 in the peer's, at the same address.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on this CTA's `bar` when every cta_group::2 tcgen05 operation
+// this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// Whole warp, in both CTAs of the pair together: allocate `cols` columns of
+// tensor memory at the same address in both (written to *slot in each), then
+// give up the right to allocate more; and the matching free.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)), "r"(cols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t addr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(addr), "r"(cols) : "memory");
+}
+
+// Arrive on an mbarrier of a CTA of the cluster (cluster address) with the
+// instruction's default semantics (release at CTA scope). A release at
+// cluster scope costs a cluster-wide memory barrier on every call (measured:
+// it starved the 2-SM MMA pipeline when issued once per stage); the events
+// passed on this way are completions of asynchronous operations (tensor-core
+// reads and writes, tcgen05.ld) that the arriving thread has itself waited
+// for.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -217,5 +273,8 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Wait until every bulk group of this thread has finished reading its shared-
+// memory source (the writes to global memory may still be in flight).
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 }  // namespace qkvp

@@ -27,10 +27,14 @@
 //                CTA for half of the tile's head blocks, so thread i owns
 //                token row i and holds every value of a head itself: the
 //                RMSNorm sum and the rotate-half pairs need no shuffles. The
-//                leader's epilogue passes "accumulator ready" on to the peer;
-//                both CTAs' epilogue warps report "accumulator drained" to the
-//                leader's MMA issuer. While they work on one accumulator the
-//                MMAs fill the other.
+//                values are rounded to bf16 as they leave tensor memory (kept
+//                as bf16 pairs) and, for head_dim 64, the accumulator is
+//                handed back before any arithmetic; results leave through a
+//                per-warp 128B-swizzled buffer as TMA stores of 32-token x
+//                64-value boxes. The leader's epilogue passes "accumulator
+//                ready" on to the peer; both CTAs' epilogue warps report
+//                "accumulator drained" to the leader's MMA issuer. While they
+//                work on one accumulator the MMAs fill the other.
 // Work items (256-token M tiles x 256-column N tiles) go M-fastest inside
 // groups of 16 M tiles, so the 4096 x rows of a group stay in L2 while the W
 // tiles stream past (W is read from DRAM once per group). Every wait is
@@ -101,19 +105,14 @@ struct UnitStore {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// One head block of the tile for this thread's token row: the head's fp32
-// accumulator columns are loaded once and rounded to bf16 (the packed value,
-// kept as bf16 pairs: half the registers), then the norm sum, the scaling
-// and the rotation run on registers; the results go out through the warp's
-// staging buffer (UnitStore). Rows past T are clipped by the tensor maps.
-template <int HD, bool SECTIONED, bool ROPE, bool SAVE>
-__device__ __forceinline__ void gemm_epilogue_head(const GemmArgs& a, const GemmOutMaps& m, const float* s_w,
-                                                   uint32_t col0, int32_t p, int hb, const UnitStore& st) {
-  constexpr int HALF = HD / 2, UNITS = HD / 64;
-  int role;
-  uint32_t oh;
-  classify<SECTIONED>((uint32_t)hb, a.n_q, a.n_kv, a.group, a.gs_magic, role, oh);
-  uint32_t xb[HD / 2];  // element 2i in the low half of xb[i], 2i + 1 in the high half
+// One head block of the tile for this thread's token row, from its rounded
+// packed values (gemm_load_head): the norm sum, the scaling and the rotation
+// run on registers; the results go out through the warp's staging buffer
+// (UnitStore). Rows past T are clipped by the tensor maps.
+// The head's fp32 accumulator columns for this thread's token row, rounded to
+// bf16 pairs: element 2i in the low half of xb[i], 2i + 1 in the high half.
+template <int HD>
+__device__ __forceinline__ void gemm_load_head(uint32_t col0, uint32_t (&xb)[HD / 2]) {
 #pragma unroll
   for (int c = 0; c < HD; c += 32) {
     float v[32];
@@ -121,6 +120,16 @@ __device__ __forceinline__ void gemm_epilogue_head(const GemmArgs& a, const Gemm
 #pragma unroll
     for (int i = 0; i < 16; ++i) xb[c / 2 + i] = pack2(v[2 * i], v[2 * i + 1]);
   }
+}
+
+template <int HD, bool SECTIONED, bool ROPE, bool SAVE>
+__device__ __forceinline__ void gemm_epilogue_head(const GemmArgs& a, const GemmOutMaps& m, const float* s_w,
+                                                   const uint32_t (&xb)[HD / 2], int32_t p, int hb,
+                                                   const UnitStore& st) {
+  constexpr int HALF = HD / 2, UNITS = HD / 64;
+  int role;
+  uint32_t oh;
+  classify<SECTIONED>((uint32_t)hb, a.n_q, a.n_kv, a.group, a.gs_magic, role, oh);
   auto xv = [&](int e) { return (e & 1) ? bf_hi(xb[e >> 1]) : bf_lo(xb[e >> 1]); };
   const int col = (int)oh * HD;  // the head's first column in its output's 2-D view
   if (role == kRoleV || SAVE) {  // the packed values themselves: v, or the pre-norm save
@@ -329,17 +338,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       st.row0 = mt * 2 * kGemmBM + (int)rank * kGemmBM + qtr * 32;
       const int64_t t = (int64_t)st.row0 + lane;
       const int32_t p = (ROPE && t < a.T) ? a.pos[t] : 0;
-#pragma unroll 1
-      for (int j = part * PER; j < (part + 1) * PER; ++j) {
-        const int hb = nt * HEADS + j;
-        if (hb >= a.n_blocks) break;  // the same for the whole warp
-        gemm_epilogue_head<HD, SECTIONED, ROPE, SAVE>(a, maps, s_w,
-                                                      tmem + b * kGemmBN + lane_base + (uint32_t)(j * HD), p, hb, st);
+      if constexpr (PER > 1) {
+        // Take this warp's columns out of tensor memory first and hand the
+        // accumulator back at once: the MMAs of the tile after next never
+        // wait for the epilogue's arithmetic and stores.
+        uint32_t xb[PER][HD / 2];
+#pragma unroll
+        for (int j = 0; j < PER; ++j)
+          if (nt * HEADS + part * PER + j < a.n_blocks)  // the same for the whole warp
+            gemm_load_head<HD>(tmem + b * kGemmBN + lane_base + (uint32_t)((part * PER + j) * HD), xb[j]);
+        tc_fence_before();
         __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty0 + b * 8u);  // this warp is done with accumulator b
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+          const int hb = nt * HEADS + part * PER + j;
+          if (hb < a.n_blocks) gemm_epilogue_head<HD, SECTIONED, ROPE, SAVE>(a, maps, s_w, xb[j], p, hb, st);
+          __syncwarp();
+        }
+      } else {
+        // one head of 128 per warp: its 64 packed registers stay live through
+        // the arithmetic, so the accumulator is handed back after it (holding
+        // the loads in registers across the hand-back spilled)
+        const int hb = nt * HEADS + part;
+        if (hb < a.n_blocks) {
+          uint32_t xb[HD / 2];
+          gemm_load_head<HD>(tmem + b * kGemmBN + lane_base + (uint32_t)(part * HD), xb);
+          gemm_epilogue_head<HD, SECTIONED, ROPE, SAVE>(a, maps, s_w, xb, p, hb, st);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty0 + b * 8u);  // this warp is done with accumulator b
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty0 + b * 8u);  // this warp is done with accumulator b
     }
     if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
   }

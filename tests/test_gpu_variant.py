@@ -296,18 +296,45 @@ def test_variant_backward_deterministic_and_accumulate(lib, cuda):
     assert torch.allclose(acc, ref, rtol=1e-6, atol=1e-6)
 
 
-@pytest.mark.parametrize("model", ["llama3", "gpt_oss"])
+def _check_bwd_all(wl, kind, got, what, chunk=2048):
+    """The packed gradient of every token (chunk by chunk) and the weight and
+    bias gradients over all tokens (sums of the chunks' float64 sums)."""
+    dp, dwq, dwk, db = got
+    L = _layout(wl, kind)
+    xq, xk, _ = P.split_heads(L, u16(_rows(wl, kind)))
+    dq, dk, dv = u16(wl.dq), u16(wl.dk), u16(wl.dv)
+    pos, opts = wl.pos.numpy(), _oracle_opts(wl, kind)
+    wq, wk = wl.w_q.numpy(), wl.w_k.numpy()
+    got_dp = u16(dp)
+    rq, rk, rb = np.zeros(wl.head_dim), np.zeros(wl.head_dim), np.zeros(wl.row_width)
+    for s in range(0, wl.T, chunk):
+        sl = slice(s, min(wl.T, s + chunk))
+        r = P.prologue_bwd(L, dq[sl], dk[sl], dv[sl], xq[sl], xk[sl], pos[sl], wq, wk, wl.eps, wl.rope_base,
+                           wl.nope, **opts)
+        assert_bf16_close(got_dp[sl], r["dpacked"], f"{what} dpacked tokens {s}+")
+        rq += r["dw_q"]
+        rk += r["dw_k"]
+        if r["db"] is not None:
+            rb += r["db"]
+    if wl.norm:
+        assert_dw_close(dwq.cpu().numpy(), rq, f"{what} dw_q")
+        assert_dw_close(dwk.cpu().numpy(), rk, f"{what} dw_k")
+    if wl.bias is not None:
+        assert_dw_close(db.cpu().numpy(), rb, f"{what} db")
+
+
+@pytest.mark.parametrize("model", list(MODELS))
 def test_variant_train_full_size(lib, cuda, model):
-    # the bench's training step (T = 16384, sectioned rows), sampled tokens and all-token sums
+    # the bench's training step (T = 16384, sectioned rows): every token of the
+    # forward and of the packed gradient against the oracle, sums over all tokens
     T = 16384
     wl = MODELS[model](T)
     out = _gpu_fwd(lib, wl, "sectioned", cuda, save=wl.norm)
     got = _gpu_bwd(lib, wl, "sectioned", cuda, out[3:5] if wl.norm else None)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(T)
-    tokens = np.unique(np.concatenate([[0, 1, T - 1], rng.choice(T, 200, replace=False)]))
-    _check_fwd(wl, "sectioned", out, tokens, what=f"{model} train fwd")
-    _check_bwd(wl, "sectioned", got, tokens, f"{model} train bwd")
+    for s in range(0, T, 2048):
+        _check_fwd(wl, "sectioned", out, np.arange(s, min(T, s + 2048)), what=f"{model} train fwd tokens {s}+")
+    _check_bwd_all(wl, "sectioned", got, f"{model} train bwd")
     if wl.bias is not None:
         # the bias gradient against the written packed gradient: they differ only by
         # dpacked's rounding to bf16 (at most 2^-9 relative per element)

@@ -962,7 +962,7 @@ int qkv_prologue_bwd_ex(const qkvp_layout* layout, const qkvp_variant* variant, 
   a.bias = vr.bias;
   if (rope) rope_table(rope_base, hd, vr.inv_freq, vr.scale, &a.rope);
 
-  const BwdVariant var{hd, layout->kind == QKVP_SECTIONED, rope, norm, bias};
+  BwdVariant var{hd, layout->kind == QKVP_SECTIONED, rope, norm, bias, 0};
   const int64_t heads_qkv = norm ? (2 * layout->n_q + 3 * layout->n_kv) : (layout->n_q + 2 * layout->n_kv);
   const int64_t token_bytes = heads_qkv * hd * 2;
   const StreamShape shape = bwd_stream_shape();
@@ -976,6 +976,7 @@ int qkv_prologue_bwd_ex(const qkvp_layout* layout, const qkvp_variant* variant, 
                       bias ? kBiasMaxSteps : kStreamMaxSteps, &a.sg, &smem) &&
       (a.err = device_error_word()) != nullptr) {
     a.sg.dense = 1;
+    var.steps = a.sg.steps;
     const void* kern = bwd_stream_kernel(var);
     const int threads = (shape.warps + 1) * 32;
     const int bps = allow_smem(kern, smem) ? blocks_per_sm(kern, threads, smem) : 0;

@@ -44,7 +44,7 @@ struct BwdPick {
   static const void* get() {
     if constexpr (STREAM) {
       constexpr StreamShape sh = bwd_stream_shape();
-      return reinterpret_cast<const void*>(&qkvp_bwd_stream_kernel<HD, S, R, NORM, B, sh.warps, sh.ctas_per_sm>);
+      return reinterpret_cast<const void*>(&qkvp_bwd_stream_kernel<HD, S, R, NORM, B, sh.warps, sh.ctas_per_sm, 0>);
     } else {
       return reinterpret_cast<const void*>(&qkvp_bwd_kernel<HD, S, R, NORM, B>);
     }
@@ -58,7 +58,21 @@ struct BwdPick {
     if (v.sectioned) return v.rope ? bias<HD, true, true>(v) : bias<HD, true, false>(v);
     return v.rope ? bias<HD, false, true>(v) : bias<HD, false, false>(v);
   }
-  static const void* pick(const BwdVariant& v) { return v.head_dim == 64 ? layout<64>(v) : layout<128>(v); }
+  static const void* pick(const BwdVariant& v) {
+    if constexpr (STREAM && NORM) {
+      // two chunk pairs per thread (head_dim 64 rows of up to 640 chunk pairs):
+      // the weight-gradient sums are kept per step
+      constexpr StreamShape sh = bwd_stream_shape();
+      if (v.steps == 2 && v.head_dim == 64 && !v.bias) {
+        if (v.sectioned)
+          return v.rope ? reinterpret_cast<const void*>(&qkvp_bwd_stream_kernel<64, true, true, true, false, sh.warps, sh.ctas_per_sm, 2>)
+                        : reinterpret_cast<const void*>(&qkvp_bwd_stream_kernel<64, true, false, true, false, sh.warps, sh.ctas_per_sm, 2>);
+        return v.rope ? reinterpret_cast<const void*>(&qkvp_bwd_stream_kernel<64, false, true, true, false, sh.warps, sh.ctas_per_sm, 2>)
+                      : reinterpret_cast<const void*>(&qkvp_bwd_stream_kernel<64, false, false, true, false, sh.warps, sh.ctas_per_sm, 2>);
+      }
+    }
+    return v.head_dim == 64 ? layout<64>(v) : layout<128>(v);
+  }
 };
 
 }  // namespace inst

@@ -207,6 +207,7 @@ struct BwdVariant {
   bool rope;
   bool norm;
   bool bias;
+  int steps;  // chunk pairs per consumer thread of the pipelined kernel (0: not known yet)
 };
 
 // Kernel entry points (host stubs for cudaLaunchKernel / occupancy queries).

@@ -79,6 +79,19 @@ __device__ __forceinline__ void load_pairs(const float* p, float2 (&w)[4]) {
   w[0] = f2(a.x, a.y); w[1] = f2(a.z, a.w); w[2] = f2(b.x, b.y); w[3] = f2(b.z, b.w);
 }
 
+// Sum over the CPH lanes of a head of one value per lane, in the head's tree
+// order: first each lane with its rotate-half partner (lane ^ CPH/2), then
+// xor rounds 1, 2, .., CPH/4. The pair-per-lane kernels hold a chunk and its
+// partner in one lane, so they start with a local add and save a round of
+// shuffles per sum; the order is the same, so both give the same bits.
+template <int CPH>
+__device__ __forceinline__ float head_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, CPH / 2);
+#pragma unroll
+  for (int o = 1; o < CPH / 2; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 // Sum of squares of this lane's 8 values, then over the CPH lanes of the head.
 template <int CPH>
 __device__ __forceinline__ float head_sum_sq(const float2 (&x)[4]) {
@@ -86,10 +99,7 @@ __device__ __forceinline__ float head_sum_sq(const float2 (&x)[4]) {
   a = __ffma2_rn(x[1], x[1], a);
   a = __ffma2_rn(x[2], x[2], a);
   a = __ffma2_rn(x[3], x[3], a);
-  float ss = a.x + a.y;
-#pragma unroll
-  for (int o = 1; o < CPH; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  return ss;
+  return head_sum<CPH>(a.x + a.y);
 }
 
 // x + b on pairs (the qkv bias of the GQAttention variant, added before
@@ -164,12 +174,7 @@ __device__ __forceinline__ void chunk_backward(const float2 (&d)[4], const float
     sq = __ffma2_rn(x[i], x[i], sq);
     dt = __ffma2_rn(x[i], wg[i], dt);
   }
-  float ss = sq.x + sq.y, dot = dt.x + dt.y;
-#pragma unroll
-  for (int o = 1; o < CPH; o <<= 1) {
-    ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    dot += __shfl_xor_sync(0xffffffffu, dot, o);
-  }
+  const float ss = head_sum<CPH>(sq.x + sq.y), dot = head_sum<CPH>(dt.x + dt.y);
   const float r = rsqrtf(fmaf(ss, inv_hd, eps));
   const float kx = r * r * r * dot * inv_hd;
   const float2 rr = f2(r, r), nk = f2(-kx, -kx);
@@ -185,10 +190,10 @@ __device__ __forceinline__ void chunk_backward(const float2 (&d)[4], const float
 //
 // The same arithmetic with a different lane layout: one lane holds chunk e of
 // a head ("lo", values 8e .. 8e+7) and its rotate-half partner chunk e + CPH/2
-// ("hi"), so CPH/2 lanes share a head. The sum of squares is added in exactly
-// the tree order of head_sum_sq (xor rounds 1, 2, .. inside each half, then
-// lo + hi), and the rotation uses the same operations on the same operands,
-// so results are bit-identical to chunk_forward / chunk_backward.
+// ("hi"), so CPH/2 lanes share a head. The head sums are added in exactly the
+// tree order of head_sum (lo + hi, then xor rounds 1, 2, .. over the CPH/2
+// lanes), and the rotation uses the same operations on the same operands, so
+// results are bit-identical to chunk_forward / chunk_backward.
 
 __device__ __forceinline__ float chunk_partial_sq(const float2 (&x)[4]) {
   float2 a = __fmul2_rn(x[0], x[0]);
@@ -201,12 +206,10 @@ __device__ __forceinline__ float chunk_partial_sq(const float2 (&x)[4]) {
 // Sum over the head of per-chunk partials p_lo, p_hi held by the CPH/2 lanes.
 template <int CPH>
 __device__ __forceinline__ float pair_head_sum(float lo, float hi) {
+  float v = lo + hi;
 #pragma unroll
-  for (int o = 1; o < CPH / 2; o <<= 1) {
-    lo += __shfl_xor_sync(0xffffffffu, lo, o);
-    hi += __shfl_xor_sync(0xffffffffu, hi, o);
-  }
-  return lo + hi;
+  for (int o = 1; o < CPH / 2; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
 }
 
 // Forward of a chunk pair (widened, biased): y = x * r * w (y = x without the
@@ -294,15 +297,8 @@ __device__ __forceinline__ void pair_backward(const float2 (&dlo)[4], const floa
     dtl = __ffma2_rn(xlo[i], wglo[i], dtl);
     dth = __ffma2_rn(xhi[i], wghi[i], dth);
   }
-  float sl = sql.x + sql.y, sh = sqh.x + sqh.y, ql = dtl.x + dtl.y, qh = dth.x + dth.y;
-#pragma unroll
-  for (int o = 1; o < CPH / 2; o <<= 1) {
-    sl += __shfl_xor_sync(0xffffffffu, sl, o);
-    sh += __shfl_xor_sync(0xffffffffu, sh, o);
-    ql += __shfl_xor_sync(0xffffffffu, ql, o);
-    qh += __shfl_xor_sync(0xffffffffu, qh, o);
-  }
-  const float ss = sl + sh, dot = ql + qh;
+  const float ss = pair_head_sum<CPH>(sql.x + sql.y, sqh.x + sqh.y);
+  const float dot = pair_head_sum<CPH>(dtl.x + dtl.y, dth.x + dth.y);
   const float r = rsqrtf(fmaf(ss, inv_hd, eps));
   const float kx = r * r * r * dot * inv_hd;
   const float2 rr = f2(r, r), nk = f2(-kx, -kx);

@@ -204,7 +204,10 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_fwd_stream_kernel(co
     const bool dense = a.sg.dense != 0;
     stream_producer<HALF, ROPE, POOL>(
         smem, HD, tpt, stages, stage_bytes, a.sg.n_tiles, a.T, a.pos, a.rope, a.page, a.offset, a.num_pages,
-        a.page_size, a.dev_status, a.err, false,  // measured: the forward streams faster with normal L2 aging
+        // L2 policy of the loads, measured at T = 16384: with the pre-norm save
+        // normal aging is faster (149.2 -> 147.8 us), without it evict-first
+        // (prefill 117.5 -> 106.4 us; Llama 3 and GPT-OSS steps 7-8 us)
+        a.page_size, a.dev_status, a.err, !SAVE,
         [&](unsigned char* dst, int64_t t0, int ntok, uint64_t* bar, uint64_t pol) {
           mbar_expect_tx(bar, (uint32_t)ntok * row_bytes);
           if (dense) {

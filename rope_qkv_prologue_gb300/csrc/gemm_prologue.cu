@@ -190,7 +190,8 @@ __device__ __forceinline__ void gemm_epilogue_head(const GemmArgs& a, const Gemm
 #pragma unroll
     for (int c = 0; c < 8; ++c) st.put(c, make_uint4(hib[4 * c], hib[4 * c + 1], hib[4 * c + 2], hib[4 * c + 3]));
     st.issue(map, col + 64);
-  }}
+  }
+}
 
 }  // namespace
 

@@ -533,33 +533,46 @@ class GemmStep(_Step):
                                 wl.rope_base, C.QKVP_SAVE_PRE, self.q, self.k, self.v, self.q_pre, self.k_pre,
                                 self.stream)
 
-    def unfused_us(self, reps=20):
-        """cuBLAS projection into a packed tensor + qkv_prologue_fwd, per call."""
+    def unfused_us(self, reps=20, rounds=5):
+        """The fused call against cuBLAS projection into a packed tensor +
+        qkv_prologue_fwd, and against cuBLAS alone, measured in alternating
+        blocks of `reps` calls (`rounds` of each, medians), so that all three
+        see the same clocks and power state. Returns (fused, unfused, cuBLAS
+        alone) in us per call."""
+        import statistics
+
         import torch
 
         C, wl = self.C, self.wl
         packed = torch.empty(self.T, ROW, **self.bf)
 
-        def run():
+        def unfused():
             torch.matmul(self.x, self.w.T, out=packed)
             C.qkv_prologue_fwd(self.L, self.T, packed, self.pos, self.w_q, self.w_k, wl.eps, wl.rope_base,
                                C.QKVP_SAVE_PRE, self.q, self.k, self.v, self.q_pre, self.k_pre)
 
-        for _ in range(3):
-            run()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(reps):
-            run()
-        b.record()
-        torch.cuda.synchronize()
-        t = a.elapsed_time(b) * 1e3 / reps
-        a.record()
-        for _ in range(reps):
+        def gemm_only():
             torch.matmul(self.x, self.w.T, out=packed)
-        b.record()
+
+        def block(fn):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) * 1e3 / reps
+
+        for fn in (self.fwd, unfused, gemm_only):
+            for _ in range(3):
+                fn()
         torch.cuda.synchronize()
-        return t, a.elapsed_time(b) * 1e3 / reps
+        times = {"fused": [], "unfused": [], "gemm": []}
+        for _ in range(rounds):
+            times["fused"].append(block(self.fwd))
+            times["unfused"].append(block(unfused))
+            times["gemm"].append(block(gemm_only))
+        return tuple(statistics.median(times[k]) for k in ("fused", "unfused", "gemm"))
 
 
 class NewtonSchulzStep(_Step):
@@ -1077,7 +1090,11 @@ def run_ours(args):
                            "traffic": traffic_from_profile(f"{args.workload}:{dom}"),
                            "traffic_source": TRAFFIC_SOURCE}
         if hasattr(ws, "unfused_us"):
-            unf, gemm_only = ws.unfused_us()
+            fused_alt, unf, gemm_only = ws.unfused_us()
+            out["fused_in_alternating_blocks_us"] = round(fused_alt, 2)
+            out["comparison_note"] = ("fused, unfused (cuBLAS projection + qkv_prologue_fwd) and cuBLAS alone timed "
+                                      "in alternating blocks of 20 calls, 5 rounds each, medians: same clocks and "
+                                      "power state for all three")
             out["unfused_cublas_projection_plus_prologue_us"] = round(unf, 2)
             out["cublas_projection_alone_us"] = round(gemm_only, 2)
         if hasattr(ws, "comparison"):

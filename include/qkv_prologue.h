@@ -61,7 +61,7 @@ typedef enum {
   QKVP_ERR_SHAPE = -2,     /* bad T / head counts / head_dim / row_stride       */
   QKVP_ERR_ALIGN = -3,     /* a tensor is not 16-byte aligned                   */
   QKVP_ERR_ARCH = -4,      /* no CUDA device, or the device is not sm_103       */
-  QKVP_ERR_WORKSPACE = -5, /* backward workspace smaller than required          */
+  QKVP_ERR_WORKSPACE = -5, /* workspace missing or smaller than required         */
   QKVP_ERR_LAUNCH = -6,    /* the CUDA runtime reported an error at launch      */
   QKVP_ERR_FLAGS = -7,     /* unknown or contradictory flag bits                */
   QKVP_ERR_VALUE = -8      /* eps < 0, rope_base <= 0, non-finite, pool sizes   */
@@ -369,50 +369,68 @@ QKVP_API int qkv_prologue_gemm_fwd(const qkvp_layout* layout, int64_t T, int32_t
  *     X = G / (||G||_F + 1e-7);  5 times:  A = X X^T,  X = a X + (b A + c A A) X
  * with (a, b, c) = (3.4445, -4.7750, 2.0315).
  *
- * Arithmetic: bf16 operands on the tensor cores with fp32 accumulation; X, A
- * and b A + c A A are held in bf16 between the products (as in the published
- * bf16 iteration), norms and sums in fp32. The result differs from an exact
- * evaluation by about 1-2 % (relative Frobenius norm per block), as any bf16
- * evaluation of the iteration does. Deterministic.
+ * Evaluation: every matrix of the iteration is a polynomial in the block's
+ * Gram matrix A_0 = X X^T (P_k = a I + b A_k + c A_k^2, A_{k+1} = P_k A_k P_k),
+ * so the result is M X with M = P_4 P_3 P_2 P_1 P_0: three kernels, one pass
+ * over m for the Gram matrices, the five steps on head_dim x head_dim
+ * matrices, one pass over m to apply M. The same function of G as the
+ * iteration; only the rounding differs.
+ * Arithmetic: tensor-core products with fp32 accumulation whose matrix
+ * operands are each held as the sum of two bf16 numbers (about 16 significant
+ * bits; three bf16 MMAs per product), norms and sums in fp32. The result is
+ * much closer to the exact iteration than the published bf16 iteration (whose
+ * own distance from it is 1-2 % in relative Frobenius norm per block).
+ * Deterministic: the same inputs and split give the same bits.
  *
- * layout   INTERLEAVED or SECTIONED; n_q, n_kv, head_dim (64 or 128) give the
- *          rows; row_stride is not used.
- * cols     in_features: a multiple of 64, at most 8192.
- * m        bf16 [rows, cols] row-major (the update: gradient or momentum).
- * out      bf16 [rows, cols] row-major; must not overlap m (QKVP_ERR_VALUE).
- * cluster  0: the library picks how many CTAs share one 128-row unit (a
- *          thread-block cluster splitting its columns); else that number
- *          (it must divide cols / 64 with cols / cluster <= 512, and be at
- *          most 16), for tests. A size the device cannot co-schedule gives
- *          QKVP_ERR_SHAPE.
- * A wait that times out inside the kernel sets bit 1 of the device error
- * word (qkv_prologue_device_error); the launch's output is then invalid.
+ * layout     INTERLEAVED or SECTIONED; n_q, n_kv, head_dim (64 or 128) give
+ *            the rows; row_stride is not used.
+ * cols       in_features: a multiple of 64, at most 2^20.
+ * m          bf16 [rows, cols] row-major (the update: gradient or momentum).
+ * out        bf16 [rows, cols] row-major; must not overlap m (QKVP_ERR_VALUE).
+ * split      0: the library picks how many CTAs share the Gram pass of one
+ *            128-row unit (each a contiguous range of 64-column boxes; the
+ *            fp32 partials are summed in a fixed order); else that number,
+ *            at most min(64, cols / 64) (QKVP_ERR_SHAPE otherwise). The bits
+ *            of the result depend on it.
+ * workspace  device memory of at least qkv_newton_schulz_workspace() bytes
+ *            for the same arguments, 16-byte aligned, any contents, not
+ *            overlapping m or out (QKVP_ERR_WORKSPACE if missing or smaller,
+ *            QKVP_ERR_ALIGN, QKVP_ERR_VALUE). Owned by the caller; it must not
+ *            be used by anything else until the launches are done.
+ * The three kernels are queued on `stream` and return at once. A wait that
+ * times out inside a kernel sets bit 1 of the device error word
+ * (qkv_prologue_device_error); the output is then invalid.
  * ------------------------------------------------------------------------- */
 QKVP_API int qkv_newton_schulz(const qkvp_layout* layout, int64_t cols, const void* m, void* out,
-                               int32_t cluster, void* stream);
+                               int32_t split, void* workspace, size_t workspace_bytes, void* stream);
 
 /* The same for `count` fused updates of one shape stacked along dim 0
- * (m and out: bf16 [count, rows, cols], contiguous), in one launch: the
- * optimizer step of every layer at once. Head blocks are independent and the
- * factor depends only on head_dim and cols, so the stack is one taller weight
- * of count * (n_q + 2 n_kv) blocks. count 0 enqueues nothing; otherwise as
- * qkv_newton_schulz (count * rows at most 2^30). */
+ * (m and out: bf16 [count, rows, cols], contiguous), in one set of launches:
+ * the optimizer step of every layer at once. Head blocks are independent and
+ * the factor depends only on head_dim and cols, so the stack is one taller
+ * weight of count * (n_q + 2 n_kv) blocks. count 0 enqueues nothing;
+ * otherwise as qkv_newton_schulz (count * rows at most 2^30). */
 QKVP_API int qkv_newton_schulz_batch(const qkvp_layout* layout, int64_t count, int64_t cols, const void* m,
-                                     void* out, int32_t cluster, void* stream);
+                                     void* out, int32_t split, void* workspace, size_t workspace_bytes,
+                                     void* stream);
 
-/* The cluster size and grid qkv_newton_schulz_batch would use for these
- * arguments (host only, nothing is launched; count 0 gives 0, 0). */
-QKVP_API int qkv_newton_schulz_plan(const qkvp_layout* layout, int64_t count, int64_t cols, int32_t cluster,
-                                    int32_t* cluster_out, int32_t* grid_out);
+/* Workspace bytes qkv_newton_schulz_batch needs for these arguments (count 0:
+ * 0): ceil(count rows / 128) * (split * 128 * (head_dim + 4) * 4 + 65536). Host
+ * only; with split 0 it plans the split for the current device. */
+QKVP_API int qkv_newton_schulz_workspace(const qkvp_layout* layout, int64_t count, int64_t cols, int32_t split,
+                                         size_t* bytes);
+
+/* The split and the Gram pass's grid qkv_newton_schulz_batch would use for
+ * these arguments (host only, nothing is launched; count 0 gives 0, 0). */
+QKVP_API int qkv_newton_schulz_plan(const qkvp_layout* layout, int64_t count, int64_t cols, int32_t split,
+                                    int32_t* split_out, int32_t* grid_out);
 
 /* ---------------------------------------------------------------------------
  * qkv_prologue_device_error -- read (and with clear != 0, reset) the
  * library's device error word on the current device. Bit 1 means a
  * pipelined kernel's bounded wait on its shared-memory pipeline gave up
  * (after 2 s) and the kernel returned early: the results of that launch are
- * invalid. Bit 2 means a kernel that needs an explicit thread-block cluster
- * launch (qkv_newton_schulz) found none and did nothing. Synchronises with the
- * device (it copies the word to the host).
+ * invalid. Synchronises with the device (it copies the word to the host).
  * ------------------------------------------------------------------------- */
 QKVP_API int qkv_prologue_device_error(int clear, int* value);
 

@@ -102,8 +102,9 @@ _SIGS = {
                              _vp, _vp, _vp, ctypes.c_size_t, _vp], ctypes.c_int),
     "qkv_prologue_gemm_fwd": ([_LP, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _f32, _f64, _u32, _vp, _vp, _vp, _vp, _vp,
                                _vp], ctypes.c_int),
-    "qkv_newton_schulz": ([_LP, _i64, _vp, _vp, _i32, _vp], ctypes.c_int),
-    "qkv_newton_schulz_batch": ([_LP, _i64, _i64, _vp, _vp, _i32, _vp], ctypes.c_int),
+    "qkv_newton_schulz": ([_LP, _i64, _vp, _vp, _i32, _vp, ctypes.c_size_t, _vp], ctypes.c_int),
+    "qkv_newton_schulz_batch": ([_LP, _i64, _i64, _vp, _vp, _i32, _vp, ctypes.c_size_t, _vp], ctypes.c_int),
+    "qkv_newton_schulz_workspace": ([_LP, _i64, _i64, _i32, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
     "qkv_newton_schulz_plan": ([_LP, _i64, _i64, _i32, ctypes.POINTER(ctypes.c_int32),
                                 ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
     "qkv_prologue_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -272,21 +273,34 @@ def qkv_prologue_gemm_fwd(L, T, hidden, x, w_qkv, pos, w_q, w_k, eps, rope_base,
     return _ret(st, "qkv_prologue_gemm_fwd", check)
 
 
-def qkv_newton_schulz(L, cols, m, out, cluster=0, stream=None, check=True):
-    st = _lib.qkv_newton_schulz(ctypes.byref(L), int(cols), _ptr(m), _ptr(out), int(cluster), _stream(stream))
+def qkv_newton_schulz(L, cols, m, out, split=0, workspace=None, workspace_bytes=0, stream=None, check=True):
+    st = _lib.qkv_newton_schulz(ctypes.byref(L), int(cols), _ptr(m), _ptr(out), int(split), _ptr(workspace),
+                                int(workspace_bytes), _stream(stream))
     return _ret(st, "qkv_newton_schulz", check)
 
 
-def qkv_newton_schulz_batch(L, count, cols, m, out, cluster=0, stream=None, check=True):
-    st = _lib.qkv_newton_schulz_batch(ctypes.byref(L), int(count), int(cols), _ptr(m), _ptr(out), int(cluster),
-                                      _stream(stream))
+def qkv_newton_schulz_batch(L, count, cols, m, out, split=0, workspace=None, workspace_bytes=0, stream=None,
+                            check=True):
+    st = _lib.qkv_newton_schulz_batch(ctypes.byref(L), int(count), int(cols), _ptr(m), _ptr(out), int(split),
+                                      _ptr(workspace), int(workspace_bytes), _stream(stream))
     return _ret(st, "qkv_newton_schulz_batch", check)
 
 
-def qkv_newton_schulz_plan(L, cols, cluster=0, count=1):
-    """(cluster size, grid) the library would launch for these arguments."""
+def qkv_newton_schulz_workspace(L, cols, split=0, count=1, check=True):
+    """Workspace bytes the Newton-Schulz launches need for these arguments
+    (status code instead when check is False and the call fails)."""
+    n = ctypes.c_size_t(0)
+    st = _lib.qkv_newton_schulz_workspace(ctypes.byref(L), int(count), int(cols), int(split), ctypes.byref(n))
+    if not check and st != QKVP_OK:
+        return st
+    _ret(st, "qkv_newton_schulz_workspace", True)
+    return n.value
+
+
+def qkv_newton_schulz_plan(L, cols, split=0, count=1):
+    """(split, Gram grid) the library would launch for these arguments."""
     c, g = ctypes.c_int32(0), ctypes.c_int32(0)
-    st = _lib.qkv_newton_schulz_plan(ctypes.byref(L), int(count), int(cols), int(cluster), ctypes.byref(c),
+    st = _lib.qkv_newton_schulz_plan(ctypes.byref(L), int(count), int(cols), int(split), ctypes.byref(c),
                                      ctypes.byref(g))
     _ret(st, "qkv_newton_schulz_plan", True)
     return c.value, g.value

@@ -452,92 +452,29 @@ constexpr int kBiasMaxChunks = kThreads * kBwdChunksPerThread;
 
 // ------------------------------------------- per-head Newton-Schulz ----
 
-// Clusters of `nc` Newton-Schulz CTAs (smem bytes each) that can be resident
-// at once on the current device, cached per device; 0 if none.
-int ns_active_clusters(int nc, size_t smem) {
-  struct Entry {
-    int dev, nc;
-    size_t smem;
-    int n;
-  };
-  static std::mutex mu;
-  static Entry cache[64];
-  static int n_cached = 0;
-  int dev = -1;
-  cudaGetDevice(&dev);
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < n_cached; ++i)
-      if (cache[i].dev == dev && cache[i].nc == nc && cache[i].smem == smem) return cache[i].n;
-  }
-  const void* kern = ns_kernel();
-  int n = 0;
-  if (nc > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-    cudaGetLastError();
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)nc);
-    cfg.blockDim = dim3((unsigned)ns_threads());
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)nc;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      n = 0;
-    }
-  }
-  std::lock_guard<std::mutex> lock(mu);
-  if (n_cached < 64) cache[n_cached++] = Entry{dev, nc, smem, n};
-  return n;
+// Gram CTAs per 128-row unit: `want` when given, else enough for about two
+// Gram CTAs per SM over all units (they are small: three fit on one SM),
+// keeping at least four 64-column boxes (64 KiB of the weight) per CTA.
+int ns_split(int64_t units, int nb, int want, int sms) {
+  if (want > 0) return want;
+  int64_t s = (2 * (int64_t)sms + units - 1) / units;
+  const int64_t cap = nb / 4 > 1 ? nb / 4 : 1;
+  if (s > cap) s = cap;
+  if (s > kNsMaxSplit) s = kNsMaxSplit;
+  return s < 1 ? 1 : (int)s;
 }
 
-// A step costs about as much as kNsStepColumns more columns per CTA would:
-// on GB300 the exchange, A A and the epilogues take ~5 us of a step, the Gram
-// and B X products ~0.5 us per 100 columns of the slice.
-constexpr int kNsStepColumns = 1000;
-
-
-// Cluster size for a fused weight of `units` 128-row units and `cols` columns:
-// the one with the lowest cost waves * (columns per CTA + kNsStepColumns)
-// among the sizes that divide the 64-column boxes, keep a slice within
-// kNsMaxSliceCols and can be resident; `want` > 0 forces that size.
-// Returns 0 when none fits.
-int ns_plan(int64_t units, int64_t cols, int want, size_t* smem) {
-  const void* kern = ns_kernel();
-  const int boxes = (int)(cols / 64);
-  int nc = 0;
-  int64_t best = -1;
-  for (int c = 1; c <= kNsMaxCluster; ++c) {
-    if (boxes % c != 0 || boxes / c > kNsMaxSliceCols / 64 || (want > 0 && c != want)) continue;
-    const size_t sm = (size_t)ns_smem_bytes((int)(cols / c));
-    if (!allow_smem(kern, sm)) continue;
-    int per_sm = 0;  // resident CTAs per SM must not ask for more than 512 TMEM columns together
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, ns_threads(), sm) != cudaSuccess) {
-      cudaGetLastError();
-      continue;
-    }
-    if (per_sm < 1 || per_sm * ns_tmem_cols((int)(cols / c)) > 512) continue;
-    const int act = ns_active_clusters(c, sm);
-    if (act < 1) continue;
-    const int64_t waves = (units + act - 1) / act;
-    const int64_t cost = waves * (cols / c + kNsStepColumns);
-    if (best < 0 || cost < best) {
-      best = cost;
-      nc = c;
-      *smem = sm;
-    }
-  }
-  return nc;
+// Workspace: the fp32 Gram partials, then each unit's M image (64 KiB).
+size_t ns_partial_bytes(int64_t units, int split, int head_dim) {
+  return (size_t)units * (size_t)split * kNsUnitRows * (size_t)ns_partial_stride(head_dim) * 4;
+}
+size_t ns_workspace_bytes(int64_t units, int split, int head_dim) {
+  return ns_partial_bytes(units, split, head_dim) + (size_t)units * 65536;
 }
 
 // Shape checks shared by the Newton-Schulz entry points; *rows = the rows of
 // `count` fused weights stacked along dim 0.
-int check_ns(const qkvp_layout* layout, int64_t count, int64_t cols, int32_t cluster, int64_t* rows) {
+int check_ns(const qkvp_layout* layout, int64_t count, int64_t cols, int32_t split, int64_t* rows) {
   if (!layout) return QKVP_ERR_NULL;
   if (layout->kind != QKVP_INTERLEAVED && layout->kind != QKVP_SECTIONED) return QKVP_ERR_SHAPE;
   if (layout->n_q <= 0 || layout->n_kv <= 0 || layout->n_q % layout->n_kv) return QKVP_ERR_SHAPE;
@@ -545,12 +482,14 @@ int check_ns(const qkvp_layout* layout, int64_t count, int64_t cols, int32_t clu
   if (count < 0 || count > (1 << 20)) return QKVP_ERR_SHAPE;
   *rows = ((int64_t)layout->n_q + 2 * (int64_t)layout->n_kv) * layout->head_dim * count;
   if (*rows > (1 << 30)) return QKVP_ERR_SHAPE;
-  if (cols < 64 || cols % 64 != 0 || cols > (int64_t)kNsMaxCluster * kNsMaxSliceCols) return QKVP_ERR_SHAPE;
-  const int boxes = (int)(cols / 64);
-  if (cluster < 0 || cluster > kNsMaxCluster ||
-      (cluster > 0 && (boxes % cluster != 0 || boxes / cluster > kNsMaxSliceCols / 64)))
-    return QKVP_ERR_SHAPE;
+  if (cols < 64 || cols % 64 != 0 || cols > (1 << 20)) return QKVP_ERR_SHAPE;
+  if (split < 0 || split > kNsMaxSplit || split > cols / 64) return QKVP_ERR_SHAPE;
   return QKVP_OK;
+}
+
+bool overlaps(const void* p, size_t pn, const void* q, size_t qn) {
+  const uintptr_t a = (uintptr_t)p, b = (uintptr_t)q;
+  return a < b + qn && b < a + pn;
 }
 
 }  // namespace
@@ -569,7 +508,7 @@ const char* qkv_prologue_status_string(int status) {
     case QKVP_ERR_SHAPE: return "invalid shape (T, head counts, head_dim, row_stride or layout kind)";
     case QKVP_ERR_ALIGN: return "a tensor is not 16-byte aligned (index tensors: 4-byte)";
     case QKVP_ERR_ARCH: return "no usable CUDA device, or the device is not sm_103";
-    case QKVP_ERR_WORKSPACE: return "backward workspace smaller than qkv_prologue_bwd_workspace_size";
+    case QKVP_ERR_WORKSPACE: return "workspace missing or smaller than its size query gives";
     case QKVP_ERR_LAUNCH: return "CUDA launch failed";
     case QKVP_ERR_FLAGS: return "unknown or unsupported flag bits for this call";
     case QKVP_ERR_VALUE: return "invalid scalar (eps, rope_base, num_pages or page_size)";
@@ -1118,66 +1057,103 @@ int qkv_prologue_gemm_fwd(const qkvp_layout* layout, int64_t T, int32_t hidden, 
   return launch_args(kern, grid, threads, smem, static_cast<cudaStream_t>(stream), args, 2);
 }
 
-int qkv_newton_schulz_batch(const qkvp_layout* layout, int64_t count, int64_t cols, const void* m, void* out,
-                            int32_t cluster, void* stream) {
+int qkv_newton_schulz_workspace(const qkvp_layout* layout, int64_t count, int64_t cols, int32_t split,
+                                size_t* bytes) {
   using namespace qkvp;
   int64_t rows = 0;
-  QKVP_TRY(check_ns(layout, count, cols, cluster, &rows));
+  QKVP_TRY(check_ns(layout, count, cols, split, &rows));
+  if (!bytes) return QKVP_ERR_NULL;
+  if (count == 0) {
+    *bytes = 0;
+    return QKVP_OK;
+  }
+  const int64_t units = (rows + kNsUnitRows - 1) / kNsUnitRows;
+  int sp = split;
+  if (sp == 0) {
+    int sms = 0;
+    QKVP_TRY(current_device(&sms));
+    sp = ns_split(units, (int)(cols / 64), 0, sms);
+  }
+  *bytes = ns_workspace_bytes(units, sp, layout->head_dim);
+  return QKVP_OK;
+}
+
+int qkv_newton_schulz_batch(const qkvp_layout* layout, int64_t count, int64_t cols, const void* m, void* out,
+                            int32_t split, void* workspace, size_t workspace_bytes, void* stream) {
+  using namespace qkvp;
+  int64_t rows = 0;
+  QKVP_TRY(check_ns(layout, count, cols, split, &rows));
   if (!m || !out) return QKVP_ERR_NULL;
   if (!aligned16(m) || !aligned16(out)) return QKVP_ERR_ALIGN;
-  const uintptr_t bytes = (uintptr_t)(rows * cols * 2), pm = (uintptr_t)m, po = (uintptr_t)out;
-  if (pm < po + bytes && po < pm + bytes) return QKVP_ERR_VALUE;  // out overlaps m
+  const size_t bytes = (size_t)(rows * cols * 2);
+  if (overlaps(m, bytes, out, bytes)) return QKVP_ERR_VALUE;
 
   if (count == 0) return QKVP_OK;
   int sms = 0;
-  QKVP_TRY(current_device(&sms));
+  if (split == 0) QKVP_TRY(current_device(&sms));  // the planned split depends on the device
   const int64_t units = (rows + kNsUnitRows - 1) / kNsUnitRows;
-  size_t smem = 0;
-  const int nc = ns_plan(units, cols, cluster, &smem);
-  if (nc == 0) return cluster > 0 ? QKVP_ERR_SHAPE : QKVP_ERR_LAUNCH;
+  const int nb = (int)(cols / 64);
+  const int sp = ns_split(units, nb, split, sms);
+  const size_t need = ns_workspace_bytes(units, sp, layout->head_dim);
+  if (!workspace || workspace_bytes < need) return QKVP_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return QKVP_ERR_ALIGN;
+  if (overlaps(workspace, need, m, bytes) || overlaps(workspace, need, out, bytes)) return QKVP_ERR_VALUE;
+  if (sms == 0) QKVP_TRY(current_device(&sms));
 
   CUtensorMap tm, to;
-  if (!bf16_tile_map(&tm, m, rows, cols, kNsUnitRows) || !bf16_tile_map(&to, out, rows, cols, kNsUnitRows))
+  if (!bf16_tile_map(&tm, m, rows, cols, kNsUnitRows) || !bf16_tile_map(&to, out, rows, cols, 32))
     return QKVP_ERR_LAUNCH;
   NsArgs a;
   std::memset(&a, 0, sizeof(a));
   a.rows = (int32_t)rows;
   a.cols = (int32_t)cols;
   a.head_dim = layout->head_dim;
-  a.nc = nc;
-  a.cs = (int32_t)(cols / nc);
-  a.tmem_cols = ns_tmem_cols(a.cs);
+  a.units = (int32_t)units;
+  a.nb = nb;
+  a.split = sp;
   a.scale = (float)std::sqrt(std::max(1.0, (double)layout->head_dim / (double)cols));
   a.eps = 1e-7f;
+  a.partial = static_cast<float*>(workspace);
+  a.mh = reinterpret_cast<uint4*>(static_cast<unsigned char*>(workspace) +
+                                  ns_partial_bytes(units, sp, layout->head_dim));
   if ((a.err = device_error_word()) == nullptr) return QKVP_ERR_LAUNCH;
-  void* args[] = {&tm, &to, &a};
-  return launch_args(ns_kernel(), units * nc, ns_threads(), smem, static_cast<cudaStream_t>(stream), args, nc,
-                     false, true);
+  const void* kg = ns_gram_kernel();
+  const void* kp = ns_poly_kernel(layout->head_dim);
+  const void* ky = ns_apply_kernel();
+  if (!allow_smem(kg, ns_gram_smem_bytes()) || !allow_smem(kp, ns_poly_smem_bytes(layout->head_dim)) ||
+      !allow_smem(ky, ns_apply_smem_bytes()))
+    return QKVP_ERR_LAUNCH;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* gargs[] = {&tm, &a};
+  QKVP_TRY(launch_args(kg, units * sp, ns_gram_threads(), ns_gram_smem_bytes(), st, gargs));
+  void* pargs[] = {&a};
+  QKVP_TRY(launch_args(kp, units, ns_poly_threads(), ns_poly_smem_bytes(layout->head_dim), st, pargs));
+  const int64_t boxes = units * nb;
+  void* yargs[] = {&tm, &to, &a};
+  return launch_args(ky, boxes < sms ? boxes : sms, ns_apply_threads(), ns_apply_smem_bytes(), st, yargs);
 }
 
-int qkv_newton_schulz(const qkvp_layout* layout, int64_t cols, const void* m, void* out, int32_t cluster,
-                      void* stream) {
-  return qkv_newton_schulz_batch(layout, 1, cols, m, out, cluster, stream);
+int qkv_newton_schulz(const qkvp_layout* layout, int64_t cols, const void* m, void* out, int32_t split,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  return qkv_newton_schulz_batch(layout, 1, cols, m, out, split, workspace, workspace_bytes, stream);
 }
 
-int qkv_newton_schulz_plan(const qkvp_layout* layout, int64_t count, int64_t cols, int32_t cluster,
-                           int32_t* cluster_out, int32_t* grid_out) {
+int qkv_newton_schulz_plan(const qkvp_layout* layout, int64_t count, int64_t cols, int32_t split,
+                           int32_t* split_out, int32_t* grid_out) {
   using namespace qkvp;
   int64_t rows = 0;
-  QKVP_TRY(check_ns(layout, count, cols, cluster, &rows));
-  if (!cluster_out || !grid_out) return QKVP_ERR_NULL;
+  QKVP_TRY(check_ns(layout, count, cols, split, &rows));
+  if (!split_out || !grid_out) return QKVP_ERR_NULL;
   if (count == 0) {
-    *cluster_out = *grid_out = 0;
+    *split_out = *grid_out = 0;
     return QKVP_OK;
   }
   int sms = 0;
   QKVP_TRY(current_device(&sms));
   const int64_t units = (rows + kNsUnitRows - 1) / kNsUnitRows;
-  size_t smem = 0;
-  const int nc = ns_plan(units, cols, cluster, &smem);
-  if (nc == 0) return cluster > 0 ? QKVP_ERR_SHAPE : QKVP_ERR_LAUNCH;
-  *cluster_out = nc;
-  *grid_out = (int32_t)(units * nc);
+  const int sp = ns_split(units, (int)(cols / 64), split, sms);
+  *split_out = sp;
+  *grid_out = (int32_t)(units * sp);
   return QKVP_OK;
 }
 

@@ -299,30 +299,39 @@ const void* gemm_fwd_kernel(int head_dim, bool sectioned, bool rope, bool save);
 int gemm_fwd_smem_bytes();
 int gemm_fwd_threads();
 
-// Per-head Newton-Schulz of a fused QKV update: one cluster of `nc` CTAs per
-// unit of 128 weight rows (two 64-row heads or one 128-row head), CTA r of the
-// cluster holding columns [r cs, (r + 1) cs) of the unit in shared memory.
+// Per-head Newton-Schulz of a fused QKV update through the block Gram
+// matrices: a Gram pass (split CTAs per unit of 128 weight rows, each a range
+// of 64-column boxes), a polynomial pass (one CTA per unit) and an apply pass
+// (persistent, boxes of 128 rows x 64 columns).
 constexpr int kNsUnitRows = 128;
-constexpr int kNsMaxSliceCols = 512;   // cs limit: the slice, A/B and the exchange fit one SM
-constexpr int kNsMaxCluster = 16;      // non-portable cluster size limit
+constexpr int kNsMaxSplit = 64;  // Gram CTAs per unit
 struct NsArgs {
-  int32_t rows;      // (n_q + 2 n_kv) head_dim
+  int32_t rows;      // count (n_q + 2 n_kv) head_dim: rows of the (stacked) weight
   int32_t cols;      // in_features
   int32_t head_dim;  // 64 or 128
-  int32_t nc;        // CTAs per cluster (column slices of a unit)
-  int32_t cs;        // columns per CTA, a multiple of 64, at most kNsMaxSliceCols
-  int32_t tmem_cols; // 256 (cs <= 256) or 512: B X needs cs columns, the Gram and A A 128 each
+  int32_t units;     // ceil(rows / 128)
+  int32_t nb;        // cols / 64
+  int32_t split;     // Gram CTAs per unit, at most nb
   float scale;       // max(1, head_dim / cols) ** 0.5
   float eps;         // added to each block's Frobenius norm
+  float* partial;    // workspace: [units * split][128][head_dim + 4] fp32 Gram partials
+  uint4* mh;         // workspace: [units][2][128 x 128] bf16 hi, lo planes of M (swizzled box images)
   int* err;
 };
-const void* ns_kernel();
-// Dynamic shared memory per CTA for a slice of cs columns, padded so that no
-// more CTAs fit on one SM than its 512 TMEM columns can serve at once (a CTA
-// waiting in tcgen05.alloc for another cluster's CTA could deadlock both).
-int ns_smem_bytes(int cs);
-inline int ns_tmem_cols(int cs) { return cs <= 256 ? 256 : 512; }
-int ns_threads();
+// Row stride of a Gram partial, in floats: head_dim plus 4, so that the 32
+// rows a warp reads from shared memory start in different banks.
+QKVP_HD constexpr int ns_partial_stride(int head_dim) { return head_dim + 4; }
+// Gram partials the polynomial kernel stages in shared memory at a time.
+QKVP_HD constexpr int ns_poly_stage_parts(int head_dim) { return head_dim == 64 ? 6 : 3; }
+const void* ns_gram_kernel();
+const void* ns_poly_kernel(int head_dim);
+const void* ns_apply_kernel();
+int ns_gram_smem_bytes();
+int ns_poly_smem_bytes(int head_dim);
+int ns_apply_smem_bytes();
+int ns_gram_threads();
+int ns_poly_threads();
+int ns_apply_threads();
 
 constexpr int kLatentWarps = 8;        // warps per CTA of the latent kernel
 constexpr int kLatentTokensPerWarp = 2;

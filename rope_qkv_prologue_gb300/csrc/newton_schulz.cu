@@ -7,50 +7,39 @@
 // max(1, head_dim / in_features) ** 0.5. The iteration is Muon's published
 // quintic Newton-Schulz: X = G / (||G||_F + eps), then five times
 //     A = X X^T,   B = b A + c A A,   X = a X + B X,
-// with (a, b, c) = (3.4445, -4.7750, 2.0315). (The published code transposes a
-// tall block first only to work on the smaller Gram matrix; a X + B X with
-// A = X X^T is the same polynomial in X either way.)
+// with (a, b, c) = (3.4445, -4.7750, 2.0315).
 //
-// Work split. A unit is 128 consecutive weight rows, two 64-row heads or one
-// 128-row head (the tensor cores' M = 128). One cluster of nc CTAs takes one
-// unit; CTA r keeps columns [r cs, (r + 1) cs) of it resident in shared memory
-// for the whole iteration (bf16, 128-byte-swizzled boxes of 64 columns, loaded
-// once by TMA). Each step:
-//   1. Gram partial P_r = X_r X_r^T: tcgen05, K = cs, into TMEM columns 0-127.
-//   2. A = sum over the cluster of P_r: every thread pushes its row's 64
-//      columns of the partial (straight from TMEM via registers) to the CTA
-//      that owns the row (CTA r owns rows [128 r / nc, 128 (r + 1) / nc)),
-//      with st.async into that CTA's receive buffer, counted in bytes on its
-//      mbarrier; the owner sums the nc partials of its rows in rank order,
-//      rounds them to bf16 and pushes them the same way into the A tile of
-//      every CTA of the cluster. No remote loads, no fences, no barrier
-//      round trips: each CTA arms its two barriers with the bytes it expects.
-//   3. A A: tcgen05, K = 128, into TMEM columns 128-255 (TMEM: 256 columns
-//      when cs <= 256, else 512; the three products reuse the same columns
-//      one after the other).
-//   4. B = b A + c A A, rounded to bf16, in place of A.
-//   5. B X_r with X_r as the MN-major B operand: tcgen05, N = cs, into TMEM
-//      columns 0 .. cs-1.
-//   6. X_r = a X_r + B X_r, rounded to bf16, in place; after the last step
-//      times the scale, then TMA-stored to the output. (a stays an fp32
-//      factor: folded into B's diagonal it would be rounded to bf16 too,
-//      0.2 % off, which is what X gets when B is small.)
-// With 64-row heads only the two diagonal 64 x 64 blocks of A are reduced and
-// written; the rest of the A tile stays 0, so B is block diagonal and the two
-// heads of a unit never mix. Before the first step each block's squared norm
-// is summed the same way (row sums, then over the cluster) and X is scaled in
-// place to X / (norm + eps).
+// Evaluation through the Gram matrix. With P_k = a I + b A_k + c A_k^2 a step
+// is X_{k+1} = P_k X_k, hence A_{k+1} = X_{k+1} X_{k+1}^T = P_k A_k P_k: every
+// matrix of the iteration is a polynomial in A_0 = X_0 X_0^T (symmetric, and
+// all of them commute), and
+//     X_5 = M X_0,   M = P_4 P_3 P_2 P_1 P_0.
+// So the weight is read twice instead of once per step, and the five steps run
+// on head_dim x head_dim matrices:
+//   1. qkvp_ns_gram_kernel: partial Gram matrices G_u G_u^T over column ranges
+//      of each 128-row unit (two 64-row heads or one 128-row head), streamed
+//      through shared memory by TMA, fp32 accumulation in tensor memory;
+//   2. qkvp_ns_poly_kernel: per unit, the partials summed in a fixed order, the
+//      block norms (trace of each head's diagonal block), then the fourteen
+//      dependent 128 x 128 products of the steps on the tensor cores, and
+//      M * (1 / (||G|| + eps)) * factor written out;
+//   3. qkvp_ns_apply_kernel: out = M G, unit by unit and box by box of 64
+//      columns, streamed through shared memory, stored by TMA.
+// With 64-row heads every matrix of a unit is block diagonal (the two heads
+// never mix): the products only compute the two 64 x 64 diagonal blocks and the
+// rest of every matrix stays exactly 0.
 //
-// B X is committed in two sections of the slice's columns, and the next
-// step's Gram starts on section 0 while the epilogue still updates section 1.
+// Precision. M has the eigenvalue a^5 (about 488) on every direction in which
+// the block is (nearly) rank deficient, so the small eigenvalues that carry the
+// result are differences of numbers that large: held in bf16 (or tf32) the
+// steps lose them. Every matrix operand of the steps is therefore held as the
+// sum of two bf16 numbers (hi = bf16(v), lo = bf16(v - hi): about 16
+// significant bits) and a product is three bf16 MMAs (hi hi + hi lo + lo hi)
+// with fp32 accumulation; M is applied the same way (hi G + lo G). The result is
+// much closer to the exact iteration than the published bf16 iteration is.
 //
-// Roles: warp 0 issues the TMA load; warp 1 owns TMEM and one of its threads
-// issues every MMA; warps 2-9 are the epilogue: warp w reads TMEM lanes
-// 32 (w % 4) .. 32 (w % 4) + 31 (= weight rows of the unit) and one half of
-// the columns. The grid is always launched as an explicit cluster (st.async
-// needs one, even for one CTA); without one the kernel does nothing and sets
-// an error bit. Every wait is bounded (2 s); after a timeout the device error
-// word is set and every thread still passes every barrier, without waiting.
+// Every wait is bounded (2 s); after a timeout the device error word is set and
+// every thread still passes every barrier, without waiting.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -63,26 +52,29 @@
 namespace qkvp {
 namespace {
 
-constexpr int kNsThreads = 320, kNsEpiThreads = 256, kNsEpiBar = 1;
 constexpr int kBox = kNsUnitRows * 128;  // bytes of one 128-row x 64-column bf16 box
-// Receive buffer of a row owner: nc slots of ceil(128 / nc) rows x 64 fp32
-// columns; nc ceil(128 / nc) is at most 140 (nc = 14) for nc <= 16.
-constexpr int kRecvBytes = 140 * 64 * 4;
+constexpr int kPlane = 2 * kBox;         // one bf16 plane of a 128 x 128 matrix: two boxes
 constexpr float kNsA = 3.4445f, kNsB = -4.7750f, kNsC = 2.0315f;
 constexpr int kNsSteps = 5;
+
+constexpr int kGramThreads = 192, kGramStages = 4;
+constexpr int kPolyThreads = 320, kPolyEpiWarps = 8;
+constexpr int kApplyThreads = 192, kApplyStages = 9, kApplyAcc = 8;
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a swizzled box.
 __device__ __forceinline__ int swz(int row, int chunk) { return row * 128 + ((chunk ^ (row & 7)) << 4); }
 
+__device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
+  return reinterpret_cast<unsigned char*>(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+}
+
 // Bounded wait that gives up at once when another thread of the CTA already
 // gave up (*fail): after one timeout the rest of the kernel runs through its
 // barriers without waiting.
-template <bool CLUSTER>
 __device__ __forceinline__ bool ns_wait(uint64_t* bar, uint32_t parity, int* err, volatile int* fail) {
-  auto test = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-  if (test()) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  while (!test()) {
+  while (!mbar_try_wait(bar, parity)) {
     if (*fail) return false;
     if (global_ns() - t0 > kWaitLimitNs) {
       *fail = 1;
@@ -93,363 +85,540 @@ __device__ __forceinline__ bool ns_wait(uint64_t* bar, uint32_t parity, int* err
   return true;
 }
 
+// ns_wait by lane 0 of the calling warp, its result shared with the whole warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* err, volatile int* fail) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = ns_wait(bar, parity, err, fail) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void bulk_wait_read_but1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
+// The 32 fp32 columns of this warp's TMEM lanes starting at `addr`.
+__device__ __forceinline__ void tmem_ld32f(uint32_t addr, float (&v)[32]) {
+  uint32_t r[32];
+  tmem_ld32_issue(addr, r);
+  tmem_wait_ld32(r);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Eight consecutive values of row r, from matrix column c (a multiple of 8),
+// into the hi and lo bf16 planes of a 128 x 128 matrix: hi = bf16(v),
+// lo = bf16(v - hi), both rounded to nearest even.
+__device__ __forceinline__ void put8_split(unsigned char* hi, unsigned char* lo, int r, int c, const float* v) {
+  const int off = (c >> 6) * kBox + swz(r, (c & 63) >> 3);
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 hb = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    const float2 hf = __bfloat1622float2(hb);
+    h[i] = *reinterpret_cast<const uint32_t*>(&hb);
+    l[i] = pack2(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
+  }
+  *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// D (+)= X Y^T on the tensor cores (issued by the calling thread), X and Y
+// held as bf16 hi/lo planes (three MMAs per K step of 16: hi hi, hi lo, lo hi),
+// fp32 in TMEM columns d ..
+// d + 127; K steps [k0, k1) of the HD / 16 (the first step of 0 overwrites D).
+// All matrices of the iteration are symmetric, so Y's rows serve as its
+// columns. With 128-row heads a plane is the 128 x 128 matrix (two boxes).
+// With 64-row heads it is stacked: row r holds the 64 columns of its own
+// head's block (one box), so D[r][n] is the wanted X_h Y_h^T entry when rows r
+// and n are in the same head h (columns 64 h..) and a cross-head value, never
+// read, otherwise.
+template <int HD>
+__device__ __forceinline__ void ns_product(uint32_t d, const unsigned char* xh, const unsigned char* xl,
+                                           const unsigned char* yh, const unsigned char* yl, int k0, int k1) {
+  const uint32_t id = umma_idesc_bf16(128, 128);
+  for (int ks = k0; ks < k1; ++ks) {
+    const int j = ks >> 2, kk = ks & 3;
+    const uint64_t ah = umma_desc_sw128(xh + j * kBox) + 2 * kk, al = umma_desc_sw128(xl + j * kBox) + 2 * kk;
+    const uint64_t bh = umma_desc_sw128(yh + j * kBox) + 2 * kk, bl = umma_desc_sw128(yl + j * kBox) + 2 * kk;
+    umma_bf16(d, ah, bh, id, ks != 0);
+    umma_bf16(d, ah, bl, id, 1);
+    umma_bf16(d, al, bh, id, 1);
+  }
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to global memory.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src)),
+               "r"(bytes)
+               : "memory");
+}
+
 }  // namespace
 
-__global__ void __launch_bounds__(kNsThreads, 1)
-    qkvp_newton_schulz_kernel(const __grid_constant__ CUtensorMap tmap_m, const __grid_constant__ CUtensorMap tmap_out,
-                              const NsArgs a) {
+// ----------------------------------------------------------------- Gram ----
+// CTA b: unit b / split, boxes [p nb / split, (p + 1) nb / split) of it with
+// p = b % split. Warp 0 loads, warp 1 owns TMEM (128 columns) and issues the
+// MMAs, warps 2-5 write the partial: row r's columns of its own head block
+// (rows padded to head_dim + 4 floats).
+__global__ void __launch_bounds__(kGramThreads)
+    qkvp_ns_gram_kernel(const __grid_constant__ CUtensorMap tmap_m, const NsArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t bar_load, bar_gram, bar_aready, bar_sq, bar_bready, bar_fin;
-  // Section s of the slice written (one arrive per epilogue warp; the Gram of
-  // the next step starts on section 0 while section 1 is being written) and
-  // B X of section s done
-  __shared__ __align__(8) uint64_t bar_xsec[2], bar_bx[2];
-  __shared__ __align__(8) uint64_t bar_efull, bar_afull;  // completed by arrivals from every CTA of the cluster
+  unsigned char* ring = align1024(smem_raw);
+  __shared__ __align__(8) uint64_t full[kGramStages], empty[kGramStages], done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_fail;
-  __shared__ float s_red[8], s_inv[2];
-  __shared__ __align__(16) float2 s_nrecv[kNsMaxCluster];  // the cluster's block-norm partials
-
-  if (!is_explicit_cluster()) {  // the exchange needs a cluster launch (the host always makes one)
-    if (threadIdx.x == 0) atomicOr(a.err, kErrNotCluster);
-    return;
-  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t nc = (uint32_t)a.nc, rank = cluster_ctarank();
-  const int unit = blockIdx.x / a.nc;
-  const int cs = a.cs, nbox = cs >> 6, hd = a.head_dim;
-  const int npass = hd == 64 ? 1 : 2;  // exchange passes per Gram (64 columns each)
-  // Sections: boxes [0, sb) and [sb, nbox) when the slice has 4 boxes or more
-  // (the Gram accumulator, TMEM columns 0-127, then lies in section 0's part
-  // of the last B X), else one section.
-  const int nsec = nbox >= 4 ? 2 : 1, sb = nsec == 2 ? nbox >> 1 : nbox;
-  // Phases: every waiter below waits each phase of a barrier in order and can
-  // never be more than one phase behind it, so a parity names one phase.
-  // bar_xsec[s] completes once for the normalised input (phase 0) and once per
-  // step's update (phase it + 1); the Gram of step it waits phase it.
-  unsigned char* xs = smem;                 // nbox boxes: this CTA's columns of the unit
-  unsigned char* ab = smem + nbox * kBox;   // 2 boxes: A, then B in place (128 x 128)
-  float* R = reinterpret_cast<float*>(ab + 2 * kBox);  // receive buffer: [nc][rmax][64] fp32
-  const int rmax = (kNsUnitRows + a.nc - 1) / a.nc;
-  const int r0 = (int)(kNsUnitRows * rank / nc), r1 = (int)(kNsUnitRows * (rank + 1) / nc);  // rows owned
+  const int unit = blockIdx.x / a.split, part = blockIdx.x % a.split;
+  const int j0 = (int)((int64_t)part * a.nb / a.split), j1 = (int)((int64_t)(part + 1) * a.nb / a.split);
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar_load, 1);
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(&bar_xsec[k], kNsEpiThreads / 32);
-      mbar_init(&bar_bx[k], 1);
+    for (int s = 0; s < kGramStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
     }
-    mbar_init(&bar_gram, 1);
-    mbar_init(&bar_aready, 1);
-    mbar_init(&bar_sq, 1);
-    mbar_init(&bar_bready, 1);
-    mbar_init(&bar_fin, 1);
-    mbar_init(&bar_efull, 1);  // armed once per phase by this CTA, completed by bytes from the cluster
-    mbar_init(&bar_afull, 1);
+    mbar_init(&done, 1);
     s_fail = 0;
     mbar_init_fence();
   }
-  // The A tile starts at 0: with 64-row heads its off-diagonal blocks stay 0.
-  for (int i = threadIdx.x; i < 2 * kBox / 16; i += kNsThreads) reinterpret_cast<uint4*>(ab)[i] = make_uint4(0, 0, 0, 0);
-  fence_proxy_async_cta();
-  if (warp == 1) tmem_alloc(&s_tmem, (uint32_t)a.tmem_cols);
+  if (warp == 1) tmem_alloc(&s_tmem, 128);
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // every CTA's barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  griddep_launch_dependents();
+  griddep_wait();  // the update may come from, and the partials be read by, the kernels before this one
 
   if (warp == 0) {
-    // ------------------------------------------------------------ loads
     if (lane == 0) {
-      mbar_arrive_expect_tx(&bar_load, (uint32_t)(nbox * kBox));
-      for (int j = 0; j < nbox; ++j)
-        tma_load_2d(xs + j * kBox, &tmap_m, (int)rank * cs + 64 * j, unit * kNsUnitRows, &bar_load);
+      for (int j = j0, i = 0; j < j1; ++j, ++i) {
+        const int s = i % kGramStages;
+        if (i >= kGramStages && !ns_wait(&empty[s], ((i / kGramStages) - 1) & 1, a.err, &s_fail)) break;
+        mbar_arrive_expect_tx(&full[s], kBox);
+        tma_load_2d(ring + s * kBox, &tmap_m, 64 * j, unit * kNsUnitRows, &full[s]);
+      }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------- MMAs
-    if (lane == 0) {
-      const uint32_t id_sq = umma_idesc_bf16(128, 128);
-      for (int it = 0; it < kNsSteps; ++it) {
-        // P = X_r X_r^T, section by section as the epilogue finishes them
-        bool ok = true;
-        for (int sec = 0; sec < nsec && ok; ++sec) {
-          ok = ns_wait<false>(&bar_xsec[sec], it & 1, a.err, &s_fail);
-          tc_fence_after();
-          for (int j = sec * sb; j < (sec == 0 ? sb : nbox); ++j) {
-            const uint64_t d = umma_desc_sw128(xs + j * kBox);
+    const uint32_t id = umma_idesc_bf16(128, 128);
+    for (int j = j0, i = 0; j < j1; ++j, ++i) {
+      const int s = i % kGramStages;
+      if (!warp_wait(&full[s], (i / kGramStages) & 1, a.err, &s_fail)) break;
+      tc_fence_after();
+      const uint64_t d = umma_desc_sw128(ring + s * kBox);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) umma_bf16(tmem, d + 2 * k, d + 2 * k, id_sq, (j | k) != 0);
-          }
-        }
-        if (!ok) break;
-        umma_commit(&bar_gram);
-        // A is complete in this CTA (the epilogue has seen every exchange pass
-        // of this step finish; waiting on the cluster barrier here could skip
-        // a phase when a step has two passes)
-        if (!ns_wait<false>(&bar_aready, it & 1, a.err, &s_fail)) break;
-        tc_fence_after();
-        fence_proxy_async_cta();  // A arrived by st.async (generic proxy); the MMA reads it
-        for (int j = 0; j < 2; ++j) {  // A A (A is symmetric: both operands are its rows)
-          const uint64_t d = umma_desc_sw128(ab + j * kBox);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) umma_bf16(tmem + 128, d + 2 * k, d + 2 * k, id_sq, (j | k) != 0);
-        }
-        umma_commit(&bar_sq);
-        if (!ns_wait<false>(&bar_bready, it & 1, a.err, &s_fail)) break;
-        tc_fence_after();
-        for (int sec = 0; sec < nsec; ++sec) {  // B X_r, one section (at most 256 columns) at a time
-          const int n0 = 64 * sec * sb, n = 64 * (sec == 0 ? sb : nbox - sb);
-          const uint32_t id = umma_idesc_bf16_bmn(128, n);
-          const uint64_t bd = umma_desc_sw128_mn(xs + (n0 >> 6) * kBox, kBox);
-#pragma unroll
-          for (int s = 0; s < 8; ++s) {
-            const uint64_t ad = umma_desc_sw128(ab + (s >> 2) * kBox) + 2 * (s & 3);
-            umma_bf16(tmem + n0, ad, bd + (uint64_t)(128 * s), id, s != 0);  // +2048 B: 16 rows of X
-          }
-          umma_commit(&bar_bx[sec]);
-        }
-      }
-      umma_commit(&bar_fin);  // arrives once everything issued above has completed
-      mbar_wait(&bar_fin, 0, a.err);
+      for (int k = 0; k < 4; ++k) umma_bf16_warp(tmem, d + 2 * k, d + 2 * k, id, (i | k) != 0);
+      umma_commit_warp(&empty[s]);
     }
+    umma_commit_warp(&done);
   } else {
-    // --------------------------------------------------------- epilogue
-    const int et = threadIdx.x - 64, q = warp & 3, h = (warp - 2) >> 2, row = 32 * q + lane;
-    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
-    const uint32_t efull = smem_addr(&bar_efull), afull = smem_addr(&bar_afull);
-    uint32_t pass = 0;
-
-    // ---- block norms: row sums of squares, then over the cluster
-    ns_wait<false>(&bar_load, 0, a.err, &s_fail);
-    const int half_ch = nbox * 4;  // 16-byte chunks per row in one column half
-    float ss = 0.f;
-    for (int ch = h * half_ch; ch < (h + 1) * half_ch; ++ch) {
-      float f[8];
-      unpack8(*reinterpret_cast<const uint4*>(xs + (ch >> 3) * kBox + swz(row, ch & 7)), f);
+    const int q = warp & 3, r = 32 * q + lane;
+    const int c0 = a.head_dim == 64 ? 64 * (q >> 1) : 0;  // the row's head block starts at this column
+    ns_wait(&done, 0, a.err, &s_fail);
+    tc_fence_after();
+    float4* dst = reinterpret_cast<float4*>(a.partial + ((size_t)blockIdx.x * kNsUnitRows + r) *
+                                                            ns_partial_stride(a.head_dim));
+    for (int c = 0; c < a.head_dim; c += 32) {
+      float v[32];
+      tmem_ld32f(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(c0 + c), v);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
-    }
-    ss = warp_sum(ss);
-    if (lane == 0) s_red[warp - 2] = ss;
-    named_sync(kNsEpiBar, kNsEpiThreads);
-    if (warp == 2) {  // the cluster exchange of the block norms: lane r talks to CTA r
-      float lo = 0.f, hi = 0.f;  // rows 0-63, rows 64-127 of this CTA's columns
-      for (int i = 0; i < 8; ++i) {
-        if (((i + 2) & 3) < 2)
-          lo += s_red[i];
-        else
-          hi += s_red[i];
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&bar_efull, 8u * nc);
-      if ((uint32_t)lane < nc)
-        st_async_u2(cluster_map(smem_addr(&s_nrecv[rank]), lane), __float_as_uint(lo), __float_as_uint(hi),
-                    cluster_map(efull, lane));
-      float tlo = 0.f, thi = 0.f;
-      if (ns_wait<true>(&bar_efull, pass & 1, a.err, &s_fail) && (uint32_t)lane < nc) {
-        tlo = s_nrecv[lane].x;
-        thi = s_nrecv[lane].y;
-      }
-      tlo = warp_sum(tlo);  // the same order in every CTA of the cluster
-      thi = warp_sum(thi);
-      if (lane == 0) {
-        if (hd == 64) {
-          s_inv[0] = 1.f / (sqrtf(tlo) + a.eps);
-          s_inv[1] = 1.f / (sqrtf(thi) + a.eps);
-        } else {
-          s_inv[0] = s_inv[1] = 1.f / (sqrtf(tlo + thi) + a.eps);
-        }
-      }
-    }
-    ++pass;  // bar_efull: phase 0 was the norms; bar_afull starts with the first Gram
-    uint32_t apass = 0;
-    named_sync(kNsEpiBar, kNsEpiThreads);
-    {
-      const float inv = s_inv[row >> 6];
-      for (int j = 0; j < nbox; ++j) {  // box j: this warp's rows, 32 columns
-        uint4* pch[4];
-        uint4 xv[4];
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          pch[kk] = reinterpret_cast<uint4*>(xs + j * kBox + swz(row, 4 * h + kk));
-          xv[kk] = *pch[kk];
-        }
-        const float2 inv2 = f2(inv, inv);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          float2 x2[4];
-          unpack_pairs(xv[kk], x2);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) x2[i] = __fmul2_rn(x2[i], inv2);
-          *pch[kk] = pack_pairs(x2);
-        }
-        if (j == sb - 1 || j == nbox - 1) {  // end of a section
-          fence_proxy_async_cta();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar_xsec[j == nbox - 1 ? nsec - 1 : 0]);
-        }
-      }
-    }
-
-    for (int it = 0; it < kNsSteps; ++it) {
-      // ---- 1-2: Gram partial -> exchange -> A (bf16) in every CTA
-      ns_wait<false>(&bar_gram, it & 1, a.err, &s_fail);
-      tc_fence_after();
-      for (int p = 0; p < npass; ++p) {
-        if (et == 0) {  // the bytes this CTA receives in this pass
-          mbar_arrive_expect_tx(&bar_efull, (uint32_t)(nc * (r1 - r0) * 256));
-          mbar_arrive_expect_tx(&bar_afull, (uint32_t)(kNsUnitRows * 64 * 2));
-        }
-        {  // push this row's 32 columns of the partial to the row's owner
-          uint32_t v[32];
-          tmem_ld32_issue(trow + (uint32_t)((hd == 64 ? 64 * (q >> 1) : 64 * p) + 32 * h), v);
-          const uint32_t o = (uint32_t)(((row + 1) * (int)nc - 1) / kNsUnitRows);  // owner of this row
-          const int lo_row = (int)(kNsUnitRows * o / nc);
-          const uint32_t dst = cluster_map(smem_addr(R + ((int)rank * rmax + row - lo_row) * 64 + 32 * h), o);
-          const uint32_t bar = cluster_map(efull, o);
-          tmem_wait_ld32(v);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            st_async_f4(dst + 16 * i,
-                        make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                    __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])),
-                        bar);
-        }
-        ns_wait<true>(&bar_efull, pass & 1, a.err, &s_fail);
-        // this CTA's rows: the nc partials summed in rank order, then pushed as
-        // bf16 into the A tile of every CTA of the cluster
-        for (int idx = et; idx < (r1 - r0) * 16; idx += kNsEpiThreads) {
-          const int li = idx >> 4, c4 = idx & 15, i = r0 + li;
-          const float* src = R + li * 64 + 4 * c4;
-          float4 s4 = *reinterpret_cast<const float4*>(src);
-          for (uint32_t r = 1; r < nc; ++r) {
-            const float4 t = *reinterpret_cast<const float4*>(src + (int)r * rmax * 64);
-            s4.x += t.x;
-            s4.y += t.y;
-            s4.z += t.z;
-            s4.w += t.w;
-          }
-          const int col = (hd == 64 ? 64 * (i >> 6) : 64 * p) + 4 * c4;
-          const uint32_t d = smem_addr(ab + (col >> 6) * kBox + swz(i, (col & 63) >> 3) + (col & 7) * 2);
-          const uint32_t lo = pack2(s4.x, s4.y), hi2 = pack2(s4.z, s4.w);
-          for (uint32_t r = 0; r < nc; ++r) st_async_u2(cluster_map(d, r), lo, hi2, cluster_map(afull, r));
-        }
-        ns_wait<true>(&bar_afull, apass & 1, a.err, &s_fail);  // A complete in this CTA
-        ++pass;
-        ++apass;
-      }
-      if (et == 0) mbar_arrive(&bar_aready);
-
-      // ---- 3-4: B = b A + c A A, in place of A
-      ns_wait<false>(&bar_sq, it & 1, a.err, &s_fail);
-      tc_fence_after();
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {  // 32 columns of A A, and of A, at a time
-        uint32_t sq[32];
-        tmem_ld32_issue(trow + (uint32_t)(128 + 64 * h + 32 * half), sq);
-        uint4* pch[4];
-        uint4 av[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          pch[k] = reinterpret_cast<uint4*>(ab + h * kBox + swz(row, 4 * half + k));
-          av[k] = *pch[k];
-        }
-        tmem_wait_ld32(sq);
-        const float2 b2 = f2(kNsB, kNsB), c2 = f2(kNsC, kNsC);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {  // on pairs: c (A A) + b A
-          float2 a2[4];
-          unpack_pairs(av[k], a2);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            a2[i] = __ffma2_rn(c2, f2(__uint_as_float(sq[8 * k + 2 * i]), __uint_as_float(sq[8 * k + 2 * i + 1])),
-                               __fmul2_rn(b2, a2[i]));
-          *pch[k] = pack_pairs(a2);
-        }
-      }
-      tc_fence_before();
-      fence_proxy_async_cta();
-      named_sync(kNsEpiBar, kNsEpiThreads);
-      if (et == 0) mbar_arrive(&bar_bready);
-
-      // ---- 5-6: X = a X + B X (after the last step: times the scale, then stored)
-      const bool last = it == kNsSteps - 1;
-      const float fa = last ? a.scale * kNsA : kNsA, fd = last ? a.scale : 1.f;
-      const float2 fa2 = f2(fa, fa), fd2 = f2(fd, fd);
-      // 32 columns from c: X = a X + B X. The TMEM load is issued first, the
-      // four shared-memory loads of X go out while it is in flight, and only
-      // then are the new values computed and stored.
-      auto update = [&](int c) {
-        uint32_t d[32];
-        tmem_ld32_issue(trow + (uint32_t)c, d);
-        uint4* pch[4];
-        uint4 xv[4];
-        unsigned char* xb = xs + (c >> 6) * kBox;
-        const int k0 = (c & 63) >> 3;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          pch[kk] = reinterpret_cast<uint4*>(xb + swz(row, k0 + kk));
-          xv[kk] = *pch[kk];
-        }
-        tmem_wait_ld32(d);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {  // on pairs: a x + d (a x + s d after the last step)
-          float2 x2[4];
-          unpack_pairs(xv[kk], x2);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float2 d2 = f2(__uint_as_float(d[8 * kk + 2 * i]), __uint_as_float(d[8 * kk + 2 * i + 1]));
-            if (last) d2 = __fmul2_rn(fd2, d2);
-            x2[i] = __ffma2_rn(fa2, x2[i], d2);
-          }
-          *pch[kk] = pack_pairs(x2);
-        }
-      };
-      for (int sec = 0; sec < nsec; ++sec) {
-        ns_wait<false>(&bar_bx[sec], it & 1, a.err, &s_fail);
-        tc_fence_after();
-        for (int j = sec * sb; j < (sec == 0 ? sb : nbox); ++j) {  // box j: this warp's rows, 32 columns
-          update(64 * j + 32 * h);
-        }
-        tc_fence_before();
-        fence_proxy_async_cta();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_xsec[sec]);
-      }
-      if (last && et == 0) {  // store each section of the result as soon as every warp has written it
-        for (int sec = 0; sec < nsec; ++sec) {
-          ns_wait<false>(&bar_xsec[sec], kNsSteps & 1, a.err, &s_fail);
-          for (int j = sec * sb; j < (sec == 0 ? sb : nbox); ++j)
-            tma_store_2d(&tmap_out, xs + j * kBox, (int)rank * cs + 64 * j, unit * kNsUnitRows);
-        }
-        bulk_commit();
-        bulk_wait_all();
-      }
+      for (int i = 0; i < 8; ++i) dst[(c >> 2) + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     }
   }
-
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // no CTA leaves while another may still touch its shared memory
-  if (warp == 1) tmem_dealloc(tmem, (uint32_t)a.tmem_cols);
+  if (warp == 1) tmem_dealloc(tmem, 128);
 }
 
-const void* ns_kernel() { return reinterpret_cast<const void*>(&qkvp_newton_schulz_kernel); }
-int ns_smem_bytes(int cs) {
-  const int need = (cs / 64) * kBox + 2 * kBox + kRecvBytes + 1024;
-  // 228 KiB per SM, 1 KiB reserved per CTA: 118 KiB admits one CTA per SM,
-  // 78 KiB at most two
-  const int floor = ns_tmem_cols(cs) == 512 ? 118 * 1024 : 78 * 1024;
-  return need > floor ? need : floor;
+// ----------------------------------------------------------- polynomial ----
+// One CTA per unit. Shared memory: the hi and lo planes of A (A_k, and Q_k =
+// P_k A_k between the products), P_k and M_k, first used to stage the unit's
+// Gram partials (bulk copies, up to kStage of them at a time). TMEM: T0
+// (columns 0-127: S = A A, then A_{k+1} = Q P), T1 (128-255: Q = P A), T2
+// (256-383: M_{k+1} = P M). Warp 1 issues the MMAs: per step S; Q and the first
+// half of P M's K steps (all of them for 64-row heads); A' and the rest, so
+// that P M fills the tensor pipe while the epilogue writes Q and A'. Warps 2-9
+// are the epilogue: warp w holds TMEM lanes (= matrix rows) 32 (w % 4) .. + 31
+// and half of each row's HD columns of its head block (HD / 2 per thread), and
+// keeps its A_k in fp32 registers for b A + c A A.
+template <int HD>
+__global__ void __launch_bounds__(kPolyThreads, 1) qkvp_ns_poly_kernel(const NsArgs a) {
+  constexpr int W = HD / 2;                   // columns per epilogue thread
+  constexpr int kPl = (HD / 64) * kBox;       // bytes of one plane
+  constexpr int kNk = HD / 16;                // K steps of a product
+  constexpr int kKh = HD == 64 ? kNk : kNk / 2;  // K steps of P M issued after Q
+  constexpr int kStride = ns_partial_stride(HD);
+  constexpr int kPart = kNsUnitRows * kStride * 4;  // bytes of one staged partial
+  constexpr int kStage = ns_poly_stage_parts(HD);
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* base = align1024(smem_raw);
+  unsigned char *Ah = base, *Al = base + kPl, *Ph = base + 2 * kPl, *Pl = base + 3 * kPl;
+  unsigned char *Mh = base + 4 * kPl, *Ml = base + 5 * kPl;
+  // MMA -> epilogue (one commit each) and epilogue -> MMA (one arrival per epilogue warp)
+  __shared__ __align__(8) uint64_t bar_s, bar_q, bar_m, bar_a, bar_e1, bar_e2, bar_e2m, bar_e3, bar_stage;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_fail;
+  __shared__ float s_diag[kNsUnitRows];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_m, 1);
+    mbar_init(&bar_a, 1);
+    mbar_init(&bar_e1, kPolyEpiWarps);
+    mbar_init(&bar_e2, kPolyEpiWarps);
+    mbar_init(&bar_e2m, kPolyEpiWarps);
+    mbar_init(&bar_e3, kPolyEpiWarps);
+    mbar_init(&bar_stage, 1);
+    s_fail = 0;
+    mbar_init_fence();
+  }
+  if (warp == 1) tmem_alloc(&s_tmem, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const uint32_t T0 = tmem, T1 = tmem + 128, T2 = tmem + 256;
+  griddep_launch_dependents();
+  griddep_wait();  // the Gram partials
+
+  if (warp == 1) {
+    if (lane == 0) {
+      for (int k = 0; k < kNsSteps; ++k) {
+        const bool last = k == kNsSteps - 1;
+        if (!ns_wait(&bar_e3, k & 1, a.err, &s_fail)) break;  // A_k in the A planes
+        tc_fence_after();
+        ns_product<HD>(T0, Ah, Al, Ah, Al, 0, kNk);  // S = A A
+        umma_commit(&bar_s);
+        if (!ns_wait(&bar_e1, k & 1, a.err, &s_fail)) break;  // P_k written
+        tc_fence_after();
+        if (!last) {
+          ns_product<HD>(T1, Ph, Pl, Ah, Al, 0, kNk);  // Q = P A
+          umma_commit(&bar_q);
+        }
+        if (k > 0 && !ns_wait(&bar_e2m, (k - 1) & 1, a.err, &s_fail)) break;  // M_k written
+        tc_fence_after();
+        ns_product<HD>(T2, Ph, Pl, Mh, Ml, 0, last ? kNk : kKh);  // M_{k+1} = P M
+        if (!last) {
+          if (!ns_wait(&bar_e2, k & 1, a.err, &s_fail)) break;  // Q in the A planes
+          tc_fence_after();
+          ns_product<HD>(T0, Ah, Al, Ph, Pl, 0, kNk);  // A_{k+1} = Q P
+          umma_commit(&bar_a);
+          ns_product<HD>(T2, Ph, Pl, Mh, Ml, kKh, kNk);
+        }
+        umma_commit(&bar_m);
+      }
+    }
+  } else if (warp >= 2) {
+    const int q = warp & 3, h2 = (warp - 2) >> 2, r = 32 * q + lane;
+    const int cp = W * h2;                                  // first plane column of this thread
+    const int tc = (HD == 64 ? 64 * (q >> 1) : 0) + cp;     // its first TMEM column
+    const int dj = (r % HD) - cp;                           // the diagonal's index in them, if in [0, W)
+    const uint32_t trow = (uint32_t)(32 * q) << 16;
+    float A[W];
+
+    // fp32 tensor-memory columns tc .. tc + W - 1 of region t
+    auto ld = [&](uint32_t t, float (&v)[W]) {
+#pragma unroll
+      for (int c = 0; c < W; c += 32) {
+        float u[32];
+        tmem_ld32f(t + trow + (uint32_t)(tc + c), u);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[c + i] = u[i];
+      }
+    };
+    auto put = [&](unsigned char* hi, unsigned char* lo, const float (&v)[W]) {
+#pragma unroll
+      for (int c = 0; c < W; c += 8) put8_split(hi, lo, r, cp + c, v + c);
+    };
+    // this warp's writes are visible to the MMAs (and its TMEM reads done)
+    auto signal = [&](uint64_t* bar) {
+      tc_fence_before();
+      fence_proxy_async_cta();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+    };
+    // 1 / (||G_h|| + eps) of this row's head from the diagonal of its Gram
+    // block: every warp of the head sums it in the same order
+    auto inv_norm = [&]() {
+      const int hb = r - r % HD;
+      float t = 0.f;
+#pragma unroll
+      for (int i = 0; i < HD / 32; ++i) t += s_diag[hb + 32 * i + lane];
+      t = warp_sum(t);
+      return 1.f / (sqrtf(t) + a.eps);
+    };
+
+    // ---- A_0: the partials staged and summed in order, the block norms, the scaling
+    {
+      const int sp = a.split;
+      const float* gsrc = a.partial + (size_t)unit * sp * kNsUnitRows * kStride;
+      for (int p0 = 0, round = 0; p0 < sp; p0 += kStage, ++round) {
+        const int n = sp - p0 < kStage ? sp - p0 : kStage;
+        if (round > 0) named_sync(1, kPolyEpiWarps * 32);  // every thread is done with the last round
+        if (threadIdx.x == 64) {
+          mbar_arrive_expect_tx(&bar_stage, (uint32_t)(n * kPart));
+          bulk_load(base, gsrc + (size_t)p0 * kNsUnitRows * kStride, (uint32_t)(n * kPart), &bar_stage,
+                    policy_evict_first());
+        }
+        ns_wait(&bar_stage, round & 1, a.err, &s_fail);
+        for (int i = 0; i < n; ++i) {
+          const float4* src = reinterpret_cast<const float4*>(base + i * kPart + (r * kStride + cp) * 4);
+#pragma unroll
+          for (int c = 0; c < W / 4; ++c) {
+            const float4 v = src[c];
+            if (p0 + i == 0) {
+              A[4 * c] = v.x;
+              A[4 * c + 1] = v.y;
+              A[4 * c + 2] = v.z;
+              A[4 * c + 3] = v.w;
+            } else {
+              A[4 * c] += v.x;
+              A[4 * c + 1] += v.y;
+              A[4 * c + 2] += v.z;
+              A[4 * c + 3] += v.w;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < W; ++i)
+        if (i == dj) s_diag[r] = A[i];
+      named_sync(1, kPolyEpiWarps * 32);  // s_diag complete; the staging area is free
+      const float inv = inv_norm();
+#pragma unroll
+      for (int i = 0; i < W; ++i) A[i] = (A[i] * inv) * inv;
+      put(Ah, Al, A);
+      float e[W];  // M_0 = I
+#pragma unroll
+      for (int i = 0; i < W; ++i) e[i] = i == dj ? 1.f : 0.f;
+      put(Mh, Ml, e);
+      signal(&bar_e3);  // phase 0: A_0 and M_0
+    }
+
+    for (int k = 0; k < kNsSteps; ++k) {
+      const bool last = k == kNsSteps - 1;
+      float v[W];
+      // ---- P = a I + b A + c S
+      ns_wait(&bar_s, k & 1, a.err, &s_fail);
+      tc_fence_after();
+      ld(T0, v);
+#pragma unroll
+      for (int i = 0; i < W; ++i) {
+        v[i] = fmaf(kNsC, v[i], kNsB * A[i]);
+        if (i == dj) v[i] += kNsA;
+      }
+      put(Ph, Pl, v);
+      signal(&bar_e1);
+      if (!last) {
+        // ---- Q = P A into the A planes
+        ns_wait(&bar_q, k & 1, a.err, &s_fail);
+        tc_fence_after();
+        ld(T1, v);
+        put(Ah, Al, v);
+        signal(&bar_e2);
+        // ---- A_{k+1} = Q P
+        ns_wait(&bar_a, k & 1, a.err, &s_fail);
+        tc_fence_after();
+        ld(T0, A);
+        put(Ah, Al, A);
+        signal(&bar_e3);
+      }
+      // ---- M_{k+1} = P M
+      ns_wait(&bar_m, k & 1, a.err, &s_fail);
+      tc_fence_after();
+      ld(T2, v);
+      if (!last) {
+        put(Mh, Ml, v);
+        signal(&bar_e2m);
+      } else {
+        // M (1 / (||G|| + eps)) * factor as the apply pass's image: the hi and
+        // lo planes of the block-diagonal 128 x 128 matrix, 64 KiB from base
+        // (the A and P planes, no longer read by any MMA)
+        const float f = inv_norm() * a.scale;
+#pragma unroll
+        for (int i = 0; i < W; ++i) v[i] *= f;
+        tc_fence_before();
+        if (HD == 64) {  // the off-diagonal blocks are 0
+          for (int i = threadIdx.x - 64; i < 4 * kBox / 16; i += kPolyEpiWarps * 32)
+            reinterpret_cast<uint4*>(base)[i] = make_uint4(0, 0, 0, 0);
+          named_sync(1, kPolyEpiWarps * 32);
+        }
+        const int c0 = (HD == 64 ? 64 * (r >> 6) : 0) + cp;
+#pragma unroll
+        for (int c = 0; c < W; c += 8) put8_split(base, base + 2 * kBox, r, c0 + c, v + c);
+        fence_proxy_async_cta();
+        named_sync(1, kPolyEpiWarps * 32);
+        if (threadIdx.x == 64) {
+          bulk_store(a.mh + (size_t)unit * (4 * kBox / 16), base, 4 * kBox);
+          bulk_commit();
+          bulk_wait_all();
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
 }
-int ns_threads() { return kNsThreads; }
+
+// ---------------------------------------------------------------- apply ----
+// Persistent: CTA c takes the boxes [c n / grid, (c + 1) n / grid) of the
+// n = units * nb boxes of 128 rows x 64 columns, in unit-major order. Warp 0
+// loads the boxes of G; warp 1 loads the unit's M image (64 KiB, when the unit
+// changes, after its MMAs on the previous one are done: meanwhile the loads of
+// G run on) and issues out_box = (M_hi + M_lo) G_box (K = the unit's 128 rows,
+// G as the MN-major B operand) into one of 8 accumulators of 64 TMEM columns;
+// warps 2-5 round the result to bf16, write it over the G box it came from and
+// store it by TMA (32 rows per warp), then hand the ring slot back once the
+// store has read it.
+__global__ void __launch_bounds__(kApplyThreads, 1)
+    qkvp_ns_apply_kernel(const __grid_constant__ CUtensorMap tmap_m, const __grid_constant__ CUtensorMap tmap_out,
+                         const NsArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* mimg = align1024(smem_raw);    // hi plane, lo plane
+  unsigned char* ring = mimg + 2 * kPlane;      // kApplyStages boxes
+  __shared__ __align__(8) uint64_t full[kApplyStages], empty[kApplyStages], tfull[kApplyAcc], tempty[kApplyAcc];
+  __shared__ __align__(8) uint64_t bar_mh, mh_free;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_fail;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t n = (int64_t)a.units * a.nb;
+  const int64_t i0 = n * blockIdx.x / gridDim.x, i1 = n * (blockIdx.x + 1) / gridDim.x;
+  const int cnt = (int)(i1 - i0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kApplyStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+    }
+    for (int b = 0; b < kApplyAcc; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(&bar_mh, 1);
+    mbar_init(&mh_free, 1);
+    s_fail = 0;
+    mbar_init_fence();
+  }
+  if (warp == 1) tmem_alloc(&s_tmem, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  griddep_launch_dependents();
+  griddep_wait();  // M from the polynomial kernel
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();  // the last read of G
+      for (int t = 0; t < cnt; ++t) {
+        const int64_t i = i0 + t;
+        const int u = (int)(i / a.nb), j = (int)(i % a.nb);
+        const int s = t % kApplyStages;
+        if (t >= kApplyStages && !ns_wait(&empty[s], ((t / kApplyStages) - 1) & 1, a.err, &s_fail)) break;
+        mbar_arrive_expect_tx(&full[s], kBox);
+        tma_load_2d_hint(ring + s * kBox, &tmap_m, 64 * j, u * kNsUnitRows, &full[s], pol);
+      }
+    }
+  } else if (warp == 1) {
+    const uint32_t id = umma_idesc_bf16_bmn(128, 64);
+    int cur = -1, nchg = 0;
+    for (int t = 0; t < cnt; ++t) {
+      const int u = (int)((i0 + t) / a.nb);
+      if (u != cur) {  // the unit's M image, once the MMAs on the previous one are done
+        if (nchg > 0) {
+          umma_commit_warp(&mh_free);
+          if (!warp_wait(&mh_free, (nchg - 1) & 1, a.err, &s_fail)) break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar_mh, 2 * kPlane);
+          bulk_load(mimg, a.mh + (size_t)u * (2 * kPlane / 16), 2 * kPlane, &bar_mh, policy_evict_normal());
+        }
+        if (!warp_wait(&bar_mh, nchg & 1, a.err, &s_fail)) break;
+        cur = u;
+        ++nchg;
+      }
+      const int s = t % kApplyStages, b = t % kApplyAcc;
+      if (!warp_wait(&full[s], (t / kApplyStages) & 1, a.err, &s_fail)) break;
+      if (t >= kApplyAcc && !warp_wait(&tempty[b], ((t / kApplyAcc) - 1) & 1, a.err, &s_fail)) break;
+      tc_fence_after();
+      const uint64_t bd = umma_desc_sw128_mn(ring + s * kBox, kBox);
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = umma_desc_sw128(mimg + p * kPlane + (kk >> 2) * kBox) + 2 * (kk & 3);
+          umma_bf16_warp(tmem + 64 * b, ad, bd + (uint64_t)(128 * kk), id, (p | kk) != 0);  // +2048 B: 16 rows of G
+        }
+      }
+      umma_commit_warp(&tfull[b]);
+    }
+  } else {
+    const int q = warp & 3, r = 32 * q + lane;
+    const uint32_t trow = (uint32_t)(32 * q) << 16;
+    int t = 0;
+    for (; t < cnt; ++t) {
+      const int64_t i = i0 + t;
+      const int u = (int)(i / a.nb), j = (int)(i % a.nb);
+      const int s = t % kApplyStages, b = t % kApplyAcc;
+      if (!ns_wait(&tfull[b], (t / kApplyAcc) & 1, a.err, &s_fail)) break;
+      tc_fence_after();
+      float v0[32], v1[32];
+      tmem_ld32f(tmem + trow + (uint32_t)(64 * b), v0);
+      tmem_ld32f(tmem + trow + (uint32_t)(64 * b + 32), v1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[b]);
+      unsigned char* box = ring + s * kBox;  // the G box this result came from (the MMAs are done with it)
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const float* v = ch < 4 ? v0 + 8 * ch : v1 + 8 * (ch - 4);
+        *reinterpret_cast<uint4*>(box + swz(r, ch)) =
+            make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+      }
+      fence_proxy_async_cta();
+      __syncwarp();
+      if (lane == 0) {
+        const int row0 = u * kNsUnitRows + 32 * q;
+        if (row0 < a.rows) tma_store_2d(&tmap_out, box + 32 * q * 128, 64 * j, row0);
+        bulk_commit();
+        if (t > 0) {  // the previous box's store has read its slot: hand it back
+          bulk_wait_read_but1();
+          mbar_arrive(&empty[(t - 1) % kApplyStages]);
+        }
+      }
+      __syncwarp();
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+const void* ns_gram_kernel() { return reinterpret_cast<const void*>(&qkvp_ns_gram_kernel); }
+const void* ns_poly_kernel(int head_dim) {
+  return head_dim == 64 ? reinterpret_cast<const void*>(&qkvp_ns_poly_kernel<64>)
+                        : reinterpret_cast<const void*>(&qkvp_ns_poly_kernel<128>);
+}
+const void* ns_apply_kernel() { return reinterpret_cast<const void*>(&qkvp_ns_apply_kernel); }
+int ns_gram_smem_bytes() { return kGramStages * kBox + 1024; }
+int ns_poly_smem_bytes(int head_dim) {
+  const int planes = 6 * (head_dim / 64) * kBox;
+  const int stage = ns_poly_stage_parts(head_dim) * kNsUnitRows * ns_partial_stride(head_dim) * 4;
+  return (planes > stage ? planes : stage) + 1024;
+}
+int ns_apply_smem_bytes() { return 2 * kPlane + kApplyStages * kBox + 1024; }
+int ns_gram_threads() { return kGramThreads; }
+int ns_poly_threads() { return kPolyThreads; }
+int ns_apply_threads() { return kApplyThreads; }
 
 }  // namespace qkvp

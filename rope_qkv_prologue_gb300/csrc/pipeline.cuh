@@ -18,7 +18,6 @@ namespace qkvp {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kErrWaitTimeout = 1;
-constexpr int kErrNotCluster = 2;  // a kernel that needs an explicit cluster launch got none: it did nothing
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -2,9 +2,9 @@
 // 128-byte-swizzled shared memory, the tcgen05 matrix and instruction
 // descriptors for bf16 x bf16 -> fp32 with both operands K-major, MMA issue and
 // commit, and the tensor-memory (TMEM) accumulator: allocation and 32-lane x
-// 32-bit loads; and the cluster pieces (cluster addresses, st.async with
-// byte-counted mbarrier completion, cluster-scope waits, proxy fences) and the
-// TMA store.
+// 32-bit loads; the 2-SM (cta_group::2) forms and the cluster pieces they need
+// (cluster addresses, remote arrivals, cluster-scope waits); proxy fences and
+// the TMA store.
 //
 // Operand tiles are `rows x 64` bf16 (128 bytes per row), written by TMA with
 // the 128B swizzle: 8-row groups of 1024 bytes, so a tile's descriptor has the
@@ -30,6 +30,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// The same with an L2 cache policy (createpolicy) for the loaded lines.
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // The same load for a CTA pair working on one 2-SM MMA (cta_group::2): the
 // data lands in this CTA's shared memory, the completed bytes are counted on
 // the mbarrier at cluster address `bar_cluster` (the leader CTA's barrier).
@@ -40,14 +50,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
       "l"(map), "r"(c0), "r"(c1), "r"(bar_cluster)
       : "memory");
-}
-
-// True when the grid was launched with an explicit thread-block cluster
-// (required by st.async, even for a cluster of one CTA).
-__device__ __forceinline__ bool is_explicit_cluster() {
-  uint32_t r;
-  asm volatile("{\n\t.reg .pred p;\n\tmov.pred p, %%is_explicit_cluster;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(r));
-  return r != 0;
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -111,6 +113,27 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
                : "memory");
+}
+
+// Whole-warp forms: every lane executes them with the same (warp-uniform)
+// operands and elect.sync picks the one lane that issues, always the same one
+// (the lowest), so that its commits track its MMAs. Computed by the whole
+// warp, the descriptors stay in uniform registers, which keeps the issue of
+// back-to-back MMAs cheap.
+__device__ __forceinline__ void umma_bf16_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_addr(bar))
+      : "memory");
 }
 
 // The 2-SM forms (cta_group::2), issued by the pair's leader CTA: A is the
@@ -236,21 +259,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return done != 0;
 }
 
-// Asynchronous store into shared memory of a CTA of this cluster (cluster
-// address `addr`), its bytes counted on that CTA's mbarrier at cluster address
-// `bar` (complete_tx: the receiver arms the barrier with the bytes it expects
-// and waits; the data is visible to it once the phase completes).
-__device__ __forceinline__ void st_async_f4(uint32_t addr, const float4& v, uint32_t bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
-               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
-               : "memory");
-}
 
-__device__ __forceinline__ void st_async_u2(uint32_t addr, uint32_t lo, uint32_t hi, uint32_t bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(addr),
-               "r"(lo), "r"(hi), "r"(bar)
-               : "memory");
-}
 
 
 // Order this thread's generic-proxy shared-memory writes (or those it has

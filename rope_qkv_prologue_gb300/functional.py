@@ -152,14 +152,17 @@ def gemm_prologue_forward(x, w_qkv, pos, w_q, w_k, n_q, n_kv, head_dim=64, kind=
     return (q, k, v, q_pre, k_pre) if save_pre else (q, k, v)
 
 
-def per_head_newton_schulz(m, n_q, n_kv, head_dim=64, kind="interleaved", cluster=0, out=None, stream=None):
+def per_head_newton_schulz(m, n_q, n_kv, head_dim=64, kind="interleaved", split=0, out=None, workspace=None,
+                           stream=None):
     """Per-head Newton-Schulz of a fused QKV weight's update m
     [(n_q + 2 n_kv) * head_dim, in_features] bf16: every head_dim-row block
     orthogonalised on its own (Muon's quintic iteration, five steps) and scaled
     by max(1, head_dim / in_features) ** 0.5 ("[muon] Per-head Newton-Schulz for
     fused QKV projections", What this PR does). `kind` names the packing of the
     rows; the result does not depend on it. A 3-D m [count, rows, cols] (one
-    update per layer) is done in a single launch."""
+    update per layer) is done in one set of launches. `workspace` (a device
+    tensor of at least newton_schulz_workspace_bytes bytes) is allocated here
+    when not given; `split` fixes the Gram pass's CTAs per 128-row unit."""
     _check_dev(m)
     if m.dim() not in (2, 3) or m.dtype != torch.bfloat16:
         raise ValueError("m must be a bf16 [rows, cols] or [count, rows, cols] tensor")
@@ -169,11 +172,22 @@ def per_head_newton_schulz(m, n_q, n_kv, head_dim=64, kind="interleaved", cluste
     if out is None:
         out = torch.empty_like(m)
     L = C.layout(kind, n_q, n_kv, head_dim)
+    count = 1 if m.dim() == 2 else m.shape[0]
+    need = C.qkv_newton_schulz_workspace(L, m.shape[-1], split, count)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=m.device)
+    nbytes = workspace.numel() * workspace.element_size()
     if m.dim() == 2:
-        C.qkv_newton_schulz(L, m.shape[1], m, out, cluster, stream)
-    else:  # every weight of the stack in one launch
-        C.qkv_newton_schulz_batch(L, m.shape[0], m.shape[2], m, out, cluster, stream)
+        C.qkv_newton_schulz(L, m.shape[1], m, out, split, workspace, nbytes, stream)
+    else:  # every weight of the stack in one set of launches
+        C.qkv_newton_schulz_batch(L, count, m.shape[2], m, out, split, workspace, nbytes, stream)
     return out
+
+
+def newton_schulz_workspace_bytes(m_shape, n_q, n_kv, head_dim=64, kind="interleaved", split=0):
+    """Workspace bytes per_head_newton_schulz needs for an update of this shape."""
+    count = 1 if len(m_shape) == 2 else m_shape[0]
+    return C.qkv_newton_schulz_workspace(C.layout(kind, n_q, n_kv, head_dim), m_shape[-1], split, count)
 
 
 def on_side_stream(side, fn, *args, **kwargs):

@@ -32,7 +32,8 @@ def test_header_declares_the_boundary():
     assert {"qkv_prologue_fwd", "qkv_prologue_bwd", "qkv_prologue_pool_write",
             "qkv_prologue_pool_scatter", "qkv_prologue_bwd_workspace_size",
             "qkv_prologue_status_string", "qkv_prologue_version", "qkv_prologue_device_error",
-            "qkv_newton_schulz", "qkv_newton_schulz_batch", "qkv_newton_schulz_plan"} <= names
+            "qkv_newton_schulz", "qkv_newton_schulz_batch", "qkv_newton_schulz_plan",
+            "qkv_newton_schulz_workspace"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -354,25 +355,49 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
     assert res.returncode != 0 and "libqkv_prologue.so is missing" in res.stderr
 
 
+def _ns_ws(units, split, head_dim):
+    # the header's formula: per 128-row unit, split fp32 Gram partials of
+    # 128 rows of head_dim + 4 and a 64 KiB image of M (bf16 hi and lo planes)
+    return units * (split * 128 * (head_dim + 4) * 4 + 65536)
+
+
+def test_newton_schulz_workspace_size(lib):
+    C = lib
+    L = C.layout("interleaved", 128, 16, 64)  # 160 blocks of 64 rows: 80 units
+    assert C.qkv_newton_schulz_workspace(L, 5120, 4) == _ns_ws(80, 4, 64)
+    assert C.qkv_newton_schulz_workspace(L, 5120, 1) == _ns_ws(80, 1, 64)
+    L3 = C.layout("interleaved", 3, 1, 64)  # 5 blocks: 3 units, the last half empty
+    assert C.qkv_newton_schulz_workspace(L3, 256, 2) == _ns_ws(3, 2, 64)
+    assert C.qkv_newton_schulz_workspace(L3, 256, 2, count=3) == _ns_ws(8, 2, 64)  # 15 blocks: 8 units
+    L8 = C.layout("sectioned", 8, 2, 128)
+    assert C.qkv_newton_schulz_workspace(L8, 1024, 16) == _ns_ws(12, 16, 128)
+    assert C.qkv_newton_schulz_workspace(L8, 1024, 2, count=0) == 0
+    assert C.qkv_newton_schulz_workspace(L8, 1024, 17, check=False) == C.QKVP_ERR_SHAPE  # more than cols / 64
+    assert C.qkv_newton_schulz_workspace(L8, 64 * 65, 65, check=False) == C.QKVP_ERR_SHAPE  # more than 64
+
+
 @cpu_only
 def test_newton_schulz_argument_checks(lib):
     C = lib
     L = C.layout("interleaved", 128, 16, 64)
     rows = 160 * 64
+    W = A + 2 * rows * 5120 * 2  # a workspace after m and out
+    ws4 = _ns_ws(80, 4, 64)
 
-    def ns(L=L, cols=5120, m=A, out=A + rows * 5120 * 2, cluster=0):
-        return C.qkv_newton_schulz(L, cols, m, out, cluster, stream=0, check=False)
+    def ns(L=L, cols=5120, m=A, out=A + rows * 5120 * 2, split=4, ws=W, wsb=ws4):
+        return C.qkv_newton_schulz(L, cols, m, out, split, ws, wsb, stream=0, check=False)
 
     assert ns() == C.QKVP_ERR_ARCH  # valid: reaches the device check
-    assert ns(cluster=10) == C.QKVP_ERR_ARCH
-    assert ns(L=C.layout("sectioned", 8, 2, 128), cols=1024, out=A + 1536 * 1024 * 2) == C.QKVP_ERR_ARCH
+    assert ns(split=0) == C.QKVP_ERR_ARCH  # planning the split needs the device
+    assert ns(split=80, wsb=_ns_ws(80, 80, 64)) == C.QKVP_ERR_SHAPE  # at most 64
+    assert ns(split=64, wsb=_ns_ws(80, 64, 64)) == C.QKVP_ERR_ARCH
+    assert ns(L=C.layout("sectioned", 8, 2, 128), cols=1024, out=A + 1536 * 1024 * 2, split=16,
+              wsb=_ns_ws(12, 16, 128)) == C.QKVP_ERR_ARCH
     assert ns(cols=5121) == C.QKVP_ERR_SHAPE    # a multiple of 64
     assert ns(cols=32) == C.QKVP_ERR_SHAPE
-    assert ns(cols=16384) == C.QKVP_ERR_SHAPE   # more than 16 slices of 512
-    assert ns(cluster=3) == C.QKVP_ERR_SHAPE    # must divide the 80 boxes of 64 columns
-    assert ns(cluster=2) == C.QKVP_ERR_SHAPE    # 2560 columns per CTA is more than 512
-    assert ns(cluster=17) == C.QKVP_ERR_SHAPE
-    assert ns(cluster=-1) == C.QKVP_ERR_SHAPE
+    assert ns(cols=(1 << 20) + 64) == C.QKVP_ERR_SHAPE
+    assert ns(cols=128, split=3) == C.QKVP_ERR_SHAPE  # more than the 2 boxes of 64 columns
+    assert ns(split=-1) == C.QKVP_ERR_SHAPE
     assert ns(L=C.layout("interleaved", 8, 2, 96)) == C.QKVP_ERR_SHAPE
     assert ns(L=C.layout("interleaved", 8, 3, 64)) == C.QKVP_ERR_SHAPE
     assert ns(L=C.layout("latent", norm_dim=512, rope_dim=64)) == C.QKVP_ERR_SHAPE
@@ -380,7 +405,12 @@ def test_newton_schulz_argument_checks(lib):
     assert ns(out=None) == C.QKVP_ERR_NULL
     assert ns(m=A + 8) == C.QKVP_ERR_ALIGN
     assert ns(out=A + 16) == C.QKVP_ERR_VALUE   # the output overlaps the input
-    assert ns(out=A - rows * 5120 * 2) == C.QKVP_ERR_ARCH  # just below: no overlap
+    assert ns(out=A - rows * 5120 * 2, ws=A + rows * 5120 * 2) == C.QKVP_ERR_ARCH  # just below: no overlap
+    assert ns(ws=None) == C.QKVP_ERR_WORKSPACE
+    assert ns(wsb=ws4 - 1) == C.QKVP_ERR_WORKSPACE
+    assert ns(ws=W + 8) == C.QKVP_ERR_ALIGN
+    assert ns(ws=A + 2 * rows * 5120 * 2 - 16) == C.QKVP_ERR_VALUE  # overlaps the output
+    assert ns(ws=A - 16) == C.QKVP_ERR_VALUE                     # overlaps the input
     with pytest.raises(C.QkvpError):
         C.qkv_newton_schulz_plan(L, 5120)      # planning needs the device
 
@@ -390,9 +420,10 @@ def test_newton_schulz_batch_argument_checks(lib):
     C = lib
     L = C.layout("interleaved", 8, 2, 64)
     one = 768 * 512 * 2
+    ws = _ns_ws(36, 2, 64)  # six layers of 12 blocks: 36 units
 
-    def nb(count=6, cols=512, m=A, out=A + 6 * one, cluster=0):
-        return C.qkv_newton_schulz_batch(L, count, cols, m, out, cluster, stream=0, check=False)
+    def nb(count=6, cols=512, m=A, out=A + 6 * one, split=2, w=A + 12 * one, wsb=ws):
+        return C.qkv_newton_schulz_batch(L, count, cols, m, out, split, w, wsb, stream=0, check=False)
 
     assert nb() == C.QKVP_ERR_ARCH            # valid: reaches the device check
     assert nb(count=0) == C.QKVP_OK           # nothing to do
@@ -401,3 +432,5 @@ def test_newton_schulz_batch_argument_checks(lib):
     assert nb(out=A + 5 * one) == C.QKVP_ERR_VALUE  # overlaps the last weight of the stack
     assert nb(out=A + 6 * one, m=None) == C.QKVP_ERR_NULL
     assert nb(cols=500) == C.QKVP_ERR_SHAPE
+    assert nb(wsb=ws - 16) == C.QKVP_ERR_WORKSPACE  # sized for 36 units
+    assert nb(count=5, wsb=_ns_ws(30, 2, 64)) == C.QKVP_ERR_ARCH

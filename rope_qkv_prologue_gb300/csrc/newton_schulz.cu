@@ -59,7 +59,7 @@ constexpr int kNsSteps = 5;
 
 constexpr int kGramThreads = 192, kGramStages = 4;
 constexpr int kPolyThreads = 320, kPolyEpiWarps = 8;
-constexpr int kApplyThreads = 192, kApplyStages = 9, kApplyAcc = 8;
+constexpr int kApplyThreads = 320, kApplyStages = 9, kApplyAcc = 8;
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a swizzled box.
 __device__ __forceinline__ int swz(int row, int chunk) { return row * 128 + ((chunk ^ (row & 7)) << 4); }
@@ -189,8 +189,11 @@ __global__ void __launch_bounds__(kGramThreads)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  // The update may come from, and the partials be read by, the kernels before
+  // this one. The dependents are let go only after that wait: the apply kernel
+  // starts reading the update before its own wait.
+  griddep_wait();
   griddep_launch_dependents();
-  griddep_wait();  // the update may come from, and the partials be read by, the kernels before this one
 
   if (warp == 0) {
     if (lane == 0) {
@@ -513,12 +516,15 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   griddep_launch_dependents();
-  griddep_wait();  // M from the polynomial kernel
 
   if (warp == 0) {
     if (lane == 0) {
+      // The first boxes of G go out before the wait for the polynomial kernel
+      // (G itself was ready before the Gram kernel let its dependents go);
+      // the rest of the kernel waits for M.
       const uint64_t pol = policy_evict_first();  // the last read of G
       for (int t = 0; t < cnt; ++t) {
+        if (t == kApplyStages) griddep_wait();
         const int64_t i = i0 + t;
         const int u = (int)(i / a.nb), j = (int)(i % a.nb);
         const int s = t % kApplyStages;
@@ -528,6 +534,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
       }
     }
   } else if (warp == 1) {
+    griddep_wait();  // M from the polynomial kernel
     const uint32_t id = umma_idesc_bf16_bmn(128, 64);
     int cur = -1, nchg = 0;
     for (int t = 0; t < cnt; ++t) {
@@ -561,10 +568,13 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
       umma_commit_warp(&tfull[b]);
     }
   } else {
-    const int q = warp & 3, r = 32 * q + lane;
+    griddep_wait();  // the output may still be read by the kernels before this one
+    // two groups of four warps take alternate boxes, so that one group's
+    // stores drain while the other converts
+    const int q = warp & 3, g = (warp - 2) >> 2, r = 32 * q + lane;
     const uint32_t trow = (uint32_t)(32 * q) << 16;
-    int t = 0;
-    for (; t < cnt; ++t) {
+    int prev = -1;
+    for (int t = g; t < cnt; t += 2) {
       const int64_t i = i0 + t;
       const int u = (int)(i / a.nb), j = (int)(i % a.nb);
       const int s = t % kApplyStages, b = t % kApplyAcc;
@@ -589,11 +599,12 @@ __global__ void __launch_bounds__(kApplyThreads, 1)
         const int row0 = u * kNsUnitRows + 32 * q;
         if (row0 < a.rows) tma_store_2d(&tmap_out, box + 32 * q * 128, 64 * j, row0);
         bulk_commit();
-        if (t > 0) {  // the previous box's store has read its slot: hand it back
+        if (prev >= 0) {  // this warp's previous box's store has read its slot: hand it back
           bulk_wait_read_but1();
-          mbar_arrive(&empty[(t - 1) % kApplyStages]);
+          mbar_arrive(&empty[prev % kApplyStages]);
         }
       }
+      prev = t;
       __syncwarp();
     }
     if (lane == 0) bulk_wait_all();

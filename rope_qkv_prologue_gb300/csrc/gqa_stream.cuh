@@ -621,12 +621,13 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(co
   if (BIAS || a.flags == nullptr) return;  // the finalize kernel adds the rows
 
   // Fold: the CTA that finishes last (warp_publish_and_elect) adds every CTA's
-  // partial row into dw_q and dw_k. The rows are staged through the idle ring
-  // in chunks (coalesced 16-byte loads); output o is the float32 sum of rows
-  // s, s + S, ... for each slice s of S (in that order), then of the S slice
-  // sums in order: a fixed order, so the result does not depend on which CTA
-  // folds. (Float64 adds are slow on this part; float32 over at most 1024
-  // rows is far inside the weight-gradient tolerance.)
+  // partial row into dw_q and dw_k. Thread (o, sl) adds column o of rows
+  // sl, sl + S, sl + 2S, ... (S slices of the rows), straight from L2 in
+  // batches of independent loads, into four running sums (row i of the slice
+  // into sum i % 4), combined in order; then the slices in order. A fixed order
+  // throughout, so the result does not depend on which CTA folds. (Float64
+  // adds are slow on this part; float32 over at most 1024 rows is far inside
+  // the weight-gradient tolerance.)
   __shared__ int s_last;
   __threadfence();  // this thread's partial-row stores, before the flag
   asm volatile("bar.sync 1, %0;" ::"r"(NCT) : "memory");
@@ -637,26 +638,25 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(co
   asm volatile("bar.sync 1, %0;" ::"r"(NCT) : "memory");
   if (!s_last) return;
   fence_acq_rel_gpu();
-  constexpr int OUT = 2 * HD, S = NCT / OUT > 0 ? NCT / OUT : 1;
+  constexpr int OUT = 2 * HD, S = NCT / OUT > 0 ? NCT / OUT : 1, kBatch = 40;
   float* stage = reinterpret_cast<float*>(smem + StreamSmem::data(HD, tpt, stages));  // the idle ring
   const int nrows = gridDim.x;
-  const int chunk_rows = (stages * stage_bytes) / (OUT * 4);  // >= 2 stages of >= 16 KiB: >= 32 rows of 1 KiB
   const int o = ct % OUT, sl = ct / OUT;
-  float acc = 0.f;
-  for (int r0 = 0; r0 < nrows; r0 += chunk_rows) {
-    const int nr = min(chunk_rows, nrows - r0);
-    const float4* src = reinterpret_cast<const float4*>(a.partials + (int64_t)r0 * OUT);
-    float4* dst = reinterpret_cast<float4*>(stage);
-#pragma unroll 4
-    for (int i = ct; i < nr * OUT / 4; i += NCT) dst[i] = __ldcg(src + i);
-    asm volatile("bar.sync 1, %0;" ::"r"(NCT) : "memory");
-    if (sl < S) {
-      // rows b of this chunk with b = sl (mod S), ascending
-      for (int b = (sl - r0 % S + S) % S; b < nr; b += S) acc += stage[b * OUT + o];
+  if (sl < S) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const float* col = a.partials + o;
+    for (int i0 = 0; sl + S * i0 < nrows; i0 += kBatch) {
+      float v[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int row = sl + S * (i0 + k);
+        v[k] = row < nrows ? __ldcg(col + (int64_t)row * OUT) : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) acc[k & 3] += v[k];  // kBatch is a multiple of 4: row i into sum i % 4
     }
-    asm volatile("bar.sync 1, %0;" ::"r"(NCT) : "memory");
+    stage[sl * OUT + o] = ((acc[0] + acc[1]) + acc[2]) + acc[3];
   }
-  if (sl < S) stage[sl * OUT + o] = acc;
   asm volatile("bar.sync 1, %0;" ::"r"(NCT) : "memory");
   for (int i = ct; i < OUT; i += NCT) {
     float total = stage[i];

@@ -292,7 +292,7 @@ QKVP_API int qkv_prologue_bwd_noalloc(const qkvp_layout* layout, int64_t T, cons
  * qkv_prologue_bwd_ex also takes
  * dbias   float32 [(n_q + 2 n_kv) * head_dim] out, required when the variant
  *         has a bias (else ignored): the bias gradient, dpacked's values (in
- *         float32, before rounding to bf16) summed over tokens, in float64 in a
+ *         float32, before rounding to bf16) summed over tokens in float32 in a
  *         fixed order. Overwritten, or added to with QKVP_ACCUMULATE_DW.
  *         With a bias the backward needs (n_q + 2 n_kv) * head_dim <= 12288
  *         (QKVP_ERR_SHAPE beyond).

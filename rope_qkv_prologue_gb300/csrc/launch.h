@@ -262,7 +262,7 @@ struct FinalizeArgs {
   float* db;                 // null: no bias gradient
   int32_t accumulate;
 };
-constexpr int kFinalizeOutputsPerCta = 4;
+constexpr int kFinalizeOutputsPerCta = 32;
 constexpr int kFinalizeThreads = 256;
 
 // The wqkv projection with the prologue in its epilogue (tcgen05): tile of

@@ -132,20 +132,60 @@ bool allow_smem(const void* kernel, size_t smem) {
 // their last step's fill (the bias gradient, whose step cap is small).
 bool stream_geometry(const StreamShape& shape, int upt, int lph, int hd, int64_t T, int64_t token_bytes,
                      int smem_per_sm, int static_smem, int extra_dyn, bool any_fill, int max_steps,
-                     StreamGeom* g, size_t* smem) {
+                     bool prefer_fill, StreamGeom* g, size_t* smem) {
   constexpr double kMinStepFill = 0.8;  // useful chunks / (steps * tpg)
   const int nct = shape.warps * 32;
   const int budget = smem_per_sm / shape.ctas_per_sm - 1024 - static_smem - extra_dyn;
+  // Tiles of tpt tokens, tpt dividing the consumer threads into token groups of
+  // whole heads. Larger tiles only add steps and stage bytes, so a scan stops
+  // at the first that needs more than max_steps steps or no longer fits two
+  // stages.
+  //  * prefer_fill: any such tpt; among them, preferring tiles of at least
+  //    min_stage_bytes, the highest fill of the steps times the share of
+  //    shape.max_inflight the ring can hold, then the smallest tile (the
+  //    backward and the norm-off forward at head_dim 128: 4-token tiles, 96 %
+  //    full, against 2-token tiles, 80 % full: Qwen3 backward 111 -> 99 us,
+  //    Llama 3 forward 78 -> 69 us on GB300);
+  //  * else tpt = 1, 2, 4, ...: the first of at least min_stage_bytes whose
+  //    steps are at least kMinStepFill full (the norm-on forward, whose
+  //    4-token tiles measured slower: Qwen3 forward 94 -> 98 us).
   int pick = 0;
-  for (int tpt = 1; nct / tpt >= lph && (nct / tpt) % lph == 0; tpt *= 2) {
-    const int tpg = nct / tpt;
-    const int steps = (upt + tpg - 1) / tpg;
-    if (steps > max_steps) break;  // larger tiles only add steps
-    if (!any_fill && (double)upt / ((double)steps * tpg) < kMinStepFill) continue;
-    const int64_t per_stage = (int64_t)tpt * token_bytes + StreamSmem::table_stride(hd, tpt);
-    if ((budget - StreamSmem::tables(hd) - 128) / per_stage < 2) break;  // two stages no longer fit
-    pick = tpt;
-    if ((int64_t)tpt * token_bytes >= shape.min_stage_bytes) break;
+  if (prefer_fill) {
+    double pick_score = -1.0;
+    bool pick_big = false;
+    for (int tpt = 1; tpt <= nct / lph; ++tpt) {
+      if (nct % tpt != 0 || (nct / tpt) % lph != 0) continue;
+      const int tpg = nct / tpt;
+      const int steps = (upt + tpg - 1) / tpg;
+      if (steps > max_steps) break;
+      const int64_t stage = (int64_t)tpt * token_bytes;
+      const int64_t per_stage = stage + StreamSmem::table_stride(hd, tpt);
+      const int64_t fit = (budget - StreamSmem::tables(hd) - 128) / per_stage;
+      if (fit < 2) break;
+      const double fill = (double)upt / ((double)steps * tpg);
+      if (!any_fill && fill < kMinStepFill) continue;
+      const int64_t stages = std::min<int64_t>(
+          std::min<int64_t>(fit, std::max<int64_t>(2, shape.max_inflight / stage)), kMaxStages);
+      const double held = std::min(1.0, (double)(stages * stage) / (double)shape.max_inflight);
+      const double score = fill * held;
+      const bool big = stage >= shape.min_stage_bytes;
+      if (pick == 0 || (big && !pick_big) || (big == pick_big && score > pick_score + 1e-9)) {
+        pick = tpt;
+        pick_score = score;
+        pick_big = big;
+      }
+    }
+  } else {
+    for (int tpt = 1; nct / tpt >= lph && (nct / tpt) % lph == 0; tpt *= 2) {
+      const int tpg = nct / tpt;
+      const int steps = (upt + tpg - 1) / tpg;
+      if (steps > max_steps) break;
+      if (!any_fill && (double)upt / ((double)steps * tpg) < kMinStepFill) continue;
+      const int64_t per_stage = (int64_t)tpt * token_bytes + StreamSmem::table_stride(hd, tpt);
+      if ((budget - StreamSmem::tables(hd) - 128) / per_stage < 2) break;
+      pick = tpt;
+      if ((int64_t)tpt * token_bytes >= shape.min_stage_bytes) break;
+    }
   }
   if (pick == 0) return false;
   const int tpt = pick;
@@ -591,7 +631,7 @@ static int gqa_forward(const qkvp_layout* L, const qkvp_variant* variant, int64_
   size_t smem = 0;
   if (!(flags & QKVP_FORCE_GENERIC) &&
       stream_geometry(fwd_stream_shape(save, rope), a.cpt / 2, L->head_dim / 16, L->head_dim, T,
-                      (int64_t)a.cpt * 16, smem_per_sm, 0, bias_bytes, false, kStreamMaxSteps, &a.sg, &smem) &&
+                      (int64_t)a.cpt * 16, smem_per_sm, 0, bias_bytes, false, kStreamMaxSteps, !norm, &a.sg, &smem) &&
       (a.err = device_error_word()) != nullptr) {
     a.sg.dense = g.stride == g.row;
     const void* kern = fwd_stream_kernel(var);
@@ -912,7 +952,7 @@ int qkv_prologue_bwd_ex(const qkvp_layout* layout, const qkvp_variant* variant, 
   bool streamed = false;
   if (!(flags & QKVP_FORCE_GENERIC) &&
       stream_geometry(shape, a.cpt / 2, hd / 16, hd, T, token_bytes, smem_per_sm, static_smem, bias_bytes, bias,
-                      bias ? kBiasMaxSteps : kStreamMaxSteps, &a.sg, &smem) &&
+                      bias ? kBiasMaxSteps : kStreamMaxSteps, true, &a.sg, &smem) &&
       (a.err = device_error_word()) != nullptr) {
     a.sg.dense = 1;
     var.steps = a.sg.steps;

@@ -434,6 +434,17 @@ QKVP_API int qkv_newton_schulz_plan(const qkvp_layout* layout, int64_t count, in
  * ------------------------------------------------------------------------- */
 QKVP_API int qkv_prologue_device_error(int clear, int* value);
 
+/* ---------------------------------------------------------------------------
+ * qkv_prologue_wait_selftest -- exercises the library's bounded wait on the
+ * current device: enqueues on `stream` one single-thread kernel whose only wait
+ * (an mbarrier phase that nothing completes) gives up after the library's limit
+ * (2 s), sets bit 1 of the device error word (qkv_prologue_device_error) and
+ * returns. Every pipelined kernel waits the same way; this lets a test make a
+ * wait run out without faulting or hanging the GPU. Not an operation of the
+ * pages. Returns when the kernel is enqueued.
+ * ------------------------------------------------------------------------- */
+QKVP_API int qkv_prologue_wait_selftest(void* stream);
+
 /* Static, human-readable text for a qkvp_status value. */
 QKVP_API const char* qkv_prologue_status_string(int status);
 

@@ -110,6 +110,7 @@ _SIGS = {
     "qkv_prologue_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "qkv_prologue_version": ([], ctypes.c_int),
     "qkv_prologue_device_error": ([ctypes.c_int, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
+    "qkv_prologue_wait_selftest": ([_vp], ctypes.c_int),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -183,6 +184,12 @@ def qkv_prologue_device_error(clear=True, check=True):
     v = ctypes.c_int(0)
     _ret(_lib.qkv_prologue_device_error(int(bool(clear)), ctypes.byref(v)), "qkv_prologue_device_error", check)
     return v.value
+
+
+def qkv_prologue_wait_selftest(stream=None, check=True):
+    """Enqueue the bounded-wait self-test kernel (gives up after 2 s, sets bit 1
+    of the device error word)."""
+    return _ret(_lib.qkv_prologue_wait_selftest(_stream(stream)), "qkv_prologue_wait_selftest", check)
 
 
 def qkv_prologue_fwd(L, T, packed, pos, w_q, w_k, eps, rope_base, flags, q, k, v,

@@ -1197,6 +1197,15 @@ int qkv_newton_schulz_plan(const qkvp_layout* layout, int64_t count, int64_t col
   return QKVP_OK;
 }
 
+int qkv_prologue_wait_selftest(void* stream) {
+  using namespace qkvp;
+  int sms = 0;
+  QKVP_TRY(current_device(&sms));
+  int* err = device_error_word();
+  if (err == nullptr) return QKVP_ERR_LAUNCH;
+  return launch(wait_selftest_kernel(), 1, 32, 0, static_cast<cudaStream_t>(stream), &err);
+}
+
 int qkv_prologue_device_error(int clear, int* value) {
   if (!value) return QKVP_ERR_NULL;
   int sms = 0;

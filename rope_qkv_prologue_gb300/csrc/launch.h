@@ -333,6 +333,9 @@ int ns_gram_threads();
 int ns_poly_threads();
 int ns_apply_threads();
 
+// One thread whose only wait never completes (the bounded-wait self-test).
+const void* wait_selftest_kernel();
+
 constexpr int kLatentWarps = 8;        // warps per CTA of the latent kernel
 constexpr int kLatentTokensPerWarp = 2;
 constexpr int kLatentTileTokens = 16;     // rows per tile of the pipelined latent kernel

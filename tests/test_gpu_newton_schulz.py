@@ -274,3 +274,32 @@ def test_in_features_beyond_one_smem_slice(lib, cuda):
     w = workloads.fused_qkv_update(n_q, n_kv, D, cols, seed=701)
     got = run(lib, w.to(cuda), n_q, n_kv, D).cpu()
     check_blocks(got, w, D, what="16384 columns", tight=True)
+
+
+def test_under_cuda_graph_capture(lib, cuda):
+    # 80 units, the three kernels captured in a graph on a side stream and
+    # replayed: the eager call's bits (and the eager call matches the oracle)
+    n_q, n_kv, D, cols = 128, 16, 64, 512
+    F = lib.functional
+    w = workloads.fused_qkv_update(n_q, n_kv, D, cols, seed=91).to(cuda)
+    eager = F.per_head_newton_schulz(w, n_q, n_kv, D)
+    torch.cuda.synchronize()
+    assert lib.qkv_prologue_device_error(clear=True) == 0
+    need = F.newton_schulz_workspace_bytes(w.shape, n_q, n_kv, D)
+    ws = torch.empty(need, dtype=torch.uint8, device=cuda)
+    out = torch.empty_like(w)
+    s = torch.cuda.Stream(cuda)
+    s.wait_stream(torch.cuda.current_stream(cuda))
+    with torch.cuda.stream(s):
+        F.per_head_newton_schulz(w, n_q, n_kv, D, out=out, workspace=ws)  # warm-up outside the graph
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        F.per_head_newton_schulz(w, n_q, n_kv, D, out=out, workspace=ws)
+    out.zero_()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert lib.qkv_prologue_device_error(clear=True) == 0
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    check_blocks(out.cpu(), w.cpu(), D, blocks=[0, 1, 79, 80, 159], what="graph replay", tight=True)

@@ -77,9 +77,11 @@ constexpr int stream_max_regs(int ncw, int cps) {
 // evict-first (`evict_first`) or normal. POS_AHEAD: the RoPE positions of the
 // next tile (up to 32 tokens, token l in lane l) are loaded one tile ahead,
 // so a tile's table never waits for a global load under the stream's traffic.
-// The backward takes it (T = 16384: 155.1 -> 153.3 us on GB300); the forward
-// does not: the position load paces its reads, and without it the reads go out
-// in bursts that interleave worse with its heavier writes (147 -> 162 us).
+// The backward with the norm takes it (T = 16384: 155.1 -> 152.7 us on GB300),
+// its consumers being slow enough that the producer's own latency showed. The
+// forward and the norm-off backward do not: there the position load paces the
+// reads, and without it they go out in bursts that interleave worse with the
+// writes (forward 147 -> 162 us; Llama 3 backward 67.5 -> 70.1 us).
 template <int HALF, bool ROPE, bool POOL, bool STAGE_POS = false, bool POS_AHEAD = false, class LoadTile>
 __device__ __forceinline__ void stream_producer(unsigned char* smem, int hd, int tpt, int stages,
                                                 int stage_bytes, int64_t n_tiles, int64_t T,
@@ -396,7 +398,7 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(co
   __syncthreads();
 
   if (threadIdx.x >= NCT) {
-    stream_producer<HALF, ROPE, false, false, true>(
+    stream_producer<HALF, ROPE, false, false, NORM>(
         smem, HD, tpt, stages, stage_bytes, a.sg.n_tiles, a.T, a.pos, a.rope, nullptr, nullptr, 0, 0, nullptr, a.err,
         true, [&](unsigned char* dst, int64_t t0, int ntok, uint64_t* bar, uint64_t pol) {
           const uint32_t qb = (uint32_t)qc * 16u, kb = (uint32_t)kc * 16u;

@@ -656,7 +656,9 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(co
   // Fold: the CTA that finishes last (warp_publish_and_elect) adds every CTA's
   // partial row into dw_q and dw_k. Thread (o, sl) adds column o of rows
   // sl, sl + S, sl + 2S, ... (S slices of the rows), straight from L2 in
-  // batches of independent loads, into four running sums (row i of the slice
+  // batches of 80 independent loads (one batch for a grid of up to 160 CTAs
+  // at head_dim 64, two at 128: each batch is one L2 round trip in the
+  // kernel's tail), into four running sums (row i of the slice
   // into sum i % 4), combined in order; then the slices in order. A fixed order
   // throughout, so the result does not depend on which CTA folds. (Float64
   // adds are slow on this part; float32 over at most 1024 rows is far inside
@@ -671,7 +673,7 @@ __global__ void __maxnreg__(stream_max_regs(NCW, CPS)) qkvp_bwd_stream_kernel(co
   asm volatile("bar.sync 1, %0;" ::"r"(NCT) : "memory");
   if (!s_last) return;
   fence_acq_rel_gpu();
-  constexpr int OUT = 2 * HD, S = NCT / OUT > 0 ? NCT / OUT : 1, kBatch = 40;
+  constexpr int OUT = 2 * HD, S = NCT / OUT > 0 ? NCT / OUT : 1, kBatch = 80;
   float* stage = reinterpret_cast<float*>(smem + StreamSmem::data(HD, tpt, stages));  // the idle ring
   const int nrows = gridDim.x;
   const int o = ct % OUT, sl = ct / OUT;

@@ -410,24 +410,28 @@ def test_other_head_shapes(lib, cuda, shape):
         assert_dw_close(dwk.cpu().numpy(), ref_dwk, "dw_k")
 
 
-@pytest.mark.parametrize("shape", [(24, 2, 64), (16, 8, 64)])
-@pytest.mark.parametrize("T", [3, 129])
-def test_two_step_backward_with_tail_tiles(lib, cuda, shape, T):
+@pytest.mark.parametrize("nope", [False, True])
+@pytest.mark.parametrize("shape,T", [((24, 2, 64), 3), ((24, 2, 64), 129), ((16, 8, 64), 3), ((16, 8, 64), 129),
+                                     ((128, 16, 64), 333)])
+def test_two_step_backward_with_tail_tiles(lib, cuda, shape, T, nope):
     # head_dim 64 rows of 112 / 128 chunk pairs: with one CTA of 10 consumer warps
     # per SM (228 KiB of shared memory) the planner takes 5-token tiles of two steps
     # per thread (the instance that keeps its weight-gradient sums per step), the
-    # second step 87.5 % / 100 % full; T = 3 and 129 end in a tile with missing tokens
+    # second step 87.5 % / 100 % full; T = 3 and 129 end in a tile with missing
+    # tokens. The Muse Spark rows (640 chunk pairs) take the same instance on
+    # 1-token tiles. RoPE and NoPE layers.
     n_q, n_kv, D = shape
-    wl = workloads.gqa_inputs(T, n_q, n_kv, D, seed=11 + T, rope_base=5e5, pos_high=131072, with_grads=True)
+    wl = workloads.gqa_inputs(T, n_q, n_kv, D, seed=11 + T, rope_base=5e5, pos_high=131072, nope=nope,
+                              with_grads=True)
     F = lib.functional
     for kind in ("interleaved", "sectioned"):
         out = _gpu_fwd(lib, wl, kind, cuda, save=True)
         dp, dwq, dwk = F.prologue_backward(wl.dq.to(cuda), wl.dk.to(cuda), wl.dv.to(cuda), out[3], out[4],
                                            wl.pos.to(cuda), wl.w_q.to(cuda), wl.w_k.to(cuda), n_q, n_kv, D,
-                                           kind, wl.eps, wl.rope_base)
+                                           kind, wl.eps, wl.rope_base, nope)
         torch.cuda.synchronize()
         ref_dp, ref_dwq, ref_dwk = _oracle_bwd_chunked(wl, kind, np.arange(wl.T))
-        assert_bf16_close(u16(dp), ref_dp, f"dpacked {shape} {kind} T={T}")
+        assert_bf16_close(u16(dp), ref_dp, f"dpacked {shape} {kind} T={T} nope={nope}")
         assert_dw_close(dwq.cpu().numpy(), ref_dwq, "dw_q")
         assert_dw_close(dwk.cpu().numpy(), ref_dwk, "dw_k")
 

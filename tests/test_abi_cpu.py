@@ -342,6 +342,18 @@ def test_noalloc_backward_argument_checks(lib):
     assert bwd(C.layout("interleaved", 128, 16, 64), 16384) == C.QKVP_ERR_ARCH   # fits; needs the device
 
 
+@cpu_only
+def test_device_queries_refused_without_a_device(lib):
+    C = lib
+    # the bounded-wait self-test and the device error word need the device: refused
+    assert C.qkv_prologue_wait_selftest(stream=0, check=False) == C.QKVP_ERR_ARCH
+    raw = C._lib._lib
+    v = ctypes.c_int(7)
+    assert raw.qkv_prologue_device_error(0, None) == C.QKVP_ERR_NULL
+    assert raw.qkv_prologue_device_error(1, ctypes.byref(v)) == C.QKVP_ERR_ARCH
+    assert v.value == 7  # left untouched
+
+
 def test_binding_fails_loudly_without_the_library(tmp_path):
     # a copy of the package without the .so must refuse to import
     import shutil

@@ -37,7 +37,7 @@ the pages' stated layout facts (see tests/test_oracle_pins.py). None is
 "parity unpinned".
 """
 
-from .bf16 import bf16_bits_to_f64, f64_to_f32_rne, to_bf16_rne  # noqa: F401
+from .bf16 import bf16_bits_to_f64, to_bf16_rne  # noqa: F401
 from .prologue import (  # noqa: F401
     PackedLayout,
     head_blocks,

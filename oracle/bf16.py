@@ -43,8 +43,3 @@ def to_bf16_rne(x):
     # are the bf16 pattern.
     bits = (r.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
     return np.where(np.isnan(x), np.uint16(0x7FC0), bits).astype(np.uint16)
-
-
-def f64_to_f32_rne(x):
-    """Round float64 to float32 (IEEE round to nearest even)."""
-    return np.asarray(x, dtype=np.float64).astype(np.float32)
